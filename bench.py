@@ -1,0 +1,468 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA recurrence library on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one call of the hot path on one batch of seeded synthetic input
+already resident in HBM:
+  prefill_4k         kda_prefill_chunked, H=96, T=4096, bf16 q/k/v, chunk 64 (default)
+  prefill_32k_carry  kda_prefill_chunked, H=96, T=32768 with S0
+  varlen_64k         kda_prefill_chunked over 8 packed sequences (65536 tokens)
+                     with S0, then kda_decode_step for all 8
+The JSON line's value is prefill tokens/s.  The metric's second half, decode
+state GB/s, is measured on the batched decode workload (B=64, H=96, 100
+consecutive in-place steps) and reported under "decode".
+
+Inputs (and outputs) exceed the 129 MB L2, so no L2 flush is done between
+steps.  Timing: CUDA events on the launching stream, W untimed warm-up steps,
+then exactly K timed steps between a barrier and a device synchronise on both
+sides; max over ranks.  Under torchrun each rank runs an independent replica
+on its own GPU (the path has no cross-GPU exchange): weak scaling.
+
+--impl reference times the CPU oracle (fp64, all host cores) on a bounded
+sample of the same workload and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import kda_inputs as ki  # noqa: E402
+
+METRIC = "KDA prefill tokens/s (% BF16 TC peak); decode state GB/s (% of 8 TB/s HBM)"
+UNIT = "tokens/s"
+DK = DV = 128
+# algorithmic bytes per token-head of a prefill: q, k, v bf16 (3 x 256) + g fp32
+# (512) + beta (4) + o fp32 (512)
+PREFILL_BYTES_PER_TOKEN_HEAD_BF16 = 3 * 256 + 512 + 4 + 512
+STATE_BYTES = DK * DV * 4
+# flops per token-head of the chunked form with chunk C: 2C(3dk + 2dv) + 6 dk dv
+def prefill_flops_per_token_head(C):
+    return 2 * C * (3 * DK + 2 * DV) + 6 * DK * DV
+# algorithmic bytes per (b, h) of a decode step: state read + write, q, k, v bf16,
+# g fp32, beta, o fp32
+DECODE_BYTES_PER_STATE = 2 * STATE_BYTES + 3 * 256 + 512 + 4 + 512
+FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12   # fp32 FMA lanes x 2 flop x max SM clock
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]),
+                                 hw=f[5], hwt=f[6], swt=f[7], pcap=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _to_dev(a, dev):
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def _pinned(a):
+    import torch
+    if a.dtype == np.uint16:
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.pin_memory()
+
+
+def run_ours(args):
+    import torch
+    import kda_linear_attention_gb300 as kda
+    from kda_linear_attention_gb300 import build as kbuild
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or ws > 1:
+        kbuild.build()
+    if ws > 1:
+        torch.distributed.barrier()
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    wl = args.workload
+    if wl == "varlen_64k":
+        pre, dstep = ki.workload_varlen_with_decode(wl)
+    else:
+        pre, dstep = ki.workload_prefill(wl), None
+    T, H, N, C = pre.T, pre.H, pre.N, pre.chunk
+    d = {n: _to_dev(getattr(pre, n), dev) for n in ("q", "k", "v", "g", "beta")}
+    cu = _to_dev(pre.cu_seqlens, dev)
+    S0 = None if pre.S0 is None else _to_dev(pre.S0, dev)
+    o = torch.empty((T, H, DV), dtype=torch.float32, device=dev)
+    S_out = torch.empty((N, H, DK, DV), dtype=torch.float32, device=dev)
+    if dstep is not None:
+        dd = {n: _to_dev(getattr(dstep, n), dev) for n in ("q", "k", "v", "g", "beta")}
+        od = torch.empty((N, H, DV), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 1 + (1 if dstep is not None else 0)
+
+    ev_pre = []   # per-launch (start, end) of the prefill kernel
+
+    def step(record=False):
+        if record:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+        kda.prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, S0=S0, chunk=C,
+                            o=o, S_out=S_out)
+        if record:
+            b.record(stream)
+            ev_pre.append((a, b))
+        if dstep is not None:
+            kda.decode_step(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], S_out, o=od)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(record=True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    if ws > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_per_step = ms / args.steps
+    value = ws * T / (ms_per_step / 1e3)
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_pre)
+
+    peaks = _peaks()
+    tok_heads = T * H
+    n_state = N * H
+    alg_bytes = tok_heads * (PREFILL_BYTES_PER_TOKEN_HEAD_BF16 if pre.dtype == "bf16" else
+                             (3 * 512 + 512 + 4 + 512)) + n_state * STATE_BYTES * (2 if S0 is not None else 1)
+    alg_flops = tok_heads * prefill_flops_per_token_head(C)
+    achieved_gbs = alg_bytes / (kern_ms / 1e3) / 1e9
+    achieved_tflops = alg_flops / (kern_ms / 1e3) / 1e12
+    roofline = {
+        "kernel": "kda_prefill (fp32 CUDA-core chunked)",
+        "bound": "alu",
+        "achieved": round(achieved_tflops, 3), "peak": round(FFMA_PEAK_TFLOPS, 1),
+        "unit": "TFLOP/s", "frac": round(achieved_tflops / FFMA_PEAK_TFLOPS, 4),
+        "peak_source": "fp32 FMA lanes x max SM clock (derived)",
+        "traffic": None,
+        "hbm": {"achieved_gbs": round(achieved_gbs, 1), "peak_gbs": peaks["hbm"],
+                "frac": round(achieved_gbs / peaks["hbm"], 4), "of": peaks["source"]},
+        "tensor": {"achieved_tflops": round(achieved_tflops, 2), "peak_tflops": peaks["bf16"],
+                   "frac": round(achieved_tflops / peaks["bf16"], 5), "of": peaks["source"]},
+        "kernel_ms": round(kern_ms, 4),
+        "algorithmic_bytes": int(alg_bytes), "algorithmic_flops": int(alg_flops),
+    }
+
+    # ---- decode leg: B=64, H=96, 100 consecutive in-place steps ----------
+    decode = None
+    if not args.no_decode:
+        decode = _decode_leg(kda, torch, dev, stream, peaks, args)
+
+    # ---- end to end through the public API with host buffers -------------
+    e2e = _e2e_leg(kda, torch, dev, stream, pre, dstep, args, barrier, ws)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in, fp32 state/accumulate" if pre.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded; shapes and distributions of the model's KDA layer)",
+        "config": {"workload": wl, "H": H, "T": T, "N": N, "chunk": C, "dk": DK, "dv": DV,
+                   "qkv": pre.dtype, "S0": S0 is not None,
+                   "lens": [int(x) for x in np.diff(pre.cu_seqlens)] if N > 1 else None,
+                   "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roofline,
+        "decode": decode,
+        "e2e": e2e,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = _cpu_baseline(pre, args)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _decode_leg(kda, torch, dev, stream, peaks, args):
+    w = ki.WORKLOADS["decode_b64"]
+    B, H, n_steps = w["B"], w["H"], w["steps"]
+    S_np, steps = ki.workload_decode("decode_b64")
+    S = _to_dev(S_np, dev)
+    del S_np
+    ins = [{n: _to_dev(getattr(st, n), dev) for n in ("q", "k", "v", "g", "beta")} for st in steps]
+    o = torch.empty((B, H, DV), dtype=torch.float32, device=dev)
+    for i in range(3):
+        x = ins[i]
+        kda.decode_step(x["q"], x["k"], x["v"], x["g"], x["beta"], S, o=o)
+    torch.cuda.synchronize()
+    evs = []
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for x in ins:
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        kda.decode_step(x["q"], x["k"], x["v"], x["g"], x["beta"], S, o=o)
+        b.record(stream)
+        evs.append((a, b))
+    t1.record(stream)
+    torch.cuda.synchronize()
+    per = [a.elapsed_time(b) for a, b in evs]
+    total = t0.elapsed_time(t1)
+    med = statistics.median(per)
+    state_bytes = 2 * STATE_BYTES * B * H
+    all_bytes = DECODE_BYTES_PER_STATE * B * H
+    gbs_state = state_bytes / (med / 1e3) / 1e9
+    gbs_all = all_bytes / (med / 1e3) / 1e9
+    return {
+        "workload": "decode_b64 (B=64, H=96, 100 consecutive in-place steps)",
+        "metric": "decode state GB/s", "value": round(gbs_state, 1), "unit": "GB/s",
+        "median_step_us": round(med * 1e3, 2), "total_ms_100_steps": round(total, 3),
+        "roofline": {"kernel": "kda_decode", "bound": "hbm", "achieved": round(gbs_all, 1),
+                     "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": round(gbs_all / peaks["hbm"], 4), "of": peaks["source"],
+                     "frac_of_nominal_8tbs": round(gbs_all / 8000.0, 4), "traffic": None,
+                     "algorithmic_bytes": int(all_bytes)},
+        "gpu_launches": n_steps,
+    }
+
+
+def _e2e_leg(kda, torch, dev, stream, pre, dstep, args, barrier, ws):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs from pinned host memory and reads the outputs back."""
+    names = ("q", "k", "v", "g", "beta")
+    host = {n: _pinned(getattr(pre, n)) for n in names}
+    cu_h = _pinned(pre.cu_seqlens)
+    S0_h = None if pre.S0 is None else _pinned(pre.S0)
+    T, H, N = pre.T, pre.H, pre.N
+    o_h = torch.empty((T, H, DV), dtype=torch.float32).pin_memory()
+    S_h = torch.empty((N, H, DK, DV), dtype=torch.float32).pin_memory()
+    if dstep is not None:
+        dh = {n: _pinned(getattr(dstep, n)) for n in names}
+        od_h = torch.empty((N, H, DV), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + cu_h.numel() * 4
+    h2d += 0 if S0_h is None else S0_h.numel() * 4
+    d2h = o_h.numel() * 4 + S_h.numel() * 4
+    if dstep is not None:
+        h2d += sum(t.numel() * t.element_size() for t in dh.values())
+        d2h += od_h.numel() * 4
+
+    def step():
+        dd = {n: host[n].to(dev, non_blocking=True) for n in names}
+        cu = cu_h.to(dev, non_blocking=True)
+        s0 = None if S0_h is None else S0_h.to(dev, non_blocking=True)
+        o, S = kda.prefill_chunked(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], cu, S0=s0,
+                                   chunk=pre.chunk)
+        if dstep is not None:
+            x = {n: dh[n].to(dev, non_blocking=True) for n in names}
+            od = kda.decode_step(x["q"], x["k"], x["v"], x["g"], x["beta"], S)
+            od_h.copy_(od, non_blocking=True)
+        o_h.copy_(o, non_blocking=True)
+        S_h.copy_(S, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = a.elapsed_time(b) / args.steps
+    if ws > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    return {"value": round(ws * T / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "gpu_launches": (1 + (dstep is not None)) * args.steps}
+
+
+def _oracle_sample(pre, heads):
+    """Time the oracle on the first `heads` heads of every sequence."""
+    import oracle
+    units = [(n, h) for n in range(pre.N) for h in range(heads)]
+    threads = min(oracle.default_threads(), len(units))
+    oracle.build()
+    t = time.perf_counter()
+    oracle.prefill(pre, units=units, threads=threads)
+    dt = time.perf_counter() - t
+    return dt, threads, units
+
+
+def _sample_heads(pre, args):
+    # about 4e5 token-heads per sample: roughly 10-30 s of fp64 CPU work
+    return max(1, min(pre.H, args.cpu_heads or int(round(4e5 / max(1, pre.T)))))
+
+
+def _cpu_baseline(pre, args):
+    heads = _sample_heads(pre, args)
+    dt, threads, units = _oracle_sample(pre, heads)
+    tokens_equiv = pre.T * heads / pre.H      # sampled token-heads as full-width tokens
+    return {"value": round(tokens_equiv / dt, 2), "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": "fp64 sequential oracle on %d of %d heads of every sequence (%d token-heads, "
+                      "%.1f s); value counts the sampled token-heads as %.0f full-width tokens"
+                      % (heads, pre.H, pre.T * heads, dt, tokens_equiv)}
+
+
+def run_reference(args):
+    """The CPU oracle, timed as it stands on the host cores, on the same
+    workload, metric and unit (bounded sample per step)."""
+    ws, rank, local = _dist()
+    if rank != 0:
+        return
+    import oracle
+    wl = args.workload
+    pre = ki.workload_prefill(wl) if wl != "varlen_64k" else ki.workload_varlen_with_decode(wl)[0]
+    heads = _sample_heads(pre, args)
+    oracle.build()
+    for _ in range(args.warmup):
+        _oracle_sample(pre, heads)
+    t = time.perf_counter()
+    threads = 1
+    for _ in range(args.steps):
+        _, threads, _ = _oracle_sample(pre, heads)
+    dt = (time.perf_counter() - t) / args.steps
+    tokens_equiv = pre.T * heads / pre.H
+    value = tokens_equiv / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl, "H": pre.H, "T": pre.T, "N": pre.N, "chunk": pre.chunk},
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": threads,
+                         "kind": "oracle",
+                         "sample": "%d of %d heads of every sequence per step" % (heads, pre.H)},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill_4k",
+                    choices=["prefill_4k", "prefill_32k_carry", "varlen_64k"])
+    ap.add_argument("--cpu-heads", type=int, default=0,
+                    help="heads per sequence in the oracle sample (default: ~4e5 token-heads)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("bench.py: warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

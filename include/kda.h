@@ -1,0 +1,131 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) KDA recurrence library, libkda_gb300.so.
+ *
+ * KDA (Kimi Delta Attention) keeps, per head, a dk x dv fp32 state S and for
+ * every token t applies the per-channel gated delta rule
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t                      (read out from the UPDATED state)
+ *
+ * Defined by: "Colibri Kimi K3 Metal backend" (architecture section, the
+ * state update; section 8.2, the two-pass token step and its readout;
+ * section 8.4, alpha = exp(g) per element and beta per head), with the model
+ * sizes of "Kimi K3 -> TPU v7x feasibility" (section 2 model table: 96 heads,
+ * head width 128, decay gate lower bound -5).
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers unless marked "host"; the caller owns all
+ *     memory.  The library allocates nothing and keeps no global state.
+ *   - Layouts are token-major and dense (C order):
+ *         q, k, g : [T, H, dk]      v, o : [T, H, dv]      beta : [T, H]
+ *         S       : [N, H, dk, dv]  with S[n][h][i][j], i = key channel,
+ *                                   j = value channel (the pages' S[i][j],
+ *                                   decayed per row i)
+ *   - q, k, v are bf16 (KDA_BF16) or fp32 (KDA_F32); g, beta, S and o are
+ *     always fp32.  g is the log-decay (decay = exp(g)); beta is already in
+ *     [0, 1] (any sigmoid is applied by the caller); q is used as given (any
+ *     1/sqrt(dk) scale is folded in by the caller).
+ *   - Supported sizes: dk = dv = 128.  Preconditions not checked at run time:
+ *     -5 <= g <= 0 (the model's gate bound; the chunked kernels' decay
+ *     folding relies on it), finite inputs.
+ *   - Every pointer must be 16-byte aligned (KDA_ERR_ALIGN otherwise).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream); they never synchronise.  Arguments are validated on
+ *     the host before any launch; on an argument error nothing is launched.
+ *     A launch failure is reported as KDA_ERR_CUDA.  Calls never throw.
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_NULL = 1,        /* a required pointer is NULL */
+    KDA_ERR_DIM = 2,         /* unsupported or inconsistent sizes */
+    KDA_ERR_CHUNK = 3,       /* chunk not in {16, 32, 64} */
+    KDA_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
+    KDA_ERR_DTYPE = 5,       /* dtype not a kda_dtype_t */
+    KDA_ERR_WORKSPACE = 6,   /* reserved: no call takes a workspace */
+    KDA_ERR_CUDA = 7         /* the CUDA runtime reported an error at launch */
+} kda_status_t;
+
+typedef enum {
+    KDA_BF16 = 0,            /* q, k, v stored as bfloat16 */
+    KDA_F32 = 1              /* q, k, v stored as float32 */
+} kda_dtype_t;
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int kda_version(void);
+
+/* Static string naming a status code (never NULL). */
+const char *kda_status_string(int status);
+
+/*
+ * Chunked prefill over a packed batch of N variable-length sequences.
+ *
+ * Operation: for every sequence n (tokens cu_seqlens[n] .. cu_seqlens[n+1]-1)
+ * and head h, run the recurrence above from S0[n][h] (zeros if S0 == NULL),
+ * write o for each token and the final state to S_out[n][h].  The chunked
+ * form (chunks of `chunk` tokens, UT transform inside a chunk, fp32 state
+ * carried between chunks) computes the same map up to rounding; it follows
+ * from unrolling the recurrence inside a chunk.  The varlen packing follows
+ * the per-sequence (cu_seqlens) convention of the TPU KDA kernel ("Kimi K3
+ * -> TPU v7x feasibility", section 4.2).  Sequences of any length (including
+ * 0, and lengths that are not a multiple of `chunk`) are handled in the
+ * kernel; an empty sequence copies S0 (or zeros) to S_out.
+ *
+ *   q, k       [T, H, dk]  bf16 or fp32 (dtype)
+ *   v          [T, H, dv]  bf16 or fp32
+ *   g          [T, H, dk]  fp32 log-decay
+ *   beta       [T, H]      fp32
+ *   S0         [N, H, dk, dv] fp32, or NULL for a zero initial state
+ *   o          [T, H, dv]  fp32, written
+ *   S_out      [N, H, dk, dv] fp32, written; may alias S0 exactly (in place)
+ *   cu_seqlens [N + 1]     int32 DEVICE array, cu_seqlens[0] = 0,
+ *                          non-decreasing, cu_seqlens[N] = T (not checked)
+ *   N          number of sequences (>= 1); T total tokens (>= 0, < 2^31)
+ *   H          heads (>= 1); dk, dv must be 128
+ *   chunk      16, 32 or 64 (the bf16 tensor-core path uses 64; other
+ *              values, and fp32 inputs, use the fp32 CUDA-core path)
+ *   dtype      kda_dtype_t of q, k, v
+ *   stream     cudaStream_t
+ * Returns KDA_OK or a kda_status_t.  With T == 0 only S_out is written.
+ */
+int kda_prefill_chunked(const void *q, const void *k, const void *v,
+                        const float *g, const float *beta, const float *S0,
+                        float *o, float *S_out, const int32_t *cu_seqlens,
+                        int N, int64_t T, int H, int dk, int dv, int chunk,
+                        int dtype, void *stream);
+
+/*
+ * One decode token for each of B sequences, state updated IN PLACE.
+ *
+ * Operation: the recurrence above applied once per (b, h) with
+ * S = S_inout[b][h]: decay the rows by exp(g), u = S^T k, w = beta (v - u),
+ * S += k w^T, o = S^T q (the two passes of "Colibri Kimi K3 Metal backend",
+ * section 8.2, fused into one kernel that reads and writes each state once).
+ *
+ *   q, k      [B, H, dk]  bf16 or fp32 (dtype)
+ *   v         [B, H, dv]  bf16 or fp32
+ *   g         [B, H, dk]  fp32 log-decay
+ *   beta      [B, H]      fp32
+ *   S_inout   [B, H, dk, dv] fp32, read and overwritten in place
+ *   o         [B, H, dv]  fp32, written (must not alias S_inout)
+ *   B, H      >= 1 (B = 0 is a no-op returning KDA_OK); dk, dv must be 128
+ * Returns KDA_OK or a kda_status_t.
+ */
+int kda_decode_step(const void *q, const void *k, const void *v,
+                    const float *g, const float *beta, float *S_inout, float *o,
+                    int B, int H, int dk, int dv, int dtype, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_H */

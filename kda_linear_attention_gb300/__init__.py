@@ -1,0 +1,164 @@
+"""KDA (Kimi Delta Attention) recurrence for NVIDIA GB300 (sm_103a).
+
+Thin Python binding of ``libkda_gb300.so`` (the C ABI in ``include/kda.h``):
+it checks and marshals torch tensors into pointers and sizes and calls the
+library on torch's current CUDA stream.  Every step of the computation runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback, and the
+calls raise if the library has not been built.
+
+    o, S_out = prefill_chunked(q, k, v, g, beta, cu_seqlens, S0=None, chunk=64)
+    o = decode_step(q, k, v, g, beta, S)          # S updated in place
+
+Shapes (token-major): q, k, g [T, H, 128]; v [T, H, 128]; beta [T, H];
+S [N, H, 128, 128] fp32; q/k/v bf16 or fp32, g/beta fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = ["prefill_chunked", "decode_step", "lib", "KDAError", "KDA_BF16", "KDA_F32",
+           "library_path"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libkda_gb300.so")
+_lib = None
+
+KDA_BF16 = 0
+KDA_F32 = 1
+DK = 128
+DV = 128
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s failed with status %d (%s)" % (what, status,
+                                                            lib().kda_status_string(status).decode()))
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                "libkda_gb300.so is not built (python -m kda_linear_attention_gb300.build); "
+                "this package has no CPU fallback")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        L.kda_version.argtypes = []
+        L.kda_version.restype = i32
+        L.kda_status_string.argtypes = [i32]
+        L.kda_status_string.restype = ctypes.c_char_p
+        L.kda_prefill_chunked.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                          i32, i64, i32, i32, i32, i32, i32, vp]
+        L.kda_prefill_chunked.restype = i32
+        L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+        L.kda_decode_step.restype = i32
+        _lib = L
+    return _lib
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _qkv_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError("q, k, v must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _check(name: str, t: torch.Tensor, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def _stream(device: torch.device, stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def prefill_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                    beta: torch.Tensor, cu_seqlens: torch.Tensor,
+                    S0: Optional[torch.Tensor] = None, chunk: int = 64,
+                    o: Optional[torch.Tensor] = None, S_out: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Chunked KDA prefill over packed varlen sequences (``kda_prefill_chunked``).
+
+    Returns (o [T, H, 128] fp32, S_out [N, H, 128, 128] fp32).  ``S_out`` may
+    be ``S0`` itself to update the states in place.
+    """
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    T, H = q.shape[0], q.shape[1]
+    N = cu_seqlens.numel() - 1
+    dt = _qkv_dtype(q)
+    _check("q", q, q.dtype, (T, H, DK), dev)
+    _check("k", k, q.dtype, (T, H, DK), dev)
+    _check("v", v, q.dtype, (T, H, DV), dev)
+    _check("g", g, torch.float32, (T, H, DK), dev)
+    _check("beta", beta, torch.float32, (T, H), dev)
+    _check("cu_seqlens", cu_seqlens, torch.int32, (N + 1,), dev)
+    if S0 is not None:
+        _check("S0", S0, torch.float32, (N, H, DK, DV), dev)
+    if o is None:
+        o = torch.empty((T, H, DV), dtype=torch.float32, device=dev)
+    if S_out is None:
+        S_out = torch.empty((N, H, DK, DV), dtype=torch.float32, device=dev)
+    _check("o", o, torch.float32, (T, H, DV), dev)
+    _check("S_out", S_out, torch.float32, (N, H, DK, DV), dev)
+    rc = lib().kda_prefill_chunked(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(o), _p(S_out),
+                                   _p(cu_seqlens), N, T, H, DK, DV, int(chunk), dt,
+                                   _stream(dev, stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_prefill_chunked")
+    return o, S_out
+
+
+def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                beta: torch.Tensor, S: torch.Tensor, o: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """One decode token per sequence (``kda_decode_step``); ``S`` is updated in place.
+
+    q, k, g [B, H, 128]; v [B, H, 128]; beta [B, H]; S [B, H, 128, 128] fp32.
+    Returns o [B, H, 128] fp32.
+    """
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, H = q.shape[0], q.shape[1]
+    dt = _qkv_dtype(q)
+    _check("q", q, q.dtype, (B, H, DK), dev)
+    _check("k", k, q.dtype, (B, H, DK), dev)
+    _check("v", v, q.dtype, (B, H, DV), dev)
+    _check("g", g, torch.float32, (B, H, DK), dev)
+    _check("beta", beta, torch.float32, (B, H), dev)
+    _check("S", S, torch.float32, (B, H, DK, DV), dev)
+    if o is None:
+        o = torch.empty((B, H, DV), dtype=torch.float32, device=dev)
+    _check("o", o, torch.float32, (B, H, DV), dev)
+    rc = lib().kda_decode_step(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S), _p(o), B, H, DK, DV,
+                               dt, _stream(dev, stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_decode_step")
+    return o

@@ -1,0 +1,140 @@
+// Fused KDA decode step: one token per sequence, state updated in place.
+//
+// Per (b, h) the token step of "Colibri Kimi K3 Metal backend", section 8.2,
+// done in one pass over the state:
+//   a_i = exp(g_i);  S'_ij = a_i S_ij                        (row decay)
+//   u_j = sum_i k_i S'_ij;  w_j = beta (v_j - u_j)           (prediction, delta)
+//   S_ij <- S'_ij + k_i w_j                                  (rank-1 update)
+//   o_j = sum_i q_i S_ij = sum_i q_i S'_ij + (q.k) w_j       (readout, updated S)
+// The last identity lets both column reductions run on the decayed state
+// while it is still in registers, so each 64 KiB state is read once and
+// written once: the kernel is bound by HBM bandwidth.
+//
+// Work split: a block owns COLS value-columns of one (b, h) state (columns
+// evolve independently).  Thread t holds float4 column group t % (COLS/4) for
+// rows rg, rg + NRG, ... (rg = t / (COLS/4)), so each warp load covers whole
+// 128-bit-coalesced row segments.  Column sums are reduced across row groups
+// through shared memory.
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kDecodeThreads = 256;
+
+template <typename TIn, int COLS>
+__global__ void __launch_bounds__(kDecodeThreads, (COLS == 128 ? 2 : 4))
+decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
+              const float *__restrict__ g, const float *__restrict__ beta,
+              float *__restrict__ S, float *__restrict__ o) {
+    constexpr int C4 = COLS / 4;                 // float4 column groups per block
+    constexpr int NRG = kDecodeThreads / C4;     // row groups
+    constexpr int RPT = kDK / NRG;               // rows per thread
+    constexpr int NSPLIT = kDV / COLS;           // blocks per state
+
+    const int unit = blockIdx.x / NSPLIT;        // b * H + h
+    const int cs = blockIdx.x % NSPLIT;
+    const int t = threadIdx.x;
+    const int c4 = t % C4;
+    const int rg = t / C4;
+    const int col0 = cs * COLS + c4 * 4;
+
+    float *Su = S + (size_t)unit * kDK * kDV;
+
+    // Issue the state loads first; they are independent of everything else.
+    float4 s[RPT];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r)
+        s[r] = __ldcs(reinterpret_cast<const float4 *>(Su + (size_t)(rg + r * NRG) * kDV + col0));
+
+    __shared__ float sq[kDK], sk[kDK], sa[kDK];
+    __shared__ float4 red_k[NRG][C4];
+    __shared__ float4 red_q[NRG][C4];
+    __shared__ float s_qk[kDK / 32];
+
+    if (t < kDK) {
+        const float qi = load_in(q, (size_t)unit * kDK + t);
+        const float ki = load_in(k, (size_t)unit * kDK + t);
+        sq[t] = qi;
+        sk[t] = ki;
+        sa[t] = expf(g[(size_t)unit * kDK + t]);
+        float p = qi * ki;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+        if ((t & 31) == 0) s_qk[t >> 5] = p;
+    }
+    __syncthreads();
+
+    float4 uk = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 uq = uk;
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        const int i = rg + r * NRG;
+        const float a = sa[i], ki = sk[i], qi = sq[i];
+        s[r].x *= a; s[r].y *= a; s[r].z *= a; s[r].w *= a;
+        uk.x += ki * s[r].x; uk.y += ki * s[r].y; uk.z += ki * s[r].z; uk.w += ki * s[r].w;
+        uq.x += qi * s[r].x; uq.y += qi * s[r].y; uq.z += qi * s[r].z; uq.w += qi * s[r].w;
+    }
+    red_k[rg][c4] = uk;
+    red_q[rg][c4] = uq;
+    __syncthreads();
+
+    float4 Uk = red_k[0][c4], Uq = red_q[0][c4];
+#pragma unroll
+    for (int j = 1; j < NRG; ++j) {
+        const float4 a = red_k[j][c4], b = red_q[j][c4];
+        Uk.x += a.x; Uk.y += a.y; Uk.z += a.z; Uk.w += a.w;
+        Uq.x += b.x; Uq.y += b.y; Uq.z += b.z; Uq.w += b.w;
+    }
+    float qk = 0.f;
+#pragma unroll
+    for (int j = 0; j < kDK / 32; ++j) qk += s_qk[j];
+
+    const float bt = beta[unit];
+    const size_t vo = (size_t)unit * kDV + col0;
+    float4 w;
+    w.x = bt * (load_in(v, vo + 0) - Uk.x);
+    w.y = bt * (load_in(v, vo + 1) - Uk.y);
+    w.z = bt * (load_in(v, vo + 2) - Uk.z);
+    w.w = bt * (load_in(v, vo + 3) - Uk.w);
+
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        const int i = rg + r * NRG;
+        const float ki = sk[i];
+        s[r].x += ki * w.x; s[r].y += ki * w.y; s[r].z += ki * w.z; s[r].w += ki * w.w;
+        __stcs(reinterpret_cast<float4 *>(Su + (size_t)i * kDV + col0), s[r]);
+    }
+    if (rg == 0) {
+        float4 ov;
+        ov.x = Uq.x + qk * w.x; ov.y = Uq.y + qk * w.y;
+        ov.z = Uq.z + qk * w.z; ov.w = Uq.w + qk * w.w;
+        *reinterpret_cast<float4 *>(o + vo) = ov;
+    }
+}
+
+template <typename TIn>
+cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *g,
+                         const float *beta, float *S, float *o, int B, int H,
+                         cudaStream_t stream) {
+    // Two blocks per state (64 columns each): twice the blocks of a
+    // whole-state split, a shorter tail and fewer registers per thread.
+    constexpr int COLS = 64;
+    const long long units = (long long)B * H;
+    const long long blocks = units * (kDV / COLS);
+    decode_kernel<TIn, COLS><<<(unsigned)blocks, kDecodeThreads, 0, stream>>>(
+        static_cast<const TIn *>(q), static_cast<const TIn *>(k), static_cast<const TIn *>(v),
+        g, beta, S, o);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, float *S, float *o, int B, int H, bool bf16,
+                          cudaStream_t stream) {
+    if (bf16) return launch_typed<__nv_bfloat16>(q, k, v, g, beta, S, o, B, H, stream);
+    return launch_typed<float>(q, k, v, g, beta, S, o, B, H, stream);
+}
+
+}  // namespace kda

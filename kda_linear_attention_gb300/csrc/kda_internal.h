@@ -1,0 +1,56 @@
+// Internal launcher interface of libkda_gb300 (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int kDK = 128;
+constexpr int kDV = 128;
+
+// Fused decode step (kda_decode.cu).  Returns the launch error.
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, float *S, float *o, int B, int H, bool bf16,
+                          cudaStream_t stream);
+
+// fp32 CUDA-core chunked prefill (kda_prefill_simt.cu): any chunk in {16,32,64},
+// bf16 or fp32 inputs.
+cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, const float *S0, float *o, float *S_out,
+                                const int32_t *cu_seqlens, int N, int H, int chunk, bool bf16,
+                                cudaStream_t stream);
+
+// Input loads: bf16 or fp32 element -> fp32.
+__device__ __forceinline__ float load_in(const __nv_bfloat16 *p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ float load_in(const float *p, size_t i) { return p[i]; }
+
+// Longest-first placement of sequences onto blocks: the block whose sequence
+// rank is `rank` processes the sequence with the rank-th largest length (ties
+// by index), so the hardware block scheduler starts the longest sequences
+// first.  For N above `kLptMaxN` the identity order is used.  Must be called
+// by all threads of the block; `s_out` is a __shared__ int.
+constexpr int kLptMaxN = 256;
+__device__ __forceinline__ int lpt_sequence(const int32_t *cu, int N, int rank, int *s_out) {
+    if (N > kLptMaxN) return rank;
+    if (threadIdx.x == 0) *s_out = rank;   // fallback, overwritten below
+    __syncthreads();
+    for (int i = threadIdx.x; i < N; i += blockDim.x) {
+        const int li = cu[i + 1] - cu[i];
+        int r = 0;
+        for (int j = 0; j < N; ++j) {
+            const int lj = cu[j + 1] - cu[j];
+            r += (lj > li) || (lj == li && j < i);
+        }
+        if (r == rank) *s_out = i;
+    }
+    __syncthreads();
+    const int n = *s_out;
+    __syncthreads();
+    return n;
+}
+
+}  // namespace kda

@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+function include/kda.h declares, and rejects bad arguments before launching
+anything.  Fake, never-dereferenced pointer values are used: validation must
+return before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from kda_linear_attention_gb300 import build
+    build.build()
+    import kda_linear_attention_gb300 as kda
+    return kda.lib()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(HEADER_DIR):
+        if not fn.endswith(".h"):
+            continue
+        src = open(os.path.join(HEADER_DIR, fn)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        for m in re.finditer(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\(", src):
+            name = m.group(1)
+            if name.startswith("kda_"):
+                names.add(name)
+    return names
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert {"kda_prefill_chunked", "kda_decode_step", "kda_version",
+            "kda_status_string"} <= names
+    for n in names:
+        assert hasattr(L, n), "libkda_gb300.so does not export %s" % n
+
+
+def test_version_and_status_strings(L):
+    assert L.kda_version() >= 100
+    for s in range(0, 8):
+        assert len(L.kda_status_string(s)) > 0
+    assert L.kda_status_string(12345) == b"unknown status"
+
+
+GOOD = ctypes.c_void_p(0x10000)   # aligned, never dereferenced
+
+
+def _prefill(L, **kw):
+    a = dict(q=GOOD, k=GOOD, v=GOOD, g=GOOD, beta=GOOD, S0=None, o=GOOD, S_out=GOOD, cu=GOOD,
+             N=1, T=64, H=2, dk=128, dv=128, chunk=64, dtype=0, stream=None)
+    a.update(kw)
+    return L.kda_prefill_chunked(a["q"], a["k"], a["v"], a["g"], a["beta"], a["S0"], a["o"],
+                                 a["S_out"], a["cu"], a["N"], a["T"], a["H"], a["dk"], a["dv"],
+                                 a["chunk"], a["dtype"], a["stream"])
+
+
+def _decode(L, **kw):
+    a = dict(q=GOOD, k=GOOD, v=GOOD, g=GOOD, beta=GOOD, S=GOOD, o=GOOD, B=4, H=2, dk=128, dv=128,
+             dtype=0, stream=None)
+    a.update(kw)
+    return L.kda_decode_step(a["q"], a["k"], a["v"], a["g"], a["beta"], a["S"], a["o"], a["B"],
+                             a["H"], a["dk"], a["dv"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=7), 5),
+    (dict(dk=64), 2), (dict(dv=256), 2), (dict(N=0), 2), (dict(H=0), 2), (dict(T=-1), 2),
+    (dict(T=1 << 31), 2),
+    (dict(chunk=48), 3), (dict(chunk=128), 3), (dict(chunk=0), 3),
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(g=None), 1),
+    (dict(beta=None), 1), (dict(o=None), 1), (dict(S_out=None), 1), (dict(cu=None), 1),
+    (dict(q=ctypes.c_void_p(0x10004)), 4), (dict(S0=ctypes.c_void_p(0x10008)), 4),
+    (dict(cu=ctypes.c_void_p(0x10002)), 4), (dict(o=ctypes.c_void_p(0x1000c)), 4),
+])
+def test_prefill_rejects_bad_arguments(L, kw, status):
+    assert _prefill(L, **kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=-1), 5), (dict(dk=127), 2), (dict(H=0), 2), (dict(B=-3), 2),
+    (dict(q=None), 1), (dict(S=None), 1), (dict(o=None), 1), (dict(beta=None), 1),
+    (dict(S=ctypes.c_void_p(0x10004)), 4), (dict(v=ctypes.c_void_p(0x10001)), 4),
+])
+def test_decode_rejects_bad_arguments(L, kw, status):
+    assert _decode(L, **kw) == status
+
+
+def test_decode_batch_zero_is_noop(L):
+    # B = 0 returns before touching any pointer or the GPU
+    assert _decode(L, B=0, q=None, S=None) == 0
+
+
+def test_binding_fails_loudly_without_cuda_tensors():
+    torch = pytest.importorskip("torch")
+    import kda_linear_attention_gb300 as kda
+    x = torch.zeros(4, 2, 128)
+    with pytest.raises(ValueError):
+        kda.decode_step(x, x, x, x, torch.zeros(4, 2), torch.zeros(4, 2, 128, 128))

@@ -1,0 +1,201 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle on
+the same seeded inputs.  Small cases are compared element by element over
+every output; the full-size workloads are compared on sampled (sequence,
+head) units that the oracle computes one by one, plus properties that hold
+at any size."""
+import numpy as np
+import pytest
+
+import kda_inputs as ki
+import oracle
+from kda_testlib import (TOL_BF16, TOL_F32, assert_close, decode_on_gpu, dev_tensor,
+                         prefill_on_gpu, rel_err)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from kda_linear_attention_gb300 import build
+    build.build()
+    yield
+
+
+def _tol(dtype):
+    return TOL_F32 if dtype == "f32" else TOL_BF16
+
+
+# ---------------------------------------------------------------- decode
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("B,H", [(1, 1), (3, 5), (7, 96)])
+def test_decode_small(dtype, B, H):
+    rng = np.random.Generator(np.random.PCG64(1000 + B * H))
+    S = ki.gen_decode_state(rng, B, H)
+    step = ki.gen_decode_step(rng, B, H, dtype)
+    o_ref, S_ref = oracle.decode(S, step)
+    Sd = dev_tensor(S)
+    o = decode_on_gpu(Sd, step)
+    assert_close(o, o_ref, _tol(dtype), "decode o")
+    assert_close(Sd.cpu().numpy(), S_ref, _tol(dtype), "decode S")
+
+
+def test_decode_b64_100_steps_sampled():
+    """Batched decode, B=64, H=96, 100 consecutive in-place steps; 24 sampled
+    (b, h) states are followed by the oracle in fp64 along the whole run."""
+    w = ki.WORKLOADS["decode_b64"]
+    S, steps = ki.workload_decode("decode_b64")
+    r = np.random.Generator(np.random.PCG64(77))
+    units = sorted({(int(b), int(h)) for b, h in zip(r.integers(0, w["B"], 24),
+                                                      r.integers(0, w["H"], 24))})
+    units += [(0, 0), (w["B"] - 1, w["H"] - 1)]
+    S_ref = {u: S[u].astype(np.float64) for u in units}
+    Sd = dev_tensor(S)
+    worst = 0.0
+    for it, step in enumerate(steps):
+        o = decode_on_gpu(Sd, step)
+        o_ref = np.stack([oracle.run_unit(step.q, step.k, step.v, step.g, step.beta, S_ref[u],
+                                          u[0], u[0] + 1, u[1]) for u in units], 0)
+        for i, u in enumerate(units):
+            S_ref[u] = o_ref[i][1]
+        got = np.stack([o[u] for u in units])
+        worst = max(worst, assert_close(got, np.stack([x[0][0] for x in o_ref]), TOL_BF16,
+                                        "decode o at step %d" % it))
+    S_fin = Sd.cpu().numpy()
+    assert_close(np.stack([S_fin[u] for u in units]), np.stack([S_ref[u] for u in units]),
+                 TOL_BF16, "decode S after 100 steps")
+    assert np.isfinite(S_fin).all()
+
+
+# ---------------------------------------------------------------- prefill, small
+def test_prefill_tiny_fp32_full():
+    """All-fp32 prefill: B=1, H=2, T=64, chunk 16 (element by element, 1e-5)."""
+    inp = ki.workload_prefill("tiny_fp32")
+    o_ref, S_ref = oracle.prefill(inp)
+    o, S = prefill_on_gpu(inp)
+    assert_close(o, o_ref, TOL_F32, "o")
+    assert_close(S, S_ref, TOL_F32, "S_out")
+
+
+RAGGED = [1, 63, 64, 65, 130, 0, 200, 17, 16, 33]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+@pytest.mark.parametrize("with_s0", [False, True])
+def test_prefill_ragged_varlen(dtype, chunk, with_s0):
+    inp = ki.gen_prefill(300 + chunk, RAGGED, H=3, dtype=dtype, chunk=chunk, with_s0=with_s0)
+    o_ref, S_ref = oracle.prefill(inp)
+    o, S = prefill_on_gpu(inp)
+    cu = inp.cu_seqlens
+    tol = _tol(dtype)
+    for n in range(inp.N):
+        if cu[n + 1] > cu[n]:
+            assert_close(o[cu[n]:cu[n + 1]], o_ref[cu[n]:cu[n + 1]], tol, "o seq %d" % n)
+        if with_s0 or cu[n + 1] > cu[n]:
+            assert_close(S[n], S_ref[n], tol, "S_out seq %d" % n)
+        else:
+            assert np.all(S[n] == 0)
+
+
+def test_prefill_empty_batch_copies_state():
+    inp = ki.gen_prefill(5, [0, 0], H=2, dtype="bf16", chunk=64, with_s0=True)
+    o, S = prefill_on_gpu(inp)
+    assert o.shape == (0, 2, 128)
+    np.testing.assert_array_equal(S, inp.S0)
+
+
+def test_prefill_in_place_state():
+    import torch
+    import kda_linear_attention_gb300 as kda
+    inp = ki.gen_prefill(6, [70, 5], H=4, dtype="bf16", chunk=64, with_s0=True)
+    o_ref, S_ref = oracle.prefill(inp)
+    d = {n: dev_tensor(getattr(inp, n)) for n in ("q", "k", "v", "g", "beta")}
+    S = dev_tensor(inp.S0)
+    o, S2 = kda.prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                dev_tensor(inp.cu_seqlens), S0=S, S_out=S, chunk=64)
+    torch.cuda.synchronize()
+    assert S2.data_ptr() == S.data_ptr()
+    assert_close(o.cpu().numpy(), o_ref, TOL_BF16, "o")
+    assert_close(S.cpu().numpy(), S_ref, TOL_BF16, "S in place")
+
+
+def test_prefill_split_calls_and_decode_continuation():
+    """prefill(T1) then prefill(T2, S0=S_out) == prefill(T1+T2); and
+    prefill(T) then one decode step == prefill(T+1), all on the GPU."""
+    import torch
+    import kda_linear_attention_gb300 as kda
+    T1, T2, H = 100, 77, 4
+    full = ki.gen_prefill(8, [T1 + T2], H=H, dtype="bf16", chunk=64, with_s0=True)
+    o_all, S_all = prefill_on_gpu(full)
+
+    def part(a, b):
+        return ki.PrefillInputs(*(np.ascontiguousarray(x[a:b]) for x in
+                                  (full.q, full.k, full.v, full.g, full.beta)),
+                                None, np.array([0, b - a], dtype=np.int32), "bf16", 64)
+
+    p1, p2 = part(0, T1), part(T1, T1 + T2)
+    p1.S0 = full.S0
+    o1, S1 = prefill_on_gpu(p1)
+    o2, S2 = prefill_on_gpu(p2, S0=dev_tensor(S1))
+    assert rel_err(np.concatenate([o1, o2]), o_all) < 1e-4
+    assert rel_err(S2, S_all) < 1e-4
+    # prefill(T-1) + decode of token T-1
+    pa = part(0, T1 + T2 - 1)
+    pa.S0 = full.S0
+    _, Sa = prefill_on_gpu(pa)
+    Sd = dev_tensor(Sa)
+    step = ki.DecodeStep(*(np.ascontiguousarray(x[-1:]) for x in
+                           (full.q, full.k, full.v, full.g, full.beta)), "bf16")
+    od = decode_on_gpu(Sd, step)
+    assert rel_err(od[0], o_all[-1]) < 1e-4
+    assert rel_err(Sd.cpu().numpy()[0], S_all[0]) < 1e-4
+
+
+# ---------------------------------------------------------------- full-size workloads
+def test_prefill_4k_full():
+    """bf16 prefill, H=96, T=4096, chunk 64, S0 = 0: every output against the oracle."""
+    inp = ki.workload_prefill("prefill_4k")
+    o, S = prefill_on_gpu(inp)
+    o_ref, S_ref = oracle.prefill(inp)
+    assert_close(o, o_ref, TOL_BF16, "o")
+    assert_close(S, S_ref, TOL_BF16, "S_out")
+
+
+def test_prefill_32k_carry_sampled():
+    """bf16 prefill, H=96, T=32768, S0 ~ N(0, 0.02^2): sampled heads vs the oracle."""
+    inp = ki.workload_prefill("prefill_32k_carry")
+    o, S = prefill_on_gpu(inp)
+    assert np.isfinite(o).all() and np.isfinite(S).all()
+    heads = [0, 37, 95]
+    ref = oracle.prefill(inp, units=[(0, h) for h in heads])
+    for h in heads:
+        o_r, S_r = ref[(0, h)]
+        assert_close(o[:, h], o_r, TOL_BF16, "o head %d" % h)
+        assert_close(S[0, h], S_r, TOL_BF16, "S_out head %d" % h)
+
+
+def test_varlen_64k_then_decode_sampled():
+    """Varlen packed prefill (8 sequences, 65536 tokens) with per-sequence S0,
+    then one decode step for all 8 from the prefill's final states."""
+    import torch
+    pre, step = ki.workload_varlen_with_decode("varlen_64k")
+    o, S = prefill_on_gpu(pre)
+    assert np.isfinite(o).all() and np.isfinite(S).all()
+    units = [(7, 0), (7, 95), (5, 12), (0, 3), (3, 50), (6, 64)]
+    ref = oracle.prefill(pre, units=units)
+    cu = pre.cu_seqlens
+    for (n, h) in units:
+        o_r, S_r = ref[(n, h)]
+        assert_close(o[cu[n]:cu[n + 1], h], o_r, TOL_BF16, "o seq %d head %d" % (n, h))
+        assert_close(S[n, h], S_r, TOL_BF16, "S_out seq %d head %d" % (n, h))
+    Sd = dev_tensor(S)
+    od = decode_on_gpu(Sd, step)
+    Sd_np = Sd.cpu().numpy()
+    for (n, h) in units:
+        o_r, S_r = oracle.run_unit(step.q, step.k, step.v, step.g, step.beta, ref[(n, h)][1],
+                                   n, n + 1, h)
+        assert_close(od[n, h], o_r[0], TOL_BF16, "decode o seq %d head %d" % (n, h))
+        assert_close(Sd_np[n, h], S_r, TOL_BF16, "decode S seq %d head %d" % (n, h))
