@@ -91,8 +91,9 @@ const char *kda_status_string(int status);
  *                          non-decreasing, cu_seqlens[N] = T (not checked)
  *   N          number of sequences (>= 1); T total tokens (>= 0, < 2^31)
  *   H          heads (>= 1); dk, dv must be 128
- *   chunk      16, 32 or 64 (the bf16 tensor-core path uses 64; other
- *              values, and fp32 inputs, use the fp32 CUDA-core path)
+ *   chunk      16, 32 or 64.  bf16 inputs with chunk 64 run on the
+ *              tensor cores (tcgen05, TMA); every other combination runs
+ *              the fp32 CUDA-core kernel.
  *   dtype      kda_dtype_t of q, k, v
  *   stream     cudaStream_t
  * Returns KDA_OK or a kda_status_t.  With T == 0 only S_out is written.
@@ -123,6 +124,19 @@ int kda_prefill_chunked(const void *q, const void *k, const void *v,
 int kda_decode_step(const void *q, const void *k, const void *v,
                     const float *g, const float *beta, float *S_inout, float *o,
                     int B, int H, int dk, int dv, int dtype, void *stream);
+
+/*
+ * Device-side error word of the library.  The tensor-core prefill kernel
+ * never waits without bound: if one of its waits on an asynchronous copy or
+ * on the tensor cores runs past its iteration limit it sets a bit here,
+ * releases its tensor memory and exits (its outputs are then invalid).
+ *
+ *   code   host pointer, receives the word (0 = no error since the last reset)
+ *   reset  nonzero: clear the word after reading it
+ * Synchronous with respect to the device (a cudaMemcpyFromSymbol).  Returns
+ * KDA_OK, KDA_ERR_NULL or KDA_ERR_CUDA.
+ */
+int kda_device_error(unsigned int *code, int reset);
 
 #ifdef __cplusplus
 }

@@ -20,8 +20,8 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["prefill_chunked", "decode_step", "lib", "KDAError", "KDA_BF16", "KDA_F32",
-           "library_path"]
+__all__ = ["prefill_chunked", "decode_step", "device_error", "lib", "KDAError", "KDA_BF16",
+           "KDA_F32", "library_path"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libkda_gb300.so")
@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
         L.kda_prefill_chunked.restype = i32
         L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
         L.kda_decode_step.restype = i32
+        L.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
+        L.kda_device_error.restype = i32
         _lib = L
     return _lib
 
@@ -162,3 +164,13 @@ def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
     if rc != 0:
         raise KDAError(rc, "kda_decode_step")
     return o
+
+
+def device_error(reset: bool = True) -> int:
+    """The library's device-side error word (``kda_device_error``); nonzero if
+    a bounded wait inside a kernel gave up since the last reset."""
+    code = ctypes.c_uint(0)
+    rc = lib().kda_device_error(ctypes.byref(code), int(reset))
+    if rc != 0:
+        raise KDAError(rc, "kda_device_error")
+    return int(code.value)

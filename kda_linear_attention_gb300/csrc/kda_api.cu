@@ -48,6 +48,9 @@ int kda_prefill_chunked(const void *q, const void *k, const void *v, const float
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_ALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == KDA_BF16 && chunk == 64 && T > 0)
+        return cuda_status(kda::launch_prefill_tc(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, T,
+                                                  H, s));
     return cuda_status(kda::launch_prefill_simt(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, H,
                                                 chunk, dtype == KDA_BF16, s));
 }
@@ -65,6 +68,11 @@ int kda_decode_step(const void *q, const void *k, const void *v, const float *g,
         if (!aligned16(p)) return KDA_ERR_ALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return cuda_status(kda::launch_decode(q, k, v, g, beta, S_inout, o, B, H, dtype == KDA_BF16, s));
+}
+
+int kda_device_error(unsigned int *code, int reset) {
+    if (!code) return KDA_ERR_NULL;
+    return cuda_status(kda::read_device_error(code, reset != 0));
 }
 
 }  // extern "C"

@@ -22,6 +22,16 @@ cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, con
                                 const int32_t *cu_seqlens, int N, int H, int chunk, bool bf16,
                                 cudaStream_t stream);
 
+// Tensor-core chunked prefill (kda_prefill_tc.cu): bf16 q/k/v, chunk 64, T >= 1.
+cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, const float *S0, float *o, float *S_out,
+                              const int32_t *cu_seqlens, int N, int64_t T, int H,
+                              cudaStream_t stream);
+
+// Reads (and optionally clears) the device-side error word that the
+// tensor-core kernel sets when a bounded wait gives up.
+cudaError_t read_device_error(unsigned int *code, bool reset);
+
 // Input loads: bf16 or fp32 element -> fp32.
 __device__ __forceinline__ float load_in(const __nv_bfloat16 *p, size_t i) {
     return __bfloat162float(p[i]);

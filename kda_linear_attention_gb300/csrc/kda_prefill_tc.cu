@@ -1,0 +1,790 @@
+// Chunked KDA prefill on the 5th-generation tensor cores (tcgen05 + TMEM,
+// operands staged by TMA), bf16 q/k/v, chunk 64, fp32 state.
+//
+// Math (the recurrence of "Colibri Kimi K3 Metal backend", architecture
+// section, unrolled over a chunk of L <= 64 tokens; b_r = sum_{t<=r} g_t):
+//   G^qk_rs = sum_c q_rc k_sc e^{b_rc - b_sc} (s <= r),  G^kk likewise (s < r)
+//   T  = (I + Diag(beta) G^kk)^-1 (unit lower triangular),  T' = (T - I) Diag(beta)
+//   W  = T' K0 + Diag(beta) K0,        K0_r = e^{b_r} k_r
+//   U~ = T' V  + Diag(beta) V
+//   U  = U~ - W S
+//   O  = Q0 S + A' U + Diag(q_r.k_r) U, Q0_r = e^{b_r} q_r, A' = strictly lower G^qk
+//   S <- Diag(e^{b_L}) S + Kbar^T U,    Kbar_s = e^{b_L - b_s} k_s
+// The diagonal terms (beta_r v_r, beta_r K0_r, (q_r.k_r) u_r) are added in
+// fp32 outside the MMAs so that the dominant per-token terms are never
+// rounded to a 16-bit operand.
+//
+// Decay folding for the gated Gram matrices: with 16-row sub-blocks p and
+// sigma_p = b at the last row of p, a row r in p and key s <= end(p) give
+//   e^{b_r - b_s} = e^{b_r - sigma_p} * e^{sigma_p - b_s},
+// where the first factor lies in [1, e^{75}] and the second in (0, 1] when
+// g >= -5 (the model's gate bound); the query side uses one operand
+// X = [q_r e^{b_r - sigma_p(r)} ; k_r e^{b_r - sigma_p(r)}] (128 rows) and
+// the key side a stack of four operands Khat^(p)_s = k_s e^{sigma_p - b_s}
+// (16(p+1) rows each, 160 in all): one M=128, N=160 MMA gives both Gram
+// matrices, row r reading the column block of its own sub-block.
+//
+// Precision: MMAs that carry state-side terms (W S, Q0 S, the Gram and UT
+// products) use kind::f16 with bf16 operands; MMAs that carry the fresh
+// per-token terms (A' U and Kbar^T U) use kind::tf32 with operands rounded to
+// nearest in software.  Accumulation is fp32 in TMEM; the state is kept in
+// fp32 in TMEM for the whole sequence.
+//
+// One CTA (256 threads) per (sequence, head), walking its chunks in order;
+// the MMAs are transposed so that M = 128 is always dk or dv:
+//   D_G[128 x 160] = X . Khat^T             D_W[i][r]  = (T' K0)^T
+//   D_U[j][r]      = (T' V)^T - (W S)^T     D_O[j][r]  = (Q0 S)^T + (A' U)^T
+//   D_S[j][i]     += (Kbar^T U)^T            (S^T kept in TMEM, lane j, column i)
+#include <cudaTypedefs.h>
+
+#include "kda_internal.h"
+#include "tc_ptx.cuh"
+
+namespace kda {
+
+// Nonzero when a bounded wait inside the tensor-core kernel gave up.
+__device__ unsigned int g_kda_device_error = 0;
+
+namespace {
+using namespace tc;
+
+constexpr int C = 64;
+constexpr int NT = 256;
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+// shared memory map (bytes from a 1024-aligned base).  "sw" = 128-byte
+// swizzled canonical layout, "il" = interleaved (no swizzle) canonical layout.
+constexpr uint32_t SM_STG_Q = 0;          // q chunk: 2 x [64 r][64 c] sw (TMA)
+constexpr uint32_t SM_STG_K = 16384;      // k chunk: same
+constexpr uint32_t SM_STG_V = 32768;      // v chunk: same = V^T, MN-major operand
+constexpr uint32_t SM_X = 49152;          // 32 KB: Gram A [128][128] K-major sw | M fp32 [64][68] + solve temps | U^T tf32 K-major il
+constexpr uint32_t SM_KH = 81920;         // 40 KB: Gram B Khat [160][128] K-major sw | A' (16K) + -W^T (16K) + T' (8K)
+constexpr uint32_t SM_A = SM_KH;          //   A' tf32 K-major il [r][s], 16 KB
+constexpr uint32_t SM_W = SM_KH + 16384;  //   -W^T bf16 MN-major il [i][r], 16 KB
+constexpr uint32_t SM_T = SM_KH + 32768;  //   T' bf16 K-major il [r][s], 8 KB
+constexpr uint32_t SM_Q0 = 122880;        // 16 KB: Q0 [64][128] K-major sw
+constexpr uint32_t SM_K0 = 139264;        // 16 KB: K0 [64 s][128 i] MN-major sw (A of the W product)
+constexpr uint32_t SM_KB = 155648;        // 32 KB: Kbar^T [128 i][64 s] tf32 K-major il (B of the dS product)
+constexpr uint32_t SM_S = 188416;         // 32 KB: S^T bf16 K-major il [j][i]
+constexpr uint32_t SM_MISC = 221184;
+constexpr uint32_t MISC_BETA = 0;         // float[64]
+constexpr uint32_t MISC_GAM = 256;        // float[128]  e^{b_L}
+constexpr uint32_t MISC_DQ = 768;         // float[64]   q_r . k_r
+constexpr uint32_t MISC_DQP = 1024;       // float[8][64] partial dot products
+constexpr uint32_t MISC_BAR = 3072;       // 3 x u64 mbarriers
+constexpr uint32_t MISC_TMEM = 3104;      // u32 TMEM base
+constexpr uint32_t SMEM_USED = SM_MISC + 3120;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;   // alignment slack
+constexpr int MLD = 68;                   // row stride (floats) of M / T
+
+// TMEM columns (512 allocated)
+constexpr uint32_t TM_S = 0;      // S^T master fp32 (lane j, column i), 128 cols
+constexpr uint32_t TM_DS = 128;   // (Kbar^T U)^T, 128 cols
+constexpr uint32_t TM_G = 256;    // Gram D, 160 cols
+constexpr uint32_t TM_W = 256;    // W D, 64 cols (after the Gram epilogue)
+constexpr uint32_t TM_U = 320;    // U D, 64 cols (after the Gram epilogue)
+constexpr uint32_t TM_O = 448;    // O D, 64 cols
+
+// ---- canonical operand layouts --------------------------------------------
+// interleaved K-major bf16: element (m, k)
+__device__ __forceinline__ uint32_t km_bf16(int m, int k, uint32_t sbo) {
+    return (uint32_t)(m >> 3) * sbo + (uint32_t)(k >> 3) * 128u + (uint32_t)(m & 7) * 16u +
+           (uint32_t)(k & 7) * 2u;
+}
+// interleaved K-major tf32: element (m, k)
+__device__ __forceinline__ uint32_t km_tf32(int m, int k, uint32_t sbo) {
+    return (uint32_t)(m >> 3) * sbo + (uint32_t)(k >> 2) * 128u + (uint32_t)(m & 7) * 16u +
+           (uint32_t)(k & 3) * 4u;
+}
+// interleaved MN-major bf16: element (k, mn)
+__device__ __forceinline__ uint32_t mn_bf16(int k, int mn, uint32_t lbo) {
+    return (uint32_t)(mn & 7) * 2u + (uint32_t)(mn >> 3) * 128u + (uint32_t)(k & 7) * 16u +
+           (uint32_t)(k >> 3) * lbo;
+}
+// 128B-swizzled tile with 128-byte rows: 16-byte chunk `c` (0..15 across two
+// 64-element halves, bf16) of row `row`; `half_bytes` = rows * 128.
+__device__ __forceinline__ uint32_t sw_chunk(int row, int c, uint32_t half_bytes) {
+    return (uint32_t)(c >> 3) * half_bytes + (uint32_t)row * 128u +
+           ((uint32_t)((c & 7) ^ (row & 7)) << 4);
+}
+// element (row, col) of a bf16 sw tile with two 64-column halves of 64 rows
+__device__ __forceinline__ uint32_t sw_elem64(int row, int col) {
+    return sw_chunk(row, col >> 3, 8192) + (uint32_t)(col & 7) * 2u;
+}
+
+__device__ __forceinline__ float bf(const uint8_t *p) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
+}
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint4 pack_bf8(const float (&x)[8]) {
+    return make_uint4(pack_bf2(x[0], x[1]), pack_bf2(x[2], x[3]), pack_bf2(x[4], x[5]),
+                      pack_bf2(x[6], x[7]));
+}
+__device__ __forceinline__ void unpack_bf8(uint4 u, float (&x)[8]) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+    }
+}
+
+struct Bars {
+    uint64_t *qk, *v, *mma;
+};
+
+// Bounded wait by every thread, then a block-wide verdict.
+__device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity, kWaitLimit);
+    return __syncthreads_and(ok) != 0;
+}
+
+__device__ __forceinline__ void sync_tc() {
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+// 32 consecutive TMEM columns of this thread's lane (two x16 loads, one wait)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    float a[16], b[16];
+    tmem_ld16(taddr, a);
+    tmem_ld16(taddr + 16, b);
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        v[c] = a[c];
+        v[16 + c] = b[c];
+    }
+}
+
+__device__ __forceinline__ void issue_load_qk(uint8_t *sm, const CUtensorMap *mq,
+                                              const CUtensorMap *mk, uint64_t *bar, int h,
+                                              int tok) {
+    mbar_arrive_expect_tx(bar, 32768);
+    tma_load_3d(sm + SM_STG_Q, mq, bar, 0, h, tok);
+    tma_load_3d(sm + SM_STG_Q + 8192, mq, bar, 64, h, tok);
+    tma_load_3d(sm + SM_STG_K, mk, bar, 0, h, tok);
+    tma_load_3d(sm + SM_STG_K + 8192, mk, bar, 64, h, tok);
+}
+__device__ __forceinline__ void issue_load_v(uint8_t *sm, const CUtensorMap *mv, uint64_t *bar,
+                                             int h, int tok) {
+    mbar_arrive_expect_tx(bar, 16384);
+    tma_load_3d(sm + SM_STG_V, mv, bar, 0, h, tok);
+    tma_load_3d(sm + SM_STG_V + 8192, mv, bar, 64, h, tok);
+}
+
+__global__ void __launch_bounds__(NT, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v, const float *__restrict__ g,
+                  const float *__restrict__ beta, const float *__restrict__ S0,
+                  float *__restrict__ o, float *S_out, const int32_t *__restrict__ cu, int N,
+                  int H) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    float *s_beta = reinterpret_cast<float *>(sm + SM_MISC + MISC_BETA);
+    float *s_gam = reinterpret_cast<float *>(sm + SM_MISC + MISC_GAM);
+    float *s_dq = reinterpret_cast<float *>(sm + SM_MISC + MISC_DQ);
+    float *s_dqp = reinterpret_cast<float *>(sm + SM_MISC + MISC_DQP);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM_MISC + MISC_BAR);
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SM_MISC + MISC_TMEM);
+    __shared__ int s_seq;
+
+    const int t = threadIdx.x;
+    const int warp = t >> 5;
+    const int lane = t & 31;
+    const int ch = t & 127;          // TMEM lane (i or j) owned in the epilogues
+    const int half = t >> 7;         // column half owned in the epilogues
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    // operand-build layout: row rb of each 16-row sub-block, channels 8cc..8cc+7
+    const int rb = lane & 15;
+    const int cc = 2 * warp + (lane >> 4);
+
+    const int h = blockIdx.x % H;
+    const int rank = blockIdx.x / H;
+    const int n = lpt_sequence(cu, N, rank, &s_seq);
+    const int tok0 = cu[n];
+    const int len = cu[n + 1] - tok0;
+    const size_t st_off = ((size_t)n * H + h) * kDK * kDV;
+
+    Bars B{bars + 0, bars + 1, bars + 2};
+    if (warp == 0) tmem_alloc(s_tmem, 512);
+    if (t == 0) {
+        mbar_init(B.qk, 1);
+        mbar_init(B.v, 1);
+        mbar_init(B.mma, 1);
+        fence_mbar_init();
+        prefetch_tmap(&map_q);
+        prefetch_tmap(&map_k);
+        prefetch_tmap(&map_v);
+    }
+    sync_tc();
+    const uint32_t tmem = *s_tmem;
+    uint32_t mma_phase = 0;
+    bool failed = false;
+
+    // ---- initial state: S^T master in TMEM (lane j, column i) + bf16 copy
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) {
+        float sv[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const int i = 64 * half + 32 * q2 + c;
+            sv[c] = S0 ? S0[st_off + (size_t)i * kDV + ch] : 0.f;
+        }
+        float a[16], b2[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            a[c] = sv[c];
+            b2[c] = sv[16 + c];
+        }
+        tmem_st16(tmem + lane_base + TM_S + 64 * half + 32 * q2, a);
+        tmem_st16(tmem + lane_base + TM_S + 64 * half + 32 * q2 + 16, b2);
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+            float x8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x8[u] = sv[8 * c8 + u];
+            *reinterpret_cast<uint4 *>(sm + SM_S + km_bf16(ch, 64 * half + 32 * q2 + 8 * c8, 2048)) =
+                pack_bf8(x8);
+        }
+    }
+    tmem_wait_st();
+
+    const int nchunks = (len + C - 1) / C;
+    if (t == 0 && nchunks > 0) {
+        issue_load_qk(sm, &map_q, &map_k, B.qk, h, tok0);
+        issue_load_v(sm, &map_v, B.v, h, tok0);
+    }
+    // g of rows 16u + rb, channels 8cc..8cc+7, for the next chunk to process
+    float gn[4][8];
+    float betan = 0.f;
+    auto load_g = [&](int c0) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = c0 + 16 * u + rb;
+            if (r < len) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    g + ((size_t)(tok0 + r) * H + h) * kDK + 8 * cc);
+                const float4 a = src[0], b4 = src[1];
+                gn[u][0] = a.x; gn[u][1] = a.y; gn[u][2] = a.z; gn[u][3] = a.w;
+                gn[u][4] = b4.x; gn[u][5] = b4.y; gn[u][6] = b4.z; gn[u][7] = b4.w;
+            } else {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) gn[u][c] = 0.f;
+            }
+        }
+        if (t < C) betan = (c0 + t < len) ? beta[(size_t)(tok0 + c0 + t) * H + h] : 0.f;
+    };
+    load_g(0);
+
+    for (int ci = 0; ci < nchunks && !failed; ++ci) {
+        const int c0 = ci * C;
+        const int Lc = min(C, len - c0);
+        const uint32_t par = (uint32_t)(ci & 1);
+
+        // ===== B1: decay prefix sums and every intra-chunk operand ==========
+        {
+            // inclusive prefix over the 64 rows: in-warp scan per 16-row sub-block
+            float b[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float x = gn[u][c];
+#pragma unroll
+                    for (int d = 1; d < 16; d <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, x, d, 16);
+                        if (rb >= d) x += y;
+                    }
+                    b[u][c] = x;
+                }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float carry = 0.f;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    b[u][c] += carry;
+                    carry = __shfl_sync(0xffffffffu, b[u][c], 15, 16);
+                }
+            }
+            if (t < C) s_beta[t] = betan;
+            // sigma_p = b at the last valid row of sub-block p; b_L = b at row Lc-1
+            const int last = Lc - 1;
+            const int lslab = last >> 4, llane = last & 15;
+            float sig[4][8], bl[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float src = lslab == 0 ? b[0][c] : lslab == 1 ? b[1][c] : lslab == 2 ? b[2][c] : b[3][c];
+                bl[c] = __shfl_sync(0xffffffffu, src, llane, 16);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const float v = __shfl_sync(0xffffffffu, b[p][c], p < lslab ? 15 : llane, 16);
+                    sig[p][c] = (p <= lslab) ? v : bl[c];
+                }
+            }
+            // per-channel factors from four exponentials: d0 = e^{sigma_0},
+            // dw = e^{sigma_w - sigma_{w-1}}; every inter-sub-block factor is a product
+            float dd[4][8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                dd[0][c] = __expf(sig[0][c]);
+#pragma unroll
+                for (int w = 1; w < 4; ++w) dd[w][c] = __expf(sig[w][c] - sig[w - 1][c]);
+            }
+            if (rb == 0) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) s_gam[8 * cc + c] = dd[0][c] * dd[1][c] * dd[2][c] * dd[3][c];
+            }
+            // F = e^{b - sigma_u} in [1, e^75] for valid rows (b is not needed afterwards)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    b[u][c] = (16 * u + rb < Lc) ? __expf(b[u][c] - sig[u][c]) : 0.f;
+            // prefetch the next chunk's g and beta (this chunk's are consumed)
+            load_g(c0 + C);
+
+            if (!wait_all(B.qk, par)) { failed = true; break; }
+            float dqp[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = 16 * u + rb;
+                const bool valid = r < Lc;
+                float qv[8], kv[8];
+                unpack_bf8(*reinterpret_cast<const uint4 *>(sm + SM_STG_Q + sw_chunk(r, cc, 8192)), qv);
+                unpack_bf8(*reinterpret_cast<const uint4 *>(sm + SM_STG_K + sw_chunk(r, cc, 8192)), kv);
+                float G[8], xq[8], xk[8], ep[8], el[8];
+                float dot = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    dot = fmaf(qv[c], kv[c], dot);
+                    const float F = b[u][c];                                   // [1, e^75]
+                    G[c] = valid ? __frcp_rn(F) : 0.f;                         // (0, 1]
+                    xq[c] = qv[c] * F;
+                    xk[c] = kv[c] * F;
+                    float e = dd[0][c];
+#pragma unroll
+                    for (int w = 1; w <= u; ++w) e *= dd[w][c];
+                    ep[c] = e;                                                 // e^{sigma_u}
+                    float l = 1.f;
+#pragma unroll
+                    for (int w = u + 1; w < 4; ++w) l *= dd[w][c];
+                    el[c] = l;                                                 // e^{b_L - sigma_u}
+                }
+                dqp[u] = valid ? dot : 0.f;
+                // Gram A operand: q rows 0..63, k rows 64..127
+                *reinterpret_cast<uint4 *>(sm + SM_X + sw_chunk(r, cc, 16384)) = pack_bf8(xq);
+                *reinterpret_cast<uint4 *>(sm + SM_X + sw_chunk(64 + r, cc, 16384)) = pack_bf8(xk);
+                // Khat stack: block pp >= u holds k_s e^{sigma_pp - b_s} at row 8pp(pp+1) + s
+#pragma unroll
+                for (int pp = u; pp < 4; ++pp) {
+                    float kh[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        float f = G[c];
+#pragma unroll
+                        for (int w = u + 1; w <= pp; ++w) f *= dd[w][c];
+                        kh[c] = kv[c] * f;
+                    }
+                    *reinterpret_cast<uint4 *>(sm + SM_KH + sw_chunk(8 * pp * (pp + 1) + r, cc, 20480)) =
+                        pack_bf8(kh);
+                }
+                // Q0 = q e^{b}, K0 = k e^{b}, Kbar = k e^{b_L - b}
+                float q0[8], k0[8];
+                uint32_t kb[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    q0[c] = xq[c] * ep[c];
+                    k0[c] = xk[c] * ep[c];
+                    kb[c] = to_tf32(kv[c] * G[c] * el[c]);
+                }
+                *reinterpret_cast<uint4 *>(sm + SM_Q0 + sw_chunk(r, cc, 8192)) = pack_bf8(q0);
+                *reinterpret_cast<uint4 *>(sm + SM_K0 + sw_chunk(r, cc, 8192)) = pack_bf8(k0);
+                // Kbar^T tf32 K-major il [i][s] (B of the dS product)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint32_t *>(sm + SM_KB + km_tf32(8 * cc + c, r, 2048)) = kb[c];
+            }
+            // q_r . k_r partials: combine the two channel chunks of this warp
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float d2 = dqp[u] + __shfl_xor_sync(0xffffffffu, dqp[u], 16);
+                if (lane < 16) s_dqp[warp * 64 + 16 * u + rb] = d2;
+            }
+        }
+        fence_proxy_async_smem();
+        sync_tc();
+
+        // ===== M1: Gram (X Khat^T) and O1 = S^T Q0^T ========================
+        if (t == 0) {
+            const uint32_t idg = instr_desc(kFmtBF16, 128, 160, 0, 0);
+            const uint32_t ido = instr_desc(kFmtBF16, 128, 64, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t ko = (uint32_t)(kk >> 2), kb2 = (uint32_t)(kk & 3) * 32u;
+                const uint64_t ax = smem_desc(smem_u32(sm + SM_X + ko * 16384 + kb2), 16, 1024, kSwizzle128B);
+                const uint64_t bk = smem_desc(smem_u32(sm + SM_KH + ko * 20480 + kb2), 16, 1024, kSwizzle128B);
+                mma_bf16_ss(tmem + TM_G, ax, bk, idg, kk > 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t ko = (uint32_t)(kk >> 2), kb2 = (uint32_t)(kk & 3) * 32u;
+                const uint64_t as = smem_desc(smem_u32(sm + SM_S + 256 * kk), 128, 2048, kSwizzleNone);
+                const uint64_t bq = smem_desc(smem_u32(sm + SM_Q0 + ko * 8192 + kb2), 16, 1024, kSwizzle128B);
+                mma_bf16_ss(tmem + TM_O, as, bq, ido, kk > 0);
+            }
+            mma_commit(B.mma);
+            // q/k staging is consumed: load the next chunk's q and k
+            if (ci + 1 < nchunks) issue_load_qk(sm, &map_q, &map_k, B.qk, h, tok0 + c0 + C);
+        }
+        if (!wait_all(B.mma, mma_phase)) { failed = true; break; }
+        mma_phase ^= 1;
+        tc_fence_after();
+
+        // ===== E1: Gram epilogue -> A' (tf32) and M (fp32); diagonal dots ====
+        float *Mm = reinterpret_cast<float *>(sm + SM_X);
+        if (warp < 4) {
+            const bool qside = t < 64;
+            const int r = t & 63;
+            const int p = r >> 4;
+            const bool rvalid = r < Lc;
+            const float br = s_beta[r];
+            const int npass = (warp & 1) ? 2 : 1;
+            for (int pass = 0; pass < npass; ++pass) {
+                const int wb = (warp & 1) ? (pass == 0 ? 48 : 96) : 0;
+                float v[64];
+                {
+                    float a[32], b2[32];
+                    tmem_ld16(tmem + lane_base + TM_G + wb, *reinterpret_cast<float(*)[16]>(a));
+                    tmem_ld16(tmem + lane_base + TM_G + wb + 16, *reinterpret_cast<float(*)[16]>(a + 16));
+                    tmem_ld16(tmem + lane_base + TM_G + wb + 32, *reinterpret_cast<float(*)[16]>(b2));
+                    tmem_ld16(tmem + lane_base + TM_G + wb + 48, *reinterpret_cast<float(*)[16]>(b2 + 16));
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        v[c] = a[c];
+                        v[32 + c] = b2[c];
+                    }
+                }
+                const bool mine = (warp & 1) ? ((pass == 0) == (p == 2)) : true;
+                const bool off16 = !(warp & 1) && p == 1;     // column block starts at 16
+                if (mine) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        float x4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int s = 4 * j + e;
+                            float val = 0.f;
+                            if (s + 16 < 64)
+                                val = off16 ? v[s + 16] : v[s];
+                            else
+                                val = off16 ? 0.f : v[s];
+                            x4[e] = (rvalid && s < r) ? val : 0.f;
+                        }
+                        if (qside) {
+                            *reinterpret_cast<uint4 *>(sm + SM_A + km_tf32(r, 4 * j, 2048)) =
+                                make_uint4(to_tf32(x4[0]), to_tf32(x4[1]), to_tf32(x4[2]), to_tf32(x4[3]));
+                        } else {
+                            *reinterpret_cast<float4 *>(Mm + r * MLD + 4 * j) =
+                                make_float4(br * x4[0], br * x4[1], br * x4[2], br * x4[3]);
+                        }
+                    }
+                }
+            }
+        } else if (t < 192) {
+            const int r = t - 128;
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) acc += s_dqp[w * 64 + r];
+            s_dq[r] = acc;
+        }
+        __syncthreads();
+
+        // ===== S1: T = (I + M)^-1 by 16-row blocks, in place; T' = (T-I)Diag(beta)
+        {
+            float *Yt = Mm + 64 * MLD;        // [3][16][16] temporaries
+            // column c of (I + M_pp)^-1: x = e_c, then for s = c..14,
+            // x[r] -= M[r][s] x[s] for r > s (x[s] is final once column s is applied)
+            float x[16];
+            if (t < 64) {
+                const int p = t >> 4, c = t & 15;
+                const float *Mb = Mm + (16 * p) * MLD + 16 * p;
+#pragma unroll
+                for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
+#pragma unroll
+                for (int s = 0; s < 15; ++s) {
+                    const float xs = x[s];
+#pragma unroll
+                    for (int r = s + 1; r < 16; ++r) x[r] = fmaf(-Mb[r * MLD + s], xs, x[r]);
+                }
+            }
+            __syncthreads();
+            if (t < 64) {
+                const int p = t >> 4, c = t & 15;
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Mm[(16 * p + r) * MLD + 16 * p + c] = x[r];
+            }
+            __syncthreads();
+#pragma unroll
+            for (int p = 1; p < 4; ++p) {
+                // Y_pq = sum_{m=16q}^{16p-1} M[16p+r][m] T[m][16q .. 16q+15]
+                if (t < 64 * p) {
+                    const int q = t >> 6, r = (t >> 2) & 15, c4 = t & 3;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int m = 16 * q; m < 16 * p; ++m) {
+                        const float a = Mm[(16 * p + r) * MLD + m];
+                        const float4 tv = *reinterpret_cast<const float4 *>(Mm + m * MLD + 16 * q + 4 * c4);
+                        acc.x = fmaf(a, tv.x, acc.x);
+                        acc.y = fmaf(a, tv.y, acc.y);
+                        acc.z = fmaf(a, tv.z, acc.z);
+                        acc.w = fmaf(a, tv.w, acc.w);
+                    }
+                    *reinterpret_cast<float4 *>(Yt + (q * 16 + r) * 16 + 4 * c4) = acc;
+                }
+                __syncthreads();
+                // T_pq = -T_pp Y_pq
+                if (t < 64 * p) {
+                    const int q = t >> 6, r = (t >> 2) & 15, c4 = t & 3;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+                        const float a = Mm[(16 * p + r) * MLD + 16 * p + m];
+                        const float4 yv = *reinterpret_cast<const float4 *>(Yt + (q * 16 + m) * 16 + 4 * c4);
+                        acc.x = fmaf(a, yv.x, acc.x);
+                        acc.y = fmaf(a, yv.y, acc.y);
+                        acc.z = fmaf(a, yv.z, acc.z);
+                        acc.w = fmaf(a, yv.w, acc.w);
+                    }
+                    *reinterpret_cast<float4 *>(Mm + (16 * p + r) * MLD + 16 * q + 4 * c4) =
+                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                }
+                __syncthreads();
+            }
+            // T' bf16 K-major il [r][s]
+            for (int e = t; e < 512; e += NT) {
+                const int r = e >> 3, s0 = (e & 7) * 8;
+                const float4 a = *reinterpret_cast<const float4 *>(Mm + r * MLD + s0);
+                const float4 b4 = *reinterpret_cast<const float4 *>(Mm + r * MLD + s0 + 4);
+                const float tv[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
+                float w8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) w8[u] = (s0 + u < r) ? tv[u] * s_beta[s0 + u] : 0.f;
+                *reinterpret_cast<uint4 *>(sm + SM_T + km_bf16(r, s0, 1024)) = pack_bf8(w8);
+            }
+        }
+        fence_proxy_async_smem();
+        sync_tc();
+
+        // ===== M2: W = T' K0 (as (T'K0)^T) and U~ = T' V ====================
+        if (!wait_all(B.v, par)) { failed = true; break; }
+        if (t == 0) {
+            const uint32_t idmn = instr_desc(kFmtBF16, 128, 64, 1, 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bd = smem_desc(smem_u32(sm + SM_T + 256 * kk), 128, 1024, kSwizzleNone);
+                const uint64_t aw = smem_desc(smem_u32(sm + SM_K0 + 2048 * kk), 8192, 1024, kSwizzle128B);
+                const uint64_t av = smem_desc(smem_u32(sm + SM_STG_V + 2048 * kk), 8192, 1024, kSwizzle128B);
+                mma_bf16_ss(tmem + TM_W, aw, bd, idmn, kk > 0);
+                mma_bf16_ss(tmem + TM_U, av, bd, idmn, kk > 0);
+            }
+            mma_commit(B.mma);
+        }
+        if (!wait_all(B.mma, mma_phase)) { failed = true; break; }
+        mma_phase ^= 1;
+        tc_fence_after();
+
+        // ===== E2: W = D_W + beta K0 -> -W^T bf16 MN-major il [i][r] ========
+        {
+            float wv[32];
+            tmem_ld32(tmem + lane_base + TM_W + 32 * half, wv);
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+                float w8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int r = 32 * half + 8 * c8 + u;
+                    w8[u] = -(wv[8 * c8 + u] + s_beta[r] * bf(sm + SM_K0 + sw_elem64(r, ch)));
+                }
+                *reinterpret_cast<uint4 *>(sm + SM_W + mn_bf16(ch, 32 * half + 8 * c8, 1024)) = pack_bf8(w8);
+            }
+        }
+        fence_proxy_async_smem();
+        sync_tc();
+
+        // ===== M3: U += S^T (-W^T) ===========================================
+        if (t == 0) {
+            const uint32_t idu = instr_desc(kFmtBF16, 128, 64, 0, 1);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t as = smem_desc(smem_u32(sm + SM_S + 256 * kk), 128, 2048, kSwizzleNone);
+                const uint64_t bw = smem_desc(smem_u32(sm + SM_W + 2048 * kk), 1024, 128, kSwizzleNone);
+                mma_bf16_ss(tmem + TM_U, as, bw, idu, 1);
+            }
+            mma_commit(B.mma);
+        }
+        if (!wait_all(B.mma, mma_phase)) { failed = true; break; }
+        mma_phase ^= 1;
+        tc_fence_after();
+
+        // ===== E3: u = D_U + beta v; U^T tf32 -> SM_X ========================
+        float uv[32];
+        {
+            tmem_ld32(tmem + lane_base + TM_U + 32 * half, uv);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const int r = 32 * half + k;
+                uv[k] += s_beta[r] * bf(sm + SM_STG_V + sw_elem64(r, ch));
+            }
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+                *reinterpret_cast<uint4 *>(sm + SM_X + km_tf32(ch, 32 * half + 4 * c4, 2048)) =
+                    make_uint4(to_tf32(uv[4 * c4 + 0]), to_tf32(uv[4 * c4 + 1]),
+                               to_tf32(uv[4 * c4 + 2]), to_tf32(uv[4 * c4 + 3]));
+        }
+        fence_proxy_async_smem();
+        sync_tc();
+
+        // ===== M4: O += U^T A'^T (tf32);  dS = U^T Kbar (tf32) ================
+        if (t == 0) {
+            // v staging is consumed: load the next chunk's v
+            if (ci + 1 < nchunks) issue_load_v(sm, &map_v, B.v, h, tok0 + c0 + C);
+            const uint32_t ido = instr_desc(kFmtTF32, 128, 64, 0, 0);
+            const uint32_t ids = instr_desc(kFmtTF32, 128, 128, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t au = smem_desc(smem_u32(sm + SM_X + 256 * kk), 128, 2048, kSwizzleNone);
+                const uint64_t ba = smem_desc(smem_u32(sm + SM_A + 256 * kk), 128, 2048, kSwizzleNone);
+                const uint64_t bk = smem_desc(smem_u32(sm + SM_KB + 256 * kk), 128, 2048, kSwizzleNone);
+                mma_tf32_ss(tmem + TM_O, au, ba, ido, 1);
+                mma_tf32_ss(tmem + TM_DS, au, bk, ids, kk > 0);
+            }
+            mma_commit(B.mma);
+        }
+        if (!wait_all(B.mma, mma_phase)) { failed = true; break; }
+        mma_phase ^= 1;
+        tc_fence_after();
+
+        // ===== E4: o = D_O + (q.k) u;  S = e^{b_L} S + dS (TMEM) and bf16 copy
+        {
+            float ov[32];
+            tmem_ld32(tmem + lane_base + TM_O + 32 * half, ov);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const int r = 32 * half + k;
+                if (r < Lc) o[((size_t)(tok0 + c0 + r) * H + h) * kDV + ch] = ov[k] + s_dq[r] * uv[k];
+            }
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                const uint32_t col = 64 * half + 32 * q2;
+                float sv[32], dv[32];
+                tmem_ld32(tmem + lane_base + TM_S + col, sv);
+                tmem_ld32(tmem + lane_base + TM_DS + col, dv);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) sv[c] = fmaf(s_gam[col + c], sv[c], dv[c]);
+                float a[16], b2[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    a[c] = sv[c];
+                    b2[c] = sv[16 + c];
+                }
+                tmem_st16(tmem + lane_base + TM_S + col, a);
+                tmem_st16(tmem + lane_base + TM_S + col + 16, b2);
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float x8[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) x8[u] = sv[8 * c8 + u];
+                    *reinterpret_cast<uint4 *>(sm + SM_S + km_bf16(ch, col + 8 * c8, 2048)) = pack_bf8(x8);
+                }
+            }
+            tmem_wait_st();
+        }
+        fence_proxy_async_smem();
+        sync_tc();
+    }
+
+    if (failed) {
+        if (t == 0) atomicOr(&g_kda_device_error, 1u);
+        // let any copies or MMAs in flight finish (bounded) before freeing TMEM
+        mbar_wait(B.mma, mma_phase, kWaitLimit);
+        mbar_wait(B.qk, (uint32_t)(nchunks & 1) ^ 1u, kWaitLimit);
+        mbar_wait(B.v, (uint32_t)(nchunks & 1) ^ 1u, kWaitLimit);
+        __syncthreads();
+    } else {
+        // ---- final state: S_out[i][j] from the TMEM master (lane j, column i)
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+            float sv[32];
+            tmem_ld32(tmem + lane_base + TM_S + 64 * half + 32 * q2, sv);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const int i = 64 * half + 32 * q2 + c;
+                S_out[st_off + (size_t)i * kDV + ch] = sv[c];
+            }
+        }
+    }
+    sync_tc();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 3D map over a [T, H, 128] bf16 tensor: dims (128, H, T), box (bw, 1, 64).
+bool make_map(CUtensorMap *m, const void *base, int64_t T, int H, uint32_t bw, bool swz) {
+    auto enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};
+    cuuint32_t box[3] = {bw, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, const float *S0, float *o, float *S_out,
+                              const int32_t *cu_seqlens, int N, int64_t T, int H,
+                              cudaStream_t stream) {
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, q, T, H, 64, true) || !make_map(&mk, k, T, H, 64, true) ||
+        !make_map(&mv, v, T, H, 64, true))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    const long long blocks = (long long)N * H;
+    prefill_tc_kernel<<<(unsigned)blocks, NT, SMEM_ALLOC, stream>>>(mq, mk, mv, g, beta, S0, o, S_out,
+                                                                    cu_seqlens, N, H);
+    return cudaGetLastError();
+}
+
+cudaError_t read_device_error(unsigned int *code, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_kda_device_error, sizeof(unsigned int));
+    if (e != cudaSuccess || !reset) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_kda_device_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace kda

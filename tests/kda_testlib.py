@@ -44,6 +44,7 @@ def prefill_on_gpu(inp: ki.PrefillInputs, chunk=None, S0=None, device="cuda"):
     o, S = kda.prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, S0=s0,
                                chunk=chunk or inp.chunk)
     torch.cuda.synchronize()
+    assert kda.device_error() == 0, "a bounded wait inside the prefill kernel gave up"
     return o.cpu().numpy(), S.cpu().numpy()
 
 
