@@ -265,7 +265,7 @@ def run_ours(args):
         decode = _decode_leg(kda, torch, dev, stream, peaks, args)
 
     # ---- end to end through the public API with host buffers -------------
-    e2e = _e2e_leg(kda, torch, dev, stream, pre, dstep, args, barrier, ws)
+    e2e = None if args.no_e2e else _e2e_leg(kda, torch, dev, stream, pre, dstep, args, barrier, ws)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
@@ -469,6 +469,8 @@ def main():
                     help="heads per sequence in the oracle sample (default: ~4e5 token-heads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the host-buffer end-to-end leg (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("bench.py: warning: fewer than 3 warm-up steps", file=sys.stderr)

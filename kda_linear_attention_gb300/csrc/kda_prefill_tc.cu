@@ -537,13 +537,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 if (t < 64 * p) {
                     const int q = t >> 6, r = (t >> 2) & 15, c4 = t & 3;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int m = 16 * q; m < 16 * p; ++m) {
-                        const float a = Mm[(16 * p + r) * MLD + m];
-                        const float4 tv = *reinterpret_cast<const float4 *>(Mm + m * MLD + 16 * q + 4 * c4);
-                        acc.x = fmaf(a, tv.x, acc.x);
-                        acc.y = fmaf(a, tv.y, acc.y);
-                        acc.z = fmaf(a, tv.z, acc.z);
-                        acc.w = fmaf(a, tv.w, acc.w);
+                    for (int mb = q; mb < p; ++mb) {
+#pragma unroll
+                        for (int mm = 0; mm < 16; ++mm) {
+                            const int m = 16 * mb + mm;
+                            const float a = Mm[(16 * p + r) * MLD + m];
+                            const float4 tv = *reinterpret_cast<const float4 *>(Mm + m * MLD + 16 * q + 4 * c4);
+                            acc.x = fmaf(a, tv.x, acc.x);
+                            acc.y = fmaf(a, tv.y, acc.y);
+                            acc.z = fmaf(a, tv.z, acc.z);
+                            acc.w = fmaf(a, tv.w, acc.w);
+                        }
                     }
                     *reinterpret_cast<float4 *>(Yt + (q * 16 + r) * 16 + 4 * c4) = acc;
                 }
