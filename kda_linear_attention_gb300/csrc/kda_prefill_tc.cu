@@ -30,7 +30,7 @@
 // nearest in software.  Accumulation is fp32 in TMEM; the state is kept in
 // fp32 in TMEM for the whole sequence.
 //
-// One CTA (256 threads) per (sequence, head), walking its chunks in order;
+// One CTA (512 threads) per (sequence, head), walking its chunks in order;
 // the MMAs are transposed so that M = 128 is always dk or dv:
 //   D_G[128 x 160] = X . Khat^T             D_W[i][r]  = (T' K0)^T
 //   D_U[j][r]      = (T' V)^T - (W S)^T     D_O[j][r]  = (Q0 S)^T + (A' U)^T
@@ -49,7 +49,7 @@ namespace {
 using namespace tc;
 
 constexpr int C = 64;
-constexpr int NT = 256;
+constexpr int NT = 512;
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 // shared memory map (bytes from a 1024-aligned base).  "sw" = 128-byte
@@ -62,7 +62,7 @@ constexpr uint32_t SM_KH = 81920;         // 40 KB: Gram B Khat [160][128] K-maj
 constexpr uint32_t SM_A = SM_KH;          //   A' tf32 K-major il [r][s], 16 KB
 constexpr uint32_t SM_W = SM_KH + 16384;  //   -W^T bf16 MN-major il [i][r], 16 KB
 constexpr uint32_t SM_T = SM_KH + 32768;  //   T' bf16 K-major il [r][s], 8 KB
-constexpr uint32_t SM_Q0 = 122880;        // 16 KB: Q0 [64][128] K-major sw
+constexpr uint32_t SM_Q0 = 122880;        // 16 KB: Q0 [64][128] K-major sw (with K0: next chunk's g, cp.async)
 constexpr uint32_t SM_K0 = 139264;        // 16 KB: K0 [64 s][128 i] MN-major sw (A of the W product)
 constexpr uint32_t SM_KB = 155648;        // 32 KB: Kbar^T [128 i][64 s] tf32 K-major il (B of the dS product)
 constexpr uint32_t SM_S = 188416;         // 32 KB: S^T bf16 K-major il [j][i]
@@ -71,9 +71,15 @@ constexpr uint32_t MISC_BETA = 0;         // float[64]
 constexpr uint32_t MISC_GAM = 256;        // float[128]  e^{b_L}
 constexpr uint32_t MISC_DQ = 768;         // float[64]   q_r . k_r
 constexpr uint32_t MISC_DQP = 1024;       // float[8][64] partial dot products
-constexpr uint32_t MISC_BAR = 3072;       // 3 x u64 mbarriers
-constexpr uint32_t MISC_TMEM = 3104;      // u32 TMEM base
-constexpr uint32_t SMEM_USED = SM_MISC + 3120;
+constexpr uint32_t MISC_TOT = 3072;       // float[128]  prefix total through row 31
+constexpr uint32_t MISC_SIG = 3584;       // float[4][128] sigma_p
+constexpr uint32_t MISC_BL = 5632;        // float[128]  b_L
+constexpr uint32_t MISC_DD = 6144;        // float[4][128] per-channel decay factors
+constexpr uint32_t MISC_BETAN = 8192;     // float[64]   next chunk's beta (cp.async)
+constexpr uint32_t MISC_BAR = 8448;       // 4 x u64 mbarriers
+constexpr uint32_t MISC_TMEM = 8480;      // u32 TMEM base
+constexpr uint32_t SMEM_USED = SM_MISC + 8496;
+static_assert(MISC_BAR + 32 <= MISC_TMEM, "mbarrier slots");
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;   // alignment slack
 constexpr int MLD = 68;                   // row stride (floats) of M / T
 
@@ -134,7 +140,7 @@ __device__ __forceinline__ void unpack_bf8(uint4 u, float (&x)[8]) {
 }
 
 struct Bars {
-    uint64_t *qk, *v, *mma;
+    uint64_t *qk, *v, *mma, *g;
 };
 
 // Bounded wait by every thread, then a block-wide verdict.
@@ -180,7 +186,8 @@ __device__ __forceinline__ void issue_load_v(uint8_t *sm, const CUtensorMap *mv,
 
 __global__ void __launch_bounds__(NT, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                  const __grid_constant__ CUtensorMap map_v, const float *__restrict__ g,
+                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_g,
+                  const float *__restrict__ g,
                   const float *__restrict__ beta, const float *__restrict__ S0,
                   float *__restrict__ o, float *S_out, const int32_t *__restrict__ cu, int N,
                   int H) {
@@ -190,6 +197,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     float *s_gam = reinterpret_cast<float *>(sm + SM_MISC + MISC_GAM);
     float *s_dq = reinterpret_cast<float *>(sm + SM_MISC + MISC_DQ);
     float *s_dqp = reinterpret_cast<float *>(sm + SM_MISC + MISC_DQP);
+    float *s_tot = reinterpret_cast<float *>(sm + SM_MISC + MISC_TOT);
+    float *s_sig = reinterpret_cast<float *>(sm + SM_MISC + MISC_SIG);
+    float *s_bl = reinterpret_cast<float *>(sm + SM_MISC + MISC_BL);
+    float *s_dd = reinterpret_cast<float *>(sm + SM_MISC + MISC_DD);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM_MISC + MISC_BAR);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SM_MISC + MISC_TMEM);
     __shared__ int s_seq;
@@ -198,11 +209,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const int warp = t >> 5;
     const int lane = t & 31;
     const int ch = t & 127;          // TMEM lane (i or j) owned in the epilogues
-    const int half = t >> 7;         // column half owned in the epilogues
+    const int qt = t >> 7;           // column quarter owned in the epilogues
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    // operand-build layout: row rb of each 16-row sub-block, channels 8cc..8cc+7
+    // operand-build layout: row rb of sub-blocks 2sp, 2sp+1; channels 8cc..8cc+7
     const int rb = lane & 15;
-    const int cc = 2 * warp + (lane >> 4);
+    const int cc = 2 * (warp & 7) + (lane >> 4);
+    const int sp = warp >> 3;
 
     const int h = blockIdx.x % H;
     const int rank = blockIdx.x / H;
@@ -211,13 +223,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const int len = cu[n + 1] - tok0;
     const size_t st_off = ((size_t)n * H + h) * kDK * kDV;
 
-    Bars B{bars + 0, bars + 1, bars + 2};
+    Bars B{bars + 0, bars + 1, bars + 2, bars + 3};
     if (warp == 0) tmem_alloc(s_tmem, 512);
     if (t == 0) {
         mbar_init(B.qk, 1);
         mbar_init(B.v, 1);
         mbar_init(B.mma, 1);
+        mbar_init(B.g, 1);
         fence_mbar_init();
+        prefetch_tmap(&map_g);
         prefetch_tmap(&map_q);
         prefetch_tmap(&map_k);
         prefetch_tmap(&map_v);
@@ -228,12 +242,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     bool failed = false;
 
     // ---- initial state: S^T master in TMEM (lane j, column i) + bf16 copy
-#pragma unroll
-    for (int q2 = 0; q2 < 2; ++q2) {
+    {
         float sv[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-            const int i = 64 * half + 32 * q2 + c;
+            const int i = 32 * qt + c;
             sv[c] = S0 ? S0[st_off + (size_t)i * kDV + ch] : 0.f;
         }
         float a[16], b2[16];
@@ -242,45 +255,43 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             a[c] = sv[c];
             b2[c] = sv[16 + c];
         }
-        tmem_st16(tmem + lane_base + TM_S + 64 * half + 32 * q2, a);
-        tmem_st16(tmem + lane_base + TM_S + 64 * half + 32 * q2 + 16, b2);
+        tmem_st16(tmem + lane_base + TM_S + 32 * qt, a);
+        tmem_st16(tmem + lane_base + TM_S + 32 * qt + 16, b2);
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {
             float x8[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) x8[u] = sv[8 * c8 + u];
-            *reinterpret_cast<uint4 *>(sm + SM_S + km_bf16(ch, 64 * half + 32 * q2 + 8 * c8, 2048)) =
-                pack_bf8(x8);
+            *reinterpret_cast<uint4 *>(sm + SM_S + km_bf16(ch, 32 * qt + 8 * c8, 2048)) = pack_bf8(x8);
         }
+        tmem_wait_st();
     }
-    tmem_wait_st();
 
     const int nchunks = (len + C - 1) / C;
     if (t == 0 && nchunks > 0) {
         issue_load_qk(sm, &map_q, &map_k, B.qk, h, tok0);
         issue_load_v(sm, &map_v, B.v, h, tok0);
     }
-    // g of rows 16u + rb, channels 8cc..8cc+7, for the next chunk to process
-    float gn[4][8];
-    float betan = 0.f;
-    auto load_g = [&](int c0) {
+    // The next chunk's g ([64 rows][128 channels] fp32, four 128B-swizzled TMA
+    // boxes of 32 channels) lands in the Q0/K0 region, which is free from the W
+    // epilogue to the next operand build; beta (64 floats) is copied with
+    // cp.async.  Rows past the end of the sequence are masked at use.
+    float *s_betan = reinterpret_cast<float *>(sm + SM_MISC + MISC_BETAN);
+    auto fetch_g = [&](int c0) {
+        if (c0 >= len) return;
+        if (t == 0) {
+            mbar_arrive_expect_tx(B.g, 32768);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int r = c0 + 16 * u + rb;
-            if (r < len) {
-                const float4 *src = reinterpret_cast<const float4 *>(
-                    g + ((size_t)(tok0 + r) * H + h) * kDK + 8 * cc);
-                const float4 a = src[0], b4 = src[1];
-                gn[u][0] = a.x; gn[u][1] = a.y; gn[u][2] = a.z; gn[u][3] = a.w;
-                gn[u][4] = b4.x; gn[u][5] = b4.y; gn[u][6] = b4.z; gn[u][7] = b4.w;
-            } else {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) gn[u][c] = 0.f;
-            }
+            for (int bx = 0; bx < 4; ++bx)
+                tma_load_3d(sm + SM_Q0 + 8192 * bx, &map_g, B.g, 32 * bx, h, tok0 + c0);
         }
-        if (t < C) betan = (c0 + t < len) ? beta[(size_t)(tok0 + c0 + t) * H + h] : 0.f;
+        if (t < C) {
+            const float *src = beta + (size_t)(tok0 + min(c0 + t, len - 1)) * H + h;
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(s_betan + t)), "l"(src) : "memory");
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        }
     };
-    load_g(0);
+    fetch_g(0);
 
     for (int ci = 0; ci < nchunks && !failed; ++ci) {
         const int c0 = ci * C;
@@ -289,72 +300,107 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 
         // ===== B1: decay prefix sums and every intra-chunk operand ==========
         {
-            // inclusive prefix over the 64 rows: in-warp scan per 16-row sub-block
-            float b[4][8];
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            if (!wait_all(B.g, par)) { failed = true; break; }
+            float gn[2][8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int v = 0; v < 2; ++v) {
+                // element (row, c) of the g tile: box c/32, 128-byte rows, 16-byte chunks swizzled
+                const int r = 16 * (2 * sp + v) + rb;
+                const uint8_t *rowp = sm + SM_Q0 + 8192 * (cc >> 2) + r * 128;
+                const int c4 = 2 * (cc & 3);
+                const float4 a = *reinterpret_cast<const float4 *>(rowp + ((c4 ^ (r & 7)) << 4));
+                const float4 b4 = *reinterpret_cast<const float4 *>(rowp + (((c4 + 1) ^ (r & 7)) << 4));
+                gn[v][0] = a.x; gn[v][1] = a.y; gn[v][2] = a.z; gn[v][3] = a.w;
+                gn[v][4] = b4.x; gn[v][5] = b4.y; gn[v][6] = b4.z; gn[v][7] = b4.w;
+            }
+            const float betan = (t < C) ? s_betan[t] : 0.f;
+            // inclusive prefix: in-warp scan over each 16-row sub-block, then
+            // carries from sub-block 2sp to 2sp+1 (shuffle) and across warps (smem)
+            float b[2][8];
+#pragma unroll
+            for (int v = 0; v < 2; ++v)
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    float x = gn[u][c];
+                    float x = (16 * (2 * sp + v) + rb < Lc) ? gn[v][c] : 0.f;
 #pragma unroll
                     for (int d = 1; d < 16; d <<= 1) {
                         const float y = __shfl_up_sync(0xffffffffu, x, d, 16);
                         if (rb >= d) x += y;
                     }
-                    b[u][c] = x;
+                    b[v][c] = x;
                 }
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float carry = 0.f;
+            for (int c = 0; c < 8; ++c) b[1][c] += __shfl_sync(0xffffffffu, b[0][c], 15, 16);
+            if (sp == 0 && rb == 15) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    b[u][c] += carry;
-                    carry = __shfl_sync(0xffffffffu, b[u][c], 15, 16);
+                for (int c = 0; c < 8; ++c) s_tot[8 * cc + c] = b[1][c];
+            }
+            if (t < C) s_beta[t] = (t < Lc) ? betan : 0.f;
+            __syncthreads();
+            if (sp == 1) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float base = s_tot[8 * cc + c];
+                    b[0][c] += base;
+                    b[1][c] += base;
                 }
             }
-            if (t < C) s_beta[t] = betan;
             // sigma_p = b at the last valid row of sub-block p; b_L = b at row Lc-1
             const int last = Lc - 1;
-            const int lslab = last >> 4, llane = last & 15;
-            float sig[4][8], bl[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float src = lslab == 0 ? b[0][c] : lslab == 1 ? b[1][c] : lslab == 2 ? b[2][c] : b[3][c];
-                bl[c] = __shfl_sync(0xffffffffu, src, llane, 16);
+            for (int p = 0; p < 4; ++p) {
+                const int rr = min(16 * p + 15, last);
+                if ((rr >> 5) == sp && (rr & 15) == rb) {
+                    const int v = (rr >> 4) & 1;
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    const float v = __shfl_sync(0xffffffffu, b[p][c], p < lslab ? 15 : llane, 16);
-                    sig[p][c] = (p <= lslab) ? v : bl[c];
+                    for (int c = 0; c < 8; ++c) s_sig[p * 128 + 8 * cc + c] = v ? b[1][c] : b[0][c];
                 }
             }
-            // per-channel factors from four exponentials: d0 = e^{sigma_0},
-            // dw = e^{sigma_w - sigma_{w-1}}; every inter-sub-block factor is a product
-            float dd[4][8];
+            if ((last >> 5) == sp && (last & 15) == rb) {
+                const int v = (last >> 4) & 1;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                dd[0][c] = __expf(sig[0][c]);
-#pragma unroll
-                for (int w = 1; w < 4; ++w) dd[w][c] = __expf(sig[w][c] - sig[w - 1][c]);
+                for (int c = 0; c < 8; ++c) s_bl[8 * cc + c] = v ? b[1][c] : b[0][c];
             }
-            if (rb == 0) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) s_gam[8 * cc + c] = dd[0][c] * dd[1][c] * dd[2][c] * dd[3][c];
+            __syncthreads();
+            // per-channel factors: d0 = e^{sigma_0}, dw = e^{sigma_w - sigma_{w-1}};
+            // gamma = e^{b_L} = d0 d1 d2 d3 (sigma_3 = b_L)
+            if (t < 128) {
+                const float s0 = s_sig[t], s1 = s_sig[128 + t], s2 = s_sig[256 + t], s3 = s_sig[384 + t];
+                const float d0 = __expf(s0), d1 = __expf(s1 - s0), d2 = __expf(s2 - s1), d3 = __expf(s3 - s2);
+                s_dd[t] = d0;
+                s_dd[128 + t] = d1;
+                s_dd[256 + t] = d2;
+                s_dd[384 + t] = d3;
+                s_gam[t] = d0 * d1 * d2 * d3;
             }
-            // F = e^{b - sigma_u} in [1, e^75] for valid rows (b is not needed afterwards)
+            // F = e^{b - sigma_u} in [1, e^75] for valid rows
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int v = 0; v < 2; ++v) {
+                const int u = 2 * sp + v;
+                const bool valid = 16 * u + rb < Lc;
+                const float4 sa = *reinterpret_cast<const float4 *>(s_sig + u * 128 + 8 * cc);
+                const float4 sb = *reinterpret_cast<const float4 *>(s_sig + u * 128 + 8 * cc + 4);
+                const float sg[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    b[u][c] = (16 * u + rb < Lc) ? __expf(b[u][c] - sig[u][c]) : 0.f;
-            // prefetch the next chunk's g and beta (this chunk's are consumed)
-            load_g(c0 + C);
+                for (int c = 0; c < 8; ++c) b[v][c] = valid ? __expf(b[v][c] - sg[c]) : 0.f;
+            }
+            __syncthreads();          // s_dd ready
 
             if (!wait_all(B.qk, par)) { failed = true; break; }
-            float dqp[4];
+            float dd[4][8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int w = 0; w < 4; ++w) {
+                const float4 da = *reinterpret_cast<const float4 *>(s_dd + w * 128 + 8 * cc);
+                const float4 db = *reinterpret_cast<const float4 *>(s_dd + w * 128 + 8 * cc + 4);
+                dd[w][0] = da.x; dd[w][1] = da.y; dd[w][2] = da.z; dd[w][3] = da.w;
+                dd[w][4] = db.x; dd[w][5] = db.y; dd[w][6] = db.z; dd[w][7] = db.w;
+            }
+            float dqp[2];
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+                const int u = 2 * sp + v;
                 const int r = 16 * u + rb;
-                const bool valid = r < Lc;
                 float qv[8], kv[8];
                 unpack_bf8(*reinterpret_cast<const uint4 *>(sm + SM_STG_Q + sw_chunk(r, cc, 8192)), qv);
                 unpack_bf8(*reinterpret_cast<const uint4 *>(sm + SM_STG_K + sw_chunk(r, cc, 8192)), kv);
@@ -363,58 +409,89 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     dot = fmaf(qv[c], kv[c], dot);
-                    const float F = b[u][c];                                   // [1, e^75]
-                    G[c] = valid ? __frcp_rn(F) : 0.f;                         // (0, 1]
+                    const float F = b[v][c];
+                    G[c] = (F > 0.f) ? __frcp_rn(F) : 0.f;                     // (0, 1]
                     xq[c] = qv[c] * F;
                     xk[c] = kv[c] * F;
+                    // e^{sigma_u} and e^{b_L - sigma_u} from the per-channel factors
                     float e = dd[0][c];
-#pragma unroll
-                    for (int w = 1; w <= u; ++w) e *= dd[w][c];
-                    ep[c] = e;                                                 // e^{sigma_u}
                     float l = 1.f;
 #pragma unroll
-                    for (int w = u + 1; w < 4; ++w) l *= dd[w][c];
-                    el[c] = l;                                                 // e^{b_L - sigma_u}
+                    for (int w = 1; w < 4; ++w) {
+                        if (w <= u) e *= dd[w][c];
+                        else l *= dd[w][c];
+                    }
+                    ep[c] = e;
+                    el[c] = l;
                 }
-                dqp[u] = valid ? dot : 0.f;
+                dqp[v] = (r < Lc) ? dot : 0.f;
                 // Gram A operand: q rows 0..63, k rows 64..127
                 *reinterpret_cast<uint4 *>(sm + SM_X + sw_chunk(r, cc, 16384)) = pack_bf8(xq);
                 *reinterpret_cast<uint4 *>(sm + SM_X + sw_chunk(64 + r, cc, 16384)) = pack_bf8(xk);
                 // Khat stack: block pp >= u holds k_s e^{sigma_pp - b_s} at row 8pp(pp+1) + s
+                float kh[8];
 #pragma unroll
-                for (int pp = u; pp < 4; ++pp) {
-                    float kh[8];
+                for (int c = 0; c < 8; ++c) kh[c] = kv[c] * G[c];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        float f = G[c];
+                for (int pp = 0; pp < 4; ++pp) {
+                    if (pp >= u) {
+                        if (pp > u) {
 #pragma unroll
-                        for (int w = u + 1; w <= pp; ++w) f *= dd[w][c];
-                        kh[c] = kv[c] * f;
+                            for (int c = 0; c < 8; ++c) kh[c] *= dd[pp][c];
+                        }
+                        *reinterpret_cast<uint4 *>(sm + SM_KH + sw_chunk(8 * pp * (pp + 1) + r, cc, 20480)) =
+                            pack_bf8(kh);
                     }
-                    *reinterpret_cast<uint4 *>(sm + SM_KH + sw_chunk(8 * pp * (pp + 1) + r, cc, 20480)) =
-                        pack_bf8(kh);
                 }
                 // Q0 = q e^{b}, K0 = k e^{b}, Kbar = k e^{b_L - b}
                 float q0[8], k0[8];
-                uint32_t kb[8];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     q0[c] = xq[c] * ep[c];
                     k0[c] = xk[c] * ep[c];
-                    kb[c] = to_tf32(kv[c] * G[c] * el[c]);
                 }
                 *reinterpret_cast<uint4 *>(sm + SM_Q0 + sw_chunk(r, cc, 8192)) = pack_bf8(q0);
                 *reinterpret_cast<uint4 *>(sm + SM_K0 + sw_chunk(r, cc, 8192)) = pack_bf8(k0);
-                // Kbar^T tf32 K-major il [i][s] (B of the dS product)
+                // Kbar^T tf32 K-major il [i][s] (B of the dS product).  A 4x4
+                // transpose inside each quad of lanes (4 consecutive rows) gives
+                // every lane 4 consecutive s for channels 2b, 2b+1: 16-byte stores.
+                {
+                    float kbv[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint32_t *>(sm + SM_KB + km_tf32(8 * cc + c, r, 2048)) = kb[c];
+                    for (int c = 0; c < 8; ++c) kbv[c] = kv[c] * G[c] * el[c];
+                    const int bq = rb & 3;
+                    float o0[4], o1[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        // send the pair for destination lane (bq - k) & 3, receive from (bq + k) & 3
+                        const int dst = (bq - k) & 3;
+                        const float s0 = dst == 0 ? kbv[0] : dst == 1 ? kbv[2] : dst == 2 ? kbv[4] : kbv[6];
+                        const float s1 = dst == 0 ? kbv[1] : dst == 1 ? kbv[3] : dst == 2 ? kbv[5] : kbv[7];
+                        const int srcl = (lane & ~3) | ((bq + k) & 3);
+                        const float r0 = __shfl_sync(0xffffffffu, s0, srcl);
+                        const float r1 = __shfl_sync(0xffffffffu, s1, srcl);
+                        const int srow = (bq + k) & 3;   // row offset of the received pair
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (e == srow) {
+                                o0[e] = r0;
+                                o1[e] = r1;
+                            }
+                        }
+                    }
+                    const int s0r = 16 * u + (rb & ~3);
+                    const int i0 = 8 * cc + 2 * bq;
+                    *reinterpret_cast<uint4 *>(sm + SM_KB + km_tf32(i0, s0r, 2048)) =
+                        make_uint4(to_tf32(o0[0]), to_tf32(o0[1]), to_tf32(o0[2]), to_tf32(o0[3]));
+                    *reinterpret_cast<uint4 *>(sm + SM_KB + km_tf32(i0 + 1, s0r, 2048)) =
+                        make_uint4(to_tf32(o1[0]), to_tf32(o1[1]), to_tf32(o1[2]), to_tf32(o1[3]));
+                }
             }
             // q_r . k_r partials: combine the two channel chunks of this warp
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float d2 = dqp[u] + __shfl_xor_sync(0xffffffffu, dqp[u], 16);
-                if (lane < 16) s_dqp[warp * 64 + 16 * u + rb] = d2;
+            for (int v = 0; v < 2; ++v) {
+                const float d2 = dqp[v] + __shfl_xor_sync(0xffffffffu, dqp[v], 16);
+                if (lane < 16) s_dqp[(warp & 7) * 64 + 16 * (2 * sp + v) + rb] = d2;
             }
         }
         fence_proxy_async_smem();
@@ -447,62 +524,45 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         tc_fence_after();
 
         // ===== E1: Gram epilogue -> A' (tf32) and M (fp32); diagonal dots ====
+        // lane = row (0..63 q rows, 64..127 k rows); quarter qt = columns s in [16qt, 16qt+16)
         float *Mm = reinterpret_cast<float *>(sm + SM_X);
-        if (warp < 4) {
-            const bool qside = t < 64;
-            const int r = t & 63;
+        {
+            const bool qside = ch < 64;
+            const int r = ch & 63;
             const int p = r >> 4;
-            const bool rvalid = r < Lc;
+            const int plo = (r >> 5) * 2;                      // sub-blocks of this warp's rows
+            const uint32_t col_lo = (uint32_t)min(8 * plo * (plo + 1) + 16 * qt, 144);
+            const uint32_t col_hi = (uint32_t)min(8 * (plo + 1) * (plo + 2) + 16 * qt, 144);
+            float va[16], vb[16];
+            tmem_ld16(tmem + lane_base + TM_G + col_lo, va);
+            tmem_ld16(tmem + lane_base + TM_G + col_hi, vb);
+            tmem_wait_ld();
+            const bool use_hi = p != plo;
+            const bool have = qt <= p && r < Lc;
             const float br = s_beta[r];
-            const int npass = (warp & 1) ? 2 : 1;
-            for (int pass = 0; pass < npass; ++pass) {
-                const int wb = (warp & 1) ? (pass == 0 ? 48 : 96) : 0;
-                float v[64];
-                {
-                    float a[32], b2[32];
-                    tmem_ld16(tmem + lane_base + TM_G + wb, *reinterpret_cast<float(*)[16]>(a));
-                    tmem_ld16(tmem + lane_base + TM_G + wb + 16, *reinterpret_cast<float(*)[16]>(a + 16));
-                    tmem_ld16(tmem + lane_base + TM_G + wb + 32, *reinterpret_cast<float(*)[16]>(b2));
-                    tmem_ld16(tmem + lane_base + TM_G + wb + 48, *reinterpret_cast<float(*)[16]>(b2 + 16));
-                    tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        v[c] = a[c];
-                        v[32 + c] = b2[c];
-                    }
+            for (int j = 0; j < 4; ++j) {
+                float x4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int s = 16 * qt + 4 * j + e;
+                    const float val = use_hi ? vb[4 * j + e] : va[4 * j + e];
+                    x4[e] = (have && s < r) ? val : 0.f;
                 }
-                const bool mine = (warp & 1) ? ((pass == 0) == (p == 2)) : true;
-                const bool off16 = !(warp & 1) && p == 1;     // column block starts at 16
-                if (mine) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        float x4[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int s = 4 * j + e;
-                            float val = 0.f;
-                            if (s + 16 < 64)
-                                val = off16 ? v[s + 16] : v[s];
-                            else
-                                val = off16 ? 0.f : v[s];
-                            x4[e] = (rvalid && s < r) ? val : 0.f;
-                        }
-                        if (qside) {
-                            *reinterpret_cast<uint4 *>(sm + SM_A + km_tf32(r, 4 * j, 2048)) =
-                                make_uint4(to_tf32(x4[0]), to_tf32(x4[1]), to_tf32(x4[2]), to_tf32(x4[3]));
-                        } else {
-                            *reinterpret_cast<float4 *>(Mm + r * MLD + 4 * j) =
-                                make_float4(br * x4[0], br * x4[1], br * x4[2], br * x4[3]);
-                        }
-                    }
+                if (qside) {
+                    *reinterpret_cast<uint4 *>(sm + SM_A + km_tf32(r, 16 * qt + 4 * j, 2048)) =
+                        make_uint4(to_tf32(x4[0]), to_tf32(x4[1]), to_tf32(x4[2]), to_tf32(x4[3]));
+                } else {
+                    *reinterpret_cast<float4 *>(Mm + r * MLD + 16 * qt + 4 * j) =
+                        make_float4(br * x4[0], br * x4[1], br * x4[2], br * x4[3]);
                 }
             }
-        } else if (t < 192) {
-            const int r = t - 128;
-            float acc = 0.f;
+            if (t < 64) {
+                float acc = 0.f;
 #pragma unroll
-            for (int w = 0; w < 8; ++w) acc += s_dqp[w * 64 + r];
-            s_dq[r] = acc;
+                for (int w = 0; w < 8; ++w) acc += s_dqp[w * 64 + t];
+                s_dq[t] = acc;
+            }
         }
         __syncthreads();
 
@@ -570,9 +630,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 }
                 __syncthreads();
             }
-            // T' bf16 K-major il [r][s]
-            for (int e = t; e < 512; e += NT) {
-                const int r = e >> 3, s0 = (e & 7) * 8;
+            // T' bf16 K-major il [r][s]: one 8-wide chunk per thread
+            {
+                const int r = t >> 3, s0 = (t & 7) * 8;
                 const float4 a = *reinterpret_cast<const float4 *>(Mm + r * MLD + s0);
                 const float4 b4 = *reinterpret_cast<const float4 *>(Mm + r * MLD + s0 + 4);
                 const float tv[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
@@ -605,21 +665,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 
         // ===== E2: W = D_W + beta K0 -> -W^T bf16 MN-major il [i][r] ========
         {
-            float wv[32];
-            tmem_ld32(tmem + lane_base + TM_W + 32 * half, wv);
+            float wv[16];
+            tmem_ld16(tmem + lane_base + TM_W + 16 * qt, wv);
+            tmem_wait_ld();
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
+            for (int c8 = 0; c8 < 2; ++c8) {
                 float w8[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const int r = 32 * half + 8 * c8 + u;
+                    const int r = 16 * qt + 8 * c8 + u;
                     w8[u] = -(wv[8 * c8 + u] + s_beta[r] * bf(sm + SM_K0 + sw_elem64(r, ch)));
                 }
-                *reinterpret_cast<uint4 *>(sm + SM_W + mn_bf16(ch, 32 * half + 8 * c8, 1024)) = pack_bf8(w8);
+                *reinterpret_cast<uint4 *>(sm + SM_W + mn_bf16(ch, 16 * qt + 8 * c8, 1024)) = pack_bf8(w8);
             }
         }
         fence_proxy_async_smem();
         sync_tc();
+
+        // Q0/K0 are consumed: fetch the next chunk's g and beta into that space
+        fetch_g(c0 + C);
 
         // ===== M3: U += S^T (-W^T) ===========================================
         if (t == 0) {
@@ -637,17 +701,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         tc_fence_after();
 
         // ===== E3: u = D_U + beta v; U^T tf32 -> SM_X ========================
-        float uv[32];
+        float uv[16];
         {
-            tmem_ld32(tmem + lane_base + TM_U + 32 * half, uv);
+            tmem_ld16(tmem + lane_base + TM_U + 16 * qt, uv);
+            tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const int r = 32 * half + k;
+            for (int k = 0; k < 16; ++k) {
+                const int r = 16 * qt + k;
                 uv[k] += s_beta[r] * bf(sm + SM_STG_V + sw_elem64(r, ch));
             }
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4)
-                *reinterpret_cast<uint4 *>(sm + SM_X + km_tf32(ch, 32 * half + 4 * c4, 2048)) =
+            for (int c4 = 0; c4 < 4; ++c4)
+                *reinterpret_cast<uint4 *>(sm + SM_X + km_tf32(ch, 16 * qt + 4 * c4, 2048)) =
                     make_uint4(to_tf32(uv[4 * c4 + 0]), to_tf32(uv[4 * c4 + 1]),
                                to_tf32(uv[4 * c4 + 2]), to_tf32(uv[4 * c4 + 3]));
         }
@@ -676,36 +741,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 
         // ===== E4: o = D_O + (q.k) u;  S = e^{b_L} S + dS (TMEM) and bf16 copy
         {
-            float ov[32];
-            tmem_ld32(tmem + lane_base + TM_O + 32 * half, ov);
+            float ov[16];
+            tmem_ld16(tmem + lane_base + TM_O + 16 * qt, ov);
+            float sv[32], dv[32];
+            tmem_ld32(tmem + lane_base + TM_S + 32 * qt, sv);     // waits for all loads
+            tmem_ld32(tmem + lane_base + TM_DS + 32 * qt, dv);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const int r = 32 * half + k;
+            for (int k = 0; k < 16; ++k) {
+                const int r = 16 * qt + k;
                 if (r < Lc) o[((size_t)(tok0 + c0 + r) * H + h) * kDV + ch] = ov[k] + s_dq[r] * uv[k];
             }
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                const uint32_t col = 64 * half + 32 * q2;
-                float sv[32], dv[32];
-                tmem_ld32(tmem + lane_base + TM_S + col, sv);
-                tmem_ld32(tmem + lane_base + TM_DS + col, dv);
+            for (int c = 0; c < 32; ++c) sv[c] = fmaf(s_gam[32 * qt + c], sv[c], dv[c]);
+            float a[16], b2[16];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) sv[c] = fmaf(s_gam[col + c], sv[c], dv[c]);
-                float a[16], b2[16];
+            for (int c = 0; c < 16; ++c) {
+                a[c] = sv[c];
+                b2[c] = sv[16 + c];
+            }
+            tmem_st16(tmem + lane_base + TM_S + 32 * qt, a);
+            tmem_st16(tmem + lane_base + TM_S + 32 * qt + 16, b2);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    a[c] = sv[c];
-                    b2[c] = sv[16 + c];
-                }
-                tmem_st16(tmem + lane_base + TM_S + col, a);
-                tmem_st16(tmem + lane_base + TM_S + col + 16, b2);
+            for (int c8 = 0; c8 < 4; ++c8) {
+                float x8[8];
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    float x8[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) x8[u] = sv[8 * c8 + u];
-                    *reinterpret_cast<uint4 *>(sm + SM_S + km_bf16(ch, col + 8 * c8, 2048)) = pack_bf8(x8);
-                }
+                for (int u = 0; u < 8; ++u) x8[u] = sv[8 * c8 + u];
+                *reinterpret_cast<uint4 *>(sm + SM_S + km_bf16(ch, 32 * qt + 8 * c8, 2048)) = pack_bf8(x8);
             }
             tmem_wait_st();
         }
@@ -713,24 +774,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         sync_tc();
     }
 
+    asm volatile("cp.async.wait_all;" ::: "memory");
     if (failed) {
         if (t == 0) atomicOr(&g_kda_device_error, 1u);
         // let any copies or MMAs in flight finish (bounded) before freeing TMEM
         mbar_wait(B.mma, mma_phase, kWaitLimit);
         mbar_wait(B.qk, (uint32_t)(nchunks & 1) ^ 1u, kWaitLimit);
         mbar_wait(B.v, (uint32_t)(nchunks & 1) ^ 1u, kWaitLimit);
+        mbar_wait(B.g, (uint32_t)(nchunks & 1) ^ 1u, kWaitLimit);
         __syncthreads();
     } else {
         // ---- final state: S_out[i][j] from the TMEM master (lane j, column i)
+        float sv[32];
+        tmem_ld32(tmem + lane_base + TM_S + 32 * qt, sv);
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-            float sv[32];
-            tmem_ld32(tmem + lane_base + TM_S + 64 * half + 32 * q2, sv);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const int i = 64 * half + 32 * q2 + c;
-                S_out[st_off + (size_t)i * kDV + ch] = sv[c];
-            }
+        for (int c = 0; c < 32; ++c) {
+            const int i = 32 * qt + c;
+            S_out[st_off + (size_t)i * kDV + ch] = sv[c];
         }
     }
     sync_tc();
@@ -765,21 +825,35 @@ bool make_map(CUtensorMap *m, const void *base, int64_t T, int H, uint32_t bw, b
     return r == CUDA_SUCCESS;
 }
 
+// 3D map over a [T, H, 128] fp32 tensor: dims (128, H, T), box (32, 1, 64), 128B swizzle.
+bool make_map_f32(CUtensorMap *m, const void *base, int64_t T, int H) {
+    auto enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {128 * 4, (cuuint64_t)H * 128 * 4};
+    cuuint32_t box[3] = {32, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
                               const float *beta, const float *S0, float *o, float *S_out,
                               const int32_t *cu_seqlens, int N, int64_t T, int H,
                               cudaStream_t stream) {
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mg;
     if (!make_map(&mq, q, T, H, 64, true) || !make_map(&mk, k, T, H, 64, true) ||
-        !make_map(&mv, v, T, H, 64, true))
+        !make_map(&mv, v, T, H, 64, true) || !make_map_f32(&mg, g, T, H))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     const long long blocks = (long long)N * H;
-    prefill_tc_kernel<<<(unsigned)blocks, NT, SMEM_ALLOC, stream>>>(mq, mk, mv, g, beta, S0, o, S_out,
+    prefill_tc_kernel<<<(unsigned)blocks, NT, SMEM_ALLOC, stream>>>(mq, mk, mv, mg, g, beta, S0, o, S_out,
                                                                     cu_seqlens, N, H);
     return cudaGetLastError();
 }
