@@ -569,26 +569,33 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         // ===== S1: T = (I + M)^-1 by 16-row blocks, in place; T' = (T-I)Diag(beta)
         {
             float *Yt = Mm + 64 * MLD;        // [3][16][16] temporaries
-            // column c of (I + M_pp)^-1: x = e_c, then for s = c..14,
-            // x[r] -= M[r][s] x[s] for r > s (x[s] is final once column s is applied)
-            float x[16];
-            if (t < 64) {
-                const int p = t >> 4, c = t & 15;
-                const float *Mb = Mm + (16 * p) * MLD + 16 * p;
+            // diagonal blocks (I + M_pp)^-1 by forward substitution across a
+            // 16-lane group: lane = row r, two right-hand sides (columns c0, c0+1)
+            // per thread; step s broadcasts x_s and every row r > s applies M_rs
+            {
+                const int r = t & 15;
+                const int grp = t >> 4;                 // 32 groups
+                const int p = grp >> 3, c0 = 2 * (grp & 7);
+                const float *Mr = Mm + (16 * p + r) * MLD + 16 * p;
+                float mr[16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
-#pragma unroll
-                for (int s = 0; s < 15; ++s) {
-                    const float xs = x[s];
-#pragma unroll
-                    for (int r = s + 1; r < 16; ++r) x[r] = fmaf(-Mb[r * MLD + s], xs, x[r]);
+                for (int j = 0; j < 4; ++j) {
+                    const float4 m4 = *reinterpret_cast<const float4 *>(Mr + 4 * j);
+                    mr[4 * j] = m4.x; mr[4 * j + 1] = m4.y; mr[4 * j + 2] = m4.z; mr[4 * j + 3] = m4.w;
                 }
-            }
-            __syncthreads();
-            if (t < 64) {
-                const int p = t >> 4, c = t & 15;
+                float x0 = (r == c0) ? 1.f : 0.f, x1 = (r == c0 + 1) ? 1.f : 0.f;
 #pragma unroll
-                for (int r = 0; r < 16; ++r) Mm[(16 * p + r) * MLD + 16 * p + c] = x[r];
+                for (int s2 = 0; s2 < 15; ++s2) {
+                    const float b0 = __shfl_sync(0xffffffffu, x0, s2, 16);
+                    const float b1 = __shfl_sync(0xffffffffu, x1, s2, 16);
+                    if (r > s2) {
+                        x0 = fmaf(-mr[s2], b0, x0);
+                        x1 = fmaf(-mr[s2], b1, x1);
+                    }
+                }
+                __syncthreads();
+                Mm[(16 * p + r) * MLD + 16 * p + c0] = x0;
+                Mm[(16 * p + r) * MLD + 16 * p + c0 + 1] = x1;
             }
             __syncthreads();
 #pragma unroll
@@ -743,30 +750,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         {
             float ov[16];
             tmem_ld16(tmem + lane_base + TM_O + 16 * qt, ov);
-            float sv[32], dv[32];
-            tmem_ld32(tmem + lane_base + TM_S + 32 * qt, sv);     // waits for all loads
-            tmem_ld32(tmem + lane_base + TM_DS + 32 * qt, dv);
+            tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 const int r = 16 * qt + k;
                 if (r < Lc) o[((size_t)(tok0 + c0 + r) * H + h) * kDV + ch] = ov[k] + s_dq[r] * uv[k];
             }
 #pragma unroll
-            for (int c = 0; c < 32; ++c) sv[c] = fmaf(s_gam[32 * qt + c], sv[c], dv[c]);
-            float a[16], b2[16];
+            for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t col = 32 * qt + 16 * hh;
+                float sv[16], dv[16];
+                tmem_ld16(tmem + lane_base + TM_S + col, sv);
+                tmem_ld16(tmem + lane_base + TM_DS + col, dv);
+                tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                a[c] = sv[c];
-                b2[c] = sv[16 + c];
-            }
-            tmem_st16(tmem + lane_base + TM_S + 32 * qt, a);
-            tmem_st16(tmem + lane_base + TM_S + 32 * qt + 16, b2);
+                for (int c = 0; c < 16; ++c) sv[c] = fmaf(s_gam[col + c], sv[c], dv[c]);
+                tmem_st16(tmem + lane_base + TM_S + col, sv);
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-                float x8[8];
+                for (int c8 = 0; c8 < 2; ++c8) {
+                    float x8[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) x8[u] = sv[8 * c8 + u];
-                *reinterpret_cast<uint4 *>(sm + SM_S + km_bf16(ch, 32 * qt + 8 * c8, 2048)) = pack_bf8(x8);
+                    for (int u = 0; u < 8; ++u) x8[u] = sv[8 * c8 + u];
+                    *reinterpret_cast<uint4 *>(sm + SM_S + km_bf16(ch, col + 8 * c8, 2048)) = pack_bf8(x8);
+                }
             }
             tmem_wait_st();
         }
