@@ -56,6 +56,24 @@ DECODE_BYTES_PER_STATE = 2 * STATE_BYTES + 3 * 256 + 512 + 4 + 512
 FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12   # fp32 FMA lanes x 2 flop x max SM clock
 
 
+def _traffic(kernel, source_file):
+    """DRAM bytes per launch from profiles/dram_traffic.md, if that capture was
+    taken on the current kernel source (sha256 prefix), else None."""
+    import hashlib
+    try:
+        src = os.path.join(ROOT, "kda_linear_attention_gb300", "csrc", source_file)
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(os.path.join(ROOT, "profiles", "dram_traffic.md")):
+            f = line.split()
+            if len(f) >= 4 and f[0] == "traffic:" and f[1] == kernel:
+                kv = dict(x.split("=", 1) for x in f[2:] if "=" in x)
+                if kv.get("sha256") == sha:
+                    return int(kv["bytes"])
+    except Exception:
+        pass
+    return None
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -239,7 +257,8 @@ def run_ours(args):
         roofline = {
             "kernel": "prefill_tc_kernel (tcgen05/TMEM/TMA chunked prefill)",
             "bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm"],
-            "unit": "GB/s", "frac": round(hbm_frac, 4), "of": peaks["source"], "traffic": None,
+            "unit": "GB/s", "frac": round(hbm_frac, 4), "of": peaks["source"],
+            "traffic": _traffic("prefill_tc_kernel", "kda_prefill_tc.cu") if wl == "prefill_4k" else None,
         }
     else:
         roofline = {
@@ -331,7 +350,8 @@ def _decode_leg(kda, torch, dev, stream, peaks, args):
         "roofline": {"kernel": "kda_decode", "bound": "hbm", "achieved": round(gbs_all, 1),
                      "peak": peaks["hbm"], "unit": "GB/s",
                      "frac": round(gbs_all / peaks["hbm"], 4), "of": peaks["source"],
-                     "frac_of_nominal_8tbs": round(gbs_all / 8000.0, 4), "traffic": None,
+                     "frac_of_nominal_8tbs": round(gbs_all / 8000.0, 4),
+                     "traffic": _traffic("decode_kernel", "kda_decode.cu"),
                      "algorithmic_bytes": int(all_bytes)},
         "gpu_launches": n_steps,
     }
