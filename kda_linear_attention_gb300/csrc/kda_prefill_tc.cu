@@ -60,7 +60,7 @@ constexpr uint32_t SM_STG_V = 32768;      // v chunk: same = V^T, MN-major opera
 constexpr uint32_t SM_X = 49152;          // 32 KB: Gram A [128][128] K-major sw | M fp32 [64][68] + solve temps | U^T tf32 K-major il
 constexpr uint32_t SM_KH = 81920;         // 40 KB: Gram B Khat [160][128] K-major sw | A' (16K) + -W^T (16K) + T' (8K)
 constexpr uint32_t SM_A = SM_KH;          //   A' tf32 K-major il [r][s], 16 KB
-constexpr uint32_t SM_W = SM_KH + 16384;  //   -W^T bf16 MN-major il [i][r], 16 KB
+constexpr uint32_t SM_TB = SM_KH + 16384; //   -T Diag(beta) tf32 K-major il [r][s], 16 KB
 constexpr uint32_t SM_T = SM_KH + 32768;  //   T' bf16 K-major il [r][s], 8 KB
 constexpr uint32_t SM_Q0 = 122880;        // 16 KB: Q0 [64][128] K-major sw (with K0: next chunk's g, cp.async)
 constexpr uint32_t SM_K0 = 139264;        // 16 KB: K0 [64 s][128 i] MN-major sw (A of the W product)
@@ -87,7 +87,7 @@ constexpr int MLD = 68;                   // row stride (floats) of M / T
 constexpr uint32_t TM_S = 0;      // S^T master fp32 (lane j, column i), 128 cols
 constexpr uint32_t TM_DS = 128;   // (Kbar^T U)^T, 128 cols
 constexpr uint32_t TM_G = 256;    // Gram D, 160 cols
-constexpr uint32_t TM_W = 256;    // W D, 64 cols (after the Gram epilogue)
+constexpr uint32_t TM_P = 128;    // (K0 S)^T, 64 cols inside TM_DS (M1 -> M2)
 constexpr uint32_t TM_U = 320;    // U D, 64 cols (after the Gram epilogue)
 constexpr uint32_t TM_O = 448;    // O D, 64 cols
 
@@ -498,6 +498,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         sync_tc();
 
         // ===== M1: Gram (X Khat^T) and O1 = S^T Q0^T ========================
+        // The three independent accumulators are issued interleaved so that
+        // consecutive MMAs do not wait on one another.
         if (t == 0) {
             const uint32_t idg = instr_desc(kFmtBF16, 128, 160, 0, 0);
             const uint32_t ido = instr_desc(kFmtBF16, 128, 64, 0, 0);
@@ -506,14 +508,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const uint32_t ko = (uint32_t)(kk >> 2), kb2 = (uint32_t)(kk & 3) * 32u;
                 const uint64_t ax = smem_desc(smem_u32(sm + SM_X + ko * 16384 + kb2), 16, 1024, kSwizzle128B);
                 const uint64_t bk = smem_desc(smem_u32(sm + SM_KH + ko * 20480 + kb2), 16, 1024, kSwizzle128B);
-                mma_bf16_ss(tmem + TM_G, ax, bk, idg, kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t ko = (uint32_t)(kk >> 2), kb2 = (uint32_t)(kk & 3) * 32u;
                 const uint64_t as = smem_desc(smem_u32(sm + SM_S + 256 * kk), 128, 2048, kSwizzleNone);
                 const uint64_t bq = smem_desc(smem_u32(sm + SM_Q0 + ko * 8192 + kb2), 16, 1024, kSwizzle128B);
+                const uint64_t bk0 = smem_desc(smem_u32(sm + SM_K0 + ko * 8192 + kb2), 16, 1024, kSwizzle128B);
+                mma_bf16_ss(tmem + TM_G, ax, bk, idg, kk > 0);
                 mma_bf16_ss(tmem + TM_O, as, bq, ido, kk > 0);
+                // P^T = S^T K0^T (the W S product, with W = T Diag(beta) K0 applied in M2)
+                mma_bf16_ss(tmem + TM_P, as, bk0, ido, kk > 0);
             }
             mma_commit(B.mma);
             // q/k staging is consumed: load the next chunk's q and k
@@ -522,6 +523,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (!wait_all(B.mma, mma_phase)) { failed = true; break; }
         mma_phase ^= 1;
         tc_fence_after();
+        // Q0/K0 are consumed: fetch the next chunk's g and beta into that space
+        fetch_g(c0 + C);
 
         // ===== E1: Gram epilogue -> A' (tf32) and M (fp32); diagonal dots ====
         // lane = row (0..63 q rows, 64..127 k rows); quarter qt = columns s in [16qt, 16qt+16)
@@ -637,69 +640,46 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 }
                 __syncthreads();
             }
-            // T' bf16 K-major il [r][s]: one 8-wide chunk per thread
+            // T' = (T - I) Diag(beta), bf16 K-major il [r][s] (B of U~ = T' V), and
+            // -T Diag(beta), tf32 K-major il [r][s] (B of the W S term): one
+            // 8-wide chunk of row r per thread
             {
                 const int r = t >> 3, s0 = (t & 7) * 8;
                 const float4 a = *reinterpret_cast<const float4 *>(Mm + r * MLD + s0);
                 const float4 b4 = *reinterpret_cast<const float4 *>(Mm + r * MLD + s0 + 4);
                 const float tv[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
                 float w8[8];
+                uint32_t tb[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) w8[u] = (s0 + u < r) ? tv[u] * s_beta[s0 + u] : 0.f;
+                for (int u = 0; u < 8; ++u) {
+                    const int s3 = s0 + u;
+                    const float bs = s_beta[s3];
+                    w8[u] = (s3 < r) ? tv[u] * bs : 0.f;
+                    tb[u] = to_tf32(s3 < r ? -tv[u] * bs : (s3 == r ? -bs : 0.f));
+                }
                 *reinterpret_cast<uint4 *>(sm + SM_T + km_bf16(r, s0, 1024)) = pack_bf8(w8);
+                *reinterpret_cast<uint4 *>(sm + SM_TB + km_tf32(r, s0, 2048)) = make_uint4(tb[0], tb[1], tb[2], tb[3]);
+                *reinterpret_cast<uint4 *>(sm + SM_TB + km_tf32(r, s0 + 4, 2048)) = make_uint4(tb[4], tb[5], tb[6], tb[7]);
             }
         }
         fence_proxy_async_smem();
         sync_tc();
 
-        // ===== M2: W = T' K0 (as (T'K0)^T) and U~ = T' V ====================
+        // ===== M2: U = T' V - (T Diag(beta)) (K0 S)  (transposed) ============
         if (!wait_all(B.v, par)) { failed = true; break; }
         if (t == 0) {
-            const uint32_t idmn = instr_desc(kFmtBF16, 128, 64, 1, 0);
+            const uint32_t idv = instr_desc(kFmtBF16, 128, 64, 1, 0);
+            const uint32_t idp = instr_desc(kFmtTF32, 128, 64, 0, 0);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t bd = smem_desc(smem_u32(sm + SM_T + 256 * kk), 128, 1024, kSwizzleNone);
-                const uint64_t aw = smem_desc(smem_u32(sm + SM_K0 + 2048 * kk), 8192, 1024, kSwizzle128B);
                 const uint64_t av = smem_desc(smem_u32(sm + SM_STG_V + 2048 * kk), 8192, 1024, kSwizzle128B);
-                mma_bf16_ss(tmem + TM_W, aw, bd, idmn, kk > 0);
-                mma_bf16_ss(tmem + TM_U, av, bd, idmn, kk > 0);
+                mma_bf16_ss(tmem + TM_U, av, bd, idv, kk > 0);
             }
-            mma_commit(B.mma);
-        }
-        if (!wait_all(B.mma, mma_phase)) { failed = true; break; }
-        mma_phase ^= 1;
-        tc_fence_after();
-
-        // ===== E2: W = D_W + beta K0 -> -W^T bf16 MN-major il [i][r] ========
-        {
-            float wv[16];
-            tmem_ld16(tmem + lane_base + TM_W + 16 * qt, wv);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c8 = 0; c8 < 2; ++c8) {
-                float w8[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int r = 16 * qt + 8 * c8 + u;
-                    w8[u] = -(wv[8 * c8 + u] + s_beta[r] * bf(sm + SM_K0 + sw_elem64(r, ch)));
-                }
-                *reinterpret_cast<uint4 *>(sm + SM_W + mn_bf16(ch, 16 * qt + 8 * c8, 1024)) = pack_bf8(w8);
-            }
-        }
-        fence_proxy_async_smem();
-        sync_tc();
-
-        // Q0/K0 are consumed: fetch the next chunk's g and beta into that space
-        fetch_g(c0 + C);
-
-        // ===== M3: U += S^T (-W^T) ===========================================
-        if (t == 0) {
-            const uint32_t idu = instr_desc(kFmtBF16, 128, 64, 0, 1);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t as = smem_desc(smem_u32(sm + SM_S + 256 * kk), 128, 2048, kSwizzleNone);
-                const uint64_t bw = smem_desc(smem_u32(sm + SM_W + 2048 * kk), 1024, 128, kSwizzleNone);
-                mma_bf16_ss(tmem + TM_U, as, bw, idu, 1);
+                const uint64_t bt = smem_desc(smem_u32(sm + SM_TB + 256 * kk), 128, 2048, kSwizzleNone);
+                mma_tf32_ts(tmem + TM_U, tmem + TM_P + 8 * kk, bt, idp, 1);
             }
             mma_commit(B.mma);
         }
@@ -707,26 +687,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         mma_phase ^= 1;
         tc_fence_after();
 
-        // ===== E3: u = D_U + beta v; U^T tf32 -> SM_X ========================
+        // ===== E3: u = D_U + beta v, rounded to tf32 in place in TMEM ========
         float uv[16];
         {
             tmem_ld16(tmem + lane_base + TM_U + 16 * qt, uv);
             tmem_wait_ld();
+            float ut[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 const int r = 16 * qt + k;
                 uv[k] += s_beta[r] * bf(sm + SM_STG_V + sw_elem64(r, ch));
+                ut[k] = __uint_as_float(to_tf32(uv[k]));
             }
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
-                *reinterpret_cast<uint4 *>(sm + SM_X + km_tf32(ch, 16 * qt + 4 * c4, 2048)) =
-                    make_uint4(to_tf32(uv[4 * c4 + 0]), to_tf32(uv[4 * c4 + 1]),
-                               to_tf32(uv[4 * c4 + 2]), to_tf32(uv[4 * c4 + 3]));
+            tmem_st16(tmem + lane_base + TM_U + 16 * qt, ut);
+            tmem_wait_st();
         }
-        fence_proxy_async_smem();
         sync_tc();
 
-        // ===== M4: O += U^T A'^T (tf32);  dS = U^T Kbar (tf32) ================
+        // ===== M4: O += U^T A'^T;  dS = U^T Kbar (tf32, U^T read from TMEM) ===
         if (t == 0) {
             // v staging is consumed: load the next chunk's v
             if (ci + 1 < nchunks) issue_load_v(sm, &map_v, B.v, h, tok0 + c0 + C);
@@ -734,11 +712,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             const uint32_t ids = instr_desc(kFmtTF32, 128, 128, 0, 0);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t au = smem_desc(smem_u32(sm + SM_X + 256 * kk), 128, 2048, kSwizzleNone);
                 const uint64_t ba = smem_desc(smem_u32(sm + SM_A + 256 * kk), 128, 2048, kSwizzleNone);
                 const uint64_t bk = smem_desc(smem_u32(sm + SM_KB + 256 * kk), 128, 2048, kSwizzleNone);
-                mma_tf32_ss(tmem + TM_O, au, ba, ido, 1);
-                mma_tf32_ss(tmem + TM_DS, au, bk, ids, kk > 0);
+                mma_tf32_ts(tmem + TM_O, tmem + TM_U + 8 * kk, ba, ido, 1);
+                mma_tf32_ts(tmem + TM_DS, tmem + TM_U + 8 * kk, bk, ids, kk > 0);
             }
             mma_commit(B.mma);
         }
