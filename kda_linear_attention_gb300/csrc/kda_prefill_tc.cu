@@ -69,18 +69,19 @@ constexpr uint32_t SM_S = 188416;         // 32 KB: S^T bf16 K-major il [j][i]
 constexpr uint32_t SM_MISC = 221184;
 constexpr uint32_t MISC_BETA = 0;         // float[64]
 constexpr uint32_t MISC_GAM = 256;        // float[128]  e^{b_L}
-constexpr uint32_t MISC_DQ = 768;         // float[64]   q_r . k_r
-constexpr uint32_t MISC_DQP = 1024;       // float[8][64] partial dot products
-constexpr uint32_t MISC_TOT = 3072;       // float[128]  prefix total through row 31
-constexpr uint32_t MISC_SIG = 3584;       // float[4][128] sigma_p
-constexpr uint32_t MISC_BL = 5632;        // float[128]  b_L
-constexpr uint32_t MISC_DD = 6144;        // float[4][128] per-channel decay factors
-constexpr uint32_t MISC_BETAN = 8192;     // float[64]   next chunk's beta (cp.async)
-constexpr uint32_t MISC_BAR = 8448;       // 4 x u64 mbarriers
-constexpr uint32_t MISC_TMEM = 8480;      // u32 TMEM base
-constexpr uint32_t SMEM_USED = SM_MISC + 8496;
-static_assert(MISC_BAR + 32 <= MISC_TMEM, "mbarrier slots");
+constexpr uint32_t MISC_DQ = 768;         // float[64]   q_r . k_r (shared-memory atomics)
+constexpr uint32_t MISC_TOT = 1024;       // float[128]  prefix total through row 31
+constexpr uint32_t MISC_SIG = 1536;       // float[4][128] sigma_p
+constexpr uint32_t MISC_DD = 3584;        // float[4][128] per-channel decay factors
+constexpr uint32_t MISC_BETAN = 5632;     // float[64]   next chunk's beta (cp.async)
+constexpr uint32_t MISC_EP = 5888;        // float[4][128] e^{sigma_u}
+constexpr uint32_t MISC_EL = 7936;        // float[4][128] e^{b_L - sigma_u}
+constexpr uint32_t MISC_BAR = 9984;       // 4 x u64 mbarriers
+constexpr uint32_t MISC_TMEM = 10016;     // u32 TMEM base
+constexpr uint32_t SMEM_USED = SM_MISC + 10032;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;   // alignment slack
+static_assert(MISC_BAR + 32 <= MISC_TMEM, "mbarrier slots");
+static_assert(SMEM_ALLOC <= 232448, "dynamic shared memory limit (227 KB)");
 constexpr int MLD = 68;                   // row stride (floats) of M / T
 
 // TMEM columns (512 allocated)
@@ -196,11 +197,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     float *s_beta = reinterpret_cast<float *>(sm + SM_MISC + MISC_BETA);
     float *s_gam = reinterpret_cast<float *>(sm + SM_MISC + MISC_GAM);
     float *s_dq = reinterpret_cast<float *>(sm + SM_MISC + MISC_DQ);
-    float *s_dqp = reinterpret_cast<float *>(sm + SM_MISC + MISC_DQP);
     float *s_tot = reinterpret_cast<float *>(sm + SM_MISC + MISC_TOT);
     float *s_sig = reinterpret_cast<float *>(sm + SM_MISC + MISC_SIG);
-    float *s_bl = reinterpret_cast<float *>(sm + SM_MISC + MISC_BL);
     float *s_dd = reinterpret_cast<float *>(sm + SM_MISC + MISC_DD);
+    float *s_ep = reinterpret_cast<float *>(sm + SM_MISC + MISC_EP);
+    float *s_el = reinterpret_cast<float *>(sm + SM_MISC + MISC_EL);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM_MISC + MISC_BAR);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SM_MISC + MISC_TMEM);
     __shared__ int s_seq;
@@ -336,7 +337,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 #pragma unroll
                 for (int c = 0; c < 8; ++c) s_tot[8 * cc + c] = b[1][c];
             }
-            if (t < C) s_beta[t] = (t < Lc) ? betan : 0.f;
+            if (t < C) {
+                s_beta[t] = (t < Lc) ? betan : 0.f;
+                s_dq[t] = 0.f;
+            }
             __syncthreads();
             if (sp == 1) {
 #pragma unroll
@@ -357,11 +361,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     for (int c = 0; c < 8; ++c) s_sig[p * 128 + 8 * cc + c] = v ? b[1][c] : b[0][c];
                 }
             }
-            if ((last >> 5) == sp && (last & 15) == rb) {
-                const int v = (last >> 4) & 1;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) s_bl[8 * cc + c] = v ? b[1][c] : b[0][c];
-            }
             __syncthreads();
             // per-channel factors: d0 = e^{sigma_0}, dw = e^{sigma_w - sigma_{w-1}};
             // gamma = e^{b_L} = d0 d1 d2 d3 (sigma_3 = b_L)
@@ -372,7 +371,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 s_dd[128 + t] = d1;
                 s_dd[256 + t] = d2;
                 s_dd[384 + t] = d3;
-                s_gam[t] = d0 * d1 * d2 * d3;
+                // e^{sigma_u} (prefix products) and e^{b_L - sigma_u} (suffix products)
+                const float e1 = d0 * d1, e2 = e1 * d2, e3 = e2 * d3;
+                s_ep[t] = d0;
+                s_ep[128 + t] = e1;
+                s_ep[256 + t] = e2;
+                s_ep[384 + t] = e3;
+                const float l2 = d3, l1 = d2 * d3, l0 = d1 * l1;
+                s_el[t] = l0;
+                s_el[128 + t] = l1;
+                s_el[256 + t] = l2;
+                s_el[384 + t] = 1.f;
+                s_gam[t] = e3;
             }
             // F = e^{b - sigma_u} in [1, e^75] for valid rows
 #pragma unroll
@@ -405,24 +415,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 unpack_bf8(*reinterpret_cast<const uint4 *>(sm + SM_STG_Q + sw_chunk(r, cc, 8192)), qv);
                 unpack_bf8(*reinterpret_cast<const uint4 *>(sm + SM_STG_K + sw_chunk(r, cc, 8192)), kv);
                 float G[8], xq[8], xk[8], ep[8], el[8];
+                {
+                    const float4 e0 = *reinterpret_cast<const float4 *>(s_ep + u * 128 + 8 * cc);
+                    const float4 e1 = *reinterpret_cast<const float4 *>(s_ep + u * 128 + 8 * cc + 4);
+                    const float4 l0 = *reinterpret_cast<const float4 *>(s_el + u * 128 + 8 * cc);
+                    const float4 l1 = *reinterpret_cast<const float4 *>(s_el + u * 128 + 8 * cc + 4);
+                    ep[0] = e0.x; ep[1] = e0.y; ep[2] = e0.z; ep[3] = e0.w;
+                    ep[4] = e1.x; ep[5] = e1.y; ep[6] = e1.z; ep[7] = e1.w;
+                    el[0] = l0.x; el[1] = l0.y; el[2] = l0.z; el[3] = l0.w;
+                    el[4] = l1.x; el[5] = l1.y; el[6] = l1.z; el[7] = l1.w;
+                }
                 float dot = 0.f;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     dot = fmaf(qv[c], kv[c], dot);
                     const float F = b[v][c];
-                    G[c] = (F > 0.f) ? __frcp_rn(F) : 0.f;                     // (0, 1]
+                    G[c] = (F > 0.f) ? __fdividef(1.f, F) : 0.f;               // (0, 1]
                     xq[c] = qv[c] * F;
                     xk[c] = kv[c] * F;
-                    // e^{sigma_u} and e^{b_L - sigma_u} from the per-channel factors
-                    float e = dd[0][c];
-                    float l = 1.f;
-#pragma unroll
-                    for (int w = 1; w < 4; ++w) {
-                        if (w <= u) e *= dd[w][c];
-                        else l *= dd[w][c];
-                    }
-                    ep[c] = e;
-                    el[c] = l;
                 }
                 dqp[v] = (r < Lc) ? dot : 0.f;
                 // Gram A operand: q rows 0..63, k rows 64..127
@@ -487,11 +497,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                         make_uint4(to_tf32(o1[0]), to_tf32(o1[1]), to_tf32(o1[2]), to_tf32(o1[3]));
                 }
             }
-            // q_r . k_r partials: combine the two channel chunks of this warp
+            // q_r . k_r: combine the two channel chunks of this warp, then
+            // accumulate the eight warps of this row half in shared memory
 #pragma unroll
             for (int v = 0; v < 2; ++v) {
                 const float d2 = dqp[v] + __shfl_xor_sync(0xffffffffu, dqp[v], 16);
-                if (lane < 16) s_dqp[(warp & 7) * 64 + 16 * (2 * sp + v) + rb] = d2;
+                if (lane < 16) atomicAdd(s_dq + 16 * (2 * sp + v) + rb, d2);
             }
         }
         fence_proxy_async_smem();
@@ -559,12 +570,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     *reinterpret_cast<float4 *>(Mm + r * MLD + 16 * qt + 4 * j) =
                         make_float4(br * x4[0], br * x4[1], br * x4[2], br * x4[3]);
                 }
-            }
-            if (t < 64) {
-                float acc = 0.f;
-#pragma unroll
-                for (int w = 0; w < 8; ++w) acc += s_dqp[w * 64 + t];
-                s_dq[t] = acc;
             }
         }
         __syncthreads();
