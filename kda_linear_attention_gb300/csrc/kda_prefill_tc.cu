@@ -70,15 +70,14 @@ constexpr uint32_t SM_MISC = 221184;
 constexpr uint32_t MISC_BETA = 0;         // float[64]
 constexpr uint32_t MISC_GAM = 256;        // float[128]  e^{b_L}
 constexpr uint32_t MISC_DQ = 768;         // float[64]   q_r . k_r (shared-memory atomics)
-constexpr uint32_t MISC_TOT = 1024;       // float[128]  prefix total through row 31
-constexpr uint32_t MISC_SIG = 1536;       // float[4][128] sigma_p
-constexpr uint32_t MISC_DD = 3584;        // float[4][128] per-channel decay factors
-constexpr uint32_t MISC_BETAN = 5632;     // float[64]   next chunk's beta (cp.async)
-constexpr uint32_t MISC_EP = 5888;        // float[4][128] e^{sigma_u}
-constexpr uint32_t MISC_EL = 7936;        // float[4][128] e^{b_L - sigma_u}
-constexpr uint32_t MISC_BAR = 9984;       // 4 x u64 mbarriers
-constexpr uint32_t MISC_TMEM = 10016;     // u32 TMEM base
-constexpr uint32_t SMEM_USED = SM_MISC + 10032;
+constexpr uint32_t MISC_TOT = 1024;       // float[4][128] sub-block totals, then carry - sigma_u
+constexpr uint32_t MISC_SIG = 3072;       // float[4][128] local prefix at sub-block ends, then e^{b_L - sigma_u}
+constexpr uint32_t MISC_DD = 5120;        // float[4][128] per-channel decay factors
+constexpr uint32_t MISC_BETAN = 7168;     // float[64]   next chunk's beta (cp.async)
+constexpr uint32_t MISC_EP = 7424;        // float[4][128] e^{sigma_u}
+constexpr uint32_t MISC_BAR = 9472;       // 4 x u64 mbarriers
+constexpr uint32_t MISC_TMEM = 9504;      // u32 TMEM base
+constexpr uint32_t SMEM_USED = SM_MISC + 9520;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;   // alignment slack
 static_assert(MISC_BAR + 32 <= MISC_TMEM, "mbarrier slots");
 static_assert(SMEM_ALLOC <= 232448, "dynamic shared memory limit (227 KB)");
@@ -201,7 +200,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     float *s_sig = reinterpret_cast<float *>(sm + SM_MISC + MISC_SIG);
     float *s_dd = reinterpret_cast<float *>(sm + SM_MISC + MISC_DD);
     float *s_ep = reinterpret_cast<float *>(sm + SM_MISC + MISC_EP);
-    float *s_el = reinterpret_cast<float *>(sm + SM_MISC + MISC_EL);
+    float *s_el = s_sig;             // reused once sigma is folded into the carries
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM_MISC + MISC_BAR);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SM_MISC + MISC_TMEM);
     __shared__ int s_seq;
@@ -303,99 +302,90 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         {
             asm volatile("cp.async.wait_all;" ::: "memory");
             if (!wait_all(B.g, par)) { failed = true; break; }
-            float gn[2][8];
-#pragma unroll
-            for (int v = 0; v < 2; ++v) {
-                // element (row, c) of the g tile: box c/32, 128-byte rows, 16-byte chunks swizzled
-                const int r = 16 * (2 * sp + v) + rb;
-                const uint8_t *rowp = sm + SM_Q0 + 8192 * (cc >> 2) + r * 128;
-                const int c4 = 2 * (cc & 3);
-                const float4 a = *reinterpret_cast<const float4 *>(rowp + ((c4 ^ (r & 7)) << 4));
-                const float4 b4 = *reinterpret_cast<const float4 *>(rowp + (((c4 + 1) ^ (r & 7)) << 4));
-                gn[v][0] = a.x; gn[v][1] = a.y; gn[v][2] = a.z; gn[v][3] = a.w;
-                gn[v][4] = b4.x; gn[v][5] = b4.y; gn[v][6] = b4.z; gn[v][7] = b4.w;
-            }
             const float betan = (t < C) ? s_betan[t] : 0.f;
-            // inclusive prefix: in-warp scan over each 16-row sub-block, then
-            // carries from sub-block 2sp to 2sp+1 (shuffle) and across warps (smem)
-            float b[2][8];
+            // column scan in place in the g tile: thread = (channel i, sub-block u);
+            // element (r, c) of the tile: box c/32, 128-byte rows, swizzled chunks
+            auto g_at = [&](int r, int c) -> float * {
+                return reinterpret_cast<float *>(sm + SM_Q0 + 8192 * (c >> 5) + r * 128 +
+                                                 ((((c & 31) >> 2) ^ (r & 7)) << 4) + (c & 3) * 4);
+            };
+            {
+                const int i = t & 127, u = t >> 7;
+                float acc = 0.f, at_last = 0.f;
+                const int lastrow = min(16 * u + 15, Lc - 1);
 #pragma unroll
-            for (int v = 0; v < 2; ++v)
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    float x = (16 * (2 * sp + v) + rb < Lc) ? gn[v][c] : 0.f;
-#pragma unroll
-                    for (int d = 1; d < 16; d <<= 1) {
-                        const float y = __shfl_up_sync(0xffffffffu, x, d, 16);
-                        if (rb >= d) x += y;
-                    }
-                    b[v][c] = x;
+                for (int rr = 0; rr < 16; ++rr) {
+                    const int r = 16 * u + rr;
+                    float *pg = g_at(r, i);
+                    acc += (r < Lc) ? *pg : 0.f;
+                    *pg = acc;                             // local (sub-block) prefix
+                    if (r == lastrow) at_last = acc;
                 }
-#pragma unroll
-            for (int c = 0; c < 8; ++c) b[1][c] += __shfl_sync(0xffffffffu, b[0][c], 15, 16);
-            if (sp == 0 && rb == 15) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) s_tot[8 * cc + c] = b[1][c];
+                s_tot[u * 128 + i] = acc;                  // sub-block total
+                s_sig[u * 128 + i] = at_last;              // local prefix at its last valid row
             }
             if (t < C) {
                 s_beta[t] = (t < Lc) ? betan : 0.f;
                 s_dq[t] = 0.f;
             }
             __syncthreads();
-            if (sp == 1) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const float base = s_tot[8 * cc + c];
-                    b[0][c] += base;
-                    b[1][c] += base;
-                }
-            }
-            // sigma_p = b at the last valid row of sub-block p; b_L = b at row Lc-1
-            const int last = Lc - 1;
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const int rr = min(16 * p + 15, last);
-                if ((rr >> 5) == sp && (rr & 15) == rb) {
-                    const int v = (rr >> 4) & 1;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) s_sig[p * 128 + 8 * cc + c] = v ? b[1][c] : b[0][c];
-                }
-            }
-            __syncthreads();
-            // per-channel factors: d0 = e^{sigma_0}, dw = e^{sigma_w - sigma_{w-1}};
-            // gamma = e^{b_L} = d0 d1 d2 d3 (sigma_3 = b_L)
+            // per channel: carries, sigma_u = b at the last valid row of sub-block u,
+            // d0 = e^{sigma_0}, dw = e^{sigma_w - sigma_{w-1}}, e^{sigma_u}, e^{b_L - sigma_u}
             if (t < 128) {
-                const float s0 = s_sig[t], s1 = s_sig[128 + t], s2 = s_sig[256 + t], s3 = s_sig[384 + t];
-                const float d0 = __expf(s0), d1 = __expf(s1 - s0), d2 = __expf(s2 - s1), d3 = __expf(s3 - s2);
+                const int lu = (Lc - 1) >> 4;
+                float base[4], sg[4];
+                float run = 0.f;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    base[u] = run;
+                    run += s_tot[u * 128 + t];
+                }
+                float bL = 0.f;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (u == lu) bL = base[u] + s_sig[u * 128 + t];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) sg[u] = (u <= lu) ? base[u] + s_sig[u * 128 + t] : bL;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) s_tot[u * 128 + t] = base[u] - sg[u];   // carry - sigma_u
+                const float d0 = __expf(sg[0]), d1 = __expf(sg[1] - sg[0]), d2 = __expf(sg[2] - sg[1]),
+                            d3 = __expf(sg[3] - sg[2]);
                 s_dd[t] = d0;
                 s_dd[128 + t] = d1;
                 s_dd[256 + t] = d2;
                 s_dd[384 + t] = d3;
-                // e^{sigma_u} (prefix products) and e^{b_L - sigma_u} (suffix products)
                 const float e1 = d0 * d1, e2 = e1 * d2, e3 = e2 * d3;
                 s_ep[t] = d0;
                 s_ep[128 + t] = e1;
                 s_ep[256 + t] = e2;
                 s_ep[384 + t] = e3;
                 const float l2 = d3, l1 = d2 * d3, l0 = d1 * l1;
-                s_el[t] = l0;
+                s_el[t] = l0;                              // s_sig of channel t is consumed
                 s_el[128 + t] = l1;
                 s_el[256 + t] = l2;
                 s_el[384 + t] = 1.f;
                 s_gam[t] = e3;
             }
-            // F = e^{b - sigma_u} in [1, e^75] for valid rows
+            __syncthreads();
+            // F = e^{b - sigma_u} in [1, e^75] for valid rows, b = local prefix + carry
+            float b[2][8];
 #pragma unroll
             for (int v = 0; v < 2; ++v) {
                 const int u = 2 * sp + v;
-                const bool valid = 16 * u + rb < Lc;
-                const float4 sa = *reinterpret_cast<const float4 *>(s_sig + u * 128 + 8 * cc);
-                const float4 sb = *reinterpret_cast<const float4 *>(s_sig + u * 128 + 8 * cc + 4);
-                const float sg[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+                const int r = 16 * u + rb;
+                const bool valid = r < Lc;
+                const uint8_t *rowp = sm + SM_Q0 + 8192 * (cc >> 2) + r * 128;
+                const int c4 = 2 * (cc & 3);
+                const float4 ga = *reinterpret_cast<const float4 *>(rowp + ((c4 ^ (r & 7)) << 4));
+                const float4 gb = *reinterpret_cast<const float4 *>(rowp + (((c4 + 1) ^ (r & 7)) << 4));
+                const float4 ba = *reinterpret_cast<const float4 *>(s_tot + u * 128 + 8 * cc);
+                const float4 bb = *reinterpret_cast<const float4 *>(s_tot + u * 128 + 8 * cc + 4);
+                const float gl[8] = {ga.x + ba.x, ga.y + ba.y, ga.z + ba.z, ga.w + ba.w,
+                                     gb.x + bb.x, gb.y + bb.y, gb.z + bb.z, gb.w + bb.w};
 #pragma unroll
-                for (int c = 0; c < 8; ++c) b[v][c] = valid ? __expf(b[v][c] - sg[c]) : 0.f;
+                for (int c = 0; c < 8; ++c) b[v][c] = valid ? __expf(gl[c]) : 0.f;
             }
-            __syncthreads();          // s_dd ready
+            __syncthreads();          // the g tile is read: Q0/K0 may be written
 
             if (!wait_all(B.qk, par)) { failed = true; break; }
             float dd[4][8];
