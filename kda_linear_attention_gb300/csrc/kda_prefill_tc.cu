@@ -566,7 +566,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 
         // ===== S1: T = (I + M)^-1 by 16-row blocks, in place; T' = (T-I)Diag(beta)
         {
-            float *Yt = Mm + 64 * MLD;        // [3][16][16] temporaries
+            float *Yt = Mm + 64 * MLD;        // temporaries: 2 x [16][16], then [32][32]
             // diagonal blocks (I + M_pp)^-1 by forward substitution across a
             // 16-lane group: lane = row r, two right-hand sides (columns c0, c0+1)
             // per thread; step s broadcasts x_s and every row r > s applies M_rs
@@ -596,45 +596,99 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 Mm[(16 * p + r) * MLD + 16 * p + c0 + 1] = x1;
             }
             __syncthreads();
+            // off-diagonal blocks, two levels: (1) T_10 and T_32 (16x16 each,
+            // T_pq = -T_pp M_pq T_qq); (2) the lower-left 32x32 block
+            // T_C = -T_B M_C T_A with T_A, T_B the inverted 32x32 diagonal blocks
+            if (t < 128) {
+                const int blk = t >> 6, r = (t >> 2) & 15, c4 = t & 3;
+                const int p = blk ? 3 : 1, q = p - 1;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float arow[16];
 #pragma unroll
-            for (int p = 1; p < 4; ++p) {
-                // Y_pq = sum_{m=16q}^{16p-1} M[16p+r][m] T[m][16q .. 16q+15]
-                if (t < 64 * p) {
-                    const int q = t >> 6, r = (t >> 2) & 15, c4 = t & 3;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int mb = q; mb < p; ++mb) {
-#pragma unroll
-                        for (int mm = 0; mm < 16; ++mm) {
-                            const int m = 16 * mb + mm;
-                            const float a = Mm[(16 * p + r) * MLD + m];
-                            const float4 tv = *reinterpret_cast<const float4 *>(Mm + m * MLD + 16 * q + 4 * c4);
-                            acc.x = fmaf(a, tv.x, acc.x);
-                            acc.y = fmaf(a, tv.y, acc.y);
-                            acc.z = fmaf(a, tv.z, acc.z);
-                            acc.w = fmaf(a, tv.w, acc.w);
-                        }
-                    }
-                    *reinterpret_cast<float4 *>(Yt + (q * 16 + r) * 16 + 4 * c4) = acc;
+                for (int j = 0; j < 4; ++j) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (16 * p + r) * MLD + 16 * q + 4 * j);
+                    arow[4 * j] = a4.x; arow[4 * j + 1] = a4.y; arow[4 * j + 2] = a4.z; arow[4 * j + 3] = a4.w;
                 }
-                __syncthreads();
-                // T_pq = -T_pp Y_pq
-                if (t < 64 * p) {
-                    const int q = t >> 6, r = (t >> 2) & 15, c4 = t & 3;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) {
-                        const float a = Mm[(16 * p + r) * MLD + 16 * p + m];
-                        const float4 yv = *reinterpret_cast<const float4 *>(Yt + (q * 16 + m) * 16 + 4 * c4);
-                        acc.x = fmaf(a, yv.x, acc.x);
-                        acc.y = fmaf(a, yv.y, acc.y);
-                        acc.z = fmaf(a, yv.z, acc.z);
-                        acc.w = fmaf(a, yv.w, acc.w);
-                    }
-                    *reinterpret_cast<float4 *>(Mm + (16 * p + r) * MLD + 16 * q + 4 * c4) =
-                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                for (int m = 0; m < 16; ++m) {
+                    const float a = arow[m];
+                    const float4 tv = *reinterpret_cast<const float4 *>(Mm + (16 * q + m) * MLD + 16 * q + 4 * c4);
+                    acc.x = fmaf(a, tv.x, acc.x);
+                    acc.y = fmaf(a, tv.y, acc.y);
+                    acc.z = fmaf(a, tv.z, acc.z);
+                    acc.w = fmaf(a, tv.w, acc.w);
                 }
-                __syncthreads();
+                *reinterpret_cast<float4 *>(Yt + (blk * 16 + r) * 16 + 4 * c4) = acc;
             }
+            __syncthreads();
+            if (t < 128) {
+                const int blk = t >> 6, r = (t >> 2) & 15, c4 = t & 3;
+                const int p = blk ? 3 : 1, q = p - 1;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float arow[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (16 * p + r) * MLD + 16 * p + 4 * j);
+                    arow[4 * j] = a4.x; arow[4 * j + 1] = a4.y; arow[4 * j + 2] = a4.z; arow[4 * j + 3] = a4.w;
+                }
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const float a = arow[m];
+                    const float4 yv = *reinterpret_cast<const float4 *>(Yt + (blk * 16 + m) * 16 + 4 * c4);
+                    acc.x = fmaf(a, yv.x, acc.x);
+                    acc.y = fmaf(a, yv.y, acc.y);
+                    acc.z = fmaf(a, yv.z, acc.z);
+                    acc.w = fmaf(a, yv.w, acc.w);
+                }
+                *reinterpret_cast<float4 *>(Mm + (16 * p + r) * MLD + 16 * q + 4 * c4) =
+                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            }
+            __syncthreads();
+            if (t < 256) {
+                // Y2 = M[32:64][0:32] T[0:32][0:32]
+                const int r = t >> 3, c4 = t & 7;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float arow[32];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (32 + r) * MLD + 4 * j);
+                    arow[4 * j] = a4.x; arow[4 * j + 1] = a4.y; arow[4 * j + 2] = a4.z; arow[4 * j + 3] = a4.w;
+                }
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const float a = arow[m];
+                    const float4 tv = *reinterpret_cast<const float4 *>(Mm + m * MLD + 4 * c4);
+                    acc.x = fmaf(a, tv.x, acc.x);
+                    acc.y = fmaf(a, tv.y, acc.y);
+                    acc.z = fmaf(a, tv.z, acc.z);
+                    acc.w = fmaf(a, tv.w, acc.w);
+                }
+                *reinterpret_cast<float4 *>(Yt + r * 32 + 4 * c4) = acc;
+            }
+            __syncthreads();
+            if (t < 256) {
+                // T_C = -T[32:64][32:64] Y2
+                const int r = t >> 3, c4 = t & 7;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float arow[32];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (32 + r) * MLD + 32 + 4 * j);
+                    arow[4 * j] = a4.x; arow[4 * j + 1] = a4.y; arow[4 * j + 2] = a4.z; arow[4 * j + 3] = a4.w;
+                }
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const float a = arow[m];
+                    const float4 yv = *reinterpret_cast<const float4 *>(Yt + m * 32 + 4 * c4);
+                    acc.x = fmaf(a, yv.x, acc.x);
+                    acc.y = fmaf(a, yv.y, acc.y);
+                    acc.z = fmaf(a, yv.z, acc.z);
+                    acc.w = fmaf(a, yv.w, acc.w);
+                }
+                *reinterpret_cast<float4 *>(Mm + (32 + r) * MLD + 4 * c4) =
+                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            }
+            __syncthreads();
             // T' = (T - I) Diag(beta), bf16 K-major il [r][s] (B of U~ = T' V), and
             // -T Diag(beta), tf32 K-major il [r][s] (B of the W S term): one
             // 8-wide chunk of row r per thread

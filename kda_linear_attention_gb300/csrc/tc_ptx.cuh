@@ -185,11 +185,12 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// fp32 -> tf32 with round to nearest (ties away), as a 32-bit pattern.
+// fp32 -> tf32 with round to nearest, ties away from zero, as a 32-bit
+// pattern: add half a unit of the 10-bit mantissa to the magnitude bits and
+// clear the 13 low bits (finite inputs; a carry into the exponent is the
+// correct rounding).
 __device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
+    return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
 }
 
 }  // namespace tc
