@@ -15,7 +15,12 @@
  *
  * Conventions shared by every call
  *   - Pointers are DEVICE pointers unless marked "host"; the caller owns all
- *     memory.  The library allocates nothing and keeps no global state.
+ *     memory it passes.  The tensor-core prefill (bf16, chunk 64) also needs
+ *     a scratch workspace of about 89 KB per (64-token chunk, head); it takes
+ *     it from a library-owned stream-ordered memory pool on the current
+ *     device, which keeps that memory for later calls.  That pool and the
+ *     device error word (kda_device_error) are the library's only global
+ *     state.
  *   - Layouts are token-major and dense (C order):
  *         q, k, g : [T, H, dk]      v, o : [T, H, dv]      beta : [T, H]
  *         S       : [N, H, dk, dv]  with S[n][h][i][j], i = key channel,
@@ -51,7 +56,7 @@ typedef enum {
     KDA_ERR_CHUNK = 3,       /* chunk not in {16, 32, 64} */
     KDA_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
     KDA_ERR_DTYPE = 5,       /* dtype not a kda_dtype_t */
-    KDA_ERR_WORKSPACE = 6,   /* reserved: no call takes a workspace */
+    KDA_ERR_WORKSPACE = 6,   /* the prefill's scratch workspace could not be allocated */
     KDA_ERR_CUDA = 7         /* the CUDA runtime reported an error at launch */
 } kda_status_t;
 
@@ -92,11 +97,14 @@ const char *kda_status_string(int status);
  *   N          number of sequences (>= 1); T total tokens (>= 0, < 2^31)
  *   H          heads (>= 1); dk, dv must be 128
  *   chunk      16, 32 or 64.  bf16 inputs with chunk 64 run on the
- *              tensor cores (tcgen05, TMA); every other combination runs
+ *              tensor cores (tcgen05, TMA) in two kernels: an intra-chunk
+ *              kernel over every (chunk, head) at once, then an inter-chunk
+ *              state pass per (sequence, head); every other combination runs
  *              the fp32 CUDA-core kernel.
  *   dtype      kda_dtype_t of q, k, v
  *   stream     cudaStream_t
- * Returns KDA_OK or a kda_status_t.  With T == 0 only S_out is written.
+ * Returns KDA_OK or a kda_status_t (KDA_ERR_WORKSPACE when the tensor-core
+ * path cannot get its workspace).  With T == 0 only S_out is written.
  */
 int kda_prefill_chunked(const void *q, const void *k, const void *v,
                         const float *g, const float *beta, const float *S0,
@@ -126,10 +134,12 @@ int kda_decode_step(const void *q, const void *k, const void *v,
                     int B, int H, int dk, int dv, int dtype, void *stream);
 
 /*
- * Device-side error word of the library.  The tensor-core prefill kernel
- * never waits without bound: if one of its waits on an asynchronous copy or
- * on the tensor cores runs past its iteration limit it sets a bit here,
- * releases its tensor memory and exits (its outputs are then invalid).
+ * Device-side error word of the library.  The tensor-core prefill kernels
+ * never wait without bound: if one of their waits on an asynchronous copy or
+ * on the tensor cores runs past its iteration limit they set a bit here,
+ * release their tensor memory and exit (the outputs are then invalid).  The
+ * state pass also sets it when a sequence's chunk count does not match the
+ * workspace it was sized for (cu_seqlens inconsistent with T).
  *
  *   code   host pointer, receives the word (0 = no error since the last reset)
  *   reset  nonzero: clear the word after reading it

@@ -48,9 +48,11 @@ int kda_prefill_chunked(const void *q, const void *k, const void *v, const float
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_ALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (dtype == KDA_BF16 && chunk == 64 && T > 0)
-        return cuda_status(kda::launch_prefill_tc(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, T,
-                                                  H, s));
+    if (dtype == KDA_BF16 && chunk == 64 && T > 0) {
+        const cudaError_t e = kda::launch_prefill_split(q, k, v, g, beta, S0, o, S_out, cu_seqlens,
+                                                        N, T, H, s);
+        return e == cudaErrorMemoryAllocation ? KDA_ERR_WORKSPACE : cuda_status(e);
+    }
     return cuda_status(kda::launch_prefill_simt(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, H,
                                                 chunk, dtype == KDA_BF16, s));
 }
@@ -72,7 +74,11 @@ int kda_decode_step(const void *q, const void *k, const void *v, const float *g,
 
 int kda_device_error(unsigned int *code, int reset) {
     if (!code) return KDA_ERR_NULL;
-    return cuda_status(kda::read_device_error(code, reset != 0));
+    unsigned int a = 0, b = 0;
+    const cudaError_t e1 = kda::read_device_error(&a, reset != 0);
+    const cudaError_t e2 = kda::read_split_error(&b, reset != 0);
+    *code = a | b;
+    return cuda_status(e1 != cudaSuccess ? e1 : e2);
 }
 
 }  // extern "C"

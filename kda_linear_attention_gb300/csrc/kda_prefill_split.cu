@@ -1,0 +1,959 @@
+// Chunked KDA prefill in two tensor-core kernels: an intra-chunk kernel that
+// runs on every (chunk, head) at once, and an inter-chunk state pass that
+// walks each (sequence, head) through its chunks.
+//
+// Math (the recurrence of "Colibri Kimi K3 Metal backend", architecture
+// section, unrolled over a chunk of L <= 64 tokens; b_r = sum_{t<=r} g_t):
+//   G^qk_rs = sum_c q_rc k_sc e^{b_rc - b_sc} (s <= r),  G^kk likewise (s < r)
+//   T  = (I + Diag(beta) G^kk)^-1 (unit lower triangular),  T' = (T - I) Diag(beta)
+//   W  = T' K0 + Diag(beta) K0,        K0_r = e^{b_r} k_r
+//   U  = T' V + Diag(beta) V - W S
+//   O  = Q0 S + A' U + Diag(q_r.k_r) U,  Q0_r = e^{b_r} q_r,  A' = strictly lower G^qk
+//   S <- Diag(e^{b_L}) S + Kbar^T U,      Kbar_s = e^{b_L - b_s} k_s
+// Everything that does not involve the state S (the decay prefix sums, the
+// two Gram matrices, the triangular solve for T, W, Q0, Kbar, A') depends on
+// one chunk only; the intra-chunk kernel computes it for all chunks of all
+// sequences in parallel and writes one record per (chunk, head).  The state
+// pass then does, per chunk, two rounds of MMAs and two epilogues:
+//   D_U[j][r] = -(W S)^T + (T' V)^T,   D_O[j][r] = (Q0 S)^T      (bf16)
+//   u = D_U + beta v  (fp32, rounded to tf32 in TMEM)
+//   D_O += (A' U)^T,   S^T += (Kbar^T U)^T                        (tf32)
+// with S^T kept in fp32 in TMEM for the whole sequence (lane j, column i) and
+// pre-scaled by e^{b_L} while the first round runs.
+//
+// Decay folding in the Gram matrices (16-row sub-blocks p, sigma_p = b at the
+// last row of p): e^{b_r - b_s} = e^{b_r - sigma_p} e^{sigma_p - b_s}, the
+// first factor in [1, e^75] and the second in (0, 1] for g >= -5; the query
+// side is one operand X = [q e^{b - sigma} ; k e^{b - sigma}] (128 rows), the
+// key side a stack of four operands k_s e^{sigma_p - b_s} (160 rows), and one
+// M=128, N=160 MMA gives both Gram matrices.
+//
+// Precision: bf16 operands for the products that carry state-side or Gram
+// terms; tf32 (software round-to-nearest) for A' U and Kbar^T U; the diagonal
+// terms (beta_r v_r, beta_r K0_r, (q_r.k_r) u_r) in fp32 outside the MMAs.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "kda_internal.h"
+#include "tc_layout.cuh"
+
+namespace kda {
+
+// Nonzero when a bounded wait in either kernel gave up, or the chunk plan
+// did not fit the workspace.
+__device__ unsigned int g_kda_split_error = 0;
+
+namespace {
+using namespace tc;
+
+constexpr int C = 64;
+
+// ---- the per-(chunk, head) record ------------------------------------------
+// Each piece is stored in the shared-memory operand layout in which the state
+// pass feeds it to the tensor cores, so that one bulk copy places it.
+constexpr uint32_t R_WQ = 0;        // [-W ; Q0] bf16, 128 rows x 128, K-major sw (two 16 KB halves)
+constexpr uint32_t R_T = 32768;     // T' bf16 K-major il [r][s], 8 KB
+constexpr uint32_t R_A = 40960;     // A' tf32 K-major il [r][s], 16 KB
+constexpr uint32_t R_KB = 57344;    // Kbar^T tf32 K-major il [i][s], 32 KB
+constexpr uint32_t R_VEC = 90112;   // beta[64], q.k[64], e^{b_L}[128] (fp32)
+constexpr uint32_t REC_BYTES = 91136;
+static_assert(REC_BYTES % 1024 == 0, "records stay 1 KB aligned");
+
+// ============================================================================
+// chunk plan: chunk_off[n] = sum_{m<n} ceil(len_m / 64), chunk_off[N] = total
+// ============================================================================
+__global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t *__restrict__ cu, int N,
+                                                          int32_t *__restrict__ chunk_off) {
+    __shared__ int32_t s_scan[1024];
+    __shared__ int32_t s_carry;
+    const int t = threadIdx.x;
+    if (t == 0) s_carry = 0;
+    __syncthreads();
+    for (int base = 0; base < N; base += 1024) {
+        const int n = base + t;
+        int v = 0;
+        if (n < N) v = (max(cu[n + 1] - cu[n], 0) + C - 1) / C;
+        s_scan[t] = v;
+        __syncthreads();
+        for (int off = 1; off < 1024; off <<= 1) {
+            const int x = t >= off ? s_scan[t - off] : 0;
+            __syncthreads();
+            s_scan[t] += x;
+            __syncthreads();
+        }
+        const int carry = s_carry;
+        if (n < N) chunk_off[n] = carry + s_scan[t] - v;
+        __syncthreads();
+        if (t == 1023) s_carry = carry + s_scan[1023];
+        __syncthreads();
+    }
+    if (t == 0) chunk_off[N] = s_carry;
+}
+
+// ============================================================================
+// intra-chunk kernel: one CTA (256 threads, two CTAs per SM) per (chunk, head)
+// ============================================================================
+constexpr int NTA = 256;
+constexpr uint32_t SA_X = 0;              // 32 KB: q|k staging (TMA) -> X [128][128] sw; then M fp32 [64][68] + temps
+constexpr uint32_t SA_KH = 32768;         // 40 KB: g staging fp32 (TMA) -> Khat [160][128] sw
+constexpr uint32_t SA_T = SA_KH;          //   after the Gram: T' bf16 il [r][s], 8 KB
+constexpr uint32_t SA_WST = SA_KH + 8192; //   after the Gram: -W staging, 2 x [64][128 B] sw, 16 KB
+constexpr uint32_t SA_K0 = 73728;         // 16 KB: K0 [64 s][128 i] sw (MN-major A of the W product)
+constexpr uint32_t SA_MISC = 90112;
+constexpr uint32_t MA_BETA = 0;           // float[64]
+constexpr uint32_t MA_GAM = 256;          // float[128]  e^{b_L}
+constexpr uint32_t MA_DQ = 768;           // float[64]   q_r . k_r
+constexpr uint32_t MA_TOT = 1024;         // float[4][128] sub-block totals, then carry - sigma_u
+constexpr uint32_t MA_SIG = 3072;         // float[4][128] local prefix at sub-block ends, then e^{b_L - sigma_u}
+constexpr uint32_t MA_DD = 5120;          // float[4][128] e^{sigma_0}, e^{sigma_w - sigma_{w-1}}
+constexpr uint32_t MA_EP = 7168;          // float[4][128] e^{sigma_u}
+constexpr uint32_t MA_BAR = 9216;         // 2 x u64
+constexpr uint32_t MA_TMEM = 9232;
+constexpr uint32_t SMEM_A_USED = SA_MISC + 9248;
+constexpr uint32_t SMEM_A_ALLOC = SMEM_A_USED + 1024;
+static_assert(2 * (SMEM_A_ALLOC + 1024) <= 233472, "two intra-chunk CTAs per SM");
+constexpr int MLD = 68;                   // row stride (floats) of M / T
+constexpr uint32_t TMA_G = 0;             // Gram D, 160 columns
+constexpr uint32_t TMA_W = 0;             // (T' K0)^T, 64 columns (after the Gram epilogue)
+
+__global__ void __launch_bounds__(NTA, 2)
+intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                   const __grid_constant__ CUtensorMap map_g, const float *__restrict__ beta,
+                   const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N,
+                   int H, uint8_t *__restrict__ recs) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    float *s_beta = reinterpret_cast<float *>(sm + SA_MISC + MA_BETA);
+    float *s_gam = reinterpret_cast<float *>(sm + SA_MISC + MA_GAM);
+    float *s_dq = reinterpret_cast<float *>(sm + SA_MISC + MA_DQ);
+    float *s_tot = reinterpret_cast<float *>(sm + SA_MISC + MA_TOT);
+    float *s_sig = reinterpret_cast<float *>(sm + SA_MISC + MA_SIG);
+    float *s_dd = reinterpret_cast<float *>(sm + SA_MISC + MA_DD);
+    float *s_ep = reinterpret_cast<float *>(sm + SA_MISC + MA_EP);
+    float *s_el = s_sig;
+    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + SA_MISC + MA_BAR);
+    uint64_t *bar_mma = bar_ld + 1;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SA_MISC + MA_TMEM);
+
+    const int t = threadIdx.x;
+    const int warp = t >> 5;
+    const int lane = t & 31;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+
+    // ---- which chunk: gc = global chunk index, n = its sequence
+    const int h = blockIdx.x % H;
+    const int gc = blockIdx.x / H;
+    if (gc >= chunk_off[N]) return;
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (chunk_off[mid] <= gc) lo = mid;
+        else hi = mid - 1;
+    }
+    const int n = lo;
+    const int tok = cu[n] + (gc - chunk_off[n]) * C;
+    const int Lc = min(C, cu[n + 1] - tok);
+    uint8_t *rec = recs + ((size_t)gc * H + h) * REC_BYTES;
+
+    if (warp == 0) tmem_alloc(s_tmem, 256);
+    if (t == 0) {
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        // q and k land as the two 64-row halves of X (rows 0..63 q, 64..127 k)
+        mbar_arrive_expect_tx(bar_ld, 65536);
+        tma_load_3d(sm + SA_X, &map_q, bar_ld, 0, h, tok);
+        tma_load_3d(sm + SA_X + 8192, &map_k, bar_ld, 0, h, tok);
+        tma_load_3d(sm + SA_X + 16384, &map_q, bar_ld, 64, h, tok);
+        tma_load_3d(sm + SA_X + 24576, &map_k, bar_ld, 64, h, tok);
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx)
+            tma_load_3d(sm + SA_KH + 8192 * bx, &map_g, bar_ld, 32 * bx, h, tok);
+    }
+    if (t < C) {
+        s_beta[t] = (t < Lc) ? beta[(size_t)(tok + t) * H + h] : 0.f;
+        s_dq[t] = 0.f;
+    }
+    sync_tc();
+    const uint32_t tmem = *s_tmem;
+    bool failed = !wait_all(bar_ld, 0);
+    int commits = 0;                       // MMA commits issued on bar_mma
+
+    if (!failed) {
+        // ===== decay prefix sums: column scan in place in the g tile =========
+        auto g_at = [&](int r, int c) -> float * {
+            return reinterpret_cast<float *>(sm + SA_KH + 8192 * (c >> 5) + r * 128 +
+                                             ((((c & 31) >> 2) ^ (r & 7)) << 4) + (c & 3) * 4);
+        };
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+            const int i = t & 127, u = (t >> 7) + 2 * pass;
+            float acc = 0.f, at_last = 0.f;
+            const int lastrow = min(16 * u + 15, Lc - 1);
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                const int r = 16 * u + rr;
+                float *pg = g_at(r, i);
+                acc += (r < Lc) ? *pg : 0.f;
+                *pg = acc;
+                if (r == lastrow) at_last = acc;
+            }
+            s_tot[u * 128 + i] = acc;
+            s_sig[u * 128 + i] = at_last;
+        }
+        __syncthreads();
+        if (t < 128) {
+            const int lu = (Lc - 1) >> 4;
+            float base[4], sg[4];
+            float run = 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                base[u] = run;
+                run += s_tot[u * 128 + t];
+            }
+            float bL = 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (u == lu) bL = base[u] + s_sig[u * 128 + t];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) sg[u] = (u <= lu) ? base[u] + s_sig[u * 128 + t] : bL;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) s_tot[u * 128 + t] = base[u] - sg[u];
+            const float d0 = __expf(sg[0]), d1 = __expf(sg[1] - sg[0]), d2 = __expf(sg[2] - sg[1]),
+                        d3 = __expf(sg[3] - sg[2]);
+            s_dd[t] = d0;
+            s_dd[128 + t] = d1;
+            s_dd[256 + t] = d2;
+            s_dd[384 + t] = d3;
+            const float e1 = d0 * d1, e2 = e1 * d2, e3 = e2 * d3;
+            s_ep[t] = d0;
+            s_ep[128 + t] = e1;
+            s_ep[256 + t] = e2;
+            s_ep[384 + t] = e3;
+            const float l2 = d3, l1 = d2 * d3, l0 = d1 * l1;
+            s_el[t] = l0;
+            s_el[128 + t] = l1;
+            s_el[256 + t] = l2;
+            s_el[384 + t] = 1.f;
+            s_gam[t] = e3;
+        }
+        __syncthreads();
+
+        // ===== operand build: thread = row rb of every sub-block, channels 8cc..8cc+7
+        const int rb = lane & 15;
+        const int cc = 2 * warp + (lane >> 4);
+        float F[4][8];                     // e^{b - sigma_u} (0 for rows past the end)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = 16 * u + rb;
+            const bool valid = r < Lc;
+            const uint8_t *rowp = sm + SA_KH + 8192 * (cc >> 2) + r * 128;
+            const int c4 = 2 * (cc & 3);
+            const float4 ga = *reinterpret_cast<const float4 *>(rowp + ((c4 ^ (r & 7)) << 4));
+            const float4 gb = *reinterpret_cast<const float4 *>(rowp + (((c4 + 1) ^ (r & 7)) << 4));
+            const float4 ba = *reinterpret_cast<const float4 *>(s_tot + u * 128 + 8 * cc);
+            const float4 bb = *reinterpret_cast<const float4 *>(s_tot + u * 128 + 8 * cc + 4);
+            const float gl[8] = {ga.x + ba.x, ga.y + ba.y, ga.z + ba.z, ga.w + ba.w,
+                                 gb.x + bb.x, gb.y + bb.y, gb.z + bb.z, gb.w + bb.w};
+#pragma unroll
+            for (int c = 0; c < 8; ++c) F[u][c] = valid ? __expf(gl[c]) : 0.f;
+        }
+        __syncthreads();                   // the g tile is read: Khat may be written
+
+        float dqp[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = 16 * u + rb;
+            uint8_t *pq = sm + SA_X + sw_chunk(r, cc, 16384);
+            uint8_t *pk = sm + SA_X + sw_chunk(64 + r, cc, 16384);
+            float qv[8], kv[8];
+            unpack_bf8(*reinterpret_cast<const uint4 *>(pq), qv);
+            unpack_bf8(*reinterpret_cast<const uint4 *>(pk), kv);
+            float G[8], xq[8], xk[8], ep[8], el[8];
+            {
+                const float4 e0 = *reinterpret_cast<const float4 *>(s_ep + u * 128 + 8 * cc);
+                const float4 e1 = *reinterpret_cast<const float4 *>(s_ep + u * 128 + 8 * cc + 4);
+                const float4 l0 = *reinterpret_cast<const float4 *>(s_el + u * 128 + 8 * cc);
+                const float4 l1 = *reinterpret_cast<const float4 *>(s_el + u * 128 + 8 * cc + 4);
+                ep[0] = e0.x; ep[1] = e0.y; ep[2] = e0.z; ep[3] = e0.w;
+                ep[4] = e1.x; ep[5] = e1.y; ep[6] = e1.z; ep[7] = e1.w;
+                el[0] = l0.x; el[1] = l0.y; el[2] = l0.z; el[3] = l0.w;
+                el[4] = l1.x; el[5] = l1.y; el[6] = l1.z; el[7] = l1.w;
+            }
+            float dot = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                dot = fmaf(qv[c], kv[c], dot);
+                const float Fc = F[u][c];
+                G[c] = (Fc > 0.f) ? __fdividef(1.f, Fc) : 0.f;
+                xq[c] = qv[c] * Fc;
+                xk[c] = kv[c] * Fc;
+            }
+            dqp[u] = (r < Lc) ? dot : 0.f;
+            // X in place: q rows 0..63, k rows 64..127
+            *reinterpret_cast<uint4 *>(pq) = pack_bf8(xq);
+            *reinterpret_cast<uint4 *>(pk) = pack_bf8(xk);
+            // Khat stack: block pp >= u holds k_s e^{sigma_pp - b_s} at row 8pp(pp+1) + s
+            float kh[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) kh[c] = kv[c] * G[c];
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                if (pp >= u) {
+                    if (pp > u) {
+                        const float4 da = *reinterpret_cast<const float4 *>(s_dd + pp * 128 + 8 * cc);
+                        const float4 db = *reinterpret_cast<const float4 *>(s_dd + pp * 128 + 8 * cc + 4);
+                        kh[0] *= da.x; kh[1] *= da.y; kh[2] *= da.z; kh[3] *= da.w;
+                        kh[4] *= db.x; kh[5] *= db.y; kh[6] *= db.z; kh[7] *= db.w;
+                    }
+                    *reinterpret_cast<uint4 *>(sm + SA_KH + sw_chunk(8 * pp * (pp + 1) + r, cc, 20480)) =
+                        pack_bf8(kh);
+                }
+            }
+            // Q0 = q e^{b} -> record rows 64..127 of [-W ; Q0];  K0 = k e^{b} -> smem
+            float q0[8], k0[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                q0[c] = xq[c] * ep[c];
+                k0[c] = xk[c] * ep[c];
+            }
+            *reinterpret_cast<uint4 *>(rec + R_WQ + sw_chunk(64 + r, cc, 16384)) = pack_bf8(q0);
+            *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, cc, 8192)) = pack_bf8(k0);
+            // Kbar^T tf32 K-major il [i][s]: a 4x4 transpose inside each quad of
+            // lanes (4 consecutive rows) gives every lane 4 consecutive s for
+            // channels 2b, 2b+1: 16-byte stores.
+            {
+                float kbv[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) kbv[c] = kv[c] * G[c] * el[c];
+                const int bq = rb & 3;
+                float o0[4], o1[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int dst = (bq - k) & 3;
+                    const float s0 = dst == 0 ? kbv[0] : dst == 1 ? kbv[2] : dst == 2 ? kbv[4] : kbv[6];
+                    const float s1 = dst == 0 ? kbv[1] : dst == 1 ? kbv[3] : dst == 2 ? kbv[5] : kbv[7];
+                    const int srcl = (lane & ~3) | ((bq + k) & 3);
+                    const float r0 = __shfl_sync(0xffffffffu, s0, srcl);
+                    const float r1 = __shfl_sync(0xffffffffu, s1, srcl);
+                    const int srow = (bq + k) & 3;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (e == srow) {
+                            o0[e] = r0;
+                            o1[e] = r1;
+                        }
+                    }
+                }
+                const int s0r = 16 * u + (rb & ~3);
+                const int i0 = 8 * cc + 2 * bq;
+                *reinterpret_cast<uint4 *>(rec + R_KB + km_tf32(i0, s0r, 2048)) =
+                    make_uint4(to_tf32(o0[0]), to_tf32(o0[1]), to_tf32(o0[2]), to_tf32(o0[3]));
+                *reinterpret_cast<uint4 *>(rec + R_KB + km_tf32(i0 + 1, s0r, 2048)) =
+                    make_uint4(to_tf32(o1[0]), to_tf32(o1[1]), to_tf32(o1[2]), to_tf32(o1[3]));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float d2 = dqp[u] + __shfl_xor_sync(0xffffffffu, dqp[u], 16);
+            if (lane < 16) atomicAdd(s_dq + 16 * u + rb, d2);
+        }
+        fence_proxy_async_smem();
+        sync_tc();
+
+        // ===== Gram: D_G[128 x 160] = X Khat^T ===============================
+        if (t == 0) {
+            const uint32_t idg = instr_desc(kFmtBF16, 128, 160, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t ko = (uint32_t)(kk >> 2), kb2 = (uint32_t)(kk & 3) * 32u;
+                const uint64_t ax = smem_desc(smem_u32(sm + SA_X + ko * 16384 + kb2), 16, 1024, kSwizzle128B);
+                const uint64_t bk = smem_desc(smem_u32(sm + SA_KH + ko * 20480 + kb2), 16, 1024, kSwizzle128B);
+                mma_bf16_ss(tmem + TMA_G, ax, bk, idg, kk > 0);
+            }
+            mma_commit(bar_mma);
+        }
+        ++commits;
+        {
+            float *rv = reinterpret_cast<float *>(rec + R_VEC);
+            if (t < 64) {
+                rv[t] = s_beta[t];
+                rv[64 + t] = s_dq[t];
+            }
+            if (t < 128) rv[128 + t] = s_gam[t];
+        }
+        failed = !wait_all(bar_mma, 0);
+    }
+    if (!failed) {
+        tc_fence_after();
+        // ===== Gram epilogue -> A' (tf32, record) and M = Diag(beta) G^kk (fp32)
+        float *Mm = reinterpret_cast<float *>(sm + SA_X);
+        {
+            const int ch = t & 127;
+            const bool qside = ch < 64;
+            const int r = ch & 63;
+            const int p = r >> 4;
+            const int plo = (r >> 5) * 2;
+            const float br = s_beta[r];
+#pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {
+                const int qt = 2 * (t >> 7) + qq;
+                const uint32_t col_lo = (uint32_t)min(8 * plo * (plo + 1) + 16 * qt, 144);
+                const uint32_t col_hi = (uint32_t)min(8 * (plo + 1) * (plo + 2) + 16 * qt, 144);
+                float va[16], vb[16];
+                tmem_ld16(tmem + lane_base + TMA_G + col_lo, va);
+                tmem_ld16(tmem + lane_base + TMA_G + col_hi, vb);
+                tmem_wait_ld();
+                const bool use_hi = p != plo;
+                const bool have = qt <= p && r < Lc;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float x4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = 16 * qt + 4 * j + e;
+                        const float val = use_hi ? vb[4 * j + e] : va[4 * j + e];
+                        x4[e] = (have && s < r) ? val : 0.f;
+                    }
+                    if (qside) {
+                        *reinterpret_cast<uint4 *>(rec + R_A + km_tf32(r, 16 * qt + 4 * j, 2048)) =
+                            make_uint4(to_tf32(x4[0]), to_tf32(x4[1]), to_tf32(x4[2]), to_tf32(x4[3]));
+                    } else {
+                        *reinterpret_cast<float4 *>(Mm + r * MLD + 16 * qt + 4 * j) =
+                            make_float4(br * x4[0], br * x4[1], br * x4[2], br * x4[3]);
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+
+        // ===== T = (I + M)^-1 by 16-row blocks, in place ======================
+        float *Yt = Mm + 64 * MLD;
+        {
+            // diagonal blocks by forward substitution across a 16-lane group:
+            // lane = row r, four right-hand sides (columns c0..c0+3) per thread
+            const int r = t & 15;
+            const int grp = t >> 4;
+            const int p = grp >> 2, c0 = 4 * (grp & 3);
+            float mr[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 m4 = *reinterpret_cast<const float4 *>(Mm + (16 * p + r) * MLD + 16 * p + 4 * j);
+                mr[4 * j] = m4.x; mr[4 * j + 1] = m4.y; mr[4 * j + 2] = m4.z; mr[4 * j + 3] = m4.w;
+            }
+            float x[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] = (r == c0 + e) ? 1.f : 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 < 15; ++s2) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float bv = __shfl_sync(0xffffffffu, x[e], s2, 16);
+                    if (r > s2) x[e] = fmaf(-mr[s2], bv, x[e]);
+                }
+            }
+            __syncthreads();
+            *reinterpret_cast<float4 *>(Mm + (16 * p + r) * MLD + 16 * p + c0) =
+                make_float4(x[0], x[1], x[2], x[3]);
+        }
+        __syncthreads();
+        // off-diagonal blocks, two levels: T_10 and T_32 (T_pq = -T_pp M_pq T_qq),
+        // then the lower-left 32x32 block T_C = -T_B M_C T_A
+        if (t < 128) {
+            const int blk = t >> 6, r = (t >> 2) & 15, c4 = t & 3;
+            const int p = blk ? 3 : 1, q = p - 1;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float arow[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (16 * p + r) * MLD + 16 * q + 4 * j);
+                arow[4 * j] = a4.x; arow[4 * j + 1] = a4.y; arow[4 * j + 2] = a4.z; arow[4 * j + 3] = a4.w;
+            }
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const float a = arow[m];
+                const float4 tv = *reinterpret_cast<const float4 *>(Mm + (16 * q + m) * MLD + 16 * q + 4 * c4);
+                acc.x = fmaf(a, tv.x, acc.x);
+                acc.y = fmaf(a, tv.y, acc.y);
+                acc.z = fmaf(a, tv.z, acc.z);
+                acc.w = fmaf(a, tv.w, acc.w);
+            }
+            *reinterpret_cast<float4 *>(Yt + (blk * 16 + r) * 16 + 4 * c4) = acc;
+        }
+        __syncthreads();
+        if (t < 128) {
+            const int blk = t >> 6, r = (t >> 2) & 15, c4 = t & 3;
+            const int p = blk ? 3 : 1, q = p - 1;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float arow[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (16 * p + r) * MLD + 16 * p + 4 * j);
+                arow[4 * j] = a4.x; arow[4 * j + 1] = a4.y; arow[4 * j + 2] = a4.z; arow[4 * j + 3] = a4.w;
+            }
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const float a = arow[m];
+                const float4 yv = *reinterpret_cast<const float4 *>(Yt + (blk * 16 + m) * 16 + 4 * c4);
+                acc.x = fmaf(a, yv.x, acc.x);
+                acc.y = fmaf(a, yv.y, acc.y);
+                acc.z = fmaf(a, yv.z, acc.z);
+                acc.w = fmaf(a, yv.w, acc.w);
+            }
+            *reinterpret_cast<float4 *>(Mm + (16 * p + r) * MLD + 16 * q + 4 * c4) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        }
+        __syncthreads();
+        {
+            // Y2 = M[32:64][0:32] T[0:32][0:32]
+            const int r = t >> 3, c4 = t & 7;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float arow[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (32 + r) * MLD + 4 * j);
+                arow[4 * j] = a4.x; arow[4 * j + 1] = a4.y; arow[4 * j + 2] = a4.z; arow[4 * j + 3] = a4.w;
+            }
+#pragma unroll
+            for (int m = 0; m < 32; ++m) {
+                const float a = arow[m];
+                const float4 tv = *reinterpret_cast<const float4 *>(Mm + m * MLD + 4 * c4);
+                acc.x = fmaf(a, tv.x, acc.x);
+                acc.y = fmaf(a, tv.y, acc.y);
+                acc.z = fmaf(a, tv.z, acc.z);
+                acc.w = fmaf(a, tv.w, acc.w);
+            }
+            *reinterpret_cast<float4 *>(Yt + r * 32 + 4 * c4) = acc;
+        }
+        __syncthreads();
+        {
+            // T_C = -T[32:64][32:64] Y2
+            const int r = t >> 3, c4 = t & 7;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float arow[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (32 + r) * MLD + 32 + 4 * j);
+                arow[4 * j] = a4.x; arow[4 * j + 1] = a4.y; arow[4 * j + 2] = a4.z; arow[4 * j + 3] = a4.w;
+            }
+#pragma unroll
+            for (int m = 0; m < 32; ++m) {
+                const float a = arow[m];
+                const float4 yv = *reinterpret_cast<const float4 *>(Yt + m * 32 + 4 * c4);
+                acc.x = fmaf(a, yv.x, acc.x);
+                acc.y = fmaf(a, yv.y, acc.y);
+                acc.z = fmaf(a, yv.z, acc.z);
+                acc.w = fmaf(a, yv.w, acc.w);
+            }
+            *reinterpret_cast<float4 *>(Mm + (32 + r) * MLD + 4 * c4) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        }
+        __syncthreads();
+        // T' = (T - I) Diag(beta), bf16 K-major il [r][s]: shared memory (B of
+        // the W product) and the record (B of the U~ product in the state pass)
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+            const int r = (t >> 3) + 32 * pass, s0 = (t & 7) * 8;
+            const float4 a = *reinterpret_cast<const float4 *>(Mm + r * MLD + s0);
+            const float4 b4 = *reinterpret_cast<const float4 *>(Mm + r * MLD + s0 + 4);
+            const float tv[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
+            float w8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int s3 = s0 + u;
+                w8[u] = (s3 < r) ? tv[u] * s_beta[s3] : 0.f;
+            }
+            const uint4 pk = pack_bf8(w8);
+            *reinterpret_cast<uint4 *>(sm + SA_T + km_bf16(r, s0, 1024)) = pk;
+            *reinterpret_cast<uint4 *>(rec + R_T + km_bf16(r, s0, 1024)) = pk;
+        }
+        fence_proxy_async_smem();
+        sync_tc();
+
+        // ===== W^T = (T' K0)^T: D_W[i][r], A = K0 (MN-major), B = T' =========
+        if (t == 0) {
+            const uint32_t idw = instr_desc(kFmtBF16, 128, 64, 1, 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t a = smem_desc(smem_u32(sm + SA_K0 + 2048 * kk), 8192, 1024, kSwizzle128B);
+                const uint64_t b = smem_desc(smem_u32(sm + SA_T + 256 * kk), 128, 1024, kSwizzleNone);
+                mma_bf16_ss(tmem + TMA_W, a, b, idw, kk > 0);
+            }
+            mma_commit(bar_mma);
+        }
+        ++commits;
+        failed = !wait_all(bar_mma, 1);
+    }
+    if (!failed) {
+        tc_fence_after();
+        // ===== -W = -(T' K0 + Diag(beta) K0) -> bf16 sw staging -> record rows 0..63
+        {
+            const int i = t & 127, hh = t >> 7;
+            float d[32];
+            tmem_ld32(tmem + lane_base + TMA_W + 32 * hh, d);
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) {
+                const int r = 32 * hh + rr;
+                const uint32_t off = sw_elem64(r, i);
+                const float w = fmaf(s_beta[r], bf(sm + SA_K0 + off), d[rr]);
+                *reinterpret_cast<__nv_bfloat16 *>(sm + SA_WST + off) = __float2bfloat16_rn(-w);
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int e = t; e < 1024; e += NTA) {
+            const int kh = e >> 9, off = (e & 511) * 16;
+            *reinterpret_cast<uint4 *>(rec + R_WQ + kh * 16384 + off) =
+                *reinterpret_cast<const uint4 *>(sm + SA_WST + kh * 8192 + off);
+        }
+    }
+    if (failed) {
+        if (t == 0) atomicOr(&g_kda_split_error, 1u);
+        // let copies and MMAs in flight finish (bounded) before freeing TMEM
+        mbar_wait(bar_ld, 0, kWaitLimit);
+        if (commits) mbar_wait(bar_mma, (uint32_t)(commits - 1) & 1u, kWaitLimit);
+    }
+    sync_tc();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ============================================================================
+// state pass: one CTA (512 threads) per (sequence, head)
+// ============================================================================
+constexpr int NTB = 512;
+constexpr uint32_t SB_WQ = 0;             // [-W ; Q0] (bulk copy 1, with T')
+constexpr uint32_t SB_T = 32768;          // T'
+constexpr uint32_t SB_A = 40960;          // A' (bulk copy 2, with Kbar^T)
+constexpr uint32_t SB_KB = 57344;         // Kbar^T
+constexpr uint32_t SB_VEC = 90112;        // 2 x 1 KB record vectors (double-buffered)
+constexpr uint32_t SB_V = 92160;          // 16 KB: v chunk sw (TMA) = V^T, MN-major operand
+constexpr uint32_t SB_S = 108544;         // 32 KB: S^T bf16 K-major il [j][i]
+constexpr uint32_t SB_MISC = 141312;      // 3 x u64 mbarriers, TMEM base
+constexpr uint32_t SMEM_B_USED = SB_MISC + 64;
+constexpr uint32_t SMEM_B_ALLOC = SMEM_B_USED + 1024;
+static_assert(SB_T == R_T && SB_A == R_A && SB_KB == R_KB, "record pieces map onto shared memory");
+static_assert(SMEM_B_ALLOC <= 232448, "dynamic shared memory limit (227 KB)");
+constexpr uint32_t TMB_S = 0;             // S^T master fp32 (lane j, column i), 128 columns
+constexpr uint32_t TMB_U = 128;           // U^T, 64 columns
+constexpr uint32_t TMB_O = 192;           // O^T, 64 columns (N = 128 with TMB_U in the first round)
+constexpr uint32_t COPY1 = R_A - R_WQ;    // bytes of [-W ; Q0] + T'
+constexpr uint32_t COPY2 = R_VEC - R_A;   // bytes of A' + Kbar^T
+
+__global__ void __launch_bounds__(NTB, 1)
+state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const float *__restrict__ S0,
+                  float *__restrict__ o, float *__restrict__ S_out, const int32_t *__restrict__ cu,
+                  const int32_t *__restrict__ chunk_off, int N, int H, int max_chunks,
+                  const uint8_t *__restrict__ recs) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bar_a = reinterpret_cast<uint64_t *>(sm + SB_MISC);
+    uint64_t *bar_b = bar_a + 1;
+    uint64_t *bar_mma = bar_a + 2;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SB_MISC + 32);
+    __shared__ int s_seq;
+
+    const int t = threadIdx.x;
+    const int warp = t >> 5;
+    const int ch = t & 127;
+    const int qt = t >> 7;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+
+    const int h = blockIdx.x % H;
+    const int rank = blockIdx.x / H;
+    const int n = lpt_sequence(cu, N, rank, &s_seq);
+    const int tok0 = cu[n];
+    const int len = cu[n + 1] - tok0;
+    const size_t st_off = ((size_t)n * H + h) * kDK * kDV;
+    const int cbase = chunk_off[n];
+    int nch = len > 0 ? (len + C - 1) / C : 0;
+    bool failed = false;
+    if (chunk_off[n + 1] - cbase != nch || chunk_off[n + 1] > max_chunks) {
+        nch = 0;                          // the plan does not match the workspace
+        failed = true;
+    }
+
+    if (warp == 0) tmem_alloc(s_tmem, 256);
+    if (t == 0) {
+        mbar_init(bar_a, 1);
+        mbar_init(bar_b, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        prefetch_tmap(&map_v);
+    }
+    sync_tc();
+    const uint32_t tmem = *s_tmem;
+
+    // ---- initial state: S^T master in TMEM (lane j, column i) + bf16 copy
+    {
+        float sv[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const int i = 32 * qt + c;
+            sv[c] = S0 ? S0[st_off + (size_t)i * kDV + ch] : 0.f;
+        }
+        float a[16], b2[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            a[c] = sv[c];
+            b2[c] = sv[16 + c];
+        }
+        tmem_st16(tmem + lane_base + TMB_S + 32 * qt, a);
+        tmem_st16(tmem + lane_base + TMB_S + 32 * qt + 16, b2);
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+            float x8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x8[u] = sv[8 * c8 + u];
+            *reinterpret_cast<uint4 *>(sm + SB_S + km_bf16(ch, 32 * qt + 8 * c8, 2048)) = pack_bf8(x8);
+        }
+        tmem_wait_st();
+    }
+    fence_proxy_async_smem();
+    sync_tc();
+
+    auto rec_at = [&](int j) -> const uint8_t * {
+        return recs + ((size_t)(cbase + j) * H + h) * REC_BYTES;
+    };
+    auto issue_a = [&](int j) {
+        const uint8_t *r = rec_at(j);
+        mbar_arrive_expect_tx(bar_a, COPY1 + 1024 + 16384);
+        bulk_load(sm + SB_WQ, r + R_WQ, COPY1, bar_a);
+        bulk_load(sm + SB_VEC + 1024 * (j & 1), r + R_VEC, 1024, bar_a);
+        tma_load_3d(sm + SB_V, &map_v, bar_a, 0, h, tok0 + j * C);
+        tma_load_3d(sm + SB_V + 8192, &map_v, bar_a, 64, h, tok0 + j * C);
+    };
+    auto issue_b = [&](int j) {
+        mbar_arrive_expect_tx(bar_b, COPY2);
+        bulk_load(sm + SB_A, rec_at(j) + R_A, COPY2, bar_b);
+    };
+    if (t == 0 && nch > 0) {
+        issue_a(0);
+        issue_b(0);
+    }
+    int issued_a = nch > 0, issued_b = nch > 0, issued_mma = 0;
+    uint32_t mma_phase = 0;
+
+    for (int j = 0; j < nch && !failed; ++j) {
+        const int c0 = j * C;
+        const int Lc = min(C, len - c0);
+        const uint32_t par = (uint32_t)(j & 1);
+        const float *vec = reinterpret_cast<const float *>(sm + SB_VEC + 1024 * par);
+
+        // ===== round 1: D_U = -(W S)^T + (T' V)^T, D_O = (Q0 S)^T ============
+        if (!wait_all(bar_a, par)) { failed = true; break; }
+        if (t == 0) {
+            const uint32_t id1 = instr_desc(kFmtBF16, 128, 128, 0, 0);
+            const uint32_t idv = instr_desc(kFmtBF16, 128, 64, 1, 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t as = smem_desc(smem_u32(sm + SB_S + 256 * kk), 128, 2048, kSwizzleNone);
+                const uint64_t bw = smem_desc(
+                    smem_u32(sm + SB_WQ + (uint32_t)(kk >> 2) * 16384 + (uint32_t)(kk & 3) * 32), 16,
+                    1024, kSwizzle128B);
+                mma_bf16_ss(tmem + TMB_U, as, bw, id1, kk > 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t av = smem_desc(smem_u32(sm + SB_V + 2048 * kk), 8192, 1024, kSwizzle128B);
+                const uint64_t bt = smem_desc(smem_u32(sm + SB_T + 256 * kk), 128, 1024, kSwizzleNone);
+                mma_bf16_ss(tmem + TMB_U, av, bt, idv, 1);
+            }
+            mma_commit(bar_mma);
+        }
+        ++issued_mma;
+        // S <- Diag(e^{b_L}) S in TMEM while the MMAs run (they read shared memory only)
+        {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t col = 32 * qt + 16 * hh;
+                float sv[16];
+                tmem_ld16(tmem + lane_base + TMB_S + col, sv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 16; ++c) sv[c] *= vec[128 + col + c];
+                tmem_st16(tmem + lane_base + TMB_S + col, sv);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+        }
+        if (!wait_all(bar_mma, mma_phase)) { failed = true; break; }
+        mma_phase ^= 1;
+        tc_fence_after();
+
+        // ===== u = D_U + beta v, rounded to tf32 in place in TMEM =============
+        float uv[16];
+        {
+            tmem_ld16(tmem + lane_base + TMB_U + 16 * qt, uv);
+            tmem_wait_ld();
+            float ut[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int r = 16 * qt + k;
+                uv[k] = fmaf(vec[r], bf(sm + SB_V + sw_elem64(r, ch)), uv[k]);
+                ut[k] = __uint_as_float(to_tf32(uv[k]));
+            }
+            tmem_st16(tmem + lane_base + TMB_U + 16 * qt, ut);
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        if (!wait_all(bar_b, par)) { failed = true; break; }
+        tc_fence_after();
+
+        // ===== round 2: D_O += (A' U)^T, S^T += (Kbar^T U)^T (tf32, U^T from TMEM)
+        if (t == 0) {
+            // round-1 operands and v are consumed: fetch the next chunk's
+            if (j + 1 < nch) issue_a(j + 1);
+            const uint32_t ido = instr_desc(kFmtTF32, 128, 64, 0, 0);
+            const uint32_t ids = instr_desc(kFmtTF32, 128, 128, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t ba = smem_desc(smem_u32(sm + SB_A + 256 * kk), 128, 2048, kSwizzleNone);
+                const uint64_t bk = smem_desc(smem_u32(sm + SB_KB + 256 * kk), 128, 2048, kSwizzleNone);
+                mma_tf32_ts(tmem + TMB_O, tmem + TMB_U + 8 * kk, ba, ido, 1);
+                mma_tf32_ts(tmem + TMB_S, tmem + TMB_U + 8 * kk, bk, ids, 1);
+            }
+            mma_commit(bar_mma);
+        }
+        issued_a += (j + 1 < nch);
+        ++issued_mma;
+        if (!wait_all(bar_mma, mma_phase)) { failed = true; break; }
+        mma_phase ^= 1;
+        tc_fence_after();
+        if (t == 0 && j + 1 < nch) issue_b(j + 1);
+        issued_b += (j + 1 < nch);
+
+        // ===== o = D_O + (q.k) u;  bf16 copy of the new S^T ====================
+        {
+            float ov[16];
+            tmem_ld16(tmem + lane_base + TMB_O + 16 * qt, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int r = 16 * qt + k;
+                if (r < Lc) o[((size_t)(tok0 + c0 + r) * H + h) * kDV + ch] = fmaf(vec[64 + r], uv[k], ov[k]);
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t col = 32 * qt + 16 * hh;
+                float sv[16];
+                tmem_ld16(tmem + lane_base + TMB_S + col, sv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c8 = 0; c8 < 2; ++c8) {
+                    float x8[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) x8[u] = sv[8 * c8 + u];
+                    *reinterpret_cast<uint4 *>(sm + SB_S + km_bf16(ch, col + 8 * c8, 2048)) = pack_bf8(x8);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        sync_tc();
+    }
+
+    if (failed) {
+        if (t == 0) atomicOr(&g_kda_split_error, 1u);
+        // let copies and MMAs in flight finish (bounded) before freeing TMEM
+        if (issued_a) mbar_wait(bar_a, (uint32_t)(issued_a - 1) & 1u, kWaitLimit);
+        if (issued_b) mbar_wait(bar_b, (uint32_t)(issued_b - 1) & 1u, kWaitLimit);
+        if (issued_mma) mbar_wait(bar_mma, (uint32_t)(issued_mma - 1) & 1u, kWaitLimit);
+    } else {
+        // ---- final state: S_out[i][j] from the TMEM master (lane j, column i)
+        float sv[32];
+        tmem_ld32(tmem + lane_base + TMB_S + 32 * qt, sv);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const int i = 32 * qt + c;
+            S_out[st_off + (size_t)i * kDV + ch] = sv[c];
+        }
+    }
+    sync_tc();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ---- workspace: a library-owned stream-ordered pool per device that keeps
+// its memory between calls (release threshold = max), so only the first call
+// of a given size reaches the driver's allocator.
+constexpr int kMaxDevices = 64;
+std::mutex g_pool_mu;
+cudaMemPool_t g_pool[kMaxDevices] = {};
+
+cudaError_t ws_alloc(void **p, size_t bytes, cudaStream_t s) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    cudaMemPool_t pool;
+    {
+        std::lock_guard<std::mutex> lk(g_pool_mu);
+        if (!g_pool[dev]) {
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            e = cudaMemPoolCreate(&g_pool[dev], &props);
+            if (e != cudaSuccess) {
+                g_pool[dev] = nullptr;
+                return e;
+            }
+            uint64_t thr = ~0ull;
+            cudaMemPoolSetAttribute(g_pool[dev], cudaMemPoolAttrReleaseThreshold, &thr);
+        }
+        pool = g_pool[dev];
+    }
+    return cudaMallocFromPoolAsync(p, bytes, pool, s);
+}
+
+}  // namespace
+
+size_t prefill_split_workspace_bytes(int N, int64_t T, int H) {
+    const int64_t max_chunks = (T + C - 1) / C + N;
+    const size_t off_bytes = ((size_t)(N + 1) * sizeof(int32_t) + 1023) & ~(size_t)1023;
+    return off_bytes + (size_t)max_chunks * (size_t)H * REC_BYTES;
+}
+
+cudaError_t launch_prefill_split(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, const float *S0, float *o, float *S_out,
+                                 const int32_t *cu_seqlens, int N, int64_t T, int H,
+                                 cudaStream_t stream) {
+    const int64_t max_chunks = (T + C - 1) / C + N;
+    if (max_chunks * H >= (int64_t(1) << 31) || max_chunks >= (int64_t(1) << 31))
+        return cudaErrorInvalidValue;
+    CUtensorMap mq, mk, mv, mg;
+    if (!make_map_bf16(&mq, q, T, H, 64, true) || !make_map_bf16(&mk, k, T, H, 64, true) ||
+        !make_map_bf16(&mv, v, T, H, 64, true) || !make_map_f32(&mg, g, T, H))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(intra_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_A_ALLOC);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_B_ALLOC);
+    if (e != cudaSuccess) return e;
+
+    void *ws = nullptr;
+    e = ws_alloc(&ws, prefill_split_workspace_bytes(N, T, H), stream);
+    if (e != cudaSuccess) return e;
+    int32_t *chunk_off = static_cast<int32_t *>(ws);
+    uint8_t *recs = static_cast<uint8_t *>(ws) +
+                    (((size_t)(N + 1) * sizeof(int32_t) + 1023) & ~(size_t)1023);
+
+    chunk_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, chunk_off);
+    intra_chunk_kernel<<<(unsigned)(max_chunks * H), NTA, SMEM_A_ALLOC, stream>>>(
+        mq, mk, mg, beta, cu_seqlens, chunk_off, N, H, recs);
+    state_pass_kernel<<<(unsigned)((int64_t)N * H), NTB, SMEM_B_ALLOC, stream>>>(
+        mv, S0, o, S_out, cu_seqlens, chunk_off, N, H, (int)max_chunks, recs);
+    e = cudaGetLastError();
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    return e != cudaSuccess ? e : ef;
+}
+
+cudaError_t read_split_error(unsigned int *code, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_kda_split_error, sizeof(unsigned int));
+    if (e != cudaSuccess || !reset) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_kda_split_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace kda

@@ -38,7 +38,7 @@
 #include <cudaTypedefs.h>
 
 #include "kda_internal.h"
-#include "tc_ptx.cuh"
+#include "tc_layout.cuh"
 
 namespace kda {
 
@@ -50,7 +50,6 @@ using namespace tc;
 
 constexpr int C = 64;
 constexpr int NT = 512;
-constexpr uint32_t kWaitLimit = 1u << 22;
 
 // shared memory map (bytes from a 1024-aligned base).  "sw" = 128-byte
 // swizzled canonical layout, "il" = interleaved (no swizzle) canonical layout.
@@ -91,82 +90,9 @@ constexpr uint32_t TM_P = 128;    // (K0 S)^T, 64 cols inside TM_DS (M1 -> M2)
 constexpr uint32_t TM_U = 320;    // U D, 64 cols (after the Gram epilogue)
 constexpr uint32_t TM_O = 448;    // O D, 64 cols
 
-// ---- canonical operand layouts --------------------------------------------
-// interleaved K-major bf16: element (m, k)
-__device__ __forceinline__ uint32_t km_bf16(int m, int k, uint32_t sbo) {
-    return (uint32_t)(m >> 3) * sbo + (uint32_t)(k >> 3) * 128u + (uint32_t)(m & 7) * 16u +
-           (uint32_t)(k & 7) * 2u;
-}
-// interleaved K-major tf32: element (m, k)
-__device__ __forceinline__ uint32_t km_tf32(int m, int k, uint32_t sbo) {
-    return (uint32_t)(m >> 3) * sbo + (uint32_t)(k >> 2) * 128u + (uint32_t)(m & 7) * 16u +
-           (uint32_t)(k & 3) * 4u;
-}
-// interleaved MN-major bf16: element (k, mn)
-__device__ __forceinline__ uint32_t mn_bf16(int k, int mn, uint32_t lbo) {
-    return (uint32_t)(mn & 7) * 2u + (uint32_t)(mn >> 3) * 128u + (uint32_t)(k & 7) * 16u +
-           (uint32_t)(k >> 3) * lbo;
-}
-// 128B-swizzled tile with 128-byte rows: 16-byte chunk `c` (0..15 across two
-// 64-element halves, bf16) of row `row`; `half_bytes` = rows * 128.
-__device__ __forceinline__ uint32_t sw_chunk(int row, int c, uint32_t half_bytes) {
-    return (uint32_t)(c >> 3) * half_bytes + (uint32_t)row * 128u +
-           ((uint32_t)((c & 7) ^ (row & 7)) << 4);
-}
-// element (row, col) of a bf16 sw tile with two 64-column halves of 64 rows
-__device__ __forceinline__ uint32_t sw_elem64(int row, int col) {
-    return sw_chunk(row, col >> 3, 8192) + (uint32_t)(col & 7) * 2u;
-}
-
-__device__ __forceinline__ float bf(const uint8_t *p) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
-}
-__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-__device__ __forceinline__ uint4 pack_bf8(const float (&x)[8]) {
-    return make_uint4(pack_bf2(x[0], x[1]), pack_bf2(x[2], x[3]), pack_bf2(x[4], x[5]),
-                      pack_bf2(x[6], x[7]));
-}
-__device__ __forceinline__ void unpack_bf8(uint4 u, float (&x)[8]) {
-    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(h[e]);
-        x[2 * e] = f.x;
-        x[2 * e + 1] = f.y;
-    }
-}
-
 struct Bars {
     uint64_t *qk, *v, *mma, *g;
 };
-
-// Bounded wait by every thread, then a block-wide verdict.
-__device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
-    const bool ok = mbar_wait(bar, parity, kWaitLimit);
-    return __syncthreads_and(ok) != 0;
-}
-
-__device__ __forceinline__ void sync_tc() {
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-}
-
-// 32 consecutive TMEM columns of this thread's lane (two x16 loads, one wait)
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    float a[16], b[16];
-    tmem_ld16(taddr, a);
-    tmem_ld16(taddr + 16, b);
-    tmem_wait_ld();
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        v[c] = a[c];
-        v[16 + c] = b[c];
-    }
-}
 
 __device__ __forceinline__ void issue_load_qk(uint8_t *sm, const CUtensorMap *mq,
                                               const CUtensorMap *mk, uint64_t *bar, int h,
@@ -829,48 +755,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        cudaDriverEntryPointQueryResult q;
-        void *p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// 3D map over a [T, H, 128] bf16 tensor: dims (128, H, T), box (bw, 1, 64).
-bool make_map(CUtensorMap *m, const void *base, int64_t T, int H, uint32_t bw, bool swz) {
-    auto enc = get_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
-    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};
-    cuuint32_t box[3] = {bw, 1, 64};
-    cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
-                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-// 3D map over a [T, H, 128] fp32 tensor: dims (128, H, T), box (32, 1, 64), 128B swizzle.
-bool make_map_f32(CUtensorMap *m, const void *base, int64_t T, int H) {
-    auto enc = get_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
-    cuuint64_t strides[2] = {128 * 4, (cuuint64_t)H * 128 * 4};
-    cuuint32_t box[3] = {32, 1, 64};
-    cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides,
-                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
@@ -878,8 +762,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               const int32_t *cu_seqlens, int N, int64_t T, int H,
                               cudaStream_t stream) {
     CUtensorMap mq, mk, mv, mg;
-    if (!make_map(&mq, q, T, H, 64, true) || !make_map(&mk, k, T, H, 64, true) ||
-        !make_map(&mv, v, T, H, 64, true) || !make_map_f32(&mg, g, T, H))
+    if (!make_map_bf16(&mq, q, T, H, 64, true) || !make_map_bf16(&mk, k, T, H, 64, true) ||
+        !make_map_bf16(&mv, v, T, H, 64, true) || !make_map_f32(&mg, g, T, H))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
