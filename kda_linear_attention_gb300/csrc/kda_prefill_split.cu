@@ -97,9 +97,9 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t *__restr
 constexpr int NTA = 256;
 constexpr uint32_t SA_X = 0;              // 32 KB: q|k staging (TMA) -> X [128][128] sw; then M fp32 [64][68] + temps
 constexpr uint32_t SA_KH = 32768;         // 40 KB: g staging fp32 (TMA) -> Khat [160][128] sw
-constexpr uint32_t SA_T = SA_KH;          //   after the Gram: T' bf16 il [r][s], 8 KB
-constexpr uint32_t SA_WST = SA_KH + 8192; //   after the Gram: -W staging, 2 x [64][128 B] sw, 16 KB
-constexpr uint32_t SA_K0 = 73728;         // 16 KB: K0 [64 s][128 i] sw (MN-major A of the W product)
+constexpr uint32_t SA_T = SA_KH;          //   after the Gram: T Diag(beta) bf16 il [r][s] (8 KB; the
+                                          //   W product reads 16 KB as its M = 128 rows)
+constexpr uint32_t SA_K0 = 73728;         // 16 KB: K0 [64 s][128 i] sw (MN-major B of the W product)
 constexpr uint32_t SA_MISC = 90112;
 constexpr uint32_t MA_BETA = 0;           // float[64]
 constexpr uint32_t MA_GAM = 256;          // float[128]  e^{b_L}
@@ -115,7 +115,7 @@ constexpr uint32_t SMEM_A_ALLOC = SMEM_A_USED + 1024;
 static_assert(2 * (SMEM_A_ALLOC + 1024) <= 233472, "two intra-chunk CTAs per SM");
 constexpr int MLD = 68;                   // row stride (floats) of M / T
 constexpr uint32_t TMA_G = 0;             // Gram D, 160 columns
-constexpr uint32_t TMA_W = 0;             // (T' K0)^T, 64 columns (after the Gram epilogue)
+constexpr uint32_t TMA_W = 0;             // W, 128 columns (after the Gram epilogue)
 
 __global__ void __launch_bounds__(NTA, 2)
 intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -182,25 +182,26 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
 
     if (!failed) {
         // ===== decay prefix sums: column scan in place in the g tile =========
-        auto g_at = [&](int r, int c) -> float * {
-            return reinterpret_cast<float *>(sm + SA_KH + 8192 * (c >> 5) + r * 128 +
-                                             ((((c & 31) >> 2) ^ (r & 7)) << 4) + (c & 3) * 4);
-        };
-#pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-            const int i = t & 127, u = (t >> 7) + 2 * pass;
-            float acc = 0.f, at_last = 0.f;
+        // thread = (channels 4qd..4qd+3, sub-block u); the tile is four 128B-
+        // swizzled boxes of [64 rows][32 channels] fp32
+        if (t < 128) {
+            const int qd = t & 31, u = t >> 5;
+            uint8_t *colp = sm + SA_KH + 8192 * (qd >> 3);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), at_last = acc;
             const int lastrow = min(16 * u + 15, Lc - 1);
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
                 const int r = 16 * u + rr;
-                float *pg = g_at(r, i);
-                acc += (r < Lc) ? *pg : 0.f;
-                *pg = acc;
+                float4 *pg = reinterpret_cast<float4 *>(colp + r * 128 + (((qd & 7) ^ (rr & 7)) << 4));
+                if (r < Lc) {
+                    const float4 x = *pg;
+                    acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+                }
+                *pg = acc;                         // local (sub-block) prefix
                 if (r == lastrow) at_last = acc;
             }
-            s_tot[u * 128 + i] = acc;
-            s_sig[u * 128 + i] = at_last;
+            *reinterpret_cast<float4 *>(s_tot + u * 128 + 4 * qd) = acc;      // sub-block total
+            *reinterpret_cast<float4 *>(s_sig + u * 128 + 4 * qd) = at_last;  // at its last valid row
         }
         __syncthreads();
         if (t < 128) {
@@ -320,38 +321,45 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             }
             *reinterpret_cast<uint4 *>(rec + R_WQ + sw_chunk(64 + r, cc, 16384)) = pack_bf8(q0);
             *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, cc, 8192)) = pack_bf8(k0);
-            // Kbar^T tf32 K-major il [i][s]: a 4x4 transpose inside each quad of
-            // lanes (4 consecutive rows) gives every lane 4 consecutive s for
-            // channels 2b, 2b+1: 16-byte stores.
+            // Kbar^T tf32 K-major il [i][s]: a 4x4 transpose of channel pairs
+            // inside each quad of lanes (4 consecutive rows) in two butterfly
+            // stages leaves every lane 4 consecutive s for channels 2bq, 2bq+1
             {
-                float kbv[8];
+                float kb[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) kbv[c] = kv[c] * G[c] * el[c];
+                for (int c = 0; c < 8; ++c) kb[c] = kv[c] * G[c] * el[c];
                 const int bq = rb & 3;
-                float o0[4], o1[4];
+                const bool b0 = (bq & 1) != 0, b1 = (bq & 2) != 0;
+                // stage 1 (lanes bq, bq^2): keep pairs 2b1, 2b1+1 of this row and
+                // receive the same pairs of row bq^2
+                float kp[4], rp[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int dst = (bq - k) & 3;
-                    const float s0 = dst == 0 ? kbv[0] : dst == 1 ? kbv[2] : dst == 2 ? kbv[4] : kbv[6];
-                    const float s1 = dst == 0 ? kbv[1] : dst == 1 ? kbv[3] : dst == 2 ? kbv[5] : kbv[7];
-                    const int srcl = (lane & ~3) | ((bq + k) & 3);
-                    const float r0 = __shfl_sync(0xffffffffu, s0, srcl);
-                    const float r1 = __shfl_sync(0xffffffffu, s1, srcl);
-                    const int srow = (bq + k) & 3;
+                for (int e = 0; e < 4; ++e) {
+                    kp[e] = b1 ? kb[4 + e] : kb[e];
+                    rp[e] = __shfl_xor_sync(0xffffffffu, b1 ? kb[e] : kb[4 + e], 2);
+                }
+                // stage 2 (lanes bq, bq^1): keep pair bq of rows bq, bq^2 and
+                // receive it for rows bq^1, bq^3; v[m] = row bq ^ m
+                float v[4][2];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (e == srow) {
-                            o0[e] = r0;
-                            o1[e] = r1;
-                        }
-                    }
+                for (int f = 0; f < 2; ++f) {
+                    v[0][f] = b0 ? kp[2 + f] : kp[f];
+                    v[2][f] = b0 ? rp[2 + f] : rp[f];
+                    v[1][f] = __shfl_xor_sync(0xffffffffu, b0 ? kp[f] : kp[2 + f], 1);
+                    v[3][f] = __shfl_xor_sync(0xffffffffu, b0 ? rp[f] : rp[2 + f], 1);
                 }
                 const int s0r = 16 * u + (rb & ~3);
                 const int i0 = 8 * cc + 2 * bq;
-                *reinterpret_cast<uint4 *>(rec + R_KB + km_tf32(i0, s0r, 2048)) =
-                    make_uint4(to_tf32(o0[0]), to_tf32(o0[1]), to_tf32(o0[2]), to_tf32(o0[3]));
-                *reinterpret_cast<uint4 *>(rec + R_KB + km_tf32(i0 + 1, s0r, 2048)) =
-                    make_uint4(to_tf32(o1[0]), to_tf32(o1[1]), to_tf32(o1[2]), to_tf32(o1[3]));
+#pragma unroll
+                for (int f = 0; f < 2; ++f) {
+                    // y[r] = v[r ^ bq]
+                    const float w0 = b0 ? v[1][f] : v[0][f], w1 = b0 ? v[0][f] : v[1][f];
+                    const float w2 = b0 ? v[3][f] : v[2][f], w3 = b0 ? v[2][f] : v[3][f];
+                    const float y0 = b1 ? w2 : w0, y1 = b1 ? w3 : w1;
+                    const float y2 = b1 ? w0 : w2, y3 = b1 ? w1 : w3;
+                    *reinterpret_cast<uint4 *>(rec + R_KB + km_tf32(i0 + f, s0r, 2048)) =
+                        make_uint4(to_tf32(y0), to_tf32(y1), to_tf32(y2), to_tf32(y3));
+                }
             }
         }
 #pragma unroll
@@ -551,34 +559,37 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         __syncthreads();
-        // T' = (T - I) Diag(beta), bf16 K-major il [r][s]: shared memory (B of
-        // the W product) and the record (B of the U~ product in the state pass)
+        // T' = (T - I) Diag(beta), bf16 K-major il [r][s], to the record (B of
+        // the U~ product in the state pass); T Diag(beta) = T' + Diag(beta) to
+        // shared memory (A of the W product)
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass) {
             const int r = (t >> 3) + 32 * pass, s0 = (t & 7) * 8;
             const float4 a = *reinterpret_cast<const float4 *>(Mm + r * MLD + s0);
             const float4 b4 = *reinterpret_cast<const float4 *>(Mm + r * MLD + s0 + 4);
             const float tv[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
-            float w8[8];
+            float w8[8], d8[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int s3 = s0 + u;
-                w8[u] = (s3 < r) ? tv[u] * s_beta[s3] : 0.f;
+                const float bs = s_beta[s3];
+                w8[u] = (s3 < r) ? tv[u] * bs : 0.f;
+                d8[u] = (s3 == r) ? bs : w8[u];
             }
-            const uint4 pk = pack_bf8(w8);
-            *reinterpret_cast<uint4 *>(sm + SA_T + km_bf16(r, s0, 1024)) = pk;
-            *reinterpret_cast<uint4 *>(rec + R_T + km_bf16(r, s0, 1024)) = pk;
+            *reinterpret_cast<uint4 *>(rec + R_T + km_bf16(r, s0, 1024)) = pack_bf8(w8);
+            *reinterpret_cast<uint4 *>(sm + SA_T + km_bf16(r, s0, 1024)) = pack_bf8(d8);
         }
         fence_proxy_async_smem();
         sync_tc();
 
-        // ===== W^T = (T' K0)^T: D_W[i][r], A = K0 (MN-major), B = T' =========
+        // ===== W = T Diag(beta) K0: D_W[r][i] (M = 128, rows 64..127 unused),
+        // A = T Diag(beta) (K-major), B = K0 (MN-major)
         if (t == 0) {
-            const uint32_t idw = instr_desc(kFmtBF16, 128, 64, 1, 0);
+            const uint32_t idw = instr_desc(kFmtBF16, 128, 128, 0, 1);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t a = smem_desc(smem_u32(sm + SA_K0 + 2048 * kk), 8192, 1024, kSwizzle128B);
-                const uint64_t b = smem_desc(smem_u32(sm + SA_T + 256 * kk), 128, 1024, kSwizzleNone);
+                const uint64_t a = smem_desc(smem_u32(sm + SA_T + 256 * kk), 128, 1024, kSwizzleNone);
+                const uint64_t b = smem_desc(smem_u32(sm + SA_K0 + 2048 * kk), 8192, 1024, kSwizzle128B);
                 mma_bf16_ss(tmem + TMA_W, a, b, idw, kk > 0);
             }
             mma_commit(bar_mma);
@@ -588,25 +599,23 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     }
     if (!failed) {
         tc_fence_after();
-        // ===== -W = -(T' K0 + Diag(beta) K0) -> bf16 sw staging -> record rows 0..63
-        {
-            const int i = t & 127, hh = t >> 7;
-            float d[32];
-            tmem_ld32(tmem + lane_base + TMA_W + 32 * hh, d);
+        // ===== -W -> record rows 0..63 (bf16, K-major sw): lane r, 64 channels
+        if ((warp & 3) < 2) {
+            const int r = 32 * (warp & 3) + lane, half = warp >> 2;
 #pragma unroll
-            for (int rr = 0; rr < 32; ++rr) {
-                const int r = 32 * hh + rr;
-                const uint32_t off = sw_elem64(r, i);
-                const float w = fmaf(s_beta[r], bf(sm + SA_K0 + off), d[rr]);
-                *reinterpret_cast<__nv_bfloat16 *>(sm + SA_WST + off) = __float2bfloat16_rn(-w);
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float d[16];
+                tmem_ld16(tmem + lane_base + TMA_W + 64 * half + 16 * q4, d);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c8 = 0; c8 < 2; ++c8) {
+                    float x8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x8[e] = -d[8 * c8 + e];
+                    *reinterpret_cast<uint4 *>(rec + R_WQ + sw_chunk(r, 8 * half + 2 * q4 + c8, 16384)) =
+                        pack_bf8(x8);
+                }
             }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int e = t; e < 1024; e += NTA) {
-            const int kh = e >> 9, off = (e & 511) * 16;
-            *reinterpret_cast<uint4 *>(rec + R_WQ + kh * 16384 + off) =
-                *reinterpret_cast<const uint4 *>(sm + SA_WST + kh * 8192 + off);
         }
     }
     if (failed) {
