@@ -639,7 +639,8 @@ constexpr uint32_t SB_KB = 57344;         // Kbar^T
 constexpr uint32_t SB_VEC = 90112;        // 2 x 1 KB record vectors (double-buffered)
 constexpr uint32_t SB_V = 92160;          // 16 KB: v chunk sw (TMA) = V^T, MN-major operand
 constexpr uint32_t SB_S = 108544;         // 32 KB: S^T bf16 K-major il [j][i]
-constexpr uint32_t SB_MISC = 141312;      // 3 x u64 mbarriers, TMEM base
+constexpr uint32_t SB_O = 141312;         // 32 KB: o chunk, 4 x [64 r][32 j] fp32 (TMA store source)
+constexpr uint32_t SB_MISC = 174080;      // 3 x u64 mbarriers, TMEM base
 constexpr uint32_t SMEM_B_USED = SB_MISC + 64;
 constexpr uint32_t SMEM_B_ALLOC = SMEM_B_USED + 1024;
 static_assert(SB_T == R_T && SB_A == R_A && SB_KB == R_KB, "record pieces map onto shared memory");
@@ -651,7 +652,8 @@ constexpr uint32_t COPY1 = R_A - R_WQ;    // bytes of [-W ; Q0] + T'
 constexpr uint32_t COPY2 = R_VEC - R_A;   // bytes of A' + Kbar^T
 
 __global__ void __launch_bounds__(NTB, 1)
-state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const float *__restrict__ S0,
+state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+                  const float *__restrict__ S0,
                   float *__restrict__ o, float *__restrict__ S_out, const int32_t *__restrict__ cu,
                   const int32_t *__restrict__ chunk_off, int N, int H, int max_chunks,
                   const uint8_t *__restrict__ recs) {
@@ -690,6 +692,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const float *__rest
         mbar_init(bar_mma, 1);
         fence_mbar_init();
         prefetch_tmap(&map_v);
+        prefetch_tmap(&map_o);
     }
     sync_tc();
     const uint32_t tmem = *s_tmem;
@@ -834,14 +837,28 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const float *__rest
         issued_b += (j + 1 < nch);
 
         // ===== o = D_O + (q.k) u;  bf16 copy of the new S^T ====================
+        // A full chunk of o goes out through shared memory and four TMA stores;
+        // the last, partial chunk of a sequence is stored row by row so that
+        // the next sequence's rows are never written.
         {
             float ov[16];
             tmem_ld16(tmem + lane_base + TMB_O + 16 * qt, ov);
             tmem_wait_ld();
+            if (Lc == C) {
+                if (t == 0) bulk_wait_read();    // the previous chunk's stores have read SB_O
+                __syncthreads();
+                float *so = reinterpret_cast<float *>(sm + SB_O + 8192 * (ch >> 5)) + (ch & 31);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int r = 16 * qt + k;
-                if (r < Lc) o[((size_t)(tok0 + c0 + r) * H + h) * kDV + ch] = fmaf(vec[64 + r], uv[k], ov[k]);
+                for (int k = 0; k < 16; ++k) {
+                    const int r = 16 * qt + k;
+                    so[r * 32] = fmaf(vec[64 + r], uv[k], ov[k]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int r = 16 * qt + k;
+                    if (r < Lc) o[((size_t)(tok0 + c0 + r) * H + h) * kDV + ch] = fmaf(vec[64 + r], uv[k], ov[k]);
+                }
             }
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -860,7 +877,13 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const float *__rest
         }
         fence_proxy_async_smem();
         sync_tc();
+        if (t == 0 && Lc == C) {
+#pragma unroll
+            for (int bx = 0; bx < 4; ++bx) tma_store_3d(&map_o, sm + SB_O + 8192 * bx, 32 * bx, h, tok0 + c0);
+            bulk_commit();
+        }
     }
+    if (t == 0) bulk_wait();                 // o stores complete before the CTA exits
 
     if (failed) {
         if (t == 0) atomicOr(&g_kda_split_error, 1u);
@@ -930,9 +953,10 @@ cudaError_t launch_prefill_split(const void *q, const void *k, const void *v, co
     const int64_t max_chunks = (T + C - 1) / C + N;
     if (max_chunks * H >= (int64_t(1) << 31) || max_chunks >= (int64_t(1) << 31))
         return cudaErrorInvalidValue;
-    CUtensorMap mq, mk, mv, mg;
+    CUtensorMap mq, mk, mv, mg, mo;
     if (!make_map_bf16(&mq, q, T, H, 64, true) || !make_map_bf16(&mk, k, T, H, 64, true) ||
-        !make_map_bf16(&mv, v, T, H, 64, true) || !make_map_f32(&mg, g, T, H))
+        !make_map_bf16(&mv, v, T, H, 64, true) || !make_map_f32(&mg, g, T, H) ||
+        !make_map_f32_plain(&mo, o, T, H))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(intra_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_A_ALLOC);
@@ -952,7 +976,7 @@ cudaError_t launch_prefill_split(const void *q, const void *k, const void *v, co
     intra_chunk_kernel<<<(unsigned)(max_chunks * H), NTA, SMEM_A_ALLOC, stream>>>(
         mq, mk, mg, beta, cu_seqlens, chunk_off, N, H, recs);
     state_pass_kernel<<<(unsigned)((int64_t)N * H), NTB, SMEM_B_ALLOC, stream>>>(
-        mv, S0, o, S_out, cu_seqlens, chunk_off, N, H, (int)max_chunks, recs);
+        mv, mo, S0, o, S_out, cu_seqlens, chunk_off, N, H, (int)max_chunks, recs);
     e = cudaGetLastError();
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     return e != cudaSuccess ? e : ef;

@@ -130,5 +130,20 @@ inline bool make_map_f32(CUtensorMap *m, const void *base, int64_t T, int H) {
     return r == CUDA_SUCCESS;
 }
 
+// 3D map over a [T, H, 128] fp32 tensor: dims (128, H, T), box (32, 1, 64), no swizzle
+// (for TMA stores of [64 rows][32 channels] tiles).
+inline bool make_map_f32_plain(CUtensorMap *m, const void *base, int64_t T, int H) {
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {128 * 4, (cuuint64_t)H * 128 * 4};
+    cuuint32_t box[3] = {32, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace tc
 }  // namespace kda
