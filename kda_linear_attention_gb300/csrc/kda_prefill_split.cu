@@ -946,13 +946,15 @@ size_t prefill_split_workspace_bytes(int N, int64_t T, int H) {
     return off_bytes + (size_t)max_chunks * (size_t)H * REC_BYTES;
 }
 
-cudaError_t launch_prefill_split(const void *q, const void *k, const void *v, const float *g,
-                                 const float *beta, const float *S0, float *o, float *S_out,
-                                 const int32_t *cu_seqlens, int N, int64_t T, int H,
-                                 cudaStream_t stream) {
+namespace {
+
+// The three launches of one prefill, with the workspace at `ws` (at least
+// prefill_split_workspace_bytes(N, T, H) bytes).
+cudaError_t run_split(const void *q, const void *k, const void *v, const float *g,
+                      const float *beta, const float *S0, float *o, float *S_out,
+                      const int32_t *cu_seqlens, int N, int64_t T, int H, void *ws,
+                      cudaStream_t stream) {
     const int64_t max_chunks = (T + C - 1) / C + N;
-    if (max_chunks * H >= (int64_t(1) << 31) || max_chunks >= (int64_t(1) << 31))
-        return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv, mg, mo;
     if (!make_map_bf16(&mq, q, T, H, 64, true) || !make_map_bf16(&mk, k, T, H, 64, true) ||
         !make_map_bf16(&mv, v, T, H, 64, true) || !make_map_f32(&mg, g, T, H) ||
@@ -964,20 +966,33 @@ cudaError_t launch_prefill_split(const void *q, const void *k, const void *v, co
     e = cudaFuncSetAttribute(state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_B_ALLOC);
     if (e != cudaSuccess) return e;
-
-    void *ws = nullptr;
-    e = ws_alloc(&ws, prefill_split_workspace_bytes(N, T, H), stream);
-    if (e != cudaSuccess) return e;
     int32_t *chunk_off = static_cast<int32_t *>(ws);
     uint8_t *recs = static_cast<uint8_t *>(ws) +
                     (((size_t)(N + 1) * sizeof(int32_t) + 1023) & ~(size_t)1023);
-
     chunk_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, chunk_off);
     intra_chunk_kernel<<<(unsigned)(max_chunks * H), NTA, SMEM_A_ALLOC, stream>>>(
         mq, mk, mg, beta, cu_seqlens, chunk_off, N, H, recs);
     state_pass_kernel<<<(unsigned)((int64_t)N * H), NTB, SMEM_B_ALLOC, stream>>>(
         mv, mo, S0, o, S_out, cu_seqlens, chunk_off, N, H, (int)max_chunks, recs);
-    e = cudaGetLastError();
+    return cudaGetLastError();
+}
+
+bool grid_fits(int N, int64_t T, int H) {
+    const int64_t max_chunks = (T + C - 1) / C + N;
+    return max_chunks * H < (int64_t(1) << 31) && max_chunks < (int64_t(1) << 31);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_split(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, const float *S0, float *o, float *S_out,
+                                 const int32_t *cu_seqlens, int N, int64_t T, int H,
+                                 cudaStream_t stream) {
+    if (!grid_fits(N, T, H)) return cudaErrorInvalidValue;
+    void *ws = nullptr;
+    cudaError_t e = ws_alloc(&ws, prefill_split_workspace_bytes(N, T, H), stream);
+    if (e != cudaSuccess) return e;
+    e = run_split(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, T, H, ws, stream);
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     return e != cudaSuccess ? e : ef;
 }
