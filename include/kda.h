@@ -113,6 +113,39 @@ int kda_prefill_chunked(const void *q, const void *k, const void *v,
                         int dtype, void *stream);
 
 /*
+ * kda_prefill_chunked without any device allocation during the call.
+ *
+ * Same operation, arguments, layouts and results as kda_prefill_chunked.
+ * The recurrence itself has no such variant (the pages describe no
+ * workspace at all); this entry point exists for callers that may not
+ * allocate device memory inside a call: runtimes that budget all device
+ * memory in a fixed arena up front, where a library pool growing mid-call
+ * would break the budget, and latency-critical loops where the first growth
+ * of a pool (a driver allocation, which synchronises the device) cannot be
+ * afforded.
+ *
+ * The tensor-core path (bf16, chunk 64, T > 0) takes its workspace from a
+ * fixed 64 MiB array in the library's device image instead of the pool.  It
+ * needs 1024 * ceil(4 (N + 1) / 1024) + (ceil(T / 64) + N) * H * 91136
+ * bytes; larger inputs are rejected with KDA_ERR_WORKSPACE before anything
+ * is launched (for H = 96 and one sequence: T <= 384).  Every other dtype /
+ * chunk combination runs the CUDA-core kernel, which needs no workspace.
+ * Nothing in the array has to be cleared between calls.
+ *
+ * First call on each device: the library looks up the array's address
+ * (cudaGetSymbolAddress, which may load the library's device image); make
+ * that first call before any stream capture begins.  The array is shared by
+ * all calls on a device: two calls whose executions overlap (different
+ * streams, or different host threads) race on it and must be serialised by
+ * the caller.  Returns KDA_OK or a kda_status_t.
+ */
+int kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v,
+                                const float *g, const float *beta, const float *S0,
+                                float *o, float *S_out, const int32_t *cu_seqlens,
+                                int N, int64_t T, int H, int dk, int dv, int chunk,
+                                int dtype, void *stream);
+
+/*
  * One decode token for each of B sequences, state updated IN PLACE.
  *
  * Operation: the recurrence above applied once per (b, h) with

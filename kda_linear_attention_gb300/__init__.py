@@ -7,6 +7,7 @@ in the library's CUDA kernels; there is no CPU or PyTorch fallback, and the
 calls raise if the library has not been built.
 
     o, S_out = prefill_chunked(q, k, v, g, beta, cu_seqlens, S0=None, chunk=64)
+    o, S_out = prefill_chunked_noalloc(...)      # same, no device allocation
     o = decode_step(q, k, v, g, beta, S)          # S updated in place
 
 Shapes (token-major): q, k, g [T, H, 128]; v [T, H, 128]; beta [T, H];
@@ -20,8 +21,8 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["prefill_chunked", "decode_step", "device_error", "lib", "KDAError", "KDA_BF16",
-           "KDA_F32", "library_path"]
+__all__ = ["prefill_chunked", "prefill_chunked_noalloc", "decode_step", "device_error", "lib",
+           "KDAError", "KDA_BF16", "KDA_F32", "library_path"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libkda_gb300.so")
@@ -61,6 +62,8 @@ def lib() -> ctypes.CDLL:
         L.kda_prefill_chunked.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                           i32, i64, i32, i32, i32, i32, i32, vp]
         L.kda_prefill_chunked.restype = i32
+        L.kda_prefill_chunked_noalloc.argtypes = L.kda_prefill_chunked.argtypes
+        L.kda_prefill_chunked_noalloc.restype = i32
         L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
         L.kda_decode_step.restype = i32
         L.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
@@ -99,16 +102,7 @@ def _stream(device: torch.device, stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def prefill_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
-                    beta: torch.Tensor, cu_seqlens: torch.Tensor,
-                    S0: Optional[torch.Tensor] = None, chunk: int = 64,
-                    o: Optional[torch.Tensor] = None, S_out: Optional[torch.Tensor] = None,
-                    stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Chunked KDA prefill over packed varlen sequences (``kda_prefill_chunked``).
-
-    Returns (o [T, H, 128] fp32, S_out [N, H, 128, 128] fp32).  ``S_out`` may
-    be ``S0`` itself to update the states in place.
-    """
+def _prefill(fn_name: str, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_out, stream):
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("inputs must be CUDA tensors")
@@ -129,12 +123,39 @@ def prefill_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.
         S_out = torch.empty((N, H, DK, DV), dtype=torch.float32, device=dev)
     _check("o", o, torch.float32, (T, H, DV), dev)
     _check("S_out", S_out, torch.float32, (N, H, DK, DV), dev)
-    rc = lib().kda_prefill_chunked(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(o), _p(S_out),
-                                   _p(cu_seqlens), N, T, H, DK, DV, int(chunk), dt,
-                                   _stream(dev, stream))
+    rc = getattr(lib(), fn_name)(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(o), _p(S_out),
+                                 _p(cu_seqlens), N, T, H, DK, DV, int(chunk), dt,
+                                 _stream(dev, stream))
     if rc != 0:
-        raise KDAError(rc, "kda_prefill_chunked")
+        raise KDAError(rc, fn_name)
     return o, S_out
+
+
+def prefill_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                    beta: torch.Tensor, cu_seqlens: torch.Tensor,
+                    S0: Optional[torch.Tensor] = None, chunk: int = 64,
+                    o: Optional[torch.Tensor] = None, S_out: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Chunked KDA prefill over packed varlen sequences (``kda_prefill_chunked``).
+
+    Returns (o [T, H, 128] fp32, S_out [N, H, 128, 128] fp32).  ``S_out`` may
+    be ``S0`` itself to update the states in place.
+    """
+    return _prefill("kda_prefill_chunked", q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_out,
+                    stream)
+
+
+def prefill_chunked_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                            beta: torch.Tensor, cu_seqlens: torch.Tensor,
+                            S0: Optional[torch.Tensor] = None, chunk: int = 64,
+                            o: Optional[torch.Tensor] = None, S_out: Optional[torch.Tensor] = None,
+                            stream: Optional[torch.cuda.Stream] = None
+                            ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """``prefill_chunked`` through ``kda_prefill_chunked_noalloc``: the library
+    allocates nothing (its fixed scratch array bounds the input size; pass
+    ``o`` and ``S_out`` to keep this binding from allocating them either)."""
+    return _prefill("kda_prefill_chunked_noalloc", q, k, v, g, beta, cu_seqlens, S0, chunk, o,
+                    S_out, stream)
 
 
 def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,

@@ -38,6 +38,15 @@ cudaError_t launch_prefill_split(const void *q, const void *k, const void *v, co
                                  cudaStream_t stream);
 size_t prefill_split_workspace_bytes(int N, int64_t T, int H);
 
+// The same prefill with its workspace in a fixed file-scope device array of
+// kNoAllocScratchBytes (no allocation during the call); cudaErrorInvalidValue
+// when the workspace the sizes need is larger.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
+cudaError_t launch_prefill_split_noalloc(const void *q, const void *k, const void *v,
+                                         const float *g, const float *beta, const float *S0,
+                                         float *o, float *S_out, const int32_t *cu_seqlens, int N,
+                                         int64_t T, int H, cudaStream_t stream);
+
 // Read (and optionally clear) the device-side error words that the
 // tensor-core kernels set when a bounded wait gives up.
 cudaError_t read_device_error(unsigned int *code, bool reset);

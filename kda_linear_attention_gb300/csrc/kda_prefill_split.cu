@@ -997,6 +997,43 @@ cudaError_t launch_prefill_split(const void *q, const void *k, const void *v, co
     return e != cudaSuccess ? e : ef;
 }
 
+// ---- fixed scratch for kda_prefill_chunked_noalloc -------------------------
+// A file-scope device array replaces the pool workspace for callers that may
+// not allocate device memory during a call.  Nothing in it needs to start at
+// zero: the plan kernel writes every chunk offset and the intra-chunk kernel
+// every record before the state pass reads them.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+}  // namespace
+
+cudaError_t launch_prefill_split_noalloc(const void *q, const void *k, const void *v,
+                                         const float *g, const float *beta, const float *S0,
+                                         float *o, float *S_out, const int32_t *cu_seqlens, int N,
+                                         int64_t T, int H, cudaStream_t stream) {
+    if (!grid_fits(N, T, H) || prefill_split_workspace_bytes(N, T, H) > kNoAllocScratchBytes)
+        return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    void *ws = nullptr;
+    {
+        // first call on a device: look up the array's address once
+        std::lock_guard<std::mutex> lk(g_scratch_mu);
+        if (!g_scratch_addr[dev]) {
+            void *addr = nullptr;
+            e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+            if (e != cudaSuccess) return e;
+            g_scratch_addr[dev] = addr;
+        }
+        ws = g_scratch_addr[dev];
+    }
+    return run_split(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, T, H, ws, stream);
+}
+
 cudaError_t read_split_error(unsigned int *code, bool reset) {
     cudaError_t e = cudaMemcpyFromSymbol(code, g_kda_split_error, sizeof(unsigned int));
     if (e != cudaSuccess || !reset) return e;
