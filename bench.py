@@ -199,20 +199,28 @@ def run_ours(args):
         dd = {n: _to_dev(getattr(dstep, n), dev) for n in ("q", "k", "v", "g", "beta")}
         od = torch.empty((N, H, DV), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 1 + (1 if dstep is not None else 0)
+    tc_path = pre.dtype == "bf16" and C == 64 and T > 0
+    # tensor-core path: chunk plan + intra-chunk kernel + state pass per call
+    launches_per_step = (3 if tc_path else 1) + (1 if dstep is not None else 0)
 
-    ev_pre = []   # per-launch (start, end) of the prefill kernel
+    ev_pre = []   # per call: (start, end) of the prefill, or the four kernel-boundary events
 
     def step(record=False):
-        if record:
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-        kda.prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, S0=S0, chunk=C,
-                            o=o, S_out=S_out)
-        if record:
-            b.record(stream)
-            ev_pre.append((a, b))
+        if record and tc_path:
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            kda.prefill_chunked_events(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, evs,
+                                       S0=S0, o=o, S_out=S_out)
+            ev_pre.append(evs)
+        else:
+            if record:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+            kda.prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, S0=S0, chunk=C,
+                                o=o, S_out=S_out)
+            if record:
+                b.record(stream)
+                ev_pre.append([a, b])
         if dstep is not None:
             kda.decode_step(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], S_out, o=od)
 
@@ -238,7 +246,9 @@ def run_ours(args):
         ms = float(tt.item())
     ms_per_step = ms / args.steps
     value = ws * T / (ms_per_step / 1e3)
-    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_pre)
+    kern_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in ev_pre)
+    if tc_path:
+        part_ms = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev_pre) for i in range(3)]
 
     peaks = _peaks()
     tok_heads = T * H
@@ -248,17 +258,38 @@ def run_ours(args):
     alg_flops = tok_heads * prefill_flops_per_token_head(C)
     achieved_gbs = alg_bytes / (kern_ms / 1e3) / 1e9
     achieved_tflops = alg_flops / (kern_ms / 1e3) / 1e12
-    tc_path = pre.dtype == "bf16" and C == 64
     hbm_frac = achieved_gbs / peaks["hbm"]
     tc_frac = achieved_tflops / peaks["bf16"]
     if tc_path:
-        # the tensor-core prefill is designed against the HBM roofline (its
-        # arithmetic intensity, ~100 flop/B, is below the bf16 ridge point)
+        # The tensor-core prefill is designed against the HBM roofline (its
+        # arithmetic intensity, ~100 flop/B, is below the bf16 ridge point).
+        # One call = chunk plan + intra-chunk kernel + state pass; the
+        # roofline is that of the call (algorithmic bytes / call time: the
+        # per-chunk records the two kernels exchange count against it), and
+        # each kernel is reported with the bytes it moves in this design.
+        lens = np.diff(pre.cu_seqlens)
+        nchunk = int(sum((int(x) + 63) // 64 for x in lens))
+        rec = 91136
+        intra_bytes = nchunk * H * (2 * 64 * 256 + 64 * 512 + 64 * 4 + rec)
+        state_bytes = nchunk * H * (rec + 64 * 256) + T * H * 512 + n_state * STATE_BYTES * (
+            2 if S0 is not None else 1)
+        tr = [_traffic(kname, "kda_prefill_split.cu") for kname in ("intra_chunk_kernel", "state_pass_kernel")]
+        kernels = {}
+        for kname, ms_k, mb in (("chunk_plan_kernel", part_ms[0], None),
+                                ("intra_chunk_kernel", part_ms[1], intra_bytes),
+                                ("state_pass_kernel", part_ms[2], state_bytes)):
+            kd = {"ms": round(ms_k, 4), "share": round(ms_k / kern_ms, 4)}
+            if mb is not None:
+                kd.update({"moved_bytes": int(mb), "gbs": round(mb / (ms_k / 1e3) / 1e9, 1),
+                           "frac_hbm": round(mb / (ms_k / 1e3) / 1e9 / peaks["hbm"], 4)})
+            kernels[kname] = kd
         roofline = {
-            "kernel": "prefill_tc_kernel (tcgen05/TMEM/TMA chunked prefill)",
+            "kernel": "prefill call: chunk_plan_kernel + intra_chunk_kernel + state_pass_kernel "
+                      "(tcgen05/TMEM/TMA); dominant: intra_chunk_kernel",
             "bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm"],
             "unit": "GB/s", "frac": round(hbm_frac, 4), "of": peaks["source"],
-            "traffic": _traffic("prefill_tc_kernel", "kda_prefill_tc.cu") if wl == "prefill_4k" else None,
+            "traffic": (tr[0] + tr[1]) if (wl == "prefill_4k" and None not in tr) else None,
+            "kernels": kernels,
         }
     else:
         roofline = {

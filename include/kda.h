@@ -113,6 +113,20 @@ int kda_prefill_chunked(const void *q, const void *k, const void *v,
                         int dtype, void *stream);
 
 /*
+ * Measurement form of kda_prefill_chunked for the tensor-core path (bf16,
+ * chunk 64, T > 0; KDA_ERR_CHUNK otherwise): the same computation, and it
+ * records the caller's four timing events (cudaEvent_t, created by the
+ * caller) on `stream` before the chunk-plan kernel, before the intra-chunk
+ * kernel, before the state pass and after it, so that each kernel's time can
+ * be read with cudaEventElapsedTime.  events: host array of 4 cudaEvent_t.
+ */
+int kda_prefill_chunked_events(const void *q, const void *k, const void *v,
+                               const float *g, const float *beta, const float *S0,
+                               float *o, float *S_out, const int32_t *cu_seqlens,
+                               int N, int64_t T, int H, int dk, int dv, int chunk,
+                               int dtype, void *stream, void *const *events);
+
+/*
  * kda_prefill_chunked without any device allocation during the call.
  *
  * Same operation, arguments, layouts and results as kda_prefill_chunked.

@@ -21,7 +21,7 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["prefill_chunked", "prefill_chunked_noalloc", "decode_step", "device_error", "lib",
+__all__ = ["prefill_chunked", "prefill_chunked_noalloc", "prefill_chunked_events", "decode_step", "device_error", "lib",
            "KDAError", "KDA_BF16", "KDA_F32", "library_path"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -64,6 +64,9 @@ def lib() -> ctypes.CDLL:
         L.kda_prefill_chunked.restype = i32
         L.kda_prefill_chunked_noalloc.argtypes = L.kda_prefill_chunked.argtypes
         L.kda_prefill_chunked_noalloc.restype = i32
+        L.kda_prefill_chunked_events.argtypes = L.kda_prefill_chunked.argtypes + [
+            ctypes.POINTER(ctypes.c_void_p)]
+        L.kda_prefill_chunked_events.restype = i32
         L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
         L.kda_decode_step.restype = i32
         L.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
@@ -102,7 +105,7 @@ def _stream(device: torch.device, stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _prefill(fn_name: str, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_out, stream):
+def _prefill(fn_name: str, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_out, stream, extra=()):
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("inputs must be CUDA tensors")
@@ -125,7 +128,7 @@ def _prefill(fn_name: str, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_out, st
     _check("S_out", S_out, torch.float32, (N, H, DK, DV), dev)
     rc = getattr(lib(), fn_name)(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(o), _p(S_out),
                                  _p(cu_seqlens), N, T, H, DK, DV, int(chunk), dt,
-                                 _stream(dev, stream))
+                                 _stream(dev, stream), *extra)
     if rc != 0:
         raise KDAError(rc, fn_name)
     return o, S_out
@@ -143,6 +146,28 @@ def prefill_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.
     """
     return _prefill("kda_prefill_chunked", q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_out,
                     stream)
+
+
+def prefill_chunked_events(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                           beta: torch.Tensor, cu_seqlens: torch.Tensor, events,
+                           S0: Optional[torch.Tensor] = None,
+                           o: Optional[torch.Tensor] = None, S_out: Optional[torch.Tensor] = None,
+                           stream: Optional[torch.cuda.Stream] = None
+                           ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Tensor-core ``prefill_chunked`` (bf16, chunk 64) that also records four
+    ``torch.cuda.Event`` (timing enabled) around its kernels: before the chunk
+    plan, before the intra-chunk kernel, before the state pass, after it
+    (``kda_prefill_chunked_events``)."""
+    if len(events) != 4:
+        raise ValueError("need four events")
+    s = torch.cuda.current_stream(q.device) if stream is None else stream
+    for e in events:
+        if not e.cuda_event:          # torch creates the CUDA event at its first record
+            e.record(s)
+    evs = [ctypes.c_void_p(e.cuda_event) for e in events]
+    arr = (ctypes.c_void_p * 4)(*evs)
+    return _prefill("kda_prefill_chunked_events", q, k, v, g, beta, cu_seqlens, S0, 64, o, S_out,
+                    stream, extra=(ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)),))
 
 
 def prefill_chunked_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,

@@ -57,6 +57,26 @@ int kda_prefill_chunked(const void *q, const void *k, const void *v, const float
                                                 chunk, dtype == KDA_BF16, s));
 }
 
+int kda_prefill_chunked_events(const void *q, const void *k, const void *v, const float *g,
+                               const float *beta, const float *S0, float *o, float *S_out,
+                               const int32_t *cu_seqlens, int N, int64_t T, int H, int dk, int dv,
+                               int chunk, int dtype, void *stream, void *const *events) {
+    if (!events || !events[0] || !events[1] || !events[2] || !events[3]) return KDA_ERR_NULL;
+    if (dtype != KDA_BF16 || chunk != 64 || T <= 0) return KDA_ERR_CHUNK;
+    if (dk != kda::kDK || dv != kda::kDV || N < 1 || H < 1 || T >= (int64_t(1) << 31))
+        return KDA_ERR_DIM;
+    if ((int64_t)N * H * (kda::kDV / 32) >= (int64_t(1) << 31)) return KDA_ERR_DIM;
+    if (!S_out || !cu_seqlens || !q || !k || !v || !g || !beta || !o) return KDA_ERR_NULL;
+    const void *ptrs[] = {q, k, v, g, beta, S0, o, S_out, cu_seqlens};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_ALIGN;
+    cudaEvent_t ev[4];
+    for (int i = 0; i < 4; ++i) ev[i] = static_cast<cudaEvent_t>(events[i]);
+    const cudaError_t e = kda::launch_prefill_split(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N,
+                                                    T, H, static_cast<cudaStream_t>(stream), ev);
+    return e == cudaErrorMemoryAllocation ? KDA_ERR_WORKSPACE : cuda_status(e);
+}
+
 int kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v, const float *g,
                                 const float *beta, const float *S0, float *o, float *S_out,
                                 const int32_t *cu_seqlens, int N, int64_t T, int H, int dk,

@@ -32,10 +32,13 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
 // chunk 64, T >= 1.  Takes its workspace (see prefill_split_workspace_bytes)
 // from a library-owned stream-ordered pool; returns cudaErrorMemoryAllocation
 // when it cannot.
+// `events` (optional, four timing events) are recorded on `stream` before
+// the chunk plan, before the intra-chunk kernel, before the state pass and
+// after it.
 cudaError_t launch_prefill_split(const void *q, const void *k, const void *v, const float *g,
                                  const float *beta, const float *S0, float *o, float *S_out,
                                  const int32_t *cu_seqlens, int N, int64_t T, int H,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, cudaEvent_t const *events = nullptr);
 size_t prefill_split_workspace_bytes(int N, int64_t T, int H);
 
 // The same prefill with its workspace in a fixed file-scope device array of

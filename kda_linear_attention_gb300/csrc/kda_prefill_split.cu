@@ -953,7 +953,7 @@ namespace {
 cudaError_t run_split(const void *q, const void *k, const void *v, const float *g,
                       const float *beta, const float *S0, float *o, float *S_out,
                       const int32_t *cu_seqlens, int N, int64_t T, int H, void *ws,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, cudaEvent_t const *ev = nullptr) {
     const int64_t max_chunks = (T + C - 1) / C + N;
     CUtensorMap mq, mk, mv, mg, mo;
     if (!make_map_bf16(&mq, q, T, H, 64, true) || !make_map_bf16(&mk, k, T, H, 64, true) ||
@@ -969,11 +969,15 @@ cudaError_t run_split(const void *q, const void *k, const void *v, const float *
     int32_t *chunk_off = static_cast<int32_t *>(ws);
     uint8_t *recs = static_cast<uint8_t *>(ws) +
                     (((size_t)(N + 1) * sizeof(int32_t) + 1023) & ~(size_t)1023);
+    if (ev) cudaEventRecord(ev[0], stream);
     chunk_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, chunk_off);
+    if (ev) cudaEventRecord(ev[1], stream);
     intra_chunk_kernel<<<(unsigned)(max_chunks * H), NTA, SMEM_A_ALLOC, stream>>>(
         mq, mk, mg, beta, cu_seqlens, chunk_off, N, H, recs);
+    if (ev) cudaEventRecord(ev[2], stream);
     state_pass_kernel<<<(unsigned)((int64_t)N * H), NTB, SMEM_B_ALLOC, stream>>>(
         mv, mo, S0, o, S_out, cu_seqlens, chunk_off, N, H, (int)max_chunks, recs);
+    if (ev) cudaEventRecord(ev[3], stream);
     return cudaGetLastError();
 }
 
@@ -987,12 +991,12 @@ bool grid_fits(int N, int64_t T, int H) {
 cudaError_t launch_prefill_split(const void *q, const void *k, const void *v, const float *g,
                                  const float *beta, const float *S0, float *o, float *S_out,
                                  const int32_t *cu_seqlens, int N, int64_t T, int H,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, cudaEvent_t const *events) {
     if (!grid_fits(N, T, H)) return cudaErrorInvalidValue;
     void *ws = nullptr;
     cudaError_t e = ws_alloc(&ws, prefill_split_workspace_bytes(N, T, H), stream);
     if (e != cudaSuccess) return e;
-    e = run_split(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, T, H, ws, stream);
+    e = run_split(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, T, H, ws, stream, events);
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     return e != cudaSuccess ? e : ef;
 }

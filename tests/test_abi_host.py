@@ -93,6 +93,35 @@ def test_decode_rejects_bad_arguments(L, kw, status):
     assert _decode(L, **kw) == status
 
 
+@pytest.mark.parametrize("fn", ["kda_prefill_chunked_noalloc", "kda_prefill_chunked_events"])
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=64), 2), (dict(N=0), 2), (dict(q=None), 1), (dict(S_out=None), 1),
+    (dict(q=ctypes.c_void_p(0x10004)), 4),
+])
+def test_prefill_variants_reject_bad_arguments(L, fn, kw, status):
+    a = dict(q=GOOD, k=GOOD, v=GOOD, g=GOOD, beta=GOOD, S0=None, o=GOOD, S_out=GOOD, cu=GOOD,
+             N=1, T=64, H=2, dk=128, dv=128, chunk=64, dtype=0, stream=None)
+    a.update(kw)
+    args = [a["q"], a["k"], a["v"], a["g"], a["beta"], a["S0"], a["o"], a["S_out"], a["cu"],
+            a["N"], a["T"], a["H"], a["dk"], a["dv"], a["chunk"], a["dtype"], a["stream"]]
+    if fn == "kda_prefill_chunked_events":
+        evs = (ctypes.c_void_p * 4)(GOOD, GOOD, GOOD, GOOD)
+        args.append(ctypes.cast(evs, ctypes.POINTER(ctypes.c_void_p)))
+    assert getattr(L, fn)(*args) == status
+
+
+def test_prefill_events_needs_events_and_the_tensor_core_path(L):
+    def call(evs, dtype=0, chunk=64):
+        return L.kda_prefill_chunked_events(GOOD, GOOD, GOOD, GOOD, GOOD, None, GOOD, GOOD, GOOD,
+                                            1, 64, 2, 128, 128, chunk, dtype, None, evs)
+    assert call(None) == 1
+    four = (ctypes.c_void_p * 4)(GOOD, GOOD, None, GOOD)
+    assert call(ctypes.cast(four, ctypes.POINTER(ctypes.c_void_p))) == 1
+    four = (ctypes.c_void_p * 4)(GOOD, GOOD, GOOD, GOOD)
+    ptr = ctypes.cast(four, ctypes.POINTER(ctypes.c_void_p))
+    assert call(ptr, dtype=1) == 3 and call(ptr, chunk=32) == 3
+
+
 def test_decode_batch_zero_is_noop(L):
     # B = 0 returns before touching any pointer or the GPU
     assert _decode(L, B=0, q=None, S=None) == 0

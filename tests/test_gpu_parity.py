@@ -122,6 +122,28 @@ def test_prefill_in_place_state():
     assert_close(S.cpu().numpy(), S_ref, TOL_BF16, "S in place")
 
 
+def test_prefill_events_variant_matches_and_times_each_kernel():
+    """kda_prefill_chunked_events computes the same prefill and brackets the
+    chunk plan, intra-chunk kernel and state pass with the caller's events."""
+    import torch
+    import kda_linear_attention_gb300 as kda
+    inp = ki.gen_prefill(12, [300, 64, 1], H=6, dtype="bf16", chunk=64, with_s0=True)
+    d = {n: dev_tensor(getattr(inp, n)) for n in ("q", "k", "v", "g", "beta")}
+    cu, s0 = dev_tensor(inp.cu_seqlens), dev_tensor(inp.S0)
+    o1, S1 = kda.prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, S0=s0)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    o2, S2 = kda.prefill_chunked_events(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, evs, S0=s0)
+    torch.cuda.synchronize()
+    assert kda.device_error() == 0
+    assert rel_err(o2.cpu().numpy(), o1.cpu().numpy()) <= 1e-5
+    assert rel_err(S2.cpu().numpy(), S1.cpu().numpy()) <= 1e-5
+    ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(3)]
+    assert all(m >= 0 for m in ms) and ms[1] > 0 and ms[2] > 0
+    o_ref, S_ref = oracle.prefill(inp)
+    assert_close(o2.cpu().numpy(), o_ref, TOL_BF16, "o")
+    assert_close(S2.cpu().numpy(), S_ref, TOL_BF16, "S")
+
+
 def test_prefill_split_calls_and_decode_continuation():
     """prefill(T1) then prefill(T2, S0=S_out) and prefill(T-1) then one decode
     step reproduce the single call prefill(T1+T2): each piece is checked
