@@ -33,6 +33,7 @@
 // terms (beta_r v_r, beta_r K0_r, (q_r.k_r) u_r) in fp32 outside the MMAs.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "kda_internal.h"
@@ -92,30 +93,41 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t *__restr
 }
 
 // ============================================================================
-// intra-chunk kernel: one CTA (256 threads, two CTAs per SM) per (chunk, head)
+// intra-chunk kernel: persistent, two CTAs (256 threads each) per SM.  CTA b
+// takes the (chunk, head) jobs b, b + G, b + 2G, ... (G = grid size; job =
+// gc * H + h) and prefetches the next job's inputs while it finishes the
+// current one: its q and k as soon as the Gram product has consumed X, its g
+// (L2 prefetch early, shared memory once the W product is done).
 // ============================================================================
 constexpr int NTA = 256;
-constexpr uint32_t SA_X = 0;              // 32 KB: q|k staging (TMA) -> X [128][128] sw; then M fp32 [64][68] + temps
-constexpr uint32_t SA_KH = 32768;         // 40 KB: g staging fp32 (TMA) -> Khat [160][128] sw
-constexpr uint32_t SA_T = SA_KH;          //   after the Gram: T Diag(beta) bf16 il [r][s] (8 KB; the
-                                          //   W product reads 16 KB as its M = 128 rows)
+constexpr uint32_t SA_X = 0;              // 32 KB: q|k (TMA) -> X [128][128] sw (A of the Gram)
+constexpr uint32_t SA_KH = 32768;         // 40 KB: g (TMA) -> Khat [160][128] sw (B of the Gram)
+constexpr uint32_t SA_M = SA_KH;          //   after the Gram: M / T fp32 [64][68] (17408 B)
+constexpr uint32_t SA_Y = SA_KH + 17408;  //   solve temporaries (4 KB)
+constexpr uint32_t SA_T = SA_KH + 24576;  //   T Diag(beta) bf16 il [r][s] (8 KB; the W product
+                                          //   reads 16 KB as its M = 128 rows)
 constexpr uint32_t SA_K0 = 73728;         // 16 KB: K0 [64 s][128 i] sw (MN-major B of the W product)
 constexpr uint32_t SA_MISC = 90112;
 constexpr uint32_t MA_BETA = 0;           // float[64]
 constexpr uint32_t MA_GAM = 256;          // float[128]  e^{b_L}
 constexpr uint32_t MA_DQ = 768;           // float[64]   q_r . k_r
 constexpr uint32_t MA_TOT = 1024;         // float[4][128] sub-block totals, then carry - sigma_u
-constexpr uint32_t MA_SIG = 3072;         // float[4][128] local prefix at sub-block ends, then e^{b_L - sigma_u}
+constexpr uint32_t MA_SIG = 3072;         // float[4][128] e^{b_L - sigma_u}
 constexpr uint32_t MA_DD = 5120;          // float[4][128] e^{sigma_0}, e^{sigma_w - sigma_{w-1}}
 constexpr uint32_t MA_EP = 7168;          // float[4][128] e^{sigma_u}
-constexpr uint32_t MA_BAR = 9216;         // 2 x u64
-constexpr uint32_t MA_TMEM = 9232;
+constexpr uint32_t MA_BAR = 9216;         // 3 x u64: q|k, g, MMA
+constexpr uint32_t MA_TMEM = 9240;
 constexpr uint32_t SMEM_A_USED = SA_MISC + 9248;
 constexpr uint32_t SMEM_A_ALLOC = SMEM_A_USED + 1024;
 static_assert(2 * (SMEM_A_ALLOC + 1024) <= 233472, "two intra-chunk CTAs per SM");
+static_assert(SA_T + 16384 <= SA_K0 && SA_Y + 4096 <= SA_T, "solve space inside the Khat region");
 constexpr int MLD = 68;                   // row stride (floats) of M / T
 constexpr uint32_t TMA_G = 0;             // Gram D, 160 columns
 constexpr uint32_t TMA_W = 0;             // W, 128 columns (after the Gram epilogue)
+
+struct Job {
+    int h, gc, tok, Lc;
+};
 
 __global__ void __launch_bounds__(NTA, 2)
 intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -132,8 +144,9 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     float *s_dd = reinterpret_cast<float *>(sm + SA_MISC + MA_DD);
     float *s_ep = reinterpret_cast<float *>(sm + SA_MISC + MA_EP);
     float *s_el = s_sig;
-    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + SA_MISC + MA_BAR);
-    uint64_t *bar_mma = bar_ld + 1;
+    uint64_t *bar_qk = reinterpret_cast<uint64_t *>(sm + SA_MISC + MA_BAR);
+    uint64_t *bar_g = bar_qk + 1;
+    uint64_t *bar_mma = bar_qk + 2;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SA_MISC + MA_TMEM);
 
     const int t = threadIdx.x;
@@ -141,67 +154,95 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     const int lane = t & 31;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
 
-    // ---- which chunk: gc = global chunk index, n = its sequence
-    const int h = blockIdx.x % H;
-    const int gc = blockIdx.x / H;
-    if (gc >= chunk_off[N]) return;
-    int lo = 0, hi = N - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (chunk_off[mid] <= gc) lo = mid;
-        else hi = mid - 1;
-    }
-    const int n = lo;
-    const int tok = cu[n] + (gc - chunk_off[n]) * C;
-    const int Lc = min(C, cu[n + 1] - tok);
-    uint8_t *rec = recs + ((size_t)gc * H + h) * REC_BYTES;
-
-    if (warp == 0) tmem_alloc(s_tmem, 256);
-    if (t == 0) {
-        mbar_init(bar_ld, 1);
-        mbar_init(bar_mma, 1);
-        fence_mbar_init();
-        // q and k land as the two 64-row halves of X (rows 0..63 q, 64..127 k)
-        mbar_arrive_expect_tx(bar_ld, 65536);
-        tma_load_3d(sm + SA_X, &map_q, bar_ld, 0, h, tok);
-        tma_load_3d(sm + SA_X + 8192, &map_k, bar_ld, 0, h, tok);
-        tma_load_3d(sm + SA_X + 16384, &map_q, bar_ld, 64, h, tok);
-        tma_load_3d(sm + SA_X + 24576, &map_k, bar_ld, 64, h, tok);
+    // job -> (head, global chunk, first token, rows); every thread decodes
+    const int total = chunk_off[N] * H;
+    auto decode = [&](int job) -> Job {
+        Job J;
+        J.h = job % H;
+        J.gc = job / H;
+        int lo = 0, hi = N - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (chunk_off[mid] <= J.gc) lo = mid;
+            else hi = mid - 1;
+        }
+        J.tok = cu[lo] + (J.gc - chunk_off[lo]) * C;
+        J.Lc = min(C, cu[lo + 1] - J.tok);
+        return J;
+    };
+    // q and k land as the two 64-row halves of X (rows 0..63 q, 64..127 k)
+    auto issue_qk = [&](const Job &J) {
+        mbar_arrive_expect_tx(bar_qk, 32768);
+        tma_load_3d(sm + SA_X, &map_q, bar_qk, 0, J.h, J.tok);
+        tma_load_3d(sm + SA_X + 8192, &map_k, bar_qk, 0, J.h, J.tok);
+        tma_load_3d(sm + SA_X + 16384, &map_q, bar_qk, 64, J.h, J.tok);
+        tma_load_3d(sm + SA_X + 24576, &map_k, bar_qk, 64, J.h, J.tok);
+    };
+    auto issue_g = [&](const Job &J) {
+        mbar_arrive_expect_tx(bar_g, 32768);
 #pragma unroll
         for (int bx = 0; bx < 4; ++bx)
-            tma_load_3d(sm + SA_KH + 8192 * bx, &map_g, bar_ld, 32 * bx, h, tok);
+            tma_load_3d(sm + SA_KH + 8192 * bx, &map_g, bar_g, 32 * bx, J.h, J.tok);
+    };
+    auto load_beta = [&](const Job &J) -> float {
+        return (t < J.Lc) ? beta[(size_t)(J.tok + t) * H + J.h] : 0.f;
+    };
+
+    int job = blockIdx.x;
+    if (job >= total) return;
+    Job J = decode(job);
+    if (warp == 0) tmem_alloc(s_tmem, 256);
+    if (t == 0) {
+        mbar_init(bar_qk, 1);
+        mbar_init(bar_g, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        prefetch_tmap(&map_q);
+        prefetch_tmap(&map_k);
+        prefetch_tmap(&map_g);
+        issue_qk(J);
+        issue_g(J);
     }
-    if (t < C) {
-        s_beta[t] = (t < Lc) ? beta[(size_t)(tok + t) * H + h] : 0.f;
-        s_dq[t] = 0.f;
-    }
+    float bnext = (t < C) ? load_beta(J) : 0.f;
     sync_tc();
     const uint32_t tmem = *s_tmem;
-    bool failed = !wait_all(bar_ld, 0);
+    bool failed = false;
     int commits = 0;                       // MMA commits issued on bar_mma
+    int loads_qk = 1, loads_g = 1;         // phases issued on bar_qk / bar_g
 
-    if (!failed) {
+    for (int it = 0; !failed; ++it) {
+    const int h = J.h, Lc = J.Lc;
+    uint8_t *rec = recs + ((size_t)J.gc * H + h) * REC_BYTES;
+    if (t < C) {
+        s_beta[t] = bnext;
+        s_dq[t] = 0.f;
+    }
+    const int job_next = job + gridDim.x;
+    const bool has_next = job_next < total;
+    Job Jn = J;
+    if (!wait_all(bar_qk, it & 1) || !wait_all(bar_g, it & 1)) { failed = true; break; }
+
+    {
         // ===== decay prefix sums: column scan in place in the g tile =========
         // thread = (channels 4qd..4qd+3, sub-block u); the tile is four 128B-
         // swizzled boxes of [64 rows][32 channels] fp32
         if (t < 128) {
             const int qd = t & 31, u = t >> 5;
-            uint8_t *colp = sm + SA_KH + 8192 * (qd >> 3);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), at_last = acc;
-            const int lastrow = min(16 * u + 15, Lc - 1);
+            uint8_t *colp = sm + SA_KH + 8192 * (qd >> 3) + 16 * u * 128;
+            float4 x[16];
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr)
+                x[rr] = *reinterpret_cast<const float4 *>(colp + rr * 128 + (((qd & 7) ^ (rr & 7)) << 4));
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
-                const int r = 16 * u + rr;
-                float4 *pg = reinterpret_cast<float4 *>(colp + r * 128 + (((qd & 7) ^ (rr & 7)) << 4));
-                if (r < Lc) {
-                    const float4 x = *pg;
-                    acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+                if (16 * u + rr < Lc) {           // rows past the end add nothing
+                    acc.x += x[rr].x; acc.y += x[rr].y; acc.z += x[rr].z; acc.w += x[rr].w;
                 }
-                *pg = acc;                         // local (sub-block) prefix
-                if (r == lastrow) at_last = acc;
+                *reinterpret_cast<float4 *>(colp + rr * 128 + (((qd & 7) ^ (rr & 7)) << 4)) = acc;
             }
-            *reinterpret_cast<float4 *>(s_tot + u * 128 + 4 * qd) = acc;      // sub-block total
-            *reinterpret_cast<float4 *>(s_sig + u * 128 + 4 * qd) = at_last;  // at its last valid row
+            // the sub-block total is also the prefix at its last valid row
+            *reinterpret_cast<float4 *>(s_tot + u * 128 + 4 * qd) = acc;
         }
         __syncthreads();
         if (t < 128) {
@@ -216,9 +257,9 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             float bL = 0.f;
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                if (u == lu) bL = base[u] + s_sig[u * 128 + t];
+                if (u == lu) bL = base[u] + s_tot[u * 128 + t];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) sg[u] = (u <= lu) ? base[u] + s_sig[u * 128 + t] : bL;
+            for (int u = 0; u < 4; ++u) sg[u] = (u <= lu) ? base[u] + s_tot[u * 128 + t] : bL;
 #pragma unroll
             for (int u = 0; u < 4; ++u) s_tot[u * 128 + t] = base[u] - sg[u];
             const float d0 = __expf(sg[0]), d1 = __expf(sg[1] - sg[0]), d2 = __expf(sg[2] - sg[1]),
@@ -391,12 +432,24 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             }
             if (t < 128) rv[128 + t] = s_gam[t];
         }
-        failed = !wait_all(bar_mma, 0);
+        // while the Gram runs: decode the next job, load its beta, pull its g into L2
+        if (has_next) {
+            Jn = decode(job_next);
+            if (t < C) bnext = load_beta(Jn);
+            if (t == 0) {
+#pragma unroll
+                for (int bx = 0; bx < 4; ++bx) tma_prefetch_l2_3d(&map_g, 32 * bx, Jn.h, Jn.tok);
+            }
+        }
+        if (!wait_all(bar_mma, (uint32_t)(commits - 1) & 1u)) { failed = true; break; }
     }
-    if (!failed) {
+    {
         tc_fence_after();
+        // X is consumed: the next job's q and k
+        if (t == 0 && has_next) issue_qk(Jn);
+        loads_qk += has_next;
         // ===== Gram epilogue -> A' (tf32, record) and M = Diag(beta) G^kk (fp32)
-        float *Mm = reinterpret_cast<float *>(sm + SA_X);
+        float *Mm = reinterpret_cast<float *>(sm + SA_M);
         {
             const int ch = t & 127;
             const bool qside = ch < 64;
@@ -438,7 +491,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         __syncthreads();
 
         // ===== T = (I + M)^-1 by 16-row blocks, in place ======================
-        float *Yt = Mm + 64 * MLD;
+        float *Yt = reinterpret_cast<float *>(sm + SA_Y);
         {
             // diagonal blocks by forward substitution across a 16-lane group:
             // lane = row r, four right-hand sides (columns c0..c0+3) per thread
@@ -595,10 +648,13 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             mma_commit(bar_mma);
         }
         ++commits;
-        failed = !wait_all(bar_mma, 1);
+        if (!wait_all(bar_mma, (uint32_t)(commits - 1) & 1u)) { failed = true; break; }
     }
-    if (!failed) {
+    {
         tc_fence_after();
+        // the Khat / solve space is free: the next job's g
+        if (t == 0 && has_next) issue_g(Jn);
+        loads_g += has_next;
         // ===== -W -> record rows 0..63 (bf16, K-major sw): lane r, 64 channels
         if ((warp & 3) < 2) {
             const int r = 32 * (warp & 3) + lane, half = warp >> 2;
@@ -618,10 +674,19 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             }
         }
     }
+    // end of the job: every TMEM read and shared-memory use is done
+    tc_fence_before();
+    __syncthreads();
+    if (!has_next) break;
+    J = Jn;
+    job = job_next;
+    }   // job loop
+
     if (failed) {
         if (t == 0) atomicOr(&g_kda_split_error, 1u);
         // let copies and MMAs in flight finish (bounded) before freeing TMEM
-        mbar_wait(bar_ld, 0, kWaitLimit);
+        mbar_wait(bar_qk, (uint32_t)(loads_qk - 1) & 1u, kWaitLimit);
+        mbar_wait(bar_g, (uint32_t)(loads_g - 1) & 1u, kWaitLimit);
         if (commits) mbar_wait(bar_mma, (uint32_t)(commits - 1) & 1u, kWaitLimit);
     }
     sync_tc();
@@ -948,6 +1013,18 @@ size_t prefill_split_workspace_bytes(int N, int64_t T, int H) {
 
 namespace {
 
+// Persistent intra-chunk grid: two CTAs per SM, at most one per job.
+unsigned intra_grid(int64_t jobs) {
+    static int sms[kMaxDevices] = {};
+    int dev = 0;
+    int n = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+        if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (sms[dev] > 0) n = sms[dev];
+    }
+    return (unsigned)std::min<int64_t>(jobs, 2 * (int64_t)n);
+}
+
 // The three launches of one prefill, with the workspace at `ws` (at least
 // prefill_split_workspace_bytes(N, T, H) bytes).
 cudaError_t run_split(const void *q, const void *k, const void *v, const float *g,
@@ -972,7 +1049,7 @@ cudaError_t run_split(const void *q, const void *k, const void *v, const float *
     if (ev) cudaEventRecord(ev[0], stream);
     chunk_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, chunk_off);
     if (ev) cudaEventRecord(ev[1], stream);
-    intra_chunk_kernel<<<(unsigned)(max_chunks * H), NTA, SMEM_A_ALLOC, stream>>>(
+    intra_chunk_kernel<<<intra_grid(max_chunks * H), NTA, SMEM_A_ALLOC, stream>>>(
         mq, mk, mg, beta, cu_seqlens, chunk_off, N, H, recs);
     if (ev) cudaEventRecord(ev[2], stream);
     state_pass_kernel<<<(unsigned)((int64_t)N * H), NTB, SMEM_B_ALLOC, stream>>>(
