@@ -301,6 +301,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
 #pragma unroll
             for (int c = 0; c < 8; ++c) F[u][c] = valid ? __expf(gl[c]) : 0.f;
         }
+        if (t == 0) bulk_wait_read();        // the previous job's -W copy has left the K0 tile
         __syncthreads();                   // the g tile is read: Khat may be written
 
         float dqp[4];
@@ -617,7 +618,8 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         // shared memory (A of the W product)
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass) {
-            const int r = (t >> 3) + 32 * pass, s0 = (t & 7) * 8;
+            // a warp writes 8 rows x 4 chunks: whole 128-byte lines of the il layout
+            const int r = 8 * warp + (lane & 7), s0 = 8 * ((lane >> 3) + 4 * pass);
             const float4 a = *reinterpret_cast<const float4 *>(Mm + r * MLD + s0);
             const float4 b4 = *reinterpret_cast<const float4 *>(Mm + r * MLD + s0 + 4);
             const float tv[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
@@ -655,7 +657,8 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         // the Khat / solve space is free: the next job's g
         if (t == 0 && has_next) issue_g(Jn);
         loads_g += has_next;
-        // ===== -W -> record rows 0..63 (bf16, K-major sw): lane r, 64 channels
+        // ===== -W (bf16, K-major sw) -> the free K0 tile -> record rows 0..63
+        // of both halves by two bulk copies: lane r, 64 channels
         if ((warp & 3) < 2) {
             const int r = 32 * (warp & 3) + lane, half = warp >> 2;
 #pragma unroll
@@ -668,10 +671,17 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     float x8[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x8[e] = -d[8 * c8 + e];
-                    *reinterpret_cast<uint4 *>(rec + R_WQ + sw_chunk(r, 8 * half + 2 * q4 + c8, 16384)) =
+                    *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, 8 * half + 2 * q4 + c8, 8192)) =
                         pack_bf8(x8);
                 }
             }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (t == 0) {
+            bulk_store(rec + R_WQ, sm + SA_K0, 8192);
+            bulk_store(rec + R_WQ + 16384, sm + SA_K0 + 8192, 8192);
+            bulk_commit();
         }
     }
     // end of the job: every TMEM read and shared-memory use is done
@@ -682,6 +692,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     job = job_next;
     }   // job loop
 
+    if (t == 0) bulk_wait();                 // record copies complete before the CTA exits
     if (failed) {
         if (t == 0) atomicOr(&g_kda_split_error, 1u);
         // let copies and MMAs in flight finish (bounded) before freeing TMEM
