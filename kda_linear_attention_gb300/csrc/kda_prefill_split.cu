@@ -104,15 +104,15 @@ constexpr uint32_t SA_X = 0;              // 32 KB: q|k (TMA) -> X [128][128] sw
 constexpr uint32_t SA_KH = 32768;         // 40 KB: g (TMA) -> Khat [160][128] sw (B of the Gram)
 constexpr uint32_t SA_M = SA_KH;          //   after the Gram: M / T fp32 [64][68] (17408 B)
 constexpr uint32_t SA_Y = SA_KH + 17408;  //   solve temporaries (4 KB)
-constexpr uint32_t SA_T = SA_KH + 24576;  //   T Diag(beta) bf16 il [r][s] (8 KB; the W product
-                                          //   reads 16 KB as its M = 128 rows)
+constexpr uint32_t SA_T = SA_KH + 24576;  //   T Diag(beta) bf16 il [r][s], rows 0..63 twice
+                                          //   (16 KB: the M = 128 A operand of the W product)
 constexpr uint32_t SA_K0 = 73728;         // 16 KB: K0 [64 s][128 i] sw (MN-major B of the W product)
 constexpr uint32_t SA_MISC = 90112;
 constexpr uint32_t MA_BETA = 0;           // float[64]
 constexpr uint32_t MA_GAM = 256;          // float[128]  e^{b_L}
 constexpr uint32_t MA_DQ = 768;           // float[64]   q_r . k_r
 constexpr uint32_t MA_TOT = 1024;         // float[4][128] sub-block totals, then carry - sigma_u
-constexpr uint32_t MA_SIG = 3072;         // float[4][128] e^{b_L - sigma_u}
+constexpr uint32_t MA_SIG = 3072;         // float[4][128] first-half scan totals, then e^{b_L - sigma_u}
 constexpr uint32_t MA_DD = 5120;          // float[4][128] e^{sigma_0}, e^{sigma_w - sigma_{w-1}}
 constexpr uint32_t MA_EP = 7168;          // float[4][128] e^{sigma_u}
 constexpr uint32_t MA_BAR = 9216;         // 3 x u64: q|k, g, MMA
@@ -226,23 +226,36 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         // ===== decay prefix sums: column scan in place in the g tile =========
         // thread = (channels 4qd..4qd+3, sub-block u); the tile is four 128B-
         // swizzled boxes of [64 rows][32 channels] fp32
-        if (t < 128) {
-            const int qd = t & 31, u = t >> 5;
-            uint8_t *colp = sm + SA_KH + 8192 * (qd >> 3) + 16 * u * 128;
-            float4 x[16];
+        {
+            // thread = (channels 4qd..4qd+3, sub-block u, 8-row half hf): local
+            // prefix of its 8 rows; the second half then adds the first's total
+            const int qd = t & 31, u = (t >> 5) & 3, hf = t >> 7;
+            uint8_t *colp = sm + SA_KH + 8192 * (qd >> 3) + (16 * u + 8 * hf) * 128;
+            float4 x[8];
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr)
-                x[rr] = *reinterpret_cast<const float4 *>(colp + rr * 128 + (((qd & 7) ^ (rr & 7)) << 4));
+            for (int rr = 0; rr < 8; ++rr)
+                x[rr] = *reinterpret_cast<const float4 *>(colp + rr * 128 + (((qd & 7) ^ rr) << 4));
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) {
-                if (16 * u + rr < Lc) {           // rows past the end add nothing
+            for (int rr = 0; rr < 8; ++rr) {
+                if (16 * u + 8 * hf + rr < Lc) {  // rows past the end add nothing
                     acc.x += x[rr].x; acc.y += x[rr].y; acc.z += x[rr].z; acc.w += x[rr].w;
                 }
-                *reinterpret_cast<float4 *>(colp + rr * 128 + (((qd & 7) ^ (rr & 7)) << 4)) = acc;
+                x[rr] = acc;
             }
+            float4 *half_tot = reinterpret_cast<float4 *>(s_sig) + u * 32 + qd;
+            if (hf == 0) *half_tot = acc;
+            __syncthreads();
+            float4 base = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (hf == 1) base = *half_tot;
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr)
+                *reinterpret_cast<float4 *>(colp + rr * 128 + (((qd & 7) ^ rr) << 4)) =
+                    make_float4(x[rr].x + base.x, x[rr].y + base.y, x[rr].z + base.z, x[rr].w + base.w);
             // the sub-block total is also the prefix at its last valid row
-            *reinterpret_cast<float4 *>(s_tot + u * 128 + 4 * qd) = acc;
+            if (hf == 1)
+                *reinterpret_cast<float4 *>(s_tot + u * 128 + 4 * qd) =
+                    make_float4(acc.x + base.x, acc.y + base.y, acc.z + base.z, acc.w + base.w);
         }
         __syncthreads();
         if (t < 128) {
@@ -632,12 +645,16 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 d8[u] = (s3 == r) ? bs : w8[u];
             }
             *reinterpret_cast<uint4 *>(rec + R_T + km_bf16(r, s0, 1024)) = pack_bf8(w8);
-            *reinterpret_cast<uint4 *>(sm + SA_T + km_bf16(r, s0, 1024)) = pack_bf8(d8);
+            // rows 64..127 of the M = 128 operand repeat rows 0..63, so that every
+            // TMEM lane quarter of the W accumulator holds real rows
+            const uint4 pd = pack_bf8(d8);
+            *reinterpret_cast<uint4 *>(sm + SA_T + km_bf16(r, s0, 1024)) = pd;
+            *reinterpret_cast<uint4 *>(sm + SA_T + km_bf16(64 + r, s0, 1024)) = pd;
         }
         fence_proxy_async_smem();
         sync_tc();
 
-        // ===== W = T Diag(beta) K0: D_W[r][i] (M = 128, rows 64..127 unused),
+        // ===== W = T Diag(beta) K0: D_W[r][i] (M = 128, rows 64..127 a copy),
         // A = T Diag(beta) (K-major), B = K0 (MN-major)
         if (t == 0) {
             const uint32_t idw = instr_desc(kFmtBF16, 128, 128, 0, 1);
@@ -658,20 +675,22 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         if (t == 0 && has_next) issue_g(Jn);
         loads_g += has_next;
         // ===== -W (bf16, K-major sw) -> the free K0 tile -> record rows 0..63
-        // of both halves by two bulk copies: lane r, 64 channels
-        if ((warp & 3) < 2) {
-            const int r = 32 * (warp & 3) + lane, half = warp >> 2;
+        // of both halves by two bulk copies.  TMEM lane l holds row l & 63 (the
+        // two lane halves are copies); thread: row r, 32 channels
+        {
+            const int r = (32 * (warp & 3) + lane) & 63;
+            const int cq = 2 * (warp >> 2) + ((warp & 3) >> 1);   // 32-channel quarter
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q2 = 0; q2 < 2; ++q2) {
                 float d[16];
-                tmem_ld16(tmem + lane_base + TMA_W + 64 * half + 16 * q4, d);
+                tmem_ld16(tmem + lane_base + TMA_W + 32 * cq + 16 * q2, d);
                 tmem_wait_ld();
 #pragma unroll
                 for (int c8 = 0; c8 < 2; ++c8) {
                     float x8[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x8[e] = -d[8 * c8 + e];
-                    *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, 8 * half + 2 * q4 + c8, 8192)) =
+                    *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, 4 * cq + 2 * q2 + c8, 8192)) =
                         pack_bf8(x8);
                 }
             }
