@@ -206,9 +206,13 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     float bnext = (t < C) ? load_beta(J) : 0.f;
     sync_tc();
     const uint32_t tmem = *s_tmem;
+    // Each job commits two MMA groups (the Gram: phase parity 0, W: parity 1)
+    // and one phase on each load barrier (parity it & 1).  On a failed wait,
+    // `fail_at` records what is still in flight: 1 = this job's loads, 2 = the
+    // Gram, 3 = the W product and the next job's q and k.
     bool failed = false;
-    int commits = 0;                       // MMA commits issued on bar_mma
-    int loads_qk = 1, loads_g = 1;         // phases issued on bar_qk / bar_g
+    int fail_at = 0, fail_it = 0;
+    bool fail_next = false;
 
     for (int it = 0; !failed; ++it) {
     const int h = J.h, Lc = J.Lc;
@@ -220,7 +224,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     const int job_next = job + gridDim.x;
     const bool has_next = job_next < total;
     Job Jn = J;
-    if (!wait_all(bar_qk, it & 1) || !wait_all(bar_g, it & 1)) { failed = true; break; }
+    if (!wait_all(bar_qk, it & 1) || !wait_all(bar_g, it & 1)) { failed = true; fail_at = 1; fail_it = it; fail_next = has_next; break; }
 
     {
         // ===== decay prefix sums: column scan in place in the g tile =========
@@ -437,7 +441,6 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             }
             mma_commit(bar_mma);
         }
-        ++commits;
         {
             float *rv = reinterpret_cast<float *>(rec + R_VEC);
             if (t < 64) {
@@ -455,13 +458,12 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 for (int bx = 0; bx < 4; ++bx) tma_prefetch_l2_3d(&map_g, 32 * bx, Jn.h, Jn.tok);
             }
         }
-        if (!wait_all(bar_mma, (uint32_t)(commits - 1) & 1u)) { failed = true; break; }
+        if (!wait_all(bar_mma, 0)) { failed = true; fail_at = 2; fail_it = it; fail_next = has_next; break; }
     }
     {
         tc_fence_after();
         // X is consumed: the next job's q and k
         if (t == 0 && has_next) issue_qk(Jn);
-        loads_qk += has_next;
         // ===== Gram epilogue -> A' (tf32, record) and M = Diag(beta) G^kk (fp32)
         float *Mm = reinterpret_cast<float *>(sm + SA_M);
         {
@@ -536,49 +538,59 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         __syncthreads();
         // off-diagonal blocks, two levels: T_10 and T_32 (T_pq = -T_pp M_pq T_qq),
         // then the lower-left 32x32 block T_C = -T_B M_C T_A
-        if (t < 128) {
-            const int blk = t >> 6, r = (t >> 2) & 15, c4 = t & 3;
+        {
+            // thread = (block, row r, 4 columns c4, half kh of the 16-term sum)
+            const int kh = t & 1, c4 = (t >> 1) & 3, r = (t >> 3) & 15, blk = t >> 7;
             const int p = blk ? 3 : 1, q = p - 1;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            float arow[16];
+            float arow[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (16 * p + r) * MLD + 16 * q + 4 * j);
+            for (int j = 0; j < 2; ++j) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (16 * p + r) * MLD + 16 * q + 8 * kh + 4 * j);
                 arow[4 * j] = a4.x; arow[4 * j + 1] = a4.y; arow[4 * j + 2] = a4.z; arow[4 * j + 3] = a4.w;
             }
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
+            for (int m = 0; m < 8; ++m) {
                 const float a = arow[m];
-                const float4 tv = *reinterpret_cast<const float4 *>(Mm + (16 * q + m) * MLD + 16 * q + 4 * c4);
+                const float4 tv = *reinterpret_cast<const float4 *>(Mm + (16 * q + 8 * kh + m) * MLD + 16 * q + 4 * c4);
                 acc.x = fmaf(a, tv.x, acc.x);
                 acc.y = fmaf(a, tv.y, acc.y);
                 acc.z = fmaf(a, tv.z, acc.z);
                 acc.w = fmaf(a, tv.w, acc.w);
             }
-            *reinterpret_cast<float4 *>(Yt + (blk * 16 + r) * 16 + 4 * c4) = acc;
+            acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 1);
+            acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 1);
+            acc.z += __shfl_xor_sync(0xffffffffu, acc.z, 1);
+            acc.w += __shfl_xor_sync(0xffffffffu, acc.w, 1);
+            if (kh == 0) *reinterpret_cast<float4 *>(Yt + (blk * 16 + r) * 16 + 4 * c4) = acc;
         }
         __syncthreads();
-        if (t < 128) {
-            const int blk = t >> 6, r = (t >> 2) & 15, c4 = t & 3;
+        {
+            const int kh = t & 1, c4 = (t >> 1) & 3, r = (t >> 3) & 15, blk = t >> 7;
             const int p = blk ? 3 : 1, q = p - 1;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            float arow[16];
+            float arow[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (16 * p + r) * MLD + 16 * p + 4 * j);
+            for (int j = 0; j < 2; ++j) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (16 * p + r) * MLD + 16 * p + 8 * kh + 4 * j);
                 arow[4 * j] = a4.x; arow[4 * j + 1] = a4.y; arow[4 * j + 2] = a4.z; arow[4 * j + 3] = a4.w;
             }
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
+            for (int m = 0; m < 8; ++m) {
                 const float a = arow[m];
-                const float4 yv = *reinterpret_cast<const float4 *>(Yt + (blk * 16 + m) * 16 + 4 * c4);
+                const float4 yv = *reinterpret_cast<const float4 *>(Yt + (blk * 16 + 8 * kh + m) * 16 + 4 * c4);
                 acc.x = fmaf(a, yv.x, acc.x);
                 acc.y = fmaf(a, yv.y, acc.y);
                 acc.z = fmaf(a, yv.z, acc.z);
                 acc.w = fmaf(a, yv.w, acc.w);
             }
-            *reinterpret_cast<float4 *>(Mm + (16 * p + r) * MLD + 16 * q + 4 * c4) =
-                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 1);
+            acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 1);
+            acc.z += __shfl_xor_sync(0xffffffffu, acc.z, 1);
+            acc.w += __shfl_xor_sync(0xffffffffu, acc.w, 1);
+            if (kh == 0)
+                *reinterpret_cast<float4 *>(Mm + (16 * p + r) * MLD + 16 * q + 4 * c4) =
+                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         __syncthreads();
         {
@@ -666,14 +678,12 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             }
             mma_commit(bar_mma);
         }
-        ++commits;
-        if (!wait_all(bar_mma, (uint32_t)(commits - 1) & 1u)) { failed = true; break; }
+        if (!wait_all(bar_mma, 1)) { failed = true; fail_at = 3; fail_it = it; fail_next = has_next; break; }
     }
     {
         tc_fence_after();
         // the Khat / solve space is free: the next job's g
         if (t == 0 && has_next) issue_g(Jn);
-        loads_g += has_next;
         // ===== -W (bf16, K-major sw) -> the free K0 tile -> record rows 0..63
         // of both halves by two bulk copies.  TMEM lane l holds row l & 63 (the
         // two lane halves are copies); thread: row r, 32 channels
@@ -715,9 +725,14 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     if (failed) {
         if (t == 0) atomicOr(&g_kda_split_error, 1u);
         // let copies and MMAs in flight finish (bounded) before freeing TMEM
-        mbar_wait(bar_qk, (uint32_t)(loads_qk - 1) & 1u, kWaitLimit);
-        mbar_wait(bar_g, (uint32_t)(loads_g - 1) & 1u, kWaitLimit);
-        if (commits) mbar_wait(bar_mma, (uint32_t)(commits - 1) & 1u, kWaitLimit);
+        const uint32_t par = (uint32_t)(fail_it & 1);
+        if (fail_at == 1) {
+            mbar_wait(bar_qk, par, kWaitLimit);
+            mbar_wait(bar_g, par, kWaitLimit);
+        } else {
+            mbar_wait(bar_mma, fail_at == 2 ? 0u : 1u, kWaitLimit);
+            if (fail_at == 3 && fail_next) mbar_wait(bar_qk, par ^ 1u, kWaitLimit);
+        }
     }
     sync_tc();
     if (warp == 0) tmem_dealloc(tmem, 256);
