@@ -120,11 +120,7 @@ int kda_decode_step(const void *q, const void *k, const void *v, const float *g,
 
 int kda_device_error(unsigned int *code, int reset) {
     if (!code) return KDA_ERR_NULL;
-    unsigned int a = 0, b = 0;
-    const cudaError_t e1 = kda::read_device_error(&a, reset != 0);
-    const cudaError_t e2 = kda::read_split_error(&b, reset != 0);
-    *code = a | b;
-    return cuda_status(e1 != cudaSuccess ? e1 : e2);
+    return cuda_status(kda::read_device_error(code, reset != 0));
 }
 
 }  // extern "C"

@@ -22,12 +22,6 @@ cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, con
                                 const int32_t *cu_seqlens, int N, int H, int chunk, bool bf16,
                                 cudaStream_t stream);
 
-// Tensor-core chunked prefill (kda_prefill_tc.cu): bf16 q/k/v, chunk 64, T >= 1.
-cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
-                              const float *beta, const float *S0, float *o, float *S_out,
-                              const int32_t *cu_seqlens, int N, int64_t T, int H,
-                              cudaStream_t stream);
-
 // Two-kernel tensor-core chunked prefill (kda_prefill_split.cu): bf16 q/k/v,
 // chunk 64, T >= 1.  Takes its workspace (see prefill_split_workspace_bytes)
 // from a library-owned stream-ordered pool; returns cudaErrorMemoryAllocation
@@ -50,10 +44,9 @@ cudaError_t launch_prefill_split_noalloc(const void *q, const void *k, const voi
                                          float *o, float *S_out, const int32_t *cu_seqlens, int N,
                                          int64_t T, int H, cudaStream_t stream);
 
-// Read (and optionally clear) the device-side error words that the
+// Read (and optionally clear) the device-side error word that the
 // tensor-core kernels set when a bounded wait gives up.
 cudaError_t read_device_error(unsigned int *code, bool reset);
-cudaError_t read_split_error(unsigned int *code, bool reset);
 
 // Input loads: bf16 or fp32 element -> fp32.
 __device__ __forceinline__ float load_in(const __nv_bfloat16 *p, size_t i) {

@@ -43,7 +43,7 @@ namespace kda {
 
 // Nonzero when a bounded wait in either kernel gave up, or the chunk plan
 // did not fit the workspace.
-__device__ unsigned int g_kda_split_error = 0;
+__device__ unsigned int g_kda_device_error = 0;
 
 namespace {
 using namespace tc;
@@ -723,7 +723,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
 
     if (t == 0) bulk_wait();                 // record copies complete before the CTA exits
     if (failed) {
-        if (t == 0) atomicOr(&g_kda_split_error, 1u);
+        if (t == 0) atomicOr(&g_kda_device_error, 1u);
         // let copies and MMAs in flight finish (bounded) before freeing TMEM
         const uint32_t par = (uint32_t)(fail_it & 1);
         if (fail_at == 1) {
@@ -996,7 +996,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
     if (t == 0) bulk_wait();                 // o stores complete before the CTA exits
 
     if (failed) {
-        if (t == 0) atomicOr(&g_kda_split_error, 1u);
+        if (t == 0) atomicOr(&g_kda_device_error, 1u);
         // let copies and MMAs in flight finish (bounded) before freeing TMEM
         if (issued_a) mbar_wait(bar_a, (uint32_t)(issued_a - 1) & 1u, kWaitLimit);
         if (issued_b) mbar_wait(bar_b, (uint32_t)(issued_b - 1) & 1u, kWaitLimit);
@@ -1160,11 +1160,11 @@ cudaError_t launch_prefill_split_noalloc(const void *q, const void *k, const voi
     return run_split(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, T, H, ws, stream);
 }
 
-cudaError_t read_split_error(unsigned int *code, bool reset) {
-    cudaError_t e = cudaMemcpyFromSymbol(code, g_kda_split_error, sizeof(unsigned int));
+cudaError_t read_device_error(unsigned int *code, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_kda_device_error, sizeof(unsigned int));
     if (e != cudaSuccess || !reset) return e;
     const unsigned int zero = 0;
-    return cudaMemcpyToSymbol(g_kda_split_error, &zero, sizeof(unsigned int));
+    return cudaMemcpyToSymbol(g_kda_device_error, &zero, sizeof(unsigned int));
 }
 
 }  // namespace kda
