@@ -385,7 +385,41 @@ def _decode_leg(kda, torch, dev, stream, peaks, args):
                      "traffic": _traffic("decode_kernel", "kda_decode.cu"),
                      "algorithmic_bytes": int(all_bytes)},
         "gpu_launches": n_steps,
+        "pool_bf16": _decode_pool_leg(kda, torch, dev, stream, peaks, S, ins, B, H),
     }
+
+
+def _decode_pool_leg(kda, torch, dev, stream, peaks, S32, ins, B, H):
+    """The same 100 steps on a bf16 state pool addressed by a permuted slot
+    table (kda_decode_step_pool): half the state bytes per step."""
+    P = B
+    S = S32.to(torch.bfloat16)
+    g = torch.Generator().manual_seed(7)
+    slots = torch.randperm(P, generator=g).to(torch.int32).to(dev)
+    o = torch.empty((B, H, DV), dtype=torch.float32, device=dev)
+    for i in range(3):
+        x = ins[i]
+        kda.decode_step_pool(x["q"], x["k"], x["v"], x["g"], x["beta"], S, state_indices=slots, o=o)
+    torch.cuda.synchronize()
+    evs = []
+    for x in ins:
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        kda.decode_step_pool(x["q"], x["k"], x["v"], x["g"], x["beta"], S, state_indices=slots, o=o)
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    med = statistics.median(a.elapsed_time(b) for a, b in evs)
+    state_bytes = 2 * (STATE_BYTES // 2) * B * H
+    all_bytes = (DECODE_BYTES_PER_STATE - STATE_BYTES) * B * H
+    gbs_all = all_bytes / (med / 1e3) / 1e9
+    return {"workload": "decode_b64 on a bf16 pool, permuted slots", "median_step_us": round(med * 1e3, 2),
+            "state_gbs": round(state_bytes / (med / 1e3) / 1e9, 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs_all, 1), "peak": peaks["hbm"],
+                         "unit": "GB/s", "frac": round(gbs_all / peaks["hbm"], 4),
+                         "algorithmic_bytes": int(all_bytes)},
+            "gpu_launches": len(ins)}
 
 
 def _e2e_leg(kda, torch, dev, stream, pre, dstep, args, barrier, ws):

@@ -181,12 +181,41 @@ int kda_decode_step(const void *q, const void *k, const void *v,
                     int B, int H, int dk, int dv, int dtype, void *stream);
 
 /*
- * Device-side error word of the library.  The tensor-core prefill kernels
- * never wait without bound: if one of their waits on an asynchronous copy or
+ * One decode token for each of B sequences whose states live in a pool:
+ * sequence b reads and updates pool row state_indices[b] in place (the
+ * decode-side interface of continuous batching: the TPU KDA decode kernel
+ * indexes its state the same way, "Kimi K3 -> TPU v7x feasibility", section
+ * 4.2), and the pool may be stored in bf16 to halve the state traffic (the
+ * pages list a bf16 state as not yet evaluated for stability, same review,
+ * section 6; the recurrence is computed in fp32 and each state value is
+ * rounded to nearest-even bf16 when it is stored).
+ *
+ *   q, k, v, g, beta, o   as for kda_decode_step ([B, H, ...])
+ *   S_pool        [P, H, dk, dv], fp32 (state_dtype KDA_F32) or bf16
+ *                 (KDA_BF16), read and overwritten in place
+ *   state_indices [B] int32 DEVICE array of pool rows, or NULL for the
+ *                 identity (then P >= B).  A negative entry marks a padding
+ *                 row: its o is written as zeros and no state is touched.
+ *                 Entries must be distinct (two sequences on one row race);
+ *                 an entry >= P is skipped like padding and sets bit 1 of
+ *                 the device error word.
+ *   P             pool rows (>= 0)
+ * Returns KDA_OK or a kda_status_t; B = 0 is a no-op.
+ */
+int kda_decode_step_pool(const void *q, const void *k, const void *v,
+                         const float *g, const float *beta, void *S_pool,
+                         int state_dtype, const int32_t *state_indices, int P,
+                         float *o, int B, int H, int dk, int dv, int dtype,
+                         void *stream);
+
+/*
+ * Device-side error word of the library.  Bit 0: the tensor-core prefill
+ * kernels never wait without bound: if one of their waits on an asynchronous copy or
  * on the tensor cores runs past its iteration limit they set a bit here,
  * release their tensor memory and exit (the outputs are then invalid).  The
  * state pass also sets it when a sequence's chunk count does not match the
- * workspace it was sized for (cu_seqlens inconsistent with T).
+ * workspace it was sized for (cu_seqlens inconsistent with T).  Bit 1: a
+ * kda_decode_step_pool slot index was past the end of the pool.
  *
  *   code   host pointer, receives the word (0 = no error since the last reset)
  *   reset  nonzero: clear the word after reading it

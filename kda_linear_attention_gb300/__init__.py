@@ -21,7 +21,8 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["prefill_chunked", "prefill_chunked_noalloc", "prefill_chunked_events", "decode_step", "device_error", "lib",
+__all__ = ["prefill_chunked", "prefill_chunked_noalloc", "prefill_chunked_events", "decode_step",
+           "decode_step_pool", "device_error", "lib",
            "KDAError", "KDA_BF16", "KDA_F32", "library_path"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -69,6 +70,9 @@ def lib() -> ctypes.CDLL:
         L.kda_prefill_chunked_events.restype = i32
         L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
         L.kda_decode_step.restype = i32
+        L.kda_decode_step_pool.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32,
+                                           i32, i32, i32, vp]
+        L.kda_decode_step_pool.restype = i32
         L.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         L.kda_device_error.restype = i32
         _lib = L
@@ -209,6 +213,45 @@ def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
                                dt, _stream(dev, stream))
     if rc != 0:
         raise KDAError(rc, "kda_decode_step")
+    return o
+
+
+def decode_step_pool(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                     beta: torch.Tensor, S_pool: torch.Tensor,
+                     state_indices: Optional[torch.Tensor] = None,
+                     o: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """One decode token per sequence on a state pool (``kda_decode_step_pool``).
+
+    S_pool [P, H, 128, 128] fp32 or bf16 is updated in place at rows
+    ``state_indices`` ([B] int32; negative = padding, o row zero), or at rows
+    0..B-1 when it is None.  Returns o [B, H, 128] fp32.
+    """
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, H = q.shape[0], q.shape[1]
+    dt = _qkv_dtype(q)
+    _check("q", q, q.dtype, (B, H, DK), dev)
+    _check("k", k, q.dtype, (B, H, DK), dev)
+    _check("v", v, q.dtype, (B, H, DV), dev)
+    _check("g", g, torch.float32, (B, H, DK), dev)
+    _check("beta", beta, torch.float32, (B, H), dev)
+    if S_pool.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("S_pool must be float32 or bfloat16")
+    P = S_pool.shape[0]
+    _check("S_pool", S_pool, S_pool.dtype, (P, H, DK, DV), dev)
+    if state_indices is not None:
+        _check("state_indices", state_indices, torch.int32, (B,), dev)
+    if o is None:
+        o = torch.empty((B, H, DV), dtype=torch.float32, device=dev)
+    _check("o", o, torch.float32, (B, H, DV), dev)
+    sdt = KDA_BF16 if S_pool.dtype == torch.bfloat16 else KDA_F32
+    rc = lib().kda_decode_step_pool(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S_pool), sdt,
+                                    _p(state_indices), P, _p(o), B, H, DK, DV, dt,
+                                    _stream(dev, stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_decode_step_pool")
     return o
 
 

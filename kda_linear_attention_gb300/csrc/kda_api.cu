@@ -118,9 +118,32 @@ int kda_decode_step(const void *q, const void *k, const void *v, const float *g,
     return cuda_status(kda::launch_decode(q, k, v, g, beta, S_inout, o, B, H, dtype == KDA_BF16, s));
 }
 
+int kda_decode_step_pool(const void *q, const void *k, const void *v, const float *g,
+                         const float *beta, void *S_pool, int state_dtype,
+                         const int32_t *state_indices, int P, float *o, int B, int H, int dk,
+                         int dv, int dtype, void *stream) {
+    if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_DTYPE;
+    if (state_dtype != KDA_BF16 && state_dtype != KDA_F32) return KDA_ERR_DTYPE;
+    if (dk != kda::kDK || dv != kda::kDV || B < 0 || H < 1 || P < 0) return KDA_ERR_DIM;
+    if ((int64_t)B * H * 2 >= (int64_t(1) << 31)) return KDA_ERR_DIM;
+    if (!state_indices && P < B) return KDA_ERR_DIM;
+    if (B == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !S_pool || !o) return KDA_ERR_NULL;
+    const void *ptrs[] = {q, k, v, g, beta, S_pool, o, state_indices};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(kda::launch_decode_pool(q, k, v, g, beta, S_pool, state_dtype == KDA_BF16,
+                                               state_indices, P, o, B, H, dtype == KDA_BF16, s));
+}
+
 int kda_device_error(unsigned int *code, int reset) {
     if (!code) return KDA_ERR_NULL;
-    return cuda_status(kda::read_device_error(code, reset != 0));
+    unsigned int a = 0, b = 0;
+    const cudaError_t e1 = kda::read_device_error(&a, reset != 0);
+    const cudaError_t e2 = kda::read_decode_error(&b, reset != 0);
+    *code = a | b;
+    return cuda_status(e1 != cudaSuccess ? e1 : e2);
 }
 
 }  // extern "C"

@@ -10,6 +10,11 @@
 // while it is still in registers, so each 64 KiB state is read once and
 // written once: the kernel is bound by HBM bandwidth.
 //
+// The state can live in a pool addressed by per-sequence slots (continuous
+// batching: sequence b uses pool row state_indices[b], a negative slot marks
+// a padding row that is skipped), and can be stored in bf16 (loaded into
+// fp32, updated in fp32, rounded to nearest-even on the store).
+//
 // Work split: a block owns COLS value-columns of one (b, h) state (columns
 // evolve independently).  Thread t holds float4 column group t % (COLS/4) for
 // rows rg, rg + NRG, ... (rg = t / (COLS/4)), so each warp load covers whole
@@ -18,15 +23,42 @@
 #include "kda_internal.h"
 
 namespace kda {
+
+// Set (bit 1) when a decode slot index lies past the end of the pool.
+__device__ unsigned int g_kda_decode_error = 0;
+
 namespace {
 
 constexpr int kDecodeThreads = 256;
 
-template <typename TIn, int COLS>
+// four consecutive state values <-> registers
+__device__ __forceinline__ float4 load_state4(const float *p) {
+    return __ldcs(reinterpret_cast<const float4 *>(p));
+}
+__device__ __forceinline__ float4 load_state4(const __nv_bfloat16 *p) {
+    const uint2 u = __ldcs(reinterpret_cast<const uint2 *>(p));
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void store_state4(float *p, float4 x) {
+    __stcs(reinterpret_cast<float4 *>(p), x);
+}
+__device__ __forceinline__ void store_state4(__nv_bfloat16 *p, float4 x) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(x.z, x.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t *>(&a);
+    u.y = *reinterpret_cast<const uint32_t *>(&b);
+    __stcs(reinterpret_cast<uint2 *>(p), u);
+}
+
+template <typename TIn, typename TS, int COLS>
 __global__ void __launch_bounds__(kDecodeThreads, (COLS == 128 ? 2 : 4))
 decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
               const float *__restrict__ g, const float *__restrict__ beta,
-              float *__restrict__ S, float *__restrict__ o) {
+              TS *__restrict__ S, float *__restrict__ o, const int32_t *__restrict__ slots,
+              int H, int P) {
     constexpr int C4 = COLS / 4;                 // float4 column groups per block
     constexpr int NRG = kDecodeThreads / C4;     // row groups
     constexpr int RPT = kDK / NRG;               // rows per thread
@@ -39,13 +71,24 @@ decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *_
     const int rg = t / C4;
     const int col0 = cs * COLS + c4 * 4;
 
-    float *Su = S + (size_t)unit * kDK * kDV;
+    // pool row of this sequence (the identity without a slot table)
+    int slot = unit / H;
+    if (slots) {
+        slot = slots[unit / H];
+        if (slot < 0 || slot >= P) {             // padding row (or an invalid slot)
+            if (slot >= P && t == 0) atomicOr(&g_kda_decode_error, 2u);
+            if (rg == 0)
+                *reinterpret_cast<float4 *>(o + (size_t)unit * kDV + col0) =
+                    make_float4(0.f, 0.f, 0.f, 0.f);
+            return;
+        }
+    }
+    TS *Su = S + ((size_t)slot * H + unit % H) * kDK * kDV;
 
     // Issue the state loads first; they are independent of everything else.
     float4 s[RPT];
 #pragma unroll
-    for (int r = 0; r < RPT; ++r)
-        s[r] = __ldcs(reinterpret_cast<const float4 *>(Su + (size_t)(rg + r * NRG) * kDV + col0));
+    for (int r = 0; r < RPT; ++r) s[r] = load_state4(Su + (size_t)(rg + r * NRG) * kDV + col0);
 
     __shared__ float sq[kDK], sk[kDK], sa[kDK];
     __shared__ float4 red_k[NRG][C4];
@@ -103,7 +146,7 @@ decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *_
         const int i = rg + r * NRG;
         const float ki = sk[i];
         s[r].x += ki * w.x; s[r].y += ki * w.y; s[r].z += ki * w.z; s[r].w += ki * w.w;
-        __stcs(reinterpret_cast<float4 *>(Su + (size_t)i * kDV + col0), s[r]);
+        store_state4(Su + (size_t)i * kDV + col0, s[r]);
     }
     if (rg == 0) {
         float4 ov;
@@ -113,18 +156,18 @@ decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *_
     }
 }
 
-template <typename TIn>
+template <typename TIn, typename TS>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *g,
-                         const float *beta, float *S, float *o, int B, int H,
-                         cudaStream_t stream) {
+                         const float *beta, void *S, float *o, const int32_t *slots, int B, int H,
+                         int P, cudaStream_t stream) {
     // Two blocks per state (64 columns each): twice the blocks of a
     // whole-state split, a shorter tail and fewer registers per thread.
     constexpr int COLS = 64;
     const long long units = (long long)B * H;
     const long long blocks = units * (kDV / COLS);
-    decode_kernel<TIn, COLS><<<(unsigned)blocks, kDecodeThreads, 0, stream>>>(
+    decode_kernel<TIn, TS, COLS><<<(unsigned)blocks, kDecodeThreads, 0, stream>>>(
         static_cast<const TIn *>(q), static_cast<const TIn *>(k), static_cast<const TIn *>(v),
-        g, beta, S, o);
+        g, beta, static_cast<TS *>(S), o, slots, H, P);
     return cudaGetLastError();
 }
 
@@ -133,8 +176,29 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *S, float *o, int B, int H, bool bf16,
                           cudaStream_t stream) {
-    if (bf16) return launch_typed<__nv_bfloat16>(q, k, v, g, beta, S, o, B, H, stream);
-    return launch_typed<float>(q, k, v, g, beta, S, o, B, H, stream);
+    if (bf16) return launch_typed<__nv_bfloat16, float>(q, k, v, g, beta, S, o, nullptr, B, H, B, stream);
+    return launch_typed<float, float>(q, k, v, g, beta, S, o, nullptr, B, H, B, stream);
+}
+
+cudaError_t launch_decode_pool(const void *q, const void *k, const void *v, const float *g,
+                               const float *beta, void *S_pool, bool state_bf16,
+                               const int32_t *slots, int P, float *o, int B, int H, bool bf16,
+                               cudaStream_t stream) {
+    if (bf16) {
+        if (state_bf16)
+            return launch_typed<__nv_bfloat16, __nv_bfloat16>(q, k, v, g, beta, S_pool, o, slots, B, H, P, stream);
+        return launch_typed<__nv_bfloat16, float>(q, k, v, g, beta, S_pool, o, slots, B, H, P, stream);
+    }
+    if (state_bf16)
+        return launch_typed<float, __nv_bfloat16>(q, k, v, g, beta, S_pool, o, slots, B, H, P, stream);
+    return launch_typed<float, float>(q, k, v, g, beta, S_pool, o, slots, B, H, P, stream);
+}
+
+cudaError_t read_decode_error(unsigned int *code, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_kda_decode_error, sizeof(unsigned int));
+    if (e != cudaSuccess || !reset) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_kda_decode_error, &zero, sizeof(unsigned int));
 }
 
 }  // namespace kda

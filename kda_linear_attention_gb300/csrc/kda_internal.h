@@ -15,6 +15,15 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, const flo
                           const float *beta, float *S, float *o, int B, int H, bool bf16,
                           cudaStream_t stream);
 
+// Decode step on a state pool: sequence b updates pool row slots[b] (the
+// identity when slots == nullptr; negative slots are padding rows whose o is
+// zero); the pool is fp32 or bf16 (state_bf16).  P = pool rows.
+cudaError_t launch_decode_pool(const void *q, const void *k, const void *v, const float *g,
+                               const float *beta, void *S_pool, bool state_bf16,
+                               const int32_t *slots, int P, float *o, int B, int H, bool bf16,
+                               cudaStream_t stream);
+cudaError_t read_decode_error(unsigned int *code, bool reset);
+
 // fp32 CUDA-core chunked prefill (kda_prefill_simt.cu): any chunk in {16,32,64},
 // bf16 or fp32 inputs.
 cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, const float *g,

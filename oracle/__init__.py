@@ -15,6 +15,8 @@ Contents
   chunked.py    an independent fp64 restatement in chunked (UT-transform)
                 form, used to pin the sequential oracle (they must agree to
                 rounding on tiny inputs).
+  decode_pool   the decode step on a state pool addressed by slot indices,
+                with an fp32 or a bf16-stored state (this file).
 
 Parity pins: every function here is pinned by the CPU tests in
 ``tests/test_oracle_pins.py`` (closed forms, exact retrieval, brute force,
@@ -168,3 +170,56 @@ def decode(S_in: np.ndarray, step, units: Optional[Iterable[Tuple[int, int]]] = 
         o[b, h] = ob[0]
         S[b, h] = Sb
     return o, S
+
+
+# ---------------------------------------------------------------- state pools
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Nearest bfloat16 value (8 significant bits, ties to even) of each fp64
+    element, returned as fp64.  Written from the format's definition: with
+    x = m * 2^e, 0.5 <= |m| < 1, the bf16 value is rint(m * 2^8) * 2^(e-8),
+    rint rounding half to even.  Normal range only (|x| >= 2^-126), which
+    covers every state this package stores."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) -> exact fp64 values."""
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+def decode_pool(S_pool: np.ndarray, step, state_indices: Optional[np.ndarray] = None,
+                state_bf16: bool = False, threads: Optional[int] = None):
+    """One decode token per sequence on a state pool.
+
+    Sequence b updates pool row ``state_indices[b]`` (the identity when None;
+    a negative entry is a padding row: o = 0 and no state changes), as the TPU
+    KDA decode kernel indexes its states ("Kimi K3 -> TPU v7x feasibility",
+    section 4.2).  ``S_pool`` is [P, H, dk, dv] float32, or uint16 bf16 bit
+    patterns when ``state_bf16`` (the bf16-stored state of the same review,
+    section 6): the state is read exactly, the token step runs in fp64 (the
+    sequential oracle), o comes from the updated fp64 state, and the stored
+    state is that state rounded to bf16 (``round_bf16``).
+
+    Returns (o [B, H, dv] fp64, pool after the step [P, H, dk, dv] fp64).
+    """
+    B, H = step.q.shape[0], step.q.shape[1]
+    dv = step.v.shape[2]
+    pool = bf16_bits_to_f64(S_pool) if state_bf16 else np.asarray(S_pool, dtype=np.float64)
+    P = pool.shape[0]
+    idx = np.arange(B) if state_indices is None else np.asarray(state_indices, dtype=np.int64)
+    out = pool.copy()
+    o = np.zeros((B, H, dv), dtype=np.float64)
+    todo = [(b, h) for b in range(B) for h in range(H) if 0 <= idx[b] < P]
+
+    def one(bh):
+        b, h = bh
+        return bh, run_unit(step.q, step.k, step.v, step.g, step.beta, pool[idx[b], h], b, b + 1, h)
+
+    with ThreadPoolExecutor(max_workers=threads or default_threads()) as ex:
+        for (b, h), (ob, Sb) in ex.map(one, todo):
+            o[b, h] = ob[0]
+            out[idx[b], h] = round_bf16(Sb) if state_bf16 else Sb
+    return o, out

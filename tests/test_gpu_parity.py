@@ -244,3 +244,112 @@ def test_varlen_64k_then_decode_sampled():
                                    n, n + 1, h)
         assert_close(od[n, h], o_r[0], TOL_BF16, "decode o seq %d head %d" % (n, h))
         assert_close(Sd_np[n, h], S_r, TOL_BF16, "decode S seq %d head %d" % (n, h))
+
+
+# ---------------------------------------------------------------- state pools
+def _pool_gpu(pool_in, state_bf16):
+    return dev_tensor(pool_in)     # uint16 bit patterns become a bf16 tensor
+
+
+def _pool_host(t, state_bf16):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_decode_pool_slots_padding_and_storage(state_dtype):
+    """Pool decode through kda_decode_step_pool against the oracle: permuted
+    slots, padding rows (o = 0, state untouched), rows nobody names untouched;
+    a bf16 pool stores a correct bf16 rounding of the updated state."""
+    import torch
+    import kda_linear_attention_gb300 as kda
+    bf = state_dtype == "bf16"
+    r = np.random.Generator(np.random.PCG64(46))
+    P, B, H = 9, 6, 8
+    pool32 = ki.gen_decode_state(r, P, H)
+    step = ki.gen_decode_step(r, B, H, "bf16")
+    idx = np.array([4, -1, 0, 8, 2, -1], dtype=np.int32)
+    pool_in = ki.f32_to_bf16_bits(pool32) if bf else pool32
+    o_ref, pool_ref = oracle.decode_pool(pool_in, step, idx, state_bf16=bf)
+    S = _pool_gpu(pool_in, bf)
+    d = {n: dev_tensor(getattr(step, n)) for n in ("q", "k", "v", "g", "beta")}
+    o = kda.decode_step_pool(d["q"], d["k"], d["v"], d["g"], d["beta"], S,
+                             state_indices=dev_tensor(idx))
+    torch.cuda.synchronize()
+    assert kda.device_error() == 0
+    o = o.cpu().numpy()
+    assert_close(o, o_ref, TOL_BF16, "o")
+    for b in np.nonzero(idx < 0)[0]:
+        np.testing.assert_array_equal(o[b], 0.0)
+    got = _pool_host(S, bf)
+    start = oracle.bf16_bits_to_f64(pool_in) if bf else pool32.astype(np.float64)
+    used = {int(i) for i in idx if i >= 0}
+    for row in set(range(P)) - used:
+        np.testing.assert_array_equal(got[row], start[row])
+    rows = sorted(used)
+    if not bf:
+        assert_close(got[rows], pool_ref[rows], TOL_BF16, "S")
+        return
+    # the exact (unrounded) update, and the bf16 spacing at each value
+    gathered = np.stack([start[max(i, 0)] for i in idx]).astype(np.float32)
+    _, S_exact = oracle.decode(gathered, step)
+    exact = np.stack([S_exact[list(idx).index(i)] for i in rows])
+    # a bf16 neighbour of the exact value, up to the kernel's fp32 arithmetic
+    # (which matters only where cancellation leaves a value near zero)
+    ulp = np.ldexp(1.0, np.frexp(np.abs(exact))[1] - 8)
+    slack = 1e-6 * np.abs(exact).max()
+    assert np.all(np.abs(got[rows] - exact) <= ulp + slack), "a stored value is not a neighbour"
+    same = np.mean(got[rows] == pool_ref[rows])
+    assert same > 0.99, "rounding decisions differ from the oracle's on %.2f%%" % (100 * (1 - same))
+
+
+def test_decode_pool_invalid_slot_is_flagged_and_skipped():
+    import torch
+    import kda_linear_attention_gb300 as kda
+    r = np.random.Generator(np.random.PCG64(47))
+    P, B, H = 3, 2, 4
+    pool = ki.gen_decode_state(r, P, H)
+    step = ki.gen_decode_step(r, B, H, "bf16")
+    S = dev_tensor(pool)
+    d = {n: dev_tensor(getattr(step, n)) for n in ("q", "k", "v", "g", "beta")}
+    kda.device_error(reset=True)
+    o = kda.decode_step_pool(d["q"], d["k"], d["v"], d["g"], d["beta"], S,
+                             state_indices=dev_tensor(np.array([1, 3], dtype=np.int32)))
+    torch.cuda.synchronize()
+    assert kda.device_error(reset=True) & 2
+    np.testing.assert_array_equal(o.cpu().numpy()[1], 0.0)
+    o_ref, pool_ref = oracle.decode_pool(pool, step, np.array([1, -1], dtype=np.int32))
+    assert_close(o.cpu().numpy()[0], o_ref[0], TOL_BF16, "o")
+    assert_close(S.cpu().numpy(), pool_ref, TOL_BF16, "pool")
+
+
+def test_decode_bf16_state_trajectory_against_both_oracles():
+    """50 in-place steps on a bf16 pool: against the bf16-storing oracle
+    (same rounding points) within the bf16 bar, and against the fp32/fp64
+    oracle (the drift a bf16 state costs), which must stay bounded."""
+    import torch
+    import kda_linear_attention_gb300 as kda
+    r = np.random.Generator(np.random.PCG64(48))
+    B, H, steps = 4, 16, 50
+    S32 = ki.gen_decode_state(r, B, H)
+    bits = ki.f32_to_bf16_bits(S32)
+    S = dev_tensor(bits)
+    ref_bf = bits
+    ref_f = oracle.bf16_bits_to_f64(bits).astype(np.float32)
+    worst_bf = worst_f = 0.0
+    for _ in range(steps):
+        step = ki.gen_decode_step(r, B, H, "bf16")
+        d = {n: dev_tensor(getattr(step, n)) for n in ("q", "k", "v", "g", "beta")}
+        o = kda.decode_step_pool(d["q"], d["k"], d["v"], d["g"], d["beta"], S).cpu().numpy()
+        o_bf, pool_bf = oracle.decode_pool(ref_bf, step, state_bf16=True)
+        ref_bf = ki.f32_to_bf16_bits(pool_bf.astype(np.float32))   # exact: values are bf16
+        o_f, S_f = oracle.decode(ref_f, step)
+        ref_f = S_f.astype(np.float32)
+        worst_bf = max(worst_bf, rel_err(o, o_bf))
+        worst_f = max(worst_f, rel_err(o, o_f))
+    torch.cuda.synchronize()
+    assert worst_bf <= TOL_BF16, worst_bf
+    assert worst_f <= 1e-2, worst_f
+    S_end = S.float().cpu().numpy()
+    assert rel_err(S_end, oracle.bf16_bits_to_f64(ref_bf)) <= TOL_BF16
+    print("bf16 state, %d steps: o vs bf16 oracle %.2e, vs fp32 state %.2e, S vs fp32 %.2e"
+          % (steps, worst_bf, worst_f, rel_err(S_end, ref_f)))

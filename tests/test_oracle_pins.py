@@ -262,3 +262,82 @@ def test_input_recipe_ranges():
     x = b.f32("q")
     # the bf16 values are the fp32 ones rounded to nearest even
     np.testing.assert_array_equal(ki.f32_to_bf16_bits(x), b.q)
+
+
+# ---------------------------------------------------------------- state pools
+def test_round_bf16_matches_the_format():
+    """round_bf16 against torch's bfloat16 conversion (round to nearest even)
+    on fp32-representable values, including exact ties and both signs."""
+    torch = pytest.importorskip("torch")
+    r = np.random.Generator(np.random.PCG64(41))
+    x = (r.standard_normal(200000) * np.exp(r.uniform(-20, 20, 200000))).astype(np.float32)
+    # exact ties: 8 significant bits plus a half unit in the last place
+    base = r.integers(128, 256, 2000).astype(np.float64)
+    ties = np.ldexp(base + 0.5, r.integers(-30, 10, 2000) - 8).astype(np.float32)
+    x = np.concatenate([x, ties, -ties, np.float32([0.0, 1.0, -1.0, 3.0e38])])
+    want = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    got = oracle.round_bf16(x.astype(np.float64))
+    np.testing.assert_array_equal(got, want)
+
+
+def test_pool_identity_is_the_plain_decode():
+    r = np.random.Generator(np.random.PCG64(42))
+    S = ki.gen_decode_state(r, 3, 2)
+    step = ki.gen_decode_step(r, 3, 2, "bf16")
+    o1, S1 = oracle.decode(S, step)
+    o2, S2 = oracle.decode_pool(S, step)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(S1, S2)
+
+
+def test_pool_slots_gather_update_scatter_and_padding():
+    """Sequence b updates row idx[b]; rows no sequence names are untouched;
+    a negative slot gives o = 0 and touches nothing."""
+    r = np.random.Generator(np.random.PCG64(43))
+    P, B, H = 7, 4, 2
+    pool = ki.gen_decode_state(r, P, H)
+    step = ki.gen_decode_step(r, B, H, "bf16")
+    idx = np.array([5, -1, 0, 3], dtype=np.int32)
+    o, out = oracle.decode_pool(pool, step, idx)
+    gathered = np.stack([pool[max(i, 0)] for i in idx])
+    o_ref, S_ref = oracle.decode(gathered, step)
+    for b, i in enumerate(idx):
+        if i < 0:
+            np.testing.assert_array_equal(o[b], 0.0)
+        else:
+            np.testing.assert_array_equal(o[b], o_ref[b])
+            np.testing.assert_array_equal(out[i], S_ref[b])
+    for row in set(range(P)) - {int(i) for i in idx if i >= 0}:
+        np.testing.assert_array_equal(out[row], pool[row].astype(np.float64))
+
+
+def test_bf16_pool_stores_the_rounded_updated_state():
+    """A bf16 pool: the state is read exactly, updated in fp64, o is read out
+    from the unrounded update, and the stored state is its bf16 rounding."""
+    r = np.random.Generator(np.random.PCG64(44))
+    B, H = 3, 2
+    pool32 = ki.gen_decode_state(r, B, H)
+    bits = ki.f32_to_bf16_bits(pool32)
+    exact = oracle.bf16_bits_to_f64(bits)
+    step = ki.gen_decode_step(r, B, H, "bf16")
+    o, out = oracle.decode_pool(bits, step, state_bf16=True)
+    o_ref, S_ref = oracle.decode(exact.astype(np.float32), step)   # bf16 values are exact in fp32
+    np.testing.assert_array_equal(o, o_ref)
+    np.testing.assert_array_equal(out, oracle.round_bf16(S_ref))
+    # every stored value is a bf16 value
+    np.testing.assert_array_equal(oracle.round_bf16(out), out)
+
+
+def test_bf16_pool_identity_step_is_exact():
+    """g = 0, beta = 0: a bf16 state comes back bit for bit."""
+    r = np.random.Generator(np.random.PCG64(45))
+    B, H = 2, 3
+    bits = ki.f32_to_bf16_bits(ki.gen_decode_state(r, B, H))
+    step = ki.gen_decode_step(r, B, H, "bf16")
+    step.g[...] = 0.0
+    step.beta[...] = 0.0
+    o, out = oracle.decode_pool(bits, step, state_bf16=True)
+    np.testing.assert_array_equal(out, oracle.bf16_bits_to_f64(bits))
+    q = oracle.bf16_bits_to_f64(step.q)
+    want = np.einsum("bhi,bhij->bhj", q, oracle.bf16_bits_to_f64(bits))
+    np.testing.assert_allclose(o, want, rtol=1e-12, atol=1e-14)
