@@ -30,6 +30,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -87,7 +88,12 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling (every 200 ms) around the timed
+    region.  The timed steps of a workload last only milliseconds, so the
+    sampler is started first and the GPU is kept busy with untimed steps of
+    the same workload until samples arrive (``keep_busy``) before and after
+    the timed steps: the load window the samples cover contains the timed
+    region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -95,6 +101,14 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
+        self.lines = []
+        self._lock = threading.Lock()
+        self._reader = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            with self._lock:
+                self.lines.append(line)
 
     def __enter__(self):
         try:
@@ -102,23 +116,44 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._reader = threading.Thread(target=self._read, daemon=True)
+            self._reader.start()
         except Exception:
             self.proc = None
         return self
 
+    def count(self) -> int:
+        with self._lock:
+            return len(self.lines)
+
+    def keep_busy(self, step, n_new: int, timeout_s: float = 5.0, batch: int = 16):
+        """Run untimed steps (batches of `batch`, then a device synchronise)
+        until `n_new` more samples have arrived, for at most `timeout_s`."""
+        import torch
+        if self.proc is None:
+            return
+        target = self.count() + n_new
+        t_end = time.monotonic() + timeout_s
+        while self.count() < target and time.monotonic() < t_end:
+            for _ in range(batch):
+                step()
+            torch.cuda.synchronize()
+
     def __exit__(self, *a):
-        self.out = ""
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-                self.out = ""
+            if self._reader is not None:
+                self._reader.join(timeout=5)
 
     def summary(self):
         rows = []
-        for line in (self.out or "").strip().splitlines():
+        with self._lock:
+            lines = list(self.lines)
+        for line in lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -137,7 +172,9 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(r["sm"] for r in rows),
                 "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
-                "samples": len(rows)}
+                "samples": len(rows),
+                "window": "every 200 ms over a load window of untimed steps of the same "
+                          "workload that contains the timed steps"}
 
 
 # ---------------------------------------------------------------------------
@@ -227,16 +264,18 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    barrier()
-    torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        clk.keep_busy(step, 2)             # untimed load until the sampler reports
+        barrier()
+        torch.cuda.synchronize()
         t0.record(stream)
         for _ in range(args.steps):
             step(record=True)
         t1.record(stream)
         torch.cuda.synchronize()
+        clk.keep_busy(step, 1)
     barrier()
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
@@ -357,16 +396,24 @@ def _decode_leg(kda, torch, dev, stream, peaks, args):
     evs = []
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for x in ins:
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+
+    def untimed():
+        x = ins[0]
         kda.decode_step(x["q"], x["k"], x["v"], x["g"], x["beta"], S, o=o)
-        b.record(stream)
-        evs.append((a, b))
-    t1.record(stream)
-    torch.cuda.synchronize()
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        clk.keep_busy(untimed, 2, batch=64)
+        t0.record(stream)
+        for x in ins:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            kda.decode_step(x["q"], x["k"], x["v"], x["g"], x["beta"], S, o=o)
+            b.record(stream)
+            evs.append((a, b))
+        t1.record(stream)
+        torch.cuda.synchronize()
+        clk.keep_busy(untimed, 1, batch=64)
     per = [a.elapsed_time(b) for a, b in evs]
     total = t0.elapsed_time(t1)
     med = statistics.median(per)
@@ -385,6 +432,7 @@ def _decode_leg(kda, torch, dev, stream, peaks, args):
                      "traffic": _traffic("decode_kernel", "kda_decode.cu"),
                      "algorithmic_bytes": int(all_bytes)},
         "gpu_launches": n_steps,
+        "clocks": clk.summary(),
         "pool_bf16": _decode_pool_leg(kda, torch, dev, stream, peaks, S, ins, B, H),
     }
 
