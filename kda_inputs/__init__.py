@@ -252,3 +252,101 @@ def ragged_lens(seed: int, n: int, lo: int, hi: int) -> List[int]:
     """Sequence lengths for ragged parity cases (uniform in [lo, hi])."""
     r = np.random.Generator(np.random.PCG64(seed + 7919))
     return [int(x) for x in r.integers(lo, hi + 1, size=n)]
+
+
+# --------------------------------------------------------------------------
+# the layer around the recurrence: raw projections, conv taps and windows,
+# output gate and norm weight
+# --------------------------------------------------------------------------
+CONV_K = 4          # depthwise causal conv width of the model's KDA layer
+
+
+@dataclasses.dataclass
+class LayerInputs:
+    """Inputs of the KDA layer's prologue and epilogue around the recurrence.
+
+    xq, xk, xv  [T, H, d] bf16 bits: the q/k/v projections before the conv
+    conv_w      [3, H, d, K] float32: depthwise taps of the q, k, v convs;
+                tap m multiplies the input m positions before the newest
+                one counted from the oldest (tap K-1 = the newest input)
+    conv0       [N, 3, K-1, H, d] bf16 bits (oldest first) or None (zeros):
+                the last K-1 raw inputs before each sequence
+    gate        [T, H, dv] bf16 bits: the output gate's projection (before
+                its sigmoid)
+    norm_w      [dv] float32: the output RMSNorm weight
+    g, beta     as for the recurrence
+    """
+    xq: np.ndarray
+    xk: np.ndarray
+    xv: np.ndarray
+    conv_w: np.ndarray
+    conv0: Optional[np.ndarray]
+    gate: np.ndarray
+    norm_w: np.ndarray
+    g: np.ndarray
+    beta: np.ndarray
+    cu_seqlens: np.ndarray
+    S0: Optional[np.ndarray]
+
+    @property
+    def T(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def N(self) -> int:
+        return int(self.cu_seqlens.size - 1)
+
+    @property
+    def H(self) -> int:
+        return int(self.g.shape[1])
+
+
+def gen_layer(seed: int, lens: Sequence[int], H: int, with_conv0: bool = True,
+              with_s0: bool = False, s0_std: float = 0.02, conv_std: float = 0.5,
+              dk: int = DK, dv: int = DV,
+              rng: Optional[np.random.Generator] = None) -> LayerInputs:
+    """Draw order: xq, xk, xv ~ N(0,1) bf16; conv taps ~ N(0, conv_std^2)
+    fp32; conv windows ~ N(0,1) bf16; gate ~ N(0,1) bf16; norm weight
+    1 + 0.1 N(0,1) fp32; g, beta as for the recurrence; S0."""
+    if rng is None:
+        rng = np.random.Generator(np.random.PCG64(seed))
+    lens = [int(x) for x in lens]
+    cu = np.zeros(len(lens) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lens)
+    T, N = int(cu[-1]), len(lens)
+    xq = _v(rng, (T, H, dk), True)
+    xk = _v(rng, (T, H, dk), True)
+    xv = _v(rng, (T, H, dv), True)
+    conv_w = (np.float32(conv_std) * _normal(rng, (3, H, dk, CONV_K), slab_rows=1)).astype(np.float32)
+    conv0 = _v(rng, (N, 3, CONV_K - 1, H, dk), True) if with_conv0 else None
+    gate = _v(rng, (T, H, dv), True)
+    norm_w = (np.float32(1.0) + np.float32(0.1) * rng.standard_normal(dv, dtype=np.float32)).astype(np.float32)
+    g = _g(rng, (T, H, dk))
+    beta = _sigmoid(rng.standard_normal((T, H), dtype=np.float32))
+    S0 = None
+    if with_s0:
+        S0 = np.float32(s0_std) * _normal(rng, (N, H, dk, dv), slab_rows=1)
+    return LayerInputs(xq, xk, xv, conv_w, conv0, gate, norm_w, g, beta, cu, S0)
+
+
+@dataclasses.dataclass
+class LayerDecodeStep:
+    """One token per sequence of the whole layer step: raw projections
+    [B, H, d] bf16, gate [B, H, dv] bf16, g [B, H, dk] fp32, beta [B, H]."""
+    xq: np.ndarray
+    xk: np.ndarray
+    xv: np.ndarray
+    gate: np.ndarray
+    g: np.ndarray
+    beta: np.ndarray
+
+
+def gen_layer_decode_step(rng: np.random.Generator, B: int, H: int,
+                          dk: int = DK, dv: int = DV) -> LayerDecodeStep:
+    xq = _v(rng, (B, H, dk), True)
+    xk = _v(rng, (B, H, dk), True)
+    xv = _v(rng, (B, H, dv), True)
+    gate = _v(rng, (B, H, dv), True)
+    g = _g(rng, (B, H, dk))
+    beta = _sigmoid(rng.standard_normal((B, H), dtype=np.float32))
+    return LayerDecodeStep(xq, xk, xv, gate, g, beta)

@@ -17,10 +17,15 @@ Contents
                 rounding on tiny inputs).
   decode_pool   the decode step on a state pool addressed by slot indices,
                 with an fp32 or a bf16-stored state (this file).
+  layer.py      the layer around the recurrence: conv1d + SiLU + per-head L2
+                norm before it, per-head RMSNorm + sigmoid gate after it
+                ("Colibri Kimi K3 Metal backend", sections 8.3 and 8.4), and
+                the whole-layer prefill and decode compositions.
 
 Parity pins: every function here is pinned by the CPU tests in
-``tests/test_oracle_pins.py`` (closed forms, exact retrieval, brute force,
-hand-worked example, the chunked restatement, invariants).
+``tests/test_oracle_pins.py`` and ``tests/test_oracle_layer_pins.py``
+(closed forms, exact retrieval, brute force, hand-worked examples, numpy's
+convolution, the chunked restatement, invariants).
 """
 from __future__ import annotations
 
@@ -81,12 +86,12 @@ def run_unit(q, k, v, g, beta, S0_unit, t0: int, t1: int, h: int,
              out_o: Optional[np.ndarray] = None) -> Tuple[np.ndarray, np.ndarray]:
     """Sequential recurrence for head ``h`` over tokens [t0, t1).
 
-    q, k, v: [T, H, d] arrays, uint16 (bf16 bits) or float32, C-contiguous.
+    q, k, v: [T, H, d] arrays, uint16 (bf16 bits), float32 or float64, C-contiguous.
     g: [T, H, dk] float32; beta: [T, H] float32; S0_unit: [dk, dv] float32 or
     float64 (upcast exactly), or None.  Returns (o [t1-t0, dv] float64, S_final [dk, dv] float64).
     """
     lib = _load()
-    bf16 = q.dtype == np.uint16
+    kind = {np.dtype(np.float32): 0, np.dtype(np.uint16): 1, np.dtype(np.float64): 2}[q.dtype]
     assert k.dtype == q.dtype and v.dtype == q.dtype
     for a in (q, k, v, g, beta):
         assert a.flags["C_CONTIGUOUS"]
@@ -97,7 +102,7 @@ def run_unit(q, k, v, g, beta, S0_unit, t0: int, t1: int, h: int,
     S = np.empty((dk, dv), dtype=np.float64)
     if S0_unit is not None:
         S0_unit = np.ascontiguousarray(S0_unit, dtype=np.float64)   # exact upcast
-    rc = lib.oracle_kda_unit(_ptr(q), _ptr(k), _ptr(v), int(bf16), _ptr(g), _ptr(beta),
+    rc = lib.oracle_kda_unit(_ptr(q), _ptr(k), _ptr(v), kind, _ptr(g), _ptr(beta),
                              _ptr(S0_unit), int(t0), int(t1), int(H), int(h), int(dk), int(dv),
                              _ptr(o), _ptr(S))
     if rc != 0:

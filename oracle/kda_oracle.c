@@ -33,8 +33,11 @@
 #include <stdlib.h>
 #include <string.h>
 
+/* kind: 0 fp32, 1 bf16 bit patterns, 2 double (already exact) */
 static double load_in(const void *p, int is_bf16, int64_t idx)
 {
+    if (is_bf16 == 2)
+        return ((const double *)p)[idx];
     if (is_bf16) {
         uint16_t b = ((const uint16_t *)p)[idx];
         uint32_t bits = ((uint32_t)b) << 16;
@@ -47,7 +50,7 @@ static double load_in(const void *p, int is_bf16, int64_t idx)
 
 /*
  * One (sequence, head) unit over tokens [t0, t1) of a packed [T, H, d] batch.
- *   q, k      : [T, H, dk]   (bf16 bits if qkv_bf16, else fp32)
+ *   q, k      : [T, H, dk]   (qkv_bf16: 0 fp32, 1 bf16 bits, 2 double)
  *   v         : [T, H, dv]
  *   g         : [T, H, dk]   fp32 log-decay
  *   beta      : [T, H]       fp32
