@@ -57,7 +57,8 @@ typedef enum {
     KDA_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
     KDA_ERR_DTYPE = 5,       /* dtype not a kda_dtype_t */
     KDA_ERR_WORKSPACE = 6,   /* the prefill's scratch workspace could not be allocated */
-    KDA_ERR_CUDA = 7         /* the CUDA runtime reported an error at launch */
+    KDA_ERR_CUDA = 7,        /* the CUDA runtime reported an error at launch */
+    KDA_ERR_VALUE = 8        /* a scalar argument is out of range, or buffers alias */
 } kda_status_t;
 
 typedef enum {
@@ -208,6 +209,101 @@ int kda_decode_step_pool(const void *q, const void *k, const void *v,
                          float *o, int B, int H, int dk, int dv, int dtype,
                          void *stream);
 
+/* ---------------------------------------------------------------------------
+ * The layer around the recurrence.  "Colibri Kimi K3 Metal backend",
+ * section 8 introduction: per token the KDA layer runs conv1d + SiLU on its
+ * q, k, v projections, L2-normalises q and k per head, steps the state, then
+ * applies a per-head RMSNorm and a sigmoid of its full-rank gate projection
+ * to o.  Section 8.3 gives the conv (a per-channel window of the last four
+ * raw inputs, shifted left by one per token with the new input in the last
+ * slot, dotted with the channel's four taps, then SiLU(x) = x / (1 + e^-x))
+ * and the L2 norm (n = 1 / sqrt(sum x^2 + eps) over a head's 128 channels,
+ * eps = 1e-6; q is scaled by n * q_scale, the pages' q_scale being
+ * 1/sqrt(128); k by n; v is not normalised).  Section 8.4 gives the gated
+ * norm: out = o / sqrt(mean_j o_j^2 + eps) * norm_w_j * sigmoid(gate_j).
+ *
+ * Conv windows ("conv states") are bf16 [rows, 3, 3, H, 128]: index 1 is the
+ * projection (0 = q, 1 = k, 2 = v), index 2 the window slot, oldest first
+ * (slot 2 = the input just before the next token).  They hold raw bf16
+ * projections, so they are exact.  Conv taps are fp32 [3, H, 128, 4]: tap m
+ * multiplies window slot m, tap 3 the newest input (y_t = sum_m w_m
+ * x_{t-3+m}).
+ * ------------------------------------------------------------------------- */
+
+/*
+ * conv1d + SiLU + L2-norm prologue of a packed varlen prefill: turns the raw
+ * projections into the q, k, v that kda_prefill_chunked takes.
+ *
+ *   xq, xk, xv [T, H, 128] bf16 raw projections
+ *   conv_w     [3, H, 128, 4] fp32 taps
+ *   conv_in    [N, 3, 3, H, 128] bf16 window before each sequence, or NULL
+ *              (zeros: every sequence starts fresh)
+ *   conv_out   [N, 3, 3, H, 128] bf16, written: the window after each
+ *              sequence's last token (conv_in's, or zeros, for an empty
+ *              sequence), to carry into a later call or the decode step; or
+ *              NULL.  Must not be conv_in (KDA_ERR_VALUE).
+ *   q, k, v    [T, H, 128] bf16, written (rounded to nearest even)
+ *   cu_seqlens [N + 1] int32 device array as for kda_prefill_chunked
+ *   d          must be 128; q_scale finite; eps >= 0 (the pages' 1e-6)
+ * Returns KDA_OK or a kda_status_t.
+ */
+int kda_conv_prologue(const void *xq, const void *xk, const void *xv, const float *conv_w,
+                      const void *conv_in, void *conv_out, void *q, void *k, void *v,
+                      const int32_t *cu_seqlens, int N, int64_t T, int H, int d,
+                      float q_scale, float eps, void *stream);
+
+/*
+ * kda_prefill_chunked with the layer's gated RMSNorm applied to o: writes
+ * out = o / sqrt(mean_j o_j^2 + eps) * norm_w_j * sigmoid(gate_j) per
+ * (token, head) instead of o.  On the tensor-core path (bf16, chunk 64) the
+ * norm runs inside the inter-chunk state pass on each chunk of o before it
+ * is stored; other configurations run the CUDA-core prefill into `out`, then
+ * the norm in place.
+ *
+ *   gate     [T, H, 128] bf16 gate projection (before its sigmoid)
+ *   norm_w   [128] fp32 RMSNorm weight, shared by the heads
+ *   eps      >= 0
+ *   out      [T, H, 128] fp32, written
+ *   every other argument as for kda_prefill_chunked (S_out gets the final
+ *   states, unchanged by the norm)
+ * Returns KDA_OK or a kda_status_t.
+ */
+int kda_prefill_chunked_gated(const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, const float *S0, const void *gate,
+                              const float *norm_w, float eps, float *out, float *S_out,
+                              const int32_t *cu_seqlens, int N, int64_t T, int H, int dk, int dv,
+                              int chunk, int dtype, void *stream);
+
+/*
+ * One token of the whole layer for each of B sequences on slot-indexed
+ * pools, in one kernel: conv1d + SiLU + L2 norm of the raw projections (the
+ * window of pool row state_indices[b] is read and shifted in place), the
+ * state step of kda_decode_step_pool (its q, k, v kept in fp32, not rounded
+ * to bf16), and the gated RMSNorm of o.
+ *
+ *   xq, xk, xv    [B, H, 128] bf16 raw projections of the token
+ *   conv_w        [3, H, 128, 4] fp32 taps
+ *   conv_pool     [P, 3, 3, H, 128] bf16 windows, read and updated in place
+ *   g, beta       [B, H, 128] / [B, H] fp32 as for kda_decode_step
+ *   gate          [B, H, 128] bf16; norm_w [128] fp32
+ *   S_pool        [P, H, 128, 128] fp32 (state_dtype KDA_F32) or bf16
+ *                 (KDA_BF16), updated in place
+ *   state_indices [B] int32 device array of pool rows, or NULL (rows 0..B-1;
+ *                 then P >= B).  Negative = padding: out row zero, neither
+ *                 pool touched.  Entries must be distinct; an entry >= P is
+ *                 skipped like padding and sets bit 1 of the device error
+ *                 word.
+ *   out           [B, H, 128] fp32, written
+ *   q_scale       finite; l2_eps, norm_eps >= 0
+ * Returns KDA_OK or a kda_status_t; B = 0 is a no-op.
+ */
+int kda_decode_layer_step(const void *xq, const void *xk, const void *xv, const float *conv_w,
+                          void *conv_pool, const float *g, const float *beta, const void *gate,
+                          const float *norm_w, void *S_pool, int state_dtype,
+                          const int32_t *state_indices, int P, float *out, int B, int H,
+                          int dk, int dv, float q_scale, float l2_eps, float norm_eps,
+                          void *stream);
+
 /*
  * Device-side error word of the library.  Bit 0: the tensor-core prefill
  * kernels never wait without bound: if one of their waits on an asynchronous copy or
@@ -215,7 +311,8 @@ int kda_decode_step_pool(const void *q, const void *k, const void *v,
  * release their tensor memory and exit (the outputs are then invalid).  The
  * state pass also sets it when a sequence's chunk count does not match the
  * workspace it was sized for (cu_seqlens inconsistent with T).  Bit 1: a
- * kda_decode_step_pool slot index was past the end of the pool.
+ * kda_decode_step_pool or kda_decode_layer_step slot index was past the end
+ * of the pool.
  *
  *   code   host pointer, receives the word (0 = no error since the last reset)
  *   reset  nonzero: clear the word after reading it

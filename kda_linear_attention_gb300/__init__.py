@@ -10,6 +10,14 @@ calls raise if the library has not been built.
     o, S_out = prefill_chunked_noalloc(...)      # same, no device allocation
     o = decode_step(q, k, v, g, beta, S)          # S updated in place
 
+The layer around the recurrence (conv1d + SiLU + L2 norm before it, gated
+RMSNorm after it):
+
+    q, k, v, conv_out = conv_prologue(xq, xk, xv, conv_w, cu_seqlens, conv_in=None)
+    out, S_out = prefill_chunked_gated(q, k, v, g, beta, cu_seqlens, gate, norm_w)
+    out, S_out, conv_out = prefill_layer(xq, xk, xv, conv_w, g, beta, gate, norm_w, cu_seqlens)
+    out = decode_layer_step(xq, xk, xv, conv_w, conv_pool, g, beta, gate, norm_w, S_pool)
+
 Shapes (token-major): q, k, g [T, H, 128]; v [T, H, 128]; beta [T, H];
 S [N, H, 128, 128] fp32; q/k/v bf16 or fp32, g/beta fp32.
 """
@@ -22,7 +30,8 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["prefill_chunked", "prefill_chunked_noalloc", "prefill_chunked_events", "decode_step",
-           "decode_step_pool", "device_error", "lib",
+           "decode_step_pool", "conv_prologue", "prefill_chunked_gated", "prefill_layer",
+           "decode_layer_step", "device_error", "lib",
            "KDAError", "KDA_BF16", "KDA_F32", "library_path"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -73,6 +82,16 @@ def lib() -> ctypes.CDLL:
         L.kda_decode_step_pool.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32,
                                            i32, i32, i32, vp]
         L.kda_decode_step_pool.restype = i32
+        f32 = ctypes.c_float
+        L.kda_conv_prologue.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32,
+                                        f32, f32, vp]
+        L.kda_conv_prologue.restype = i32
+        L.kda_prefill_chunked_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp,
+                                                i32, i64, i32, i32, i32, i32, i32, vp]
+        L.kda_prefill_chunked_gated.restype = i32
+        L.kda_decode_layer_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32,
+                                            vp, i32, i32, i32, i32, f32, f32, f32, vp]
+        L.kda_decode_layer_step.restype = i32
         L.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         L.kda_device_error.restype = i32
         _lib = L
@@ -109,7 +128,8 @@ def _stream(device: torch.device, stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _prefill(fn_name: str, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_out, stream, extra=()):
+def _prefill(fn_name: str, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_out, stream, extra=(),
+             gated=None):
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("inputs must be CUDA tensors")
@@ -130,9 +150,15 @@ def _prefill(fn_name: str, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_out, st
         S_out = torch.empty((N, H, DK, DV), dtype=torch.float32, device=dev)
     _check("o", o, torch.float32, (T, H, DV), dev)
     _check("S_out", S_out, torch.float32, (N, H, DK, DV), dev)
-    rc = getattr(lib(), fn_name)(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(o), _p(S_out),
-                                 _p(cu_seqlens), N, T, H, DK, DV, int(chunk), dt,
-                                 _stream(dev, stream), *extra)
+    if gated is not None:
+        gate, norm_w, eps = gated
+        rc = getattr(lib(), fn_name)(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(gate),
+                                     _p(norm_w), float(eps), _p(o), _p(S_out), _p(cu_seqlens), N,
+                                     T, H, DK, DV, int(chunk), dt, _stream(dev, stream))
+    else:
+        rc = getattr(lib(), fn_name)(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(o),
+                                     _p(S_out), _p(cu_seqlens), N, T, H, DK, DV, int(chunk), dt,
+                                     _stream(dev, stream), *extra)
     if rc != 0:
         raise KDAError(rc, fn_name)
     return o, S_out
@@ -253,6 +279,127 @@ def decode_step_pool(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch
     if rc != 0:
         raise KDAError(rc, "kda_decode_step_pool")
     return o
+
+
+# ------------------------------------------------------------ the layer
+CONV_K = 4
+Q_SCALE = DK ** -0.5          # the pages' q scale, 1/sqrt(head width)
+L2_EPS = 1e-6
+NORM_EPS = 1e-6
+
+
+def conv_prologue(xq: torch.Tensor, xk: torch.Tensor, xv: torch.Tensor, conv_w: torch.Tensor,
+                  cu_seqlens: torch.Tensor, conv_in: Optional[torch.Tensor] = None,
+                  conv_out: Optional[torch.Tensor] = None, q_scale: float = Q_SCALE,
+                  eps: float = L2_EPS, q=None, k=None, v=None,
+                  stream: Optional[torch.cuda.Stream] = None):
+    """conv1d + SiLU + L2 norm of the raw projections (``kda_conv_prologue``).
+
+    xq, xk, xv [T, H, 128] bf16; conv_w [3, H, 128, 4] fp32; conv_in / conv_out
+    [N, 3, 3, H, 128] bf16 windows (conv_in None = zeros; conv_out allocated
+    if None).  Returns (q, k, v [T, H, 128] bf16, conv_out).
+    """
+    dev = xq.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    T, H = xq.shape[0], xq.shape[1]
+    N = cu_seqlens.numel() - 1
+    bf = torch.bfloat16
+    for n, t in (("xq", xq), ("xk", xk), ("xv", xv)):
+        _check(n, t, bf, (T, H, DK), dev)
+    _check("conv_w", conv_w, torch.float32, (3, H, DK, CONV_K), dev)
+    _check("cu_seqlens", cu_seqlens, torch.int32, (N + 1,), dev)
+    wshape = (N, 3, CONV_K - 1, H, DK)
+    if conv_in is not None:
+        _check("conv_in", conv_in, bf, wshape, dev)
+    if conv_out is None:
+        conv_out = torch.empty(wshape, dtype=bf, device=dev)
+    _check("conv_out", conv_out, bf, wshape, dev)
+    q = torch.empty((T, H, DK), dtype=bf, device=dev) if q is None else q
+    k = torch.empty((T, H, DK), dtype=bf, device=dev) if k is None else k
+    v = torch.empty((T, H, DV), dtype=bf, device=dev) if v is None else v
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check(n, t, bf, (T, H, DK), dev)
+    rc = lib().kda_conv_prologue(_p(xq), _p(xk), _p(xv), _p(conv_w), _p(conv_in), _p(conv_out),
+                                 _p(q), _p(k), _p(v), _p(cu_seqlens), N, T, H, DK,
+                                 float(q_scale), float(eps), _stream(dev, stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_conv_prologue")
+    return q, k, v, conv_out
+
+
+def prefill_chunked_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                          beta: torch.Tensor, cu_seqlens: torch.Tensor, gate: torch.Tensor,
+                          norm_w: torch.Tensor, S0: Optional[torch.Tensor] = None,
+                          chunk: int = 64, eps: float = NORM_EPS,
+                          out: Optional[torch.Tensor] = None, S_out: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None
+                          ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Chunked prefill whose output is RMSNorm(o) * norm_w * sigmoid(gate)
+    (``kda_prefill_chunked_gated``).  gate [T, H, 128] bf16, norm_w [128] fp32.
+    Returns (out [T, H, 128] fp32, S_out)."""
+    dev = q.device
+    T, H = q.shape[0], q.shape[1]
+    _check("gate", gate, torch.bfloat16, (T, H, DV), dev)
+    _check("norm_w", norm_w, torch.float32, (DV,), dev)
+    return _prefill("kda_prefill_chunked_gated", q, k, v, g, beta, cu_seqlens, S0, chunk, out,
+                    S_out, stream, gated=(gate, norm_w, eps))
+
+
+def prefill_layer(xq, xk, xv, conv_w, g, beta, gate, norm_w, cu_seqlens,
+                  conv_in: Optional[torch.Tensor] = None, S0: Optional[torch.Tensor] = None,
+                  q_scale: float = Q_SCALE, l2_eps: float = L2_EPS, norm_eps: float = NORM_EPS,
+                  stream: Optional[torch.cuda.Stream] = None):
+    """The layer's prefill from raw projections: ``conv_prologue`` (q, k, v
+    in bf16) then ``prefill_chunked_gated``, on one stream.  Returns
+    (out [T, H, 128] fp32, S_out [N, H, 128, 128] fp32, conv_out)."""
+    q, k, v, conv_out = conv_prologue(xq, xk, xv, conv_w, cu_seqlens, conv_in=conv_in,
+                                      q_scale=q_scale, eps=l2_eps, stream=stream)
+    out, S_out = prefill_chunked_gated(q, k, v, g, beta, cu_seqlens, gate, norm_w, S0=S0,
+                                       eps=norm_eps, stream=stream)
+    return out, S_out, conv_out
+
+
+def decode_layer_step(xq: torch.Tensor, xk: torch.Tensor, xv: torch.Tensor, conv_w: torch.Tensor,
+                      conv_pool: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                      gate: torch.Tensor, norm_w: torch.Tensor, S_pool: torch.Tensor,
+                      state_indices: Optional[torch.Tensor] = None, q_scale: float = Q_SCALE,
+                      l2_eps: float = L2_EPS, norm_eps: float = NORM_EPS,
+                      out: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """One token of the whole layer per sequence (``kda_decode_layer_step``):
+    conv windows (conv_pool [P, 3, 3, H, 128] bf16) and states (S_pool
+    [P, H, 128, 128] fp32 or bf16) updated in place at rows state_indices.
+    Returns out [B, H, 128] fp32."""
+    dev = xq.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, H = xq.shape[0], xq.shape[1]
+    bf = torch.bfloat16
+    for n, t in (("xq", xq), ("xk", xk), ("xv", xv), ("gate", gate)):
+        _check(n, t, bf, (B, H, DK), dev)
+    _check("conv_w", conv_w, torch.float32, (3, H, DK, CONV_K), dev)
+    _check("g", g, torch.float32, (B, H, DK), dev)
+    _check("beta", beta, torch.float32, (B, H), dev)
+    _check("norm_w", norm_w, torch.float32, (DV,), dev)
+    if S_pool.dtype not in (torch.float32, bf):
+        raise TypeError("S_pool must be float32 or bfloat16")
+    P = S_pool.shape[0]
+    _check("S_pool", S_pool, S_pool.dtype, (P, H, DK, DV), dev)
+    _check("conv_pool", conv_pool, bf, (P, 3, CONV_K - 1, H, DK), dev)
+    if state_indices is not None:
+        _check("state_indices", state_indices, torch.int32, (B,), dev)
+    if out is None:
+        out = torch.empty((B, H, DV), dtype=torch.float32, device=dev)
+    _check("out", out, torch.float32, (B, H, DV), dev)
+    sdt = KDA_BF16 if S_pool.dtype == bf else KDA_F32
+    rc = lib().kda_decode_layer_step(_p(xq), _p(xk), _p(xv), _p(conv_w), _p(conv_pool), _p(g),
+                                     _p(beta), _p(gate), _p(norm_w), _p(S_pool), sdt,
+                                     _p(state_indices), P, _p(out), B, H, DK, DV, float(q_scale),
+                                     float(l2_eps), float(norm_eps), _stream(dev, stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_decode_layer_step")
+    return out
 
 
 def device_error(reset: bool = True) -> int:

@@ -57,6 +57,35 @@ cudaError_t launch_prefill_split_noalloc(const void *q, const void *k, const voi
 // tensor-core kernels set when a bounded wait gives up.
 cudaError_t read_device_error(unsigned int *code, bool reset);
 
+// The tensor-core prefill with the layer's gated RMSNorm fused into the state
+// pass's output: out = RMSNorm(o) * norm_w * sigmoid(gate) instead of o
+// (gate [T, H, 128] bf16, norm_w [128] fp32).
+cudaError_t launch_prefill_split_gated(const void *q, const void *k, const void *v,
+                                       const float *g, const float *beta, const float *S0,
+                                       const void *gate, const float *norm_w, float eps,
+                                       float *out, float *S_out, const int32_t *cu_seqlens, int N,
+                                       int64_t T, int H, cudaStream_t stream,
+                                       cudaEvent_t const *events = nullptr);
+
+// The layer around the recurrence (kda_layer.cu).
+// conv1d + SiLU on xq/xk/xv, L2 norm of q (times q_scale) and k; windows in
+// and out [N, 3, 3, H, 128] bf16 (conv_in may be null: zeros; conv_out may
+// be null: not written).
+cudaError_t launch_conv_prologue(const void *xq, const void *xk, const void *xv, const float *conv_w,
+                                 const void *conv_in, void *conv_out, void *q, void *k, void *v,
+                                 const int32_t *cu_seqlens, int N, int64_t T, int H, float q_scale,
+                                 float eps, cudaStream_t stream);
+// In place over `rows` rows of 128: o <- RMSNorm(o) * norm_w * sigmoid(gate).
+cudaError_t launch_gated_norm(float *o, const void *gate, const float *norm_w, float eps,
+                              long long rows, cudaStream_t stream);
+// Whole-layer decode step on slot-indexed pools (state fp32 or bf16, windows bf16).
+cudaError_t launch_decode_layer(const void *xq, const void *xk, const void *xv, const float *conv_w,
+                                void *conv_pool, const float *g, const float *beta, const void *gate,
+                                const float *norm_w, void *S_pool, bool state_bf16,
+                                const int32_t *slots, int P, float *out, int B, int H,
+                                float q_scale, float l2_eps, float norm_eps, cudaStream_t stream);
+cudaError_t read_layer_error(unsigned int *code, bool reset);
+
 // Input loads: bf16 or fp32 element -> fp32.
 __device__ __forceinline__ float load_in(const __nv_bfloat16 *p, size_t i) {
     return __bfloat162float(p[i]);

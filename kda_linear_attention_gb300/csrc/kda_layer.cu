@@ -1,0 +1,450 @@
+// The KDA layer around the recurrence: the conv1d + SiLU + per-head L2-norm
+// prologue, the per-head RMSNorm + sigmoid-gate epilogue, and the whole
+// layer's decode step fused into one kernel.
+//
+// "Colibri Kimi K3 Metal backend", section 8 and its subsections: per token,
+// conv1d of width 4 + SiLU on the q, k and v projections (8.3: each channel
+// keeps a window of its last four raw inputs, the newest in the last slot;
+// SiLU(x) = x / (1 + exp(-x))), per-head L2 normalisation of q (times
+// 1/sqrt(head width)) and k with eps 1e-6 (8.3), the state step, then per-head
+// RMSNorm of o and a sigmoid of the full-rank gate projection (8.4).
+//
+// Conv windows are stored as [rows, 3 (q, k, v), 3 (oldest first), H, 128]
+// bf16: the raw projections are bf16, so a window holds them exactly.
+#include "kda_internal.h"
+
+namespace kda {
+
+// Set (bit 1) when a decode-layer slot index lies past the end of the pool.
+__device__ unsigned int g_kda_layer_error = 0;
+
+namespace {
+
+constexpr int kConvK = 4;
+constexpr int kWin = kConvK - 1;
+
+__device__ __forceinline__ float silu(float y) { return y / (1.f + __expf(-y)); }
+__device__ __forceinline__ float sigmoid(float y) { return 1.f / (1.f + __expf(-y)); }
+
+__device__ __forceinline__ void unpack8(uint4 u, float (&x)[8]) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+    }
+}
+__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        w[e] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ============================================================================
+// Prefill prologue.  A half-warp owns one (run of kRun tokens, projection p,
+// head h); lane l holds channels 8l..8l+7 and walks the run token by token
+// with the channel's window in registers, so every raw input is read once
+// (plus a three-token halo per run).  The L2 norm of a (token, head) row is a
+// reduction over the half-warp.
+// ============================================================================
+constexpr int kRun = 64;
+constexpr int kPrologueThreads = 256;
+
+__device__ __forceinline__ int seq_of(const int32_t *cu, int N, int t) {
+    // largest n with cu[n] <= t (t < cu[N]: a non-empty sequence holding t)
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cu[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kPrologueThreads)
+conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *__restrict__ xk,
+                     const __nv_bfloat16 *__restrict__ xv, const float *__restrict__ conv_w,
+                     const __nv_bfloat16 *__restrict__ conv_in, __nv_bfloat16 *__restrict__ conv_out,
+                     __nv_bfloat16 *__restrict__ q, __nv_bfloat16 *__restrict__ k,
+                     __nv_bfloat16 *__restrict__ v, const int32_t *__restrict__ cu, int N, int T,
+                     int H, float q_scale, float eps, long long nruns) {
+    const size_t win_row = (size_t)H * 128;               // one window slot of one projection
+    // empty sequences pass their window through unchanged
+    if (conv_out) {
+        const long long per_seq = (long long)3 * kWin * H * 16;   // 16-byte pieces
+        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < (long long)N * per_seq;
+             i += (long long)gridDim.x * blockDim.x) {
+            const int n = (int)(i / per_seq);
+            if (cu[n + 1] != cu[n]) continue;
+            const size_t off = (size_t)n * 3 * kWin * win_row + (size_t)(i % per_seq) * 8;
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (conv_in) w = *reinterpret_cast<const uint4 *>(conv_in + off);
+            *reinterpret_cast<uint4 *>(conv_out + off) = w;
+        }
+    }
+
+    const int lane16 = threadIdx.x & 15;
+    const long long hw = (long long)blockIdx.x * (kPrologueThreads / 16) + (threadIdx.x >> 4);
+    const bool active = hw < nruns;
+    const long long hwc = active ? hw : 0;
+    const int h = (int)(hwc % H);
+    const int p = (int)((hwc / H) % 3);
+    const int j = (int)(hwc / (3LL * H));
+    const int c0 = 8 * lane16;
+    const __nv_bfloat16 *x = p == 0 ? xq : (p == 1 ? xk : xv);
+    __nv_bfloat16 *y_out = p == 0 ? q : (p == 1 ? k : v);
+    const float scale = p == 0 ? q_scale : 1.f;
+
+    // taps of the 8 channels: w[c][m], tap 3 on the newest input
+    float w[8][4];
+    {
+        const float4 *wp = reinterpret_cast<const float4 *>(conv_w + (((size_t)p * H + h) * 128 + c0) * kConvK);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float4 t4 = wp[c];
+            w[c][0] = t4.x; w[c][1] = t4.y; w[c][2] = t4.z; w[c][3] = t4.w;
+        }
+    }
+    const int t0 = active ? j * kRun : T;
+    const int t_end = min(t0 + kRun, T);
+    auto row = [&](int t) -> size_t { return ((size_t)t * H + h) * 128 + c0; };
+    auto win_at = [&](int n, int slot) -> size_t {
+        return (((size_t)n * 3 + p) * kWin + slot) * win_row + (size_t)h * 128 + c0;
+    };
+
+    float win[kWin][8];
+    int n = 0, start = 0, end = 0;
+    // window of token t in sequence n: the three inputs before t, from the
+    // sequence itself or (before its start) from its carried window
+    auto load_window = [&](int tt) {
+#pragma unroll
+        for (int m = 0; m < kWin; ++m) {
+            const int tau = tt - kWin + m;
+            uint4 u = make_uint4(0, 0, 0, 0);
+            if (tau >= start) u = *reinterpret_cast<const uint4 *>(x + row(tau));
+            else if (conv_in) u = *reinterpret_cast<const uint4 *>(conv_in + win_at(n, kWin + (tau - start)));
+            unpack8(u, win[m]);
+        }
+    };
+    if (t0 < t_end) {
+        n = seq_of(cu, N, t0);
+        start = cu[n];
+        end = cu[n + 1];
+        load_window(t0);
+    } else {
+#pragma unroll
+        for (int m = 0; m < kWin; ++m)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) win[m][c] = 0.f;
+    }
+
+    for (int i = 0; i < kRun; i += 4) {
+        uint4 xr[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int t = t0 + i + u;
+            xr[u] = t < t_end ? *reinterpret_cast<const uint4 *>(x + row(t)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int t = t0 + i + u;
+            const bool valid = t < t_end;
+            if (valid && t >= end && n < N - 1) {   // the run enters the next non-empty sequence
+                do {
+                    ++n;
+                } while (n < N - 1 && cu[n + 1] <= t);
+                start = cu[n];
+                end = cu[n + 1];
+                load_window(t);
+            }
+            float xn[8], z[8];
+            unpack8(xr[u], xn);
+            float ss = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float y = w[c][0] * win[0][c] + w[c][1] * win[1][c] + w[c][2] * win[2][c] +
+                                w[c][3] * xn[c];
+                z[c] = silu(y);
+                ss = fmaf(z[c], z[c], ss);
+            }
+            // every lane of the warp takes part in the reduction
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, 16);
+            const float f = p == 2 ? 1.f : scale * rsqrtf(ss + eps);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) z[c] *= f;
+            if (valid) *reinterpret_cast<uint4 *>(y_out + row(t)) = pack8(z);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                win[0][c] = win[1][c];
+                win[1][c] = win[2][c];
+                win[2][c] = xn[c];
+            }
+            if (valid && t == end - 1 && conv_out) {   // the sequence's last token: its window out
+#pragma unroll
+                for (int m = 0; m < kWin; ++m)
+                    *reinterpret_cast<uint4 *>(conv_out + win_at(n, m)) = pack8(win[m]);
+            }
+        }
+    }
+}
+
+// ============================================================================
+// Gated RMSNorm in place over [rows, 128] fp32 (one warp per row): the
+// epilogue for the prefill configurations that run on CUDA cores.
+// ============================================================================
+__global__ void __launch_bounds__(256)
+gated_norm_kernel(float *__restrict__ o, const __nv_bfloat16 *__restrict__ gate,
+                  const float *__restrict__ norm_w, float eps, long long rows) {
+    const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    const int l = threadIdx.x & 31;
+    float4 x = *reinterpret_cast<const float4 *>(o + r * 128 + 4 * l);
+    float ss = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float rs = rsqrtf(ss * (1.f / 128.f) + eps);
+    const uint2 gu = *reinterpret_cast<const uint2 *>(gate + r * 128 + 4 * l);
+    const float2 ga = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.x));
+    const float2 gb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.y));
+    const float4 wv = *reinterpret_cast<const float4 *>(norm_w + 4 * l);
+    x.x *= rs * wv.x * sigmoid(ga.x);
+    x.y *= rs * wv.y * sigmoid(ga.y);
+    x.z *= rs * wv.z * sigmoid(gb.x);
+    x.w *= rs * wv.w * sigmoid(gb.y);
+    *reinterpret_cast<float4 *>(o + r * 128 + 4 * l) = x;
+}
+
+// ============================================================================
+// Whole-layer decode step: one block per (b, h).  The conv + SiLU + L2-norm
+// prologue runs while the state loads are in flight; then the fused token
+// step of kda_decode.cu over all 128 columns (thread t: column group t % 32,
+// rows t / 32 + 8 r), then the gated RMSNorm of o in warp 0.
+// ============================================================================
+constexpr int kLayerThreads = 256;
+
+__device__ __forceinline__ float4 ld_state4(const float *p) {
+    return __ldcs(reinterpret_cast<const float4 *>(p));
+}
+__device__ __forceinline__ float4 ld_state4(const __nv_bfloat16 *p) {
+    const uint2 u = __ldcs(reinterpret_cast<const uint2 *>(p));
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void st_state4(float *p, float4 x) {
+    __stcs(reinterpret_cast<float4 *>(p), x);
+}
+__device__ __forceinline__ void st_state4(__nv_bfloat16 *p, float4 x) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(x.z, x.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t *>(&a);
+    u.y = *reinterpret_cast<const uint32_t *>(&b);
+    __stcs(reinterpret_cast<uint2 *>(p), u);
+}
+
+template <typename TS>
+__global__ void __launch_bounds__(kLayerThreads, 2)
+decode_layer_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *__restrict__ xk,
+                    const __nv_bfloat16 *__restrict__ xv, const float *__restrict__ conv_w,
+                    __nv_bfloat16 *__restrict__ conv_pool, const float *__restrict__ g,
+                    const float *__restrict__ beta, const __nv_bfloat16 *__restrict__ gate,
+                    const float *__restrict__ norm_w, TS *__restrict__ S,
+                    const int32_t *__restrict__ slots, float *__restrict__ out, int H, int P,
+                    float q_scale, float l2_eps, float norm_eps) {
+    constexpr int C4 = 32;                      // float4 column groups
+    constexpr int NRG = kLayerThreads / C4;     // 8 row groups
+    constexpr int RPT = kDK / NRG;              // 16 rows per thread
+    const int unit = blockIdx.x;                // b * H + h
+    const int b = unit / H, h = unit % H;
+    const int t = threadIdx.x;
+    const int c4 = t % C4, rg = t / C4;
+    const int col0 = 4 * c4;
+
+    int slot = b;
+    if (slots) {
+        slot = slots[b];
+        if (slot < 0 || slot >= P) {            // padding row (or an invalid slot)
+            if (slot >= P && t == 0) atomicOr(&g_kda_layer_error, 2u);
+            if (rg == 0)
+                *reinterpret_cast<float4 *>(out + (size_t)unit * kDV + col0) = make_float4(0.f, 0.f, 0.f, 0.f);
+            return;
+        }
+    }
+    TS *Su = S + ((size_t)slot * H + h) * kDK * kDV;
+    float4 s[RPT];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) s[r] = ld_state4(Su + (size_t)(rg + r * NRG) * kDV + col0);
+
+    __shared__ float sq[kDK], sk[kDK], sv[kDV], sa[kDK];
+    __shared__ float s_red[2][4];
+    __shared__ float4 red_k[NRG][C4];
+    __shared__ float4 red_q[NRG][C4];
+
+    // ---- prologue: q (threads 0..127) and k (128..255), then v (0..127)
+    const size_t win_row = (size_t)H * 128;
+    auto conv_step = [&](int p, int c, const __nv_bfloat16 *x) -> float {
+        const float xn = __bfloat162float(x[(size_t)unit * 128 + c]);
+        __nv_bfloat16 *wp = conv_pool + ((size_t)slot * 3 + p) * kWin * win_row + (size_t)h * 128 + c;
+        const float w0 = __bfloat162float(wp[0]);
+        const float w1 = __bfloat162float(wp[win_row]);
+        const float w2 = __bfloat162float(wp[2 * win_row]);
+        const float4 tp = *reinterpret_cast<const float4 *>(conv_w + (((size_t)p * H + h) * 128 + c) * kConvK);
+        const float y = tp.x * w0 + tp.y * w1 + tp.z * w2 + tp.w * xn;
+        // shift the window by one (exact: raw bf16 inputs)
+        wp[0] = __float2bfloat16_rn(w1);
+        wp[win_row] = __float2bfloat16_rn(w2);
+        wp[2 * win_row] = x[(size_t)unit * 128 + c];
+        return silu(y);
+    };
+    {
+        const int p = t >> 7, c = t & 127;
+        const float z = conv_step(p, c, p == 0 ? xq : xk);
+        float ss = z * z;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if ((t & 31) == 0) s_red[p][(t >> 5) & 3] = ss;
+        if (t < 128) {
+            sv[t] = conv_step(2, t, xv);
+            sa[t] = expf(g[(size_t)unit * kDK + t]);
+        }
+        __syncthreads();
+        const float tot = s_red[p][0] + s_red[p][1] + s_red[p][2] + s_red[p][3];
+        const float f = (p == 0 ? q_scale : 1.f) * rsqrtf(tot + l2_eps);
+        if (p == 0) sq[c] = z * f;
+        else sk[c] = z * f;
+    }
+    __syncthreads();
+    float qk = 0.f;
+    {
+        // q . k over the 128 channels (every warp computes it)
+        const int l = t & 31;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qk = fmaf(sq[l + 32 * e], sk[l + 32 * e], qk);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) qk += __shfl_xor_sync(0xffffffffu, qk, off);
+    }
+
+    // ---- the token step over this thread's rows
+    float4 uk = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 uq = uk;
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        const int i = rg + r * NRG;
+        const float a = sa[i], ki = sk[i], qi = sq[i];
+        s[r].x *= a; s[r].y *= a; s[r].z *= a; s[r].w *= a;
+        uk.x += ki * s[r].x; uk.y += ki * s[r].y; uk.z += ki * s[r].z; uk.w += ki * s[r].w;
+        uq.x += qi * s[r].x; uq.y += qi * s[r].y; uq.z += qi * s[r].z; uq.w += qi * s[r].w;
+    }
+    red_k[rg][c4] = uk;
+    red_q[rg][c4] = uq;
+    __syncthreads();
+    float4 Uk = red_k[0][c4], Uq = red_q[0][c4];
+#pragma unroll
+    for (int jj = 1; jj < NRG; ++jj) {
+        const float4 a = red_k[jj][c4], bq = red_q[jj][c4];
+        Uk.x += a.x; Uk.y += a.y; Uk.z += a.z; Uk.w += a.w;
+        Uq.x += bq.x; Uq.y += bq.y; Uq.z += bq.z; Uq.w += bq.w;
+    }
+    const float bt = beta[unit];
+    float4 w;
+    w.x = bt * (sv[col0 + 0] - Uk.x);
+    w.y = bt * (sv[col0 + 1] - Uk.y);
+    w.z = bt * (sv[col0 + 2] - Uk.z);
+    w.w = bt * (sv[col0 + 3] - Uk.w);
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        const int i = rg + r * NRG;
+        const float ki = sk[i];
+        s[r].x += ki * w.x; s[r].y += ki * w.y; s[r].z += ki * w.z; s[r].w += ki * w.w;
+        st_state4(Su + (size_t)i * kDV + col0, s[r]);
+    }
+
+    // ---- epilogue: o of the 128 columns sits in warp 0 (4 per lane)
+    if (rg == 0) {
+        float4 ov;
+        ov.x = Uq.x + qk * w.x; ov.y = Uq.y + qk * w.y;
+        ov.z = Uq.z + qk * w.z; ov.w = Uq.w + qk * w.w;
+        float ss = ov.x * ov.x + ov.y * ov.y + ov.z * ov.z + ov.w * ov.w;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float rs = rsqrtf(ss * (1.f / 128.f) + norm_eps);
+        const uint2 gu = *reinterpret_cast<const uint2 *>(gate + (size_t)unit * kDV + col0);
+        const float2 ga = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.x));
+        const float2 gb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.y));
+        const float4 wv = *reinterpret_cast<const float4 *>(norm_w + col0);
+        ov.x *= rs * wv.x * sigmoid(ga.x);
+        ov.y *= rs * wv.y * sigmoid(ga.y);
+        ov.z *= rs * wv.z * sigmoid(gb.x);
+        ov.w *= rs * wv.w * sigmoid(gb.y);
+        *reinterpret_cast<float4 *>(out + (size_t)unit * kDV + col0) = ov;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_conv_prologue(const void *xq, const void *xk, const void *xv, const float *conv_w,
+                                 const void *conv_in, void *conv_out, void *q, void *k, void *v,
+                                 const int32_t *cu_seqlens, int N, int64_t T, int H, float q_scale,
+                                 float eps, cudaStream_t stream) {
+    const long long nruns = ((T + kRun - 1) / kRun) * 3LL * H;
+    long long blocks = (nruns + kPrologueThreads / 16 - 1) / (kPrologueThreads / 16);
+    if (blocks < 1) blocks = 1;                    // empty sequences still pass their windows on
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    conv_prologue_kernel<<<(unsigned)blocks, kPrologueThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(xq), static_cast<const __nv_bfloat16 *>(xk),
+        static_cast<const __nv_bfloat16 *>(xv), conv_w, static_cast<const __nv_bfloat16 *>(conv_in),
+        static_cast<__nv_bfloat16 *>(conv_out), static_cast<__nv_bfloat16 *>(q),
+        static_cast<__nv_bfloat16 *>(k), static_cast<__nv_bfloat16 *>(v), cu_seqlens, N, (int)T, H,
+        q_scale, eps, nruns);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gated_norm(float *o, const void *gate, const float *norm_w, float eps,
+                              long long rows, cudaStream_t stream) {
+    if (rows <= 0) return cudaSuccess;
+    const long long blocks = (rows + 7) / 8;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    gated_norm_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        o, static_cast<const __nv_bfloat16 *>(gate), norm_w, eps, rows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_layer(const void *xq, const void *xk, const void *xv, const float *conv_w,
+                                void *conv_pool, const float *g, const float *beta, const void *gate,
+                                const float *norm_w, void *S_pool, bool state_bf16,
+                                const int32_t *slots, int P, float *out, int B, int H,
+                                float q_scale, float l2_eps, float norm_eps, cudaStream_t stream) {
+    const long long units = (long long)B * H;
+    if (units <= 0) return cudaSuccess;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+    auto bq = static_cast<const __nv_bfloat16 *>(xq);
+    auto bk = static_cast<const __nv_bfloat16 *>(xk);
+    auto bv = static_cast<const __nv_bfloat16 *>(xv);
+    auto cp = static_cast<__nv_bfloat16 *>(conv_pool);
+    auto gt = static_cast<const __nv_bfloat16 *>(gate);
+    if (state_bf16)
+        decode_layer_kernel<__nv_bfloat16><<<(unsigned)units, kLayerThreads, 0, stream>>>(
+            bq, bk, bv, conv_w, cp, g, beta, gt, norm_w, static_cast<__nv_bfloat16 *>(S_pool), slots,
+            out, H, P, q_scale, l2_eps, norm_eps);
+    else
+        decode_layer_kernel<float><<<(unsigned)units, kLayerThreads, 0, stream>>>(
+            bq, bk, bv, conv_w, cp, g, beta, gt, norm_w, static_cast<float *>(S_pool), slots, out, H,
+            P, q_scale, l2_eps, norm_eps);
+    return cudaGetLastError();
+}
+
+cudaError_t read_layer_error(unsigned int *code, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_kda_layer_error, sizeof(unsigned int));
+    if (e != cudaSuccess || !reset) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_kda_layer_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace kda

@@ -750,8 +750,9 @@ constexpr uint32_t SB_VEC = 90112;        // 2 x 1 KB record vectors (double-buf
 constexpr uint32_t SB_V = 92160;          // 16 KB: v chunk sw (TMA) = V^T, MN-major operand
 constexpr uint32_t SB_S = 108544;         // 32 KB: S^T bf16 K-major il [j][i]
 constexpr uint32_t SB_O = 141312;         // 32 KB: o chunk, 4 x [64 r][32 j] fp32 (TMA store source)
-constexpr uint32_t SB_MISC = 174080;      // 3 x u64 mbarriers, TMEM base
-constexpr uint32_t SMEM_B_USED = SB_MISC + 64;
+constexpr uint32_t SB_GATE = 174080;      // 16 KB: gate chunk sw (TMA; gated variant only)
+constexpr uint32_t SB_MISC = 190464;      // 3 x u64 mbarriers, TMEM base; norm weight at +64
+constexpr uint32_t SMEM_B_USED = SB_MISC + 64 + 512;
 constexpr uint32_t SMEM_B_ALLOC = SMEM_B_USED + 1024;
 static_assert(SB_T == R_T && SB_A == R_A && SB_KB == R_KB, "record pieces map onto shared memory");
 static_assert(SMEM_B_ALLOC <= 232448, "dynamic shared memory limit (227 KB)");
@@ -761,18 +762,27 @@ constexpr uint32_t TMB_O = 192;           // O^T, 64 columns (N = 128 with TMB_U
 constexpr uint32_t COPY1 = R_A - R_WQ;    // bytes of [-W ; Q0] + T'
 constexpr uint32_t COPY2 = R_VEC - R_A;   // bytes of A' + Kbar^T
 
+__device__ __forceinline__ float gate_sigmoid(float x) { return 1.f / (1.f + __expf(-x)); }
+
+// GATED: the layer's output epilogue ("Colibri Kimi K3 Metal backend",
+// section 8.4) on every row of o before it is stored: o / sqrt(mean_j o_j^2
+// + eps) * norm_w_j * sigmoid(gate_j), the gate chunk arriving by TMA beside v.
+template <bool GATED>
 __global__ void __launch_bounds__(NTB, 1)
 state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
                   const float *__restrict__ S0,
                   float *__restrict__ o, float *__restrict__ S_out, const int32_t *__restrict__ cu,
                   const int32_t *__restrict__ chunk_off, int N, int H, int max_chunks,
-                  const uint8_t *__restrict__ recs) {
+                  const uint8_t *__restrict__ recs, const __grid_constant__ CUtensorMap map_gate,
+                  const float *__restrict__ norm_w, float norm_eps) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bar_a = reinterpret_cast<uint64_t *>(sm + SB_MISC);
     uint64_t *bar_b = bar_a + 1;
     uint64_t *bar_mma = bar_a + 2;
+    uint64_t *bar_gate = bar_a + 3;           // gated variant: the gate chunk
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SB_MISC + 32);
+    float *s_normw = reinterpret_cast<float *>(sm + SB_MISC + 64);
     __shared__ int s_seq;
 
     const int t = threadIdx.x;
@@ -800,10 +810,13 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         mbar_init(bar_a, 1);
         mbar_init(bar_b, 1);
         mbar_init(bar_mma, 1);
+        mbar_init(bar_gate, 1);
         fence_mbar_init();
         prefetch_tmap(&map_v);
         prefetch_tmap(&map_o);
+        if (GATED) prefetch_tmap(&map_gate);
     }
+    if (GATED && t < kDV) s_normw[t] = norm_w[t];
     sync_tc();
     const uint32_t tmem = *s_tmem;
 
@@ -846,6 +859,13 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         tma_load_3d(sm + SB_V, &map_v, bar_a, 0, h, tok0 + j * C);
         tma_load_3d(sm + SB_V + 8192, &map_v, bar_a, 64, h, tok0 + j * C);
     };
+    // the gate chunk has a barrier of its own: it is read in the epilogue,
+    // after the next chunk's round-1 operands have been requested
+    auto issue_gate = [&](int j) {
+        mbar_arrive_expect_tx(bar_gate, 16384);
+        tma_load_3d(sm + SB_GATE, &map_gate, bar_gate, 0, h, tok0 + j * C);
+        tma_load_3d(sm + SB_GATE + 8192, &map_gate, bar_gate, 64, h, tok0 + j * C);
+    };
     auto issue_b = [&](int j) {
         mbar_arrive_expect_tx(bar_b, COPY2);
         bulk_load(sm + SB_A, rec_at(j) + R_A, COPY2, bar_b);
@@ -853,8 +873,10 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
     if (t == 0 && nch > 0) {
         issue_a(0);
         issue_b(0);
+        if (GATED) issue_gate(0);
     }
     int issued_a = nch > 0, issued_b = nch > 0, issued_mma = 0;
+    int issued_gate = (GATED && nch > 0) ? 1 : 0;
     uint32_t mma_phase = 0;
 
     for (int j = 0; j < nch && !failed; ++j) {
@@ -954,7 +976,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             float ov[16];
             tmem_ld16(tmem + lane_base + TMB_O + 16 * qt, ov);
             tmem_wait_ld();
-            if (Lc == C) {
+            if (GATED || Lc == C) {
                 if (t == 0) bulk_wait_read();    // the previous chunk's stores have read SB_O
                 __syncthreads();
                 float *so = reinterpret_cast<float *>(sm + SB_O + 8192 * (ch >> 5)) + (ch & 31);
@@ -985,12 +1007,51 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                 }
             }
         }
+        if (GATED) {
+            // per row: RMSNorm over the 128 columns, weight, sigmoid gate.
+            // Thread: row rr, columns 32 m + 4 p8 .. +3 of the four boxes m.
+            if (!wait_all(bar_gate, par)) { failed = true; break; }
+            const int rr = t >> 3, p8 = t & 7;
+            float4 x[4];
+            float ss = 0.f;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                x[m] = *reinterpret_cast<const float4 *>(sm + SB_O + 8192 * m + rr * 128 + 16 * p8);
+                ss = fmaf(x[m].x, x[m].x, fmaf(x[m].y, x[m].y, fmaf(x[m].z, x[m].z, fmaf(x[m].w, x[m].w, ss))));
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+            const float rs = rsqrtf(ss * (1.f / 128.f) + norm_eps);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int cg = (m & 1) * 4 + (p8 >> 1);          // 16-byte chunk of the gate row
+                const uint2 gu = *reinterpret_cast<const uint2 *>(
+                    sm + SB_GATE + 8192 * (m >> 1) + rr * 128 + ((cg ^ (rr & 7)) << 4) + 8 * (p8 & 1));
+                const float2 ga = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.x));
+                const float2 gb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.y));
+                const float4 wv = *reinterpret_cast<const float4 *>(s_normw + 32 * m + 4 * p8);
+                float4 y;
+                y.x = x[m].x * rs * wv.x * gate_sigmoid(ga.x);
+                y.y = x[m].y * rs * wv.y * gate_sigmoid(ga.y);
+                y.z = x[m].z * rs * wv.z * gate_sigmoid(gb.x);
+                y.w = x[m].w * rs * wv.w * gate_sigmoid(gb.y);
+                if (Lc == C)
+                    *reinterpret_cast<float4 *>(sm + SB_O + 8192 * m + rr * 128 + 16 * p8) = y;
+                else if (rr < Lc)
+                    *reinterpret_cast<float4 *>(o + ((size_t)(tok0 + c0 + rr) * H + h) * kDV + 32 * m + 4 * p8) = y;
+            }
+        }
         fence_proxy_async_smem();
         sync_tc();
         if (t == 0 && Lc == C) {
 #pragma unroll
             for (int bx = 0; bx < 4; ++bx) tma_store_3d(&map_o, sm + SB_O + 8192 * bx, 32 * bx, h, tok0 + c0);
             bulk_commit();
+        }
+        if (GATED && j + 1 < nch) {          // this chunk's gate is consumed
+            if (t == 0) issue_gate(j + 1);
+            ++issued_gate;
         }
     }
     if (t == 0) bulk_wait();                 // o stores complete before the CTA exits
@@ -1001,6 +1062,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         if (issued_a) mbar_wait(bar_a, (uint32_t)(issued_a - 1) & 1u, kWaitLimit);
         if (issued_b) mbar_wait(bar_b, (uint32_t)(issued_b - 1) & 1u, kWaitLimit);
         if (issued_mma) mbar_wait(bar_mma, (uint32_t)(issued_mma - 1) & 1u, kWaitLimit);
+        if (issued_gate) mbar_wait(bar_gate, (uint32_t)(issued_gate - 1) & 1u, kWaitLimit);
     } else {
         // ---- final state: S_out[i][j] from the TMEM master (lane j, column i)
         float sv[32];
@@ -1071,22 +1133,27 @@ unsigned intra_grid(int64_t jobs) {
 }
 
 // The three launches of one prefill, with the workspace at `ws` (at least
-// prefill_split_workspace_bytes(N, T, H) bytes).
+// prefill_split_workspace_bytes(N, T, H) bytes).  With a gate, the state pass
+// writes the gated RMSNorm of o to `o` instead of o itself.
 cudaError_t run_split(const void *q, const void *k, const void *v, const float *g,
                       const float *beta, const float *S0, float *o, float *S_out,
                       const int32_t *cu_seqlens, int N, int64_t T, int H, void *ws,
-                      cudaStream_t stream, cudaEvent_t const *ev = nullptr) {
+                      cudaStream_t stream, cudaEvent_t const *ev = nullptr,
+                      const void *gate = nullptr, const float *norm_w = nullptr,
+                      float norm_eps = 0.f) {
     const int64_t max_chunks = (T + C - 1) / C + N;
-    CUtensorMap mq, mk, mv, mg, mo;
+    CUtensorMap mq, mk, mv, mg, mo, mgate;
     if (!make_map_bf16(&mq, q, T, H, 64, true) || !make_map_bf16(&mk, k, T, H, 64, true) ||
         !make_map_bf16(&mv, v, T, H, 64, true) || !make_map_f32(&mg, g, T, H) ||
         !make_map_f32_plain(&mo, o, T, H))
         return cudaErrorInvalidValue;
+    if (gate && !make_map_bf16(&mgate, gate, T, H, 64, true)) return cudaErrorInvalidValue;
+    if (!gate) mgate = mv;                   // unused by the ungated kernel
     cudaError_t e = cudaFuncSetAttribute(intra_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_A_ALLOC);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_B_ALLOC);
+    e = cudaFuncSetAttribute(gate ? state_pass_kernel<true> : state_pass_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_B_ALLOC);
     if (e != cudaSuccess) return e;
     int32_t *chunk_off = static_cast<int32_t *>(ws);
     uint8_t *recs = static_cast<uint8_t *>(ws) +
@@ -1097,8 +1164,14 @@ cudaError_t run_split(const void *q, const void *k, const void *v, const float *
     intra_chunk_kernel<<<intra_grid(max_chunks * H), NTA, SMEM_A_ALLOC, stream>>>(
         mq, mk, mg, beta, cu_seqlens, chunk_off, N, H, recs);
     if (ev) cudaEventRecord(ev[2], stream);
-    state_pass_kernel<<<(unsigned)((int64_t)N * H), NTB, SMEM_B_ALLOC, stream>>>(
-        mv, mo, S0, o, S_out, cu_seqlens, chunk_off, N, H, (int)max_chunks, recs);
+    if (gate)
+        state_pass_kernel<true><<<(unsigned)((int64_t)N * H), NTB, SMEM_B_ALLOC, stream>>>(
+            mv, mo, S0, o, S_out, cu_seqlens, chunk_off, N, H, (int)max_chunks, recs, mgate, norm_w,
+            norm_eps);
+    else
+        state_pass_kernel<false><<<(unsigned)((int64_t)N * H), NTB, SMEM_B_ALLOC, stream>>>(
+            mv, mo, S0, o, S_out, cu_seqlens, chunk_off, N, H, (int)max_chunks, recs, mgate, nullptr,
+            0.f);
     if (ev) cudaEventRecord(ev[3], stream);
     return cudaGetLastError();
 }
@@ -1119,6 +1192,22 @@ cudaError_t launch_prefill_split(const void *q, const void *k, const void *v, co
     cudaError_t e = ws_alloc(&ws, prefill_split_workspace_bytes(N, T, H), stream);
     if (e != cudaSuccess) return e;
     e = run_split(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, T, H, ws, stream, events);
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    return e != cudaSuccess ? e : ef;
+}
+
+cudaError_t launch_prefill_split_gated(const void *q, const void *k, const void *v,
+                                       const float *g, const float *beta, const float *S0,
+                                       const void *gate, const float *norm_w, float eps,
+                                       float *out, float *S_out, const int32_t *cu_seqlens, int N,
+                                       int64_t T, int H, cudaStream_t stream,
+                                       cudaEvent_t const *events) {
+    if (!grid_fits(N, T, H)) return cudaErrorInvalidValue;
+    void *ws = nullptr;
+    cudaError_t e = ws_alloc(&ws, prefill_split_workspace_bytes(N, T, H), stream);
+    if (e != cudaSuccess) return e;
+    e = run_split(q, k, v, g, beta, S0, out, S_out, cu_seqlens, N, T, H, ws, stream, events, gate,
+                  norm_w, eps);
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     return e != cudaSuccess ? e : ef;
 }

@@ -45,8 +45,9 @@ def test_exports_every_declared_symbol(L):
 
 def test_version_and_status_strings(L):
     assert L.kda_version() >= 100
-    for s in range(0, 8):
+    for s in range(0, 9):
         assert len(L.kda_status_string(s)) > 0
+        assert L.kda_status_string(s) != b"unknown status"
     assert L.kda_status_string(12345) == b"unknown status"
 
 
@@ -133,3 +134,74 @@ def test_binding_fails_loudly_without_cuda_tensors():
     x = torch.zeros(4, 2, 128)
     with pytest.raises(ValueError):
         kda.decode_step(x, x, x, x, torch.zeros(4, 2), torch.zeros(4, 2, 128, 128))
+
+
+def _prologue(L, **kw):
+    a = dict(xq=GOOD, xk=GOOD, xv=GOOD, w=GOOD, cin=None, cout=GOOD, q=GOOD, k=GOOD, v=GOOD,
+             cu=GOOD, N=1, T=64, H=2, d=128, qs=0.088, eps=1e-6, stream=None)
+    a.update(kw)
+    return L.kda_conv_prologue(a["xq"], a["xk"], a["xv"], a["w"], a["cin"], a["cout"], a["q"],
+                               a["k"], a["v"], a["cu"], a["N"], a["T"], a["H"], a["d"], a["qs"],
+                               a["eps"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=64), 2), (dict(N=0), 2), (dict(H=0), 2), (dict(T=-1), 2),
+    (dict(eps=-1.0), 8), (dict(eps=float("nan")), 8), (dict(qs=float("inf")), 8),
+    (dict(qs=float("nan")), 8), (dict(cin=GOOD, cout=GOOD), 8),
+    (dict(xq=None), 1), (dict(w=None), 1), (dict(v=None), 1), (dict(cu=None), 1),
+    (dict(xk=ctypes.c_void_p(0x10004)), 4), (dict(cout=ctypes.c_void_p(0x10002)), 4),
+])
+def test_prologue_rejects_bad_arguments(L, kw, status):
+    assert _prologue(L, **kw) == status
+
+
+def test_prologue_without_tokens_or_windows_is_noop(L):
+    assert _prologue(L, T=0, cout=None, xq=None, q=None) == 0
+
+
+def _gated(L, **kw):
+    a = dict(q=GOOD, k=GOOD, v=GOOD, g=GOOD, beta=GOOD, S0=None, gate=GOOD, w=GOOD, eps=1e-6,
+             out=GOOD, S_out=GOOD, cu=GOOD, N=1, T=64, H=2, dk=128, dv=128, chunk=64, dtype=0,
+             stream=None)
+    a.update(kw)
+    return L.kda_prefill_chunked_gated(a["q"], a["k"], a["v"], a["g"], a["beta"], a["S0"],
+                                       a["gate"], a["w"], a["eps"], a["out"], a["S_out"], a["cu"],
+                                       a["N"], a["T"], a["H"], a["dk"], a["dv"], a["chunk"],
+                                       a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=3), 5), (dict(dk=64), 2), (dict(N=0), 2), (dict(chunk=8), 3),
+    (dict(eps=-0.5), 8), (dict(gate=None), 1), (dict(w=None), 1), (dict(out=None), 1),
+    (dict(S_out=None), 1), (dict(gate=ctypes.c_void_p(0x10006)), 4),
+    (dict(w=ctypes.c_void_p(0x10004)), 4),
+])
+def test_gated_prefill_rejects_bad_arguments(L, kw, status):
+    assert _gated(L, **kw) == status
+
+
+def _layer_step(L, **kw):
+    a = dict(xq=GOOD, xk=GOOD, xv=GOOD, w=GOOD, cp=GOOD, g=GOOD, beta=GOOD, gate=GOOD, nw=GOOD,
+             S=GOOD, sdt=1, idx=None, P=4, out=GOOD, B=4, H=2, dk=128, dv=128, qs=0.088,
+             l2=1e-6, ne=1e-6, stream=None)
+    a.update(kw)
+    return L.kda_decode_layer_step(a["xq"], a["xk"], a["xv"], a["w"], a["cp"], a["g"], a["beta"],
+                                   a["gate"], a["nw"], a["S"], a["sdt"], a["idx"], a["P"],
+                                   a["out"], a["B"], a["H"], a["dk"], a["dv"], a["qs"], a["l2"],
+                                   a["ne"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(sdt=2), 5), (dict(dk=64), 2), (dict(H=0), 2), (dict(B=-1), 2), (dict(P=3), 2),
+    (dict(l2=-1.0), 8), (dict(ne=float("nan")), 8), (dict(qs=float("-inf")), 8),
+    (dict(cp=None), 1), (dict(gate=None), 1), (dict(nw=None), 1), (dict(S=None), 1),
+    (dict(out=None), 1), (dict(cp=ctypes.c_void_p(0x10008)), 4),
+    (dict(idx=ctypes.c_void_p(0x10004)), 4),
+])
+def test_decode_layer_rejects_bad_arguments(L, kw, status):
+    assert _layer_step(L, **kw) == status
+
+
+def test_decode_layer_with_slots_allows_small_pool_and_empty_batch(L):
+    assert _layer_step(L, B=0, xq=None, S=None) == 0
