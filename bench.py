@@ -178,6 +178,13 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+def _gpu_hold(torch, ms: float):
+    """Keep the GPU busy for about `ms` milliseconds (a bounded spin kernel)
+    while the host enqueues the timed launches behind it: a timed region
+    then measures device time only, never the host's call overhead."""
+    torch.cuda._sleep(int(ms * 1e-3 * 2.0e9))
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -270,6 +277,7 @@ def run_ours(args):
         clk.keep_busy(step, 2)             # untimed load until the sampler reports
         barrier()
         torch.cuda.synchronize()
+        _gpu_hold(torch, 2.0 * args.steps)
         t0.record(stream)
         for _ in range(args.steps):
             step(record=True)
@@ -353,6 +361,11 @@ def run_ours(args):
     if not args.no_decode:
         decode = _decode_leg(kda, torch, dev, stream, peaks, args)
 
+    # ---- the layer around the recurrence (prologue, gated epilogue, fused decode)
+    layer = None
+    if not args.no_layer:
+        layer = _layer_leg(kda, torch, dev, stream, peaks)
+
     # ---- end to end through the public API with host buffers -------------
     e2e = None if args.no_e2e else _e2e_leg(kda, torch, dev, stream, pre, dstep, args, barrier, ws)
 
@@ -370,6 +383,7 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roofline,
         "decode": decode,
+        "layer": layer,
         "e2e": e2e,
         "clocks": clk.summary(),
     }
@@ -403,6 +417,7 @@ def _decode_leg(kda, torch, dev, stream, peaks, args):
 
     with ClockSampler(torch.cuda.current_device()) as clk:
         clk.keep_busy(untimed, 2, batch=64)
+        _gpu_hold(torch, 2.0 * len(ins))
         t0.record(stream)
         for x in ins:
             a = torch.cuda.Event(enable_timing=True)
@@ -437,6 +452,121 @@ def _decode_leg(kda, torch, dev, stream, peaks, args):
     }
 
 
+def _timed(torch, stream, fn, reps=10, warm=3):
+    """Median CUDA-event time (ms) of fn() on `stream` over `reps` calls,
+    enqueued back to back behind a GPU hold (so host-side call overhead
+    never leaves the GPU idle between the events)."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    _gpu_hold(torch, 2.0 * reps)
+    ts = []
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+
+# algorithmic bytes of the layer's kernels
+PROLOGUE_BYTES_PER_TOKEN_HEAD = 3 * 256 + 3 * 256        # raw q/k/v in, q/k/v out (bf16)
+# decode layer step per (b, h): state read + write, raw q/k/v, gate (bf16),
+# conv window read + write (3 x 3 x 128 bf16 each), g, beta, out (fp32)
+DECODE_LAYER_BYTES_PER_STATE = 2 * STATE_BYTES + 3 * 256 + 256 + 2 * 2304 + 512 + 4 + 512
+
+
+def _layer_leg(kda, torch, dev, stream, peaks):
+    """The layer around the recurrence at the model's sizes: the conv1d +
+    SiLU + L2-norm prologue and the gated prefill on the 4K prefill (H = 96,
+    T = 4096), the fused whole-layer decode step on the batched decode
+    (B = 64, H = 96, fp32 state pool, permuted slots)."""
+    L = ki.gen_layer(21, [4096], H=96, with_conv0=True)
+    T, H = L.T, L.H
+    d = {n: _to_dev(getattr(L, n), dev) for n in ("xq", "xk", "xv", "conv_w", "conv0", "gate",
+                                                   "norm_w", "g", "beta", "cu_seqlens")}
+    q = torch.empty((T, H, DK), dtype=torch.bfloat16, device=dev)
+    k, v = torch.empty_like(q), torch.empty_like(q)
+    conv_out = torch.empty_like(d["conv0"])
+    out = torch.empty((T, H, DV), dtype=torch.float32, device=dev)
+    S_out = torch.empty((1, H, DK, DV), dtype=torch.float32, device=dev)
+
+    def prologue():
+        kda.conv_prologue(d["xq"], d["xk"], d["xv"], d["conv_w"], d["cu_seqlens"],
+                          conv_in=d["conv0"], conv_out=conv_out, q=q, k=k, v=v)
+
+    def gated():
+        kda.prefill_chunked_gated(q, k, v, d["g"], d["beta"], d["cu_seqlens"], d["gate"],
+                                  d["norm_w"], out=out, S_out=S_out)
+
+    def plain():
+        kda.prefill_chunked(q, k, v, d["g"], d["beta"], d["cu_seqlens"], o=out, S_out=S_out)
+
+    def whole():
+        prologue()
+        gated()
+
+    t_pro = _timed(torch, stream, prologue)
+    t_gated = _timed(torch, stream, gated)
+    t_plain = _timed(torch, stream, plain)
+    t_all = _timed(torch, stream, whole)
+    pro_bytes = T * H * PROLOGUE_BYTES_PER_TOKEN_HEAD
+    pro_gbs = pro_bytes / (t_pro / 1e3) / 1e9
+    prefill = {
+        "workload": "layer prefill, H=96, T=4096, chunk 64, bf16 raw projections, carried windows",
+        "ms": round(t_all, 4), "tokens_per_s": round(T / (t_all / 1e3), 1),
+        "prologue": {"kernel": "conv_prologue_kernel", "ms": round(t_pro, 4),
+                     "roofline": {"bound": "hbm", "achieved": round(pro_gbs, 1),
+                                  "peak": peaks["hbm"], "unit": "GB/s",
+                                  "frac": round(pro_gbs / peaks["hbm"], 4),
+                                  "algorithmic_bytes": int(pro_bytes),
+                                  "bytes_per_token_head": PROLOGUE_BYTES_PER_TOKEN_HEAD}},
+        "gated_prefill": {"ms": round(t_gated, 4), "ungated_ms": round(t_plain, 4),
+                          "epilogue_cost": round(t_gated / t_plain - 1.0, 4)},
+        "gpu_launches_per_call": 4,
+    }
+    del L, d, q, k, v, out
+
+    B, Hd = 64, 96
+    rng = np.random.Generator(np.random.PCG64(22))
+    Ld = ki.gen_layer(23, [1], H=Hd)
+    step = ki.gen_layer_decode_step(rng, B, Hd)
+    S = torch.from_numpy(ki.gen_decode_state(rng, B, Hd)).to(dev)
+    conv = torch.randn((B, 3, 3, Hd, DK), generator=torch.Generator().manual_seed(24)).to(
+        torch.bfloat16).to(dev)
+    slots = torch.randperm(B, generator=torch.Generator().manual_seed(25)).to(torch.int32).to(dev)
+    x = {n: _to_dev(getattr(step, n), dev) for n in ("xq", "xk", "xv", "gate", "g", "beta")}
+    w = _to_dev(Ld.conv_w, dev)
+    nw = _to_dev(Ld.norm_w, dev)
+    o = torch.empty((B, Hd, DV), dtype=torch.float32, device=dev)
+
+    def layer_step():
+        kda.decode_layer_step(x["xq"], x["xk"], x["xv"], w, conv, x["g"], x["beta"], x["gate"], nw,
+                              S, state_indices=slots, out=o)
+
+    t_step = _timed(torch, stream, layer_step, reps=100)
+    plain = ki.gen_decode_step(rng, B, Hd, "bf16")
+    y = {n: _to_dev(getattr(plain, n), dev) for n in ("q", "k", "v", "g", "beta")}
+    t_dec = _timed(torch, stream, lambda: kda.decode_step_pool(
+        y["q"], y["k"], y["v"], y["g"], y["beta"], S, state_indices=slots, o=o), reps=100)
+    step_bytes = B * Hd * DECODE_LAYER_BYTES_PER_STATE + 3 * Hd * DK * 4 * 4 + DV * 4
+    gbs = step_bytes / (t_step / 1e3) / 1e9
+    decode = {
+        "workload": "layer decode step, B=64, H=96, fp32 state pool, permuted slots",
+        "median_step_us": round(t_step * 1e3, 2),
+        "recurrence_only_step_us": round(t_dec * 1e3, 2),
+        "roofline": {"kernel": "decode_layer_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                     "peak": peaks["hbm"], "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4),
+                     "algorithmic_bytes": int(step_bytes),
+                     "bytes_per_state": DECODE_LAYER_BYTES_PER_STATE},
+        "gpu_launches_per_step": 1,
+    }
+    return {"prefill": prefill, "decode": decode}
+
+
 def _decode_pool_leg(kda, torch, dev, stream, peaks, S32, ins, B, H):
     """The same 100 steps on a bf16 state pool addressed by a permuted slot
     table (kda_decode_step_pool): half the state bytes per step."""
@@ -450,6 +580,7 @@ def _decode_pool_leg(kda, torch, dev, stream, peaks, S32, ins, B, H):
         kda.decode_step_pool(x["q"], x["k"], x["v"], x["g"], x["beta"], S, state_indices=slots, o=o)
     torch.cuda.synchronize()
     evs = []
+    _gpu_hold(torch, 2.0 * len(ins))
     for x in ins:
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
@@ -651,6 +782,8 @@ def main():
                     help="heads per sequence in the oracle sample (default: ~4e5 token-heads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-layer", action="store_true",
+                    help="skip the layer leg (prologue, gated prefill, fused layer decode)")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end leg (profiling runs)")
     args = ap.parse_args()

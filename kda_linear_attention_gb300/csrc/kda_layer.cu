@@ -23,8 +23,11 @@ namespace {
 constexpr int kConvK = 4;
 constexpr int kWin = kConvK - 1;
 
-__device__ __forceinline__ float silu(float y) { return y / (1.f + __expf(-y)); }
-__device__ __forceinline__ float sigmoid(float y) { return 1.f / (1.f + __expf(-y)); }
+// x / (1 + e^-x) and 1 / (1 + e^-x) with the fast exponential and division
+// (a few ulp; the outputs are rounded to bf16 or checked at 2e-3).  For very
+// negative x the denominator overflows to inf and the quotient is 0.
+__device__ __forceinline__ float silu(float y) { return __fdividef(y, 1.f + __expf(-y)); }
+__device__ __forceinline__ float sigmoid(float y) { return __fdividef(1.f, 1.f + __expf(-y)); }
 
 __device__ __forceinline__ void unpack8(uint4 u, float (&x)[8]) {
     const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
@@ -46,13 +49,14 @@ __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
 }
 
 // ============================================================================
-// Prefill prologue.  A half-warp owns one (run of kRun tokens, projection p,
-// head h); lane l holds channels 8l..8l+7 and walks the run token by token
-// with the channel's window in registers, so every raw input is read once
-// (plus a three-token halo per run).  The L2 norm of a (token, head) row is a
-// reduction over the half-warp.
+// Prefill prologue.  A warp owns one (run of kRun tokens, projection p, head
+// h); lane l holds channels 4l..4l+3 and walks the run token by token with
+// the channel's window in registers, so every raw input is read once (plus a
+// three-token halo per run, mostly from L2).  Loads are issued kBatch tokens
+// at a time.  The L2 norm of a (token, head) row is a warp reduction.
 // ============================================================================
-constexpr int kRun = 64;
+constexpr int kRun = 32;
+constexpr int kBatch = 8;
 constexpr int kPrologueThreads = 256;
 
 __device__ __forceinline__ int seq_of(const int32_t *cu, int N, int t) {
@@ -66,7 +70,18 @@ __device__ __forceinline__ int seq_of(const int32_t *cu, int N, int t) {
     return lo;
 }
 
-__global__ void __launch_bounds__(kPrologueThreads)
+__device__ __forceinline__ void unpack4(uint2 u, float (&x)[4]) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+}
+__device__ __forceinline__ uint2 pack4(const float (&x)[4]) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
+    __nv_bfloat162 b = __floats2bfloat162_rn(x[2], x[3]);
+    return make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
+}
+
+__global__ void __launch_bounds__(kPrologueThreads, 2)
 conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *__restrict__ xk,
                      const __nv_bfloat16 *__restrict__ xv, const float *__restrict__ conv_w,
                      const __nv_bfloat16 *__restrict__ conv_in, __nv_bfloat16 *__restrict__ conv_out,
@@ -88,72 +103,66 @@ conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *
         }
     }
 
-    const int lane16 = threadIdx.x & 15;
-    const long long hw = (long long)blockIdx.x * (kPrologueThreads / 16) + (threadIdx.x >> 4);
-    const bool active = hw < nruns;
-    const long long hwc = active ? hw : 0;
-    const int h = (int)(hwc % H);
-    const int p = (int)((hwc / H) % 3);
-    const int j = (int)(hwc / (3LL * H));
-    const int c0 = 8 * lane16;
+    const int lane = threadIdx.x & 31;
+    const long long wid = (long long)blockIdx.x * (kPrologueThreads / 32) + (threadIdx.x >> 5);
+    if (wid >= nruns) return;                  // whole warps leave together
+    const int h = (int)(wid % H);
+    const int p = (int)((wid / H) % 3);
+    const int j = (int)(wid / (3LL * H));
+    const int c0 = 4 * lane;
     const __nv_bfloat16 *x = p == 0 ? xq : (p == 1 ? xk : xv);
     __nv_bfloat16 *y_out = p == 0 ? q : (p == 1 ? k : v);
     const float scale = p == 0 ? q_scale : 1.f;
 
-    // taps of the 8 channels: w[c][m], tap 3 on the newest input
-    float w[8][4];
+    // taps of the 4 channels: w[c][m], tap 3 on the newest input
+    float w[4][4];
     {
         const float4 *wp = reinterpret_cast<const float4 *>(conv_w + (((size_t)p * H + h) * 128 + c0) * kConvK);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
             const float4 t4 = wp[c];
             w[c][0] = t4.x; w[c][1] = t4.y; w[c][2] = t4.z; w[c][3] = t4.w;
         }
     }
-    const int t0 = active ? j * kRun : T;
+    const int t0 = j * kRun;
     const int t_end = min(t0 + kRun, T);
     auto row = [&](int t) -> size_t { return ((size_t)t * H + h) * 128 + c0; };
     auto win_at = [&](int n, int slot) -> size_t {
         return (((size_t)n * 3 + p) * kWin + slot) * win_row + (size_t)h * 128 + c0;
     };
 
-    float win[kWin][8];
-    int n = 0, start = 0, end = 0;
-    // window of token t in sequence n: the three inputs before t, from the
+    float win[kWin][4];
+    int n = seq_of(cu, N, t0);
+    int start = cu[n], end = cu[n + 1];
+    // window of token tt in sequence n: the three inputs before tt, from the
     // sequence itself or (before its start) from its carried window
     auto load_window = [&](int tt) {
 #pragma unroll
         for (int m = 0; m < kWin; ++m) {
             const int tau = tt - kWin + m;
-            uint4 u = make_uint4(0, 0, 0, 0);
-            if (tau >= start) u = *reinterpret_cast<const uint4 *>(x + row(tau));
-            else if (conv_in) u = *reinterpret_cast<const uint4 *>(conv_in + win_at(n, kWin + (tau - start)));
-            unpack8(u, win[m]);
+            uint2 u = make_uint2(0, 0);
+            if (tau >= start) u = *reinterpret_cast<const uint2 *>(x + row(tau));
+            else if (conv_in) u = *reinterpret_cast<const uint2 *>(conv_in + win_at(n, kWin + (tau - start)));
+            unpack4(u, win[m]);
         }
     };
-    if (t0 < t_end) {
-        n = seq_of(cu, N, t0);
-        start = cu[n];
-        end = cu[n + 1];
-        load_window(t0);
-    } else {
-#pragma unroll
-        for (int m = 0; m < kWin; ++m)
-#pragma unroll
-            for (int c = 0; c < 8; ++c) win[m][c] = 0.f;
-    }
+    load_window(t0);
 
-    for (int i = 0; i < kRun; i += 4) {
-        uint4 xr[4];
+    const size_t rstride = (size_t)H * 128;    // elements between consecutive tokens
+    const __nv_bfloat16 *xp = x + row(t0);
+    __nv_bfloat16 *yp = y_out + row(t0);
+    for (int i = 0; i < kRun; i += kBatch) {
+        if (t0 + i >= t_end) break;            // warp-uniform
+        uint2 xr[kBatch];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int t = t0 + i + u;
-            xr[u] = t < t_end ? *reinterpret_cast<const uint4 *>(x + row(t)) : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < kBatch; ++u) {
+            xr[u] = make_uint2(0, 0);
+            if (t0 + i + u < t_end) xr[u] = *reinterpret_cast<const uint2 *>(xp + (size_t)(i + u) * rstride);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kBatch; ++u) {
             const int t = t0 + i + u;
-            const bool valid = t < t_end;
+            const bool valid = t < t_end;      // warp-uniform
             if (valid && t >= end && n < N - 1) {   // the run enters the next non-empty sequence
                 do {
                     ++n;
@@ -162,25 +171,26 @@ conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *
                 end = cu[n + 1];
                 load_window(t);
             }
-            float xn[8], z[8];
-            unpack8(xr[u], xn);
+            float xn[4], z[4];
+            unpack4(xr[u], xn);
             float ss = 0.f;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float y = w[c][0] * win[0][c] + w[c][1] * win[1][c] + w[c][2] * win[2][c] +
-                                w[c][3] * xn[c];
+            for (int c = 0; c < 4; ++c) {
+                const float y = fmaf(w[c][0], win[0][c], fmaf(w[c][1], win[1][c],
+                                fmaf(w[c][2], win[2][c], w[c][3] * xn[c])));
                 z[c] = silu(y);
                 ss = fmaf(z[c], z[c], ss);
             }
-            // every lane of the warp takes part in the reduction
+            if (p != 2) {                      // warp-uniform: q and k are L2-normalised
 #pragma unroll
-            for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, 16);
-            const float f = p == 2 ? 1.f : scale * rsqrtf(ss + eps);
+                for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                const float f = scale * rsqrtf(ss + eps);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) z[c] *= f;
-            if (valid) *reinterpret_cast<uint4 *>(y_out + row(t)) = pack8(z);
+                for (int c = 0; c < 4; ++c) z[c] *= f;
+            }
+            if (valid) *reinterpret_cast<uint2 *>(yp + (size_t)(i + u) * rstride) = pack4(z);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 win[0][c] = win[1][c];
                 win[1][c] = win[2][c];
                 win[2][c] = xn[c];
@@ -188,7 +198,7 @@ conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *
             if (valid && t == end - 1 && conv_out) {   // the sequence's last token: its window out
 #pragma unroll
                 for (int m = 0; m < kWin; ++m)
-                    *reinterpret_cast<uint4 *>(conv_out + win_at(n, m)) = pack8(win[m]);
+                    *reinterpret_cast<uint2 *>(conv_out + win_at(n, m)) = pack4(win[m]);
             }
         }
     }
@@ -221,12 +231,13 @@ gated_norm_kernel(float *__restrict__ o, const __nv_bfloat16 *__restrict__ gate,
 }
 
 // ============================================================================
-// Whole-layer decode step: one block per (b, h).  The conv + SiLU + L2-norm
-// prologue runs while the state loads are in flight; then the fused token
-// step of kda_decode.cu over all 128 columns (thread t: column group t % 32,
-// rows t / 32 + 8 r), then the gated RMSNorm of o in warp 0.
+// Whole-layer decode step: one block of 512 threads per (b, h).  The q, k, v
+// convs and the decay exponentials run at once on four 128-thread groups
+// while the state loads are in flight; then the fused token step of
+// kda_decode.cu over all 128 columns (thread t: column group t % 32, rows
+// t / 32 + 16 r), then the gated RMSNorm of o in warp 0.
 // ============================================================================
-constexpr int kLayerThreads = 256;
+constexpr int kLayerThreads = 512;
 
 __device__ __forceinline__ float4 ld_state4(const float *p) {
     return __ldcs(reinterpret_cast<const float4 *>(p));
@@ -259,8 +270,8 @@ decode_layer_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *_
                     const int32_t *__restrict__ slots, float *__restrict__ out, int H, int P,
                     float q_scale, float l2_eps, float norm_eps) {
     constexpr int C4 = 32;                      // float4 column groups
-    constexpr int NRG = kLayerThreads / C4;     // 8 row groups
-    constexpr int RPT = kDK / NRG;              // 16 rows per thread
+    constexpr int NRG = kLayerThreads / C4;     // 16 row groups
+    constexpr int RPT = kDK / NRG;              // 8 rows per thread
     const int unit = blockIdx.x;                // b * H + h
     const int b = unit / H, h = unit % H;
     const int t = threadIdx.x;
@@ -278,49 +289,70 @@ decode_layer_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *_
         }
     }
     TS *Su = S + ((size_t)slot * H + h) * kDK * kDV;
-    float4 s[RPT];
-#pragma unroll
-    for (int r = 0; r < RPT; ++r) s[r] = ld_state4(Su + (size_t)(rg + r * NRG) * kDV + col0);
 
     __shared__ float sq[kDK], sk[kDK], sv[kDV], sa[kDK];
     __shared__ float s_red[2][4];
     __shared__ float4 red_k[NRG][C4];
     __shared__ float4 red_q[NRG][C4];
 
-    // ---- prologue: q (threads 0..127) and k (128..255), then v (0..127)
+    // ---- the prologue's few loads go out before the state stream: group 0
+    // q, 1 k, 2 v (raw input, window, taps), group 3 the log-decay; warp 0
+    // also fetches what its epilogue needs
+    const int grp = t >> 7, c = t & 127;
     const size_t win_row = (size_t)H * 128;
-    auto conv_step = [&](int p, int c, const __nv_bfloat16 *x) -> float {
-        const float xn = __bfloat162float(x[(size_t)unit * 128 + c]);
-        __nv_bfloat16 *wp = conv_pool + ((size_t)slot * 3 + p) * kWin * win_row + (size_t)h * 128 + c;
-        const float w0 = __bfloat162float(wp[0]);
-        const float w1 = __bfloat162float(wp[win_row]);
-        const float w2 = __bfloat162float(wp[2 * win_row]);
-        const float4 tp = *reinterpret_cast<const float4 *>(conv_w + (((size_t)p * H + h) * 128 + c) * kConvK);
-        const float y = tp.x * w0 + tp.y * w1 + tp.z * w2 + tp.w * xn;
-        // shift the window by one (exact: raw bf16 inputs)
-        wp[0] = __float2bfloat16_rn(w1);
-        wp[win_row] = __float2bfloat16_rn(w2);
-        wp[2 * win_row] = x[(size_t)unit * 128 + c];
-        return silu(y);
-    };
+    __nv_bfloat16 *wp = conv_pool + ((size_t)slot * 3 + (grp < 3 ? grp : 0)) * kWin * win_row +
+                        (size_t)h * 128 + c;
+    __nv_bfloat16 xb = __float2bfloat16_rn(0.f), b0 = xb, b1 = xb, b2 = xb;
+    float4 tp = make_float4(0.f, 0.f, 0.f, 0.f);
+    float gl = 0.f;
+    if (grp < 3) {
+        const __nv_bfloat16 *x = grp == 0 ? xq : (grp == 1 ? xk : xv);
+        xb = x[(size_t)unit * 128 + c];
+        b0 = wp[0];
+        b1 = wp[win_row];
+        b2 = wp[2 * win_row];
+        tp = *reinterpret_cast<const float4 *>(conv_w + (((size_t)grp * H + h) * 128 + c) * kConvK);
+    } else {
+        gl = g[(size_t)unit * kDK + c];
+    }
+    uint2 gu = make_uint2(0, 0);
+    float4 wv = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (rg == 0) {
+        gu = *reinterpret_cast<const uint2 *>(gate + (size_t)unit * kDV + col0);
+        wv = *reinterpret_cast<const float4 *>(norm_w + col0);
+    }
+    const float bt = beta[unit];
+
+    float4 s[RPT];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) s[r] = ld_state4(Su + (size_t)(rg + r * NRG) * kDV + col0);
+
+    // conv + SiLU (window shifted in place: raw bf16 inputs, exact) and the
+    // decay exponentials; q and k are kept unnormalised in shared memory and
+    // their L2-norm factors applied where they are used
     {
-        const int p = t >> 7, c = t & 127;
-        const float z = conv_step(p, c, p == 0 ? xq : xk);
+        float z = 0.f;
+        if (grp < 3) {
+            const float y = fmaf(tp.x, __bfloat162float(b0), fmaf(tp.y, __bfloat162float(b1),
+                            fmaf(tp.z, __bfloat162float(b2), tp.w * __bfloat162float(xb))));
+            wp[0] = b1;
+            wp[win_row] = b2;
+            wp[2 * win_row] = xb;
+            z = silu(y);
+            if (grp == 0) sq[c] = z;
+            else if (grp == 1) sk[c] = z;
+            else sv[c] = z;
+        } else {
+            sa[c] = expf(gl);
+        }
         float ss = z * z;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        if ((t & 31) == 0) s_red[p][(t >> 5) & 3] = ss;
-        if (t < 128) {
-            sv[t] = conv_step(2, t, xv);
-            sa[t] = expf(g[(size_t)unit * kDK + t]);
-        }
-        __syncthreads();
-        const float tot = s_red[p][0] + s_red[p][1] + s_red[p][2] + s_red[p][3];
-        const float f = (p == 0 ? q_scale : 1.f) * rsqrtf(tot + l2_eps);
-        if (p == 0) sq[c] = z * f;
-        else sk[c] = z * f;
+        if (grp < 2 && (t & 31) == 0) s_red[grp][(t >> 5) & 3] = ss;
     }
     __syncthreads();
+    const float fq = q_scale * rsqrtf(s_red[0][0] + s_red[0][1] + s_red[0][2] + s_red[0][3] + l2_eps);
+    const float fk = rsqrtf(s_red[1][0] + s_red[1][1] + s_red[1][2] + s_red[1][3] + l2_eps);
     float qk = 0.f;
     {
         // q . k over the 128 channels (every warp computes it)
@@ -329,9 +361,11 @@ decode_layer_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *_
         for (int e = 0; e < 4; ++e) qk = fmaf(sq[l + 32 * e], sk[l + 32 * e], qk);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) qk += __shfl_xor_sync(0xffffffffu, qk, off);
+        qk *= fq * fk;
     }
 
-    // ---- the token step over this thread's rows
+    // ---- the token step over this thread's rows (k and q unnormalised in
+    // the sums, their factors applied to the column totals)
     float4 uk = make_float4(0.f, 0.f, 0.f, 0.f);
     float4 uq = uk;
 #pragma unroll
@@ -352,7 +386,8 @@ decode_layer_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *_
         Uk.x += a.x; Uk.y += a.y; Uk.z += a.z; Uk.w += a.w;
         Uq.x += bq.x; Uq.y += bq.y; Uq.z += bq.z; Uq.w += bq.w;
     }
-    const float bt = beta[unit];
+    Uk.x *= fk; Uk.y *= fk; Uk.z *= fk; Uk.w *= fk;
+    Uq.x *= fq; Uq.y *= fq; Uq.z *= fq; Uq.w *= fq;
     float4 w;
     w.x = bt * (sv[col0 + 0] - Uk.x);
     w.y = bt * (sv[col0 + 1] - Uk.y);
@@ -361,7 +396,7 @@ decode_layer_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *_
 #pragma unroll
     for (int r = 0; r < RPT; ++r) {
         const int i = rg + r * NRG;
-        const float ki = sk[i];
+        const float ki = sk[i] * fk;
         s[r].x += ki * w.x; s[r].y += ki * w.y; s[r].z += ki * w.z; s[r].w += ki * w.w;
         st_state4(Su + (size_t)i * kDV + col0, s[r]);
     }
@@ -375,10 +410,8 @@ decode_layer_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *_
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         const float rs = rsqrtf(ss * (1.f / 128.f) + norm_eps);
-        const uint2 gu = *reinterpret_cast<const uint2 *>(gate + (size_t)unit * kDV + col0);
         const float2 ga = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.x));
         const float2 gb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.y));
-        const float4 wv = *reinterpret_cast<const float4 *>(norm_w + col0);
         ov.x *= rs * wv.x * sigmoid(ga.x);
         ov.y *= rs * wv.y * sigmoid(ga.y);
         ov.z *= rs * wv.z * sigmoid(gb.x);
@@ -394,7 +427,7 @@ cudaError_t launch_conv_prologue(const void *xq, const void *xk, const void *xv,
                                  const int32_t *cu_seqlens, int N, int64_t T, int H, float q_scale,
                                  float eps, cudaStream_t stream) {
     const long long nruns = ((T + kRun - 1) / kRun) * 3LL * H;
-    long long blocks = (nruns + kPrologueThreads / 16 - 1) / (kPrologueThreads / 16);
+    long long blocks = (nruns + kPrologueThreads / 32 - 1) / (kPrologueThreads / 32);
     if (blocks < 1) blocks = 1;                    // empty sequences still pass their windows on
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     conv_prologue_kernel<<<(unsigned)blocks, kPrologueThreads, 0, stream>>>(

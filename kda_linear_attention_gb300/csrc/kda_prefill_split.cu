@@ -762,7 +762,8 @@ constexpr uint32_t TMB_O = 192;           // O^T, 64 columns (N = 128 with TMB_U
 constexpr uint32_t COPY1 = R_A - R_WQ;    // bytes of [-W ; Q0] + T'
 constexpr uint32_t COPY2 = R_VEC - R_A;   // bytes of A' + Kbar^T
 
-__device__ __forceinline__ float gate_sigmoid(float x) { return 1.f / (1.f + __expf(-x)); }
+// 1 / (1 + e^-x) with the fast exponential and division (a few ulp)
+__device__ __forceinline__ float gate_sigmoid(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
 // GATED: the layer's output epilogue ("Colibri Kimi K3 Metal backend",
 // section 8.4) on every row of o before it is stored: o / sqrt(mean_j o_j^2
