@@ -94,10 +94,11 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t *__restr
 
 // ============================================================================
 // intra-chunk kernel: persistent, two CTAs (256 threads each) per SM.  CTA b
-// takes the (chunk, head) jobs b, b + G, b + 2G, ... (G = grid size; job =
-// gc * H + h) and prefetches the next job's inputs while it finishes the
-// current one: its q and k as soon as the Gram product has consumed X, its g
-// (L2 prefetch early, shared memory once the W product is done).
+// takes the (chunk, head) jobs b, b + G, b + 2G, ... (G = grid size; job j
+// is (chunk, head) = divmod(total - 1 - j, H): last chunk first) and
+// prefetches the next job's inputs while it finishes the current one: its q
+// and k as soon as the Gram product has consumed X, its g (L2 prefetch early,
+// shared memory once the W product is done).
 // ============================================================================
 constexpr int NTA = 256;
 constexpr uint32_t SA_X = 0;              // 32 KB: q|k (TMA) -> X [128][128] sw (A of the Gram)
@@ -121,7 +122,9 @@ constexpr uint32_t SMEM_A_USED = SA_MISC + 9248;
 constexpr uint32_t SMEM_A_ALLOC = SMEM_A_USED + 1024;
 static_assert(2 * (SMEM_A_ALLOC + 1024) <= 233472, "two intra-chunk CTAs per SM");
 static_assert(SA_T + 16384 <= SA_K0 && SA_Y + 4096 <= SA_T, "solve space inside the Khat region");
+static_assert(SA_Y + 32 * 40 * 4 <= SA_T, "the 32 x 32 solve temporary fits");
 constexpr int MLD = 68;                   // row stride (floats) of M / T
+constexpr int YLD = 40;                   // row stride (floats) of the 32x32 solve temporary
 constexpr uint32_t TMA_G = 0;             // Gram D, 160 columns
 constexpr uint32_t TMA_W = 0;             // W, 128 columns (after the Gram epilogue)
 
@@ -154,12 +157,16 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     const int lane = t & 31;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
 
-    // job -> (head, global chunk, first token, rows); every thread decodes
+    // job -> (head, global chunk, first token, rows); every thread decodes.
+    // Jobs run from the last chunk down, so the records of the first chunks,
+    // which the state pass reads first, are the most recently written and
+    // still in L2 when it starts.
     const int total = chunk_off[N] * H;
     auto decode = [&](int job) -> Job {
         Job J;
-        J.h = job % H;
-        J.gc = job / H;
+        const int jr = total - 1 - job;
+        J.h = jr % H;
+        J.gc = jr / H;
         int lo = 0, hi = N - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -537,105 +544,90 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         }
         __syncthreads();
         // off-diagonal blocks, two levels: T_10 and T_32 (T_pq = -T_pp M_pq T_qq),
-        // then the lower-left 32x32 block T_C = -T_B M_C T_A
+        // then the lower-left 32x32 block T_C = -T_B M_C T_A.  The 16x16
+        // products run on warp-level tf32 MMAs in warps 0..3 (warp = block,
+        // column tile of 8): P = M_pq T_qq into the temporary, then
+        // T_pq = -T_pp P over M_pq
         {
-            // thread = (block, row r, 4 columns c4, half kh of the 16-term sum)
-            const int kh = t & 1, c4 = (t >> 1) & 3, r = (t >> 3) & 15, blk = t >> 7;
+            const int g = lane >> 2, tg = lane & 3;
+            const int blk = (warp >> 1) & 1, nt = warp & 1;
             const int p = blk ? 3 : 1, q = p - 1;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            float arow[8];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (16 * p + r) * MLD + 16 * q + 8 * kh + 4 * j);
-                arow[4 * j] = a4.x; arow[4 * j + 1] = a4.y; arow[4 * j + 2] = a4.z; arow[4 * j + 3] = a4.w;
+            if (warp < 4) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int kk = nt; kk < 2; ++kk) {          // T_qq lower triangular
+                    const float *A = Mm + (16 * p) * MLD + 16 * q + 8 * kk;
+                    const float *Bm = Mm + (16 * q + 8 * kk) * MLD + 16 * q + 8 * nt;
+                    const uint32_t a[4] = {to_tf32(A[g * MLD + tg]), to_tf32(A[(g + 8) * MLD + tg]),
+                                           to_tf32(A[g * MLD + tg + 4]), to_tf32(A[(g + 8) * MLD + tg + 4])};
+                    const uint32_t b[2] = {to_tf32(Bm[tg * MLD + g]), to_tf32(Bm[(tg + 4) * MLD + g])};
+                    mma_tf32_16x8x8(d, a, b);
+                }
+                float *Y = Yt + (16 * blk) * 16 + 8 * nt;
+                Y[g * 16 + 2 * tg] = d[0];
+                Y[g * 16 + 2 * tg + 1] = d[1];
+                Y[(g + 8) * 16 + 2 * tg] = d[2];
+                Y[(g + 8) * 16 + 2 * tg + 1] = d[3];
             }
+            __syncthreads();
+            if (warp < 4) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const float a = arow[m];
-                const float4 tv = *reinterpret_cast<const float4 *>(Mm + (16 * q + 8 * kh + m) * MLD + 16 * q + 4 * c4);
-                acc.x = fmaf(a, tv.x, acc.x);
-                acc.y = fmaf(a, tv.y, acc.y);
-                acc.z = fmaf(a, tv.z, acc.z);
-                acc.w = fmaf(a, tv.w, acc.w);
+                for (int kk = 0; kk < 2; ++kk) {
+                    const float *A = Mm + (16 * p) * MLD + 16 * p + 8 * kk;
+                    const float *Bm = Yt + (16 * blk + 8 * kk) * 16 + 8 * nt;
+                    const uint32_t a[4] = {to_tf32(A[g * MLD + tg]), to_tf32(A[(g + 8) * MLD + tg]),
+                                           to_tf32(A[g * MLD + tg + 4]), to_tf32(A[(g + 8) * MLD + tg + 4])};
+                    const uint32_t b[2] = {to_tf32(Bm[tg * 16 + g]), to_tf32(Bm[(tg + 4) * 16 + g])};
+                    mma_tf32_16x8x8(d, a, b);
+                }
+                float *Tq = Mm + (16 * p) * MLD + 16 * q + 8 * nt;
+                Tq[g * MLD + 2 * tg] = -d[0];
+                Tq[g * MLD + 2 * tg + 1] = -d[1];
+                Tq[(g + 8) * MLD + 2 * tg] = -d[2];
+                Tq[(g + 8) * MLD + 2 * tg + 1] = -d[3];
             }
-            acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 1);
-            acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 1);
-            acc.z += __shfl_xor_sync(0xffffffffu, acc.z, 1);
-            acc.w += __shfl_xor_sync(0xffffffffu, acc.w, 1);
-            if (kh == 0) *reinterpret_cast<float4 *>(Yt + (blk * 16 + r) * 16 + 4 * c4) = acc;
+        }
+        __syncthreads();
+        // lower-left 32x32 block on warp-level tf32 MMAs (8 warps: row tile mt,
+        // column tile nt of 8); the triangular factors' zero tiles are skipped
+        {
+            // Y2 = M[32:64][0:32] T[0:32][0:32]   (T_A lower triangular: kk >= nt)
+            const int g = lane >> 2, tg = lane & 3;
+            const int mt = warp >> 2, nt = warp & 3;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int kk = nt; kk < 4; ++kk) {
+                const float *A = Mm + (32 + 16 * mt) * MLD + 8 * kk;
+                const float *Bm = Mm + (8 * kk) * MLD + 8 * nt;
+                const uint32_t a[4] = {to_tf32(A[g * MLD + tg]), to_tf32(A[(g + 8) * MLD + tg]),
+                                       to_tf32(A[g * MLD + tg + 4]), to_tf32(A[(g + 8) * MLD + tg + 4])};
+                const uint32_t b[2] = {to_tf32(Bm[tg * MLD + g]), to_tf32(Bm[(tg + 4) * MLD + g])};
+                mma_tf32_16x8x8(d, a, b);
+            }
+            float *Y = Yt + (16 * mt) * YLD + 8 * nt;
+            Y[g * YLD + 2 * tg] = d[0];
+            Y[g * YLD + 2 * tg + 1] = d[1];
+            Y[(g + 8) * YLD + 2 * tg] = d[2];
+            Y[(g + 8) * YLD + 2 * tg + 1] = d[3];
         }
         __syncthreads();
         {
-            const int kh = t & 1, c4 = (t >> 1) & 3, r = (t >> 3) & 15, blk = t >> 7;
-            const int p = blk ? 3 : 1, q = p - 1;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            float arow[8];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (16 * p + r) * MLD + 16 * p + 8 * kh + 4 * j);
-                arow[4 * j] = a4.x; arow[4 * j + 1] = a4.y; arow[4 * j + 2] = a4.z; arow[4 * j + 3] = a4.w;
+            // T_C = -T[32:64][32:64] Y2   (T_B lower triangular: kk <= 2 mt + 1)
+            const int g = lane >> 2, tg = lane & 3;
+            const int mt = warp >> 2, nt = warp & 3;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int kk = 0; kk <= 2 * mt + 1; ++kk) {
+                const float *A = Mm + (32 + 16 * mt) * MLD + 32 + 8 * kk;
+                const float *Bm = Yt + (8 * kk) * YLD + 8 * nt;
+                const uint32_t a[4] = {to_tf32(A[g * MLD + tg]), to_tf32(A[(g + 8) * MLD + tg]),
+                                       to_tf32(A[g * MLD + tg + 4]), to_tf32(A[(g + 8) * MLD + tg + 4])};
+                const uint32_t b[2] = {to_tf32(Bm[tg * YLD + g]), to_tf32(Bm[(tg + 4) * YLD + g])};
+                mma_tf32_16x8x8(d, a, b);
             }
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const float a = arow[m];
-                const float4 yv = *reinterpret_cast<const float4 *>(Yt + (blk * 16 + 8 * kh + m) * 16 + 4 * c4);
-                acc.x = fmaf(a, yv.x, acc.x);
-                acc.y = fmaf(a, yv.y, acc.y);
-                acc.z = fmaf(a, yv.z, acc.z);
-                acc.w = fmaf(a, yv.w, acc.w);
-            }
-            acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 1);
-            acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 1);
-            acc.z += __shfl_xor_sync(0xffffffffu, acc.z, 1);
-            acc.w += __shfl_xor_sync(0xffffffffu, acc.w, 1);
-            if (kh == 0)
-                *reinterpret_cast<float4 *>(Mm + (16 * p + r) * MLD + 16 * q + 4 * c4) =
-                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        }
-        __syncthreads();
-        {
-            // Y2 = M[32:64][0:32] T[0:32][0:32]
-            const int r = t >> 3, c4 = t & 7;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            float arow[32];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (32 + r) * MLD + 4 * j);
-                arow[4 * j] = a4.x; arow[4 * j + 1] = a4.y; arow[4 * j + 2] = a4.z; arow[4 * j + 3] = a4.w;
-            }
-#pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                const float a = arow[m];
-                const float4 tv = *reinterpret_cast<const float4 *>(Mm + m * MLD + 4 * c4);
-                acc.x = fmaf(a, tv.x, acc.x);
-                acc.y = fmaf(a, tv.y, acc.y);
-                acc.z = fmaf(a, tv.z, acc.z);
-                acc.w = fmaf(a, tv.w, acc.w);
-            }
-            *reinterpret_cast<float4 *>(Yt + r * 32 + 4 * c4) = acc;
-        }
-        __syncthreads();
-        {
-            // T_C = -T[32:64][32:64] Y2
-            const int r = t >> 3, c4 = t & 7;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            float arow[32];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(Mm + (32 + r) * MLD + 32 + 4 * j);
-                arow[4 * j] = a4.x; arow[4 * j + 1] = a4.y; arow[4 * j + 2] = a4.z; arow[4 * j + 3] = a4.w;
-            }
-#pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                const float a = arow[m];
-                const float4 yv = *reinterpret_cast<const float4 *>(Yt + m * 32 + 4 * c4);
-                acc.x = fmaf(a, yv.x, acc.x);
-                acc.y = fmaf(a, yv.y, acc.y);
-                acc.z = fmaf(a, yv.z, acc.z);
-                acc.w = fmaf(a, yv.w, acc.w);
-            }
-            *reinterpret_cast<float4 *>(Mm + (32 + r) * MLD + 4 * c4) =
-                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            float *Tc = Mm + (32 + 16 * mt) * MLD + 8 * nt;
+            Tc[g * MLD + 2 * tg] = -d[0];
+            Tc[g * MLD + 2 * tg + 1] = -d[1];
+            Tc[(g + 8) * MLD + 2 * tg] = -d[2];
+            Tc[(g + 8) * MLD + 2 * tg + 1] = -d[3];
         }
         __syncthreads();
         // T' = (T - I) Diag(beta), bf16 K-major il [r][s], to the record (B of

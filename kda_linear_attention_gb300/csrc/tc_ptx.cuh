@@ -239,5 +239,18 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
     return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
 }
 
+// Warp-level D += A B on 16x8x8 tf32 tiles (fp32 accumulate), for products
+// too small for a tcgen05 tile.  Fragments (lane = 4 g + c): A row-major
+// a = {A[g][c], A[g+8][c], A[g][c+4], A[g+8][c+4]}; B (k x n) b = {B[c][g],
+// B[c+4][g]}; D d = {D[g][2c], D[g][2c+1], D[g+8][2c], D[g+8][2c+1]}.
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4],
+                                                const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 }  // namespace tc
 }  // namespace kda
