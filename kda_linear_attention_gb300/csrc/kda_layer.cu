@@ -49,14 +49,17 @@ __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
 }
 
 // ============================================================================
-// Prefill prologue.  A warp owns one (run of kRun tokens, projection p, head
-// h); lane l holds channels 4l..4l+3 and walks the run token by token with
-// the channel's window in registers, so every raw input is read once (plus a
-// three-token halo per run, mostly from L2).  Loads are issued kBatch tokens
-// at a time.  The L2 norm of a (token, head) row is a warp reduction.
+// Prefill prologue.  A half-warp owns one (run of kRun tokens, projection p,
+// head h); lane l holds channels 8l..8l+7 (16-byte accesses) and walks the run
+// token by token with the channels' windows in registers, so every raw input
+// is read once (plus a three-token halo per run, mostly from L2).  Channel
+// pairs use packed fp32x2 arithmetic; the SiLU takes one exponential and one
+// hardware reciprocal per element.  The L2 norm of a (token, head) row is a
+// reduction over the half-warp; both half-warps of a warp always take part in
+// it (they may hold different projections, or run past the end).
 // ============================================================================
 constexpr int kRun = 32;
-constexpr int kBatch = 8;
+constexpr int kBatch = 4;
 constexpr int kPrologueThreads = 256;
 
 __device__ __forceinline__ int seq_of(const int32_t *cu, int N, int t) {
@@ -70,15 +73,24 @@ __device__ __forceinline__ int seq_of(const int32_t *cu, int N, int t) {
     return lo;
 }
 
-__device__ __forceinline__ void unpack4(uint2 u, float (&x)[4]) {
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+// bf16 pair (low half = even channel) -> float2, exactly
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
 }
-__device__ __forceinline__ uint2 pack4(const float (&x)[4]) {
-    __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
-    __nv_bfloat162 b = __floats2bfloat162_rn(x[2], x[3]);
-    return make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
+__device__ __forceinline__ uint32_t f2_to_bf2(float2 v) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+// 1 / x on the hardware reciprocal (about 1 ulp); 1 / inf = 0
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+// SiLU of a channel pair: y / (1 + e^-y)
+__device__ __forceinline__ float2 silu2(float2 y) {
+    const float2 d = __fadd2_rn(make_float2(1.f, 1.f), make_float2(__expf(-y.x), __expf(-y.y)));
+    return __fmul2_rn(y, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
 }
 
 __global__ void __launch_bounds__(kPrologueThreads, 2)
@@ -103,66 +115,82 @@ conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *
         }
     }
 
-    const int lane = threadIdx.x & 31;
-    const long long wid = (long long)blockIdx.x * (kPrologueThreads / 32) + (threadIdx.x >> 5);
-    if (wid >= nruns) return;                  // whole warps leave together
-    const int h = (int)(wid % H);
-    const int p = (int)((wid / H) % 3);
-    const int j = (int)(wid / (3LL * H));
-    const int c0 = 4 * lane;
+    const int lane16 = threadIdx.x & 15;
+    const long long hw = (long long)blockIdx.x * (kPrologueThreads / 16) + (threadIdx.x >> 4);
+    const bool active = hw < nruns;
+    const long long hwc = active ? hw : 0;
+    const int h = (int)(hwc % H);
+    const int p = (int)((hwc / H) % 3);
+    const int j = (int)(hwc / (3LL * H));
+    const int c0 = 8 * lane16;
     const __nv_bfloat16 *x = p == 0 ? xq : (p == 1 ? xk : xv);
     __nv_bfloat16 *y_out = p == 0 ? q : (p == 1 ? k : v);
     const float scale = p == 0 ? q_scale : 1.f;
 
-    // taps of the 4 channels: w[c][m], tap 3 on the newest input
-    float w[4][4];
+    // taps of the channel pairs: wt[m][tap] = (w[2m][tap], w[2m+1][tap]), tap 3 on the newest input
+    float2 wt[4][4];
     {
         const float4 *wp = reinterpret_cast<const float4 *>(conv_w + (((size_t)p * H + h) * 128 + c0) * kConvK);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const float4 t4 = wp[c];
-            w[c][0] = t4.x; w[c][1] = t4.y; w[c][2] = t4.z; w[c][3] = t4.w;
+        for (int m = 0; m < 4; ++m) {
+            const float4 a = wp[2 * m], b = wp[2 * m + 1];
+            wt[m][0] = make_float2(a.x, b.x);
+            wt[m][1] = make_float2(a.y, b.y);
+            wt[m][2] = make_float2(a.z, b.z);
+            wt[m][3] = make_float2(a.w, b.w);
         }
     }
-    const int t0 = j * kRun;
+    const int t0 = active ? j * kRun : T;
     const int t_end = min(t0 + kRun, T);
     auto row = [&](int t) -> size_t { return ((size_t)t * H + h) * 128 + c0; };
     auto win_at = [&](int n, int slot) -> size_t {
         return (((size_t)n * 3 + p) * kWin + slot) * win_row + (size_t)h * 128 + c0;
     };
 
-    float win[kWin][4];
-    int n = seq_of(cu, N, t0);
-    int start = cu[n], end = cu[n + 1];
+    float2 win[kWin][4];                       // window slots (oldest first), channel pairs
+    int n = 0, start = 0, end = 0;
     // window of token tt in sequence n: the three inputs before tt, from the
     // sequence itself or (before its start) from its carried window
     auto load_window = [&](int tt) {
 #pragma unroll
-        for (int m = 0; m < kWin; ++m) {
-            const int tau = tt - kWin + m;
-            uint2 u = make_uint2(0, 0);
-            if (tau >= start) u = *reinterpret_cast<const uint2 *>(x + row(tau));
-            else if (conv_in) u = *reinterpret_cast<const uint2 *>(conv_in + win_at(n, kWin + (tau - start)));
-            unpack4(u, win[m]);
+        for (int s2 = 0; s2 < kWin; ++s2) {
+            const int tau = tt - kWin + s2;
+            uint4 u = make_uint4(0, 0, 0, 0);
+            if (tau >= start) u = *reinterpret_cast<const uint4 *>(x + row(tau));
+            else if (conv_in) u = *reinterpret_cast<const uint4 *>(conv_in + win_at(n, kWin + (tau - start)));
+            win[s2][0] = bf2_to_f2(u.x);
+            win[s2][1] = bf2_to_f2(u.y);
+            win[s2][2] = bf2_to_f2(u.z);
+            win[s2][3] = bf2_to_f2(u.w);
         }
     };
-    load_window(t0);
+    if (t0 < t_end) {
+        n = seq_of(cu, N, t0);
+        start = cu[n];
+        end = cu[n + 1];
+        load_window(t0);
+    } else {
+#pragma unroll
+        for (int s2 = 0; s2 < kWin; ++s2)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) win[s2][m] = make_float2(0.f, 0.f);
+    }
 
     const size_t rstride = (size_t)H * 128;    // elements between consecutive tokens
-    const __nv_bfloat16 *xp = x + row(t0);
-    __nv_bfloat16 *yp = y_out + row(t0);
+    const __nv_bfloat16 *xp = x + row(t0 < T ? t0 : 0);
+    __nv_bfloat16 *yp = y_out + row(t0 < T ? t0 : 0);
+#pragma unroll 1
     for (int i = 0; i < kRun; i += kBatch) {
-        if (t0 + i >= t_end) break;            // warp-uniform
-        uint2 xr[kBatch];
+        uint4 xr[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-            xr[u] = make_uint2(0, 0);
-            if (t0 + i + u < t_end) xr[u] = *reinterpret_cast<const uint2 *>(xp + (size_t)(i + u) * rstride);
+            xr[u] = make_uint4(0, 0, 0, 0);
+            if (t0 + i + u < t_end) xr[u] = *reinterpret_cast<const uint4 *>(xp + (size_t)(i + u) * rstride);
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int t = t0 + i + u;
-            const bool valid = t < t_end;      // warp-uniform
+            const bool valid = t < t_end;
             if (valid && t >= end && n < N - 1) {   // the run enters the next non-empty sequence
                 do {
                     ++n;
@@ -171,34 +199,42 @@ conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *
                 end = cu[n + 1];
                 load_window(t);
             }
-            float xn[4], z[4];
-            unpack4(xr[u], xn);
-            float ss = 0.f;
+            const float2 xn[4] = {bf2_to_f2(xr[u].x), bf2_to_f2(xr[u].y), bf2_to_f2(xr[u].z),
+                                  bf2_to_f2(xr[u].w)};
+            float2 z[4];
+            float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float y = fmaf(w[c][0], win[0][c], fmaf(w[c][1], win[1][c],
-                                fmaf(w[c][2], win[2][c], w[c][3] * xn[c])));
-                z[c] = silu(y);
-                ss = fmaf(z[c], z[c], ss);
+            for (int m = 0; m < 4; ++m) {
+                float2 y = __fmul2_rn(wt[m][3], xn[m]);
+                y = __ffma2_rn(wt[m][2], win[2][m], y);
+                y = __ffma2_rn(wt[m][1], win[1][m], y);
+                y = __ffma2_rn(wt[m][0], win[0][m], y);
+                z[m] = silu2(y);
+                ss2 = __ffma2_rn(z[m], z[m], ss2);
             }
-            if (p != 2) {                      // warp-uniform: q and k are L2-normalised
+            float ss = ss2.x + ss2.y;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                const float f = scale * rsqrtf(ss + eps);
+            for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, 16);
+            const float f = p == 2 ? 1.f : scale * rsqrtf(ss + eps);
+            const float2 f2 = make_float2(f, f);
+            uint4 out;
+            out.x = f2_to_bf2(__fmul2_rn(z[0], f2));
+            out.y = f2_to_bf2(__fmul2_rn(z[1], f2));
+            out.z = f2_to_bf2(__fmul2_rn(z[2], f2));
+            out.w = f2_to_bf2(__fmul2_rn(z[3], f2));
+            if (valid) *reinterpret_cast<uint4 *>(yp + (size_t)(i + u) * rstride) = out;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) z[c] *= f;
-            }
-            if (valid) *reinterpret_cast<uint2 *>(yp + (size_t)(i + u) * rstride) = pack4(z);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                win[0][c] = win[1][c];
-                win[1][c] = win[2][c];
-                win[2][c] = xn[c];
+            for (int m = 0; m < 4; ++m) {
+                win[0][m] = win[1][m];
+                win[1][m] = win[2][m];
+                win[2][m] = xn[m];
             }
             if (valid && t == end - 1 && conv_out) {   // the sequence's last token: its window out
 #pragma unroll
-                for (int m = 0; m < kWin; ++m)
-                    *reinterpret_cast<uint2 *>(conv_out + win_at(n, m)) = pack4(win[m]);
+                for (int s2 = 0; s2 < kWin; ++s2)
+                    *reinterpret_cast<uint4 *>(conv_out + win_at(n, s2)) =
+                        make_uint4(f2_to_bf2(win[s2][0]), f2_to_bf2(win[s2][1]), f2_to_bf2(win[s2][2]),
+                                   f2_to_bf2(win[s2][3]));
             }
         }
     }
@@ -427,7 +463,7 @@ cudaError_t launch_conv_prologue(const void *xq, const void *xk, const void *xv,
                                  const int32_t *cu_seqlens, int N, int64_t T, int H, float q_scale,
                                  float eps, cudaStream_t stream) {
     const long long nruns = ((T + kRun - 1) / kRun) * 3LL * H;
-    long long blocks = (nruns + kPrologueThreads / 32 - 1) / (kPrologueThreads / 32);
+    long long blocks = (nruns + kPrologueThreads / 16 - 1) / (kPrologueThreads / 16);
     if (blocks < 1) blocks = 1;                    // empty sequences still pass their windows on
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     conv_prologue_kernel<<<(unsigned)blocks, kPrologueThreads, 0, stream>>>(
