@@ -867,6 +867,11 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         issue_a(0);
         issue_b(0);
         if (GATED) issue_gate(0);
+        if (nch > 1) {
+            bulk_prefetch_l2(rec_at(1), REC_BYTES);
+            tma_prefetch_l2_3d(&map_v, 0, h, tok0 + C);
+            tma_prefetch_l2_3d(&map_v, 64, h, tok0 + C);
+        }
     }
     int issued_a = nch > 0, issued_b = nch > 0, issued_mma = 0;
     int issued_gate = (GATED && nch > 0) ? 1 : 0;
@@ -940,8 +945,15 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
 
         // ===== round 2: D_O += (A' U)^T, S^T += (Kbar^T U)^T (tf32, U^T from TMEM)
         if (t == 0) {
-            // round-1 operands and v are consumed: fetch the next chunk's
+            // round-1 operands and v are consumed: fetch the next chunk's, and
+            // start the chunk after it toward L2 (the records are single-
+            // buffered in shared memory; this hides most of their DRAM latency)
             if (j + 1 < nch) issue_a(j + 1);
+            if (j + 2 < nch) {
+                bulk_prefetch_l2(rec_at(j + 2), REC_BYTES);
+                tma_prefetch_l2_3d(&map_v, 0, h, tok0 + (j + 2) * C);
+                tma_prefetch_l2_3d(&map_v, 64, h, tok0 + (j + 2) * C);
+            }
             const uint32_t ido = instr_desc(kFmtTF32, 128, 64, 0, 0);
             const uint32_t ids = instr_desc(kFmtTF32, 128, 128, 0, 0);
 #pragma unroll

@@ -227,6 +227,11 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int c
                  "r"(c0), "r"(c1), "r"(c2)
                  : "memory");
 }
+// bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
