@@ -523,7 +523,8 @@ def _layer_leg(kda, torch, dev, stream, peaks):
                                   "peak": peaks["hbm"], "unit": "GB/s",
                                   "frac": round(pro_gbs / peaks["hbm"], 4),
                                   "algorithmic_bytes": int(pro_bytes),
-                                  "bytes_per_token_head": PROLOGUE_BYTES_PER_TOKEN_HEAD}},
+                                  "bytes_per_token_head": PROLOGUE_BYTES_PER_TOKEN_HEAD,
+                                  "traffic": _traffic("conv_prologue_kernel", "kda_layer.cu")}},
         "gated_prefill": {"ms": round(t_gated, 4), "ungated_ms": round(t_plain, 4),
                           "epilogue_cost": round(t_gated / t_plain - 1.0, 4)},
         "gpu_launches_per_call": 4,
@@ -561,7 +562,8 @@ def _layer_leg(kda, torch, dev, stream, peaks):
         "roofline": {"kernel": "decode_layer_kernel", "bound": "hbm", "achieved": round(gbs, 1),
                      "peak": peaks["hbm"], "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4),
                      "algorithmic_bytes": int(step_bytes),
-                     "bytes_per_state": DECODE_LAYER_BYTES_PER_STATE},
+                     "bytes_per_state": DECODE_LAYER_BYTES_PER_STATE,
+                     "traffic": _traffic("decode_layer_kernel", "kda_layer.cu")},
         "gpu_launches_per_step": 1,
     }
     return {"prefill": prefill, "decode": decode}

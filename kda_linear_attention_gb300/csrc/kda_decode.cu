@@ -19,7 +19,7 @@
 // evolve independently).  Thread t holds float4 column group t % (COLS/4) for
 // rows rg, rg + NRG, ... (rg = t / (COLS/4)), so each warp load covers whole
 // 128-bit-coalesced row segments.  Column sums are reduced across row groups
-// through shared memory.
+// through shared memory, each (component, column) sum taken by one thread.
 #include "kda_internal.h"
 
 namespace kda {
@@ -91,8 +91,8 @@ decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *_
     for (int r = 0; r < RPT; ++r) s[r] = load_state4(Su + (size_t)(rg + r * NRG) * kDV + col0);
 
     __shared__ float sq[kDK], sk[kDK], sa[kDK];
-    __shared__ float4 red_k[NRG][C4];
-    __shared__ float4 red_q[NRG][C4];
+    __shared__ float red[8][NRG][C4];            // row-group partials: k^T S (x..w), q^T S (x..w)
+    __shared__ float tot[8][C4];                 // their sums over the row groups
     __shared__ float s_qk[kDK / 32];
 
     if (t < kDK) {
@@ -118,17 +118,21 @@ decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *_
         uk.x += ki * s[r].x; uk.y += ki * s[r].y; uk.z += ki * s[r].z; uk.w += ki * s[r].w;
         uq.x += qi * s[r].x; uq.y += qi * s[r].y; uq.z += qi * s[r].z; uq.w += qi * s[r].w;
     }
-    red_k[rg][c4] = uk;
-    red_q[rg][c4] = uq;
+    // the column sums over the row groups: each of 8 * C4 threads sums one
+    // (component, column group) once, then every thread reads its 8 totals
+    red[0][rg][c4] = uk.x; red[1][rg][c4] = uk.y; red[2][rg][c4] = uk.z; red[3][rg][c4] = uk.w;
+    red[4][rg][c4] = uq.x; red[5][rg][c4] = uq.y; red[6][rg][c4] = uq.z; red[7][rg][c4] = uq.w;
     __syncthreads();
-
-    float4 Uk = red_k[0][c4], Uq = red_q[0][c4];
+    if (t < 8 * C4) {
+        const int comp = t / C4, cc = t % C4;
+        float sum = 0.f;
 #pragma unroll
-    for (int j = 1; j < NRG; ++j) {
-        const float4 a = red_k[j][c4], b = red_q[j][c4];
-        Uk.x += a.x; Uk.y += a.y; Uk.z += a.z; Uk.w += a.w;
-        Uq.x += b.x; Uq.y += b.y; Uq.z += b.z; Uq.w += b.w;
+        for (int j = 0; j < NRG; ++j) sum += red[comp][j][cc];
+        tot[comp][cc] = sum;
     }
+    __syncthreads();
+    const float4 Uk = make_float4(tot[0][c4], tot[1][c4], tot[2][c4], tot[3][c4]);
+    const float4 Uq = make_float4(tot[4][c4], tot[5][c4], tot[6][c4], tot[7][c4]);
     float qk = 0.f;
 #pragma unroll
     for (int j = 0; j < kDK / 32; ++j) qk += s_qk[j];

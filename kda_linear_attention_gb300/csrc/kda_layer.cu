@@ -326,21 +326,21 @@ decode_layer_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *_
     }
     TS *Su = S + ((size_t)slot * H + h) * kDK * kDV;
 
-    __shared__ float sq[kDK], sk[kDK], sv[kDV], sa[kDK];
+    __shared__ float sq[kDK], sk[kDK], sv[kDV], sa[kDK], sgw[kDV];
     __shared__ float s_red[2][4];
-    __shared__ float4 red_k[NRG][C4];
-    __shared__ float4 red_q[NRG][C4];
+    __shared__ float red[8][NRG][C4];           // row-group partials: k^T S (x..w), q^T S (x..w)
+    __shared__ float tot[8][C4];                // their sums over the row groups
 
     // ---- the prologue's few loads go out before the state stream: group 0
-    // q, 1 k, 2 v (raw input, window, taps), group 3 the log-decay; warp 0
-    // also fetches what its epilogue needs
+    // q, 1 k, 2 v (raw input, window, taps), group 3 the log-decay and what
+    // the epilogue needs (gate, norm weight)
     const int grp = t >> 7, c = t & 127;
     const size_t win_row = (size_t)H * 128;
     __nv_bfloat16 *wp = conv_pool + ((size_t)slot * 3 + (grp < 3 ? grp : 0)) * kWin * win_row +
                         (size_t)h * 128 + c;
     __nv_bfloat16 xb = __float2bfloat16_rn(0.f), b0 = xb, b1 = xb, b2 = xb;
     float4 tp = make_float4(0.f, 0.f, 0.f, 0.f);
-    float gl = 0.f;
+    float gl = 0.f, gt = 0.f, nw = 0.f;
     if (grp < 3) {
         const __nv_bfloat16 *x = grp == 0 ? xq : (grp == 1 ? xk : xv);
         xb = x[(size_t)unit * 128 + c];
@@ -350,12 +350,8 @@ decode_layer_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *_
         tp = *reinterpret_cast<const float4 *>(conv_w + (((size_t)grp * H + h) * 128 + c) * kConvK);
     } else {
         gl = g[(size_t)unit * kDK + c];
-    }
-    uint2 gu = make_uint2(0, 0);
-    float4 wv = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (rg == 0) {
-        gu = *reinterpret_cast<const uint2 *>(gate + (size_t)unit * kDV + col0);
-        wv = *reinterpret_cast<const float4 *>(norm_w + col0);
+        gt = __bfloat162float(gate[(size_t)unit * kDV + c]);
+        nw = norm_w[c];
     }
     const float bt = beta[unit];
 
@@ -380,6 +376,7 @@ decode_layer_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *_
             else sv[c] = z;
         } else {
             sa[c] = expf(gl);
+            sgw[c] = nw * sigmoid(gt);          // the epilogue's weight x gate
         }
         float ss = z * z;
 #pragma unroll
@@ -412,18 +409,21 @@ decode_layer_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *_
         uk.x += ki * s[r].x; uk.y += ki * s[r].y; uk.z += ki * s[r].z; uk.w += ki * s[r].w;
         uq.x += qi * s[r].x; uq.y += qi * s[r].y; uq.z += qi * s[r].z; uq.w += qi * s[r].w;
     }
-    red_k[rg][c4] = uk;
-    red_q[rg][c4] = uq;
+    // the column sums over the 16 row groups: each of 256 threads sums one
+    // (component, column group) once, then every thread reads its 8 totals
+    red[0][rg][c4] = uk.x; red[1][rg][c4] = uk.y; red[2][rg][c4] = uk.z; red[3][rg][c4] = uk.w;
+    red[4][rg][c4] = uq.x; red[5][rg][c4] = uq.y; red[6][rg][c4] = uq.z; red[7][rg][c4] = uq.w;
     __syncthreads();
-    float4 Uk = red_k[0][c4], Uq = red_q[0][c4];
+    if (t < 8 * C4) {
+        const int comp = t >> 5, cc = t & 31;
+        float sum = 0.f;
 #pragma unroll
-    for (int jj = 1; jj < NRG; ++jj) {
-        const float4 a = red_k[jj][c4], bq = red_q[jj][c4];
-        Uk.x += a.x; Uk.y += a.y; Uk.z += a.z; Uk.w += a.w;
-        Uq.x += bq.x; Uq.y += bq.y; Uq.z += bq.z; Uq.w += bq.w;
+        for (int jj = 0; jj < NRG; ++jj) sum += red[comp][jj][cc];
+        tot[comp][cc] = sum * (comp < 4 ? fk : fq);
     }
-    Uk.x *= fk; Uk.y *= fk; Uk.z *= fk; Uk.w *= fk;
-    Uq.x *= fq; Uq.y *= fq; Uq.z *= fq; Uq.w *= fq;
+    __syncthreads();
+    const float4 Uk = make_float4(tot[0][c4], tot[1][c4], tot[2][c4], tot[3][c4]);
+    const float4 Uq = make_float4(tot[4][c4], tot[5][c4], tot[6][c4], tot[7][c4]);
     float4 w;
     w.x = bt * (sv[col0 + 0] - Uk.x);
     w.y = bt * (sv[col0 + 1] - Uk.y);
@@ -446,12 +446,10 @@ decode_layer_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *_
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         const float rs = rsqrtf(ss * (1.f / 128.f) + norm_eps);
-        const float2 ga = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.x));
-        const float2 gb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.y));
-        ov.x *= rs * wv.x * sigmoid(ga.x);
-        ov.y *= rs * wv.y * sigmoid(ga.y);
-        ov.z *= rs * wv.z * sigmoid(gb.x);
-        ov.w *= rs * wv.w * sigmoid(gb.y);
+        ov.x *= rs * sgw[col0];
+        ov.y *= rs * sgw[col0 + 1];
+        ov.z *= rs * sgw[col0 + 2];
+        ov.w *= rs * sgw[col0 + 3];
         *reinterpret_cast<float4 *>(out + (size_t)unit * kDV + col0) = ov;
     }
 }
