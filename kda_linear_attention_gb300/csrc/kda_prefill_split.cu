@@ -967,11 +967,34 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         }
         issued_a += (j + 1 < nch);
         ++issued_mma;
+        // gated: while round 2 runs, each thread turns the 16 gate values of
+        // the o elements it will normalise (row rr = t / 8, columns 32 m +
+        // 4 (t % 8) .. + 3) into norm_w * sigmoid(gate), kept in registers
+        float4 gw[4];
+        if (GATED) {
+            if (!wait_all(bar_gate, par)) { failed = true; break; }
+            const int rr = t >> 3, p8 = t & 7;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int cg = (m & 1) * 4 + (p8 >> 1);          // 16-byte chunk of the gate row
+                const uint2 gu = *reinterpret_cast<const uint2 *>(
+                    sm + SB_GATE + 8192 * (m >> 1) + rr * 128 + ((cg ^ (rr & 7)) << 4) + 8 * (p8 & 1));
+                const float2 ga = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.x));
+                const float2 gb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.y));
+                const float4 wv = *reinterpret_cast<const float4 *>(s_normw + 32 * m + 4 * p8);
+                gw[m] = make_float4(wv.x * gate_sigmoid(ga.x), wv.y * gate_sigmoid(ga.y),
+                                    wv.z * gate_sigmoid(gb.x), wv.w * gate_sigmoid(gb.y));
+            }
+        }
         if (!wait_all(bar_mma, mma_phase)) { failed = true; break; }
         mma_phase ^= 1;
         tc_fence_after();
         if (t == 0 && j + 1 < nch) issue_b(j + 1);
         issued_b += (j + 1 < nch);
+        if (GATED && j + 1 < nch) {          // every thread has read this chunk's gate
+            if (t == 0) issue_gate(j + 1);
+            ++issued_gate;
+        }
 
         // ===== o = D_O + (q.k) u;  bf16 copy of the new S^T ====================
         // A full chunk of o goes out through shared memory and four TMA stores;
@@ -1013,9 +1036,9 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             }
         }
         if (GATED) {
-            // per row: RMSNorm over the 128 columns, weight, sigmoid gate.
+            // per row: RMSNorm over the 128 columns times the weighted gate.
             // Thread: row rr, columns 32 m + 4 p8 .. +3 of the four boxes m.
-            if (!wait_all(bar_gate, par)) { failed = true; break; }
+            __syncthreads();                     // every row of o is staged
             const int rr = t >> 3, p8 = t & 7;
             float4 x[4];
             float ss = 0.f;
@@ -1030,17 +1053,11 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             const float rs = rsqrtf(ss * (1.f / 128.f) + norm_eps);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                const int cg = (m & 1) * 4 + (p8 >> 1);          // 16-byte chunk of the gate row
-                const uint2 gu = *reinterpret_cast<const uint2 *>(
-                    sm + SB_GATE + 8192 * (m >> 1) + rr * 128 + ((cg ^ (rr & 7)) << 4) + 8 * (p8 & 1));
-                const float2 ga = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.x));
-                const float2 gb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.y));
-                const float4 wv = *reinterpret_cast<const float4 *>(s_normw + 32 * m + 4 * p8);
                 float4 y;
-                y.x = x[m].x * rs * wv.x * gate_sigmoid(ga.x);
-                y.y = x[m].y * rs * wv.y * gate_sigmoid(ga.y);
-                y.z = x[m].z * rs * wv.z * gate_sigmoid(gb.x);
-                y.w = x[m].w * rs * wv.w * gate_sigmoid(gb.y);
+                y.x = x[m].x * rs * gw[m].x;
+                y.y = x[m].y * rs * gw[m].y;
+                y.z = x[m].z * rs * gw[m].z;
+                y.w = x[m].w * rs * gw[m].w;
                 if (Lc == C)
                     *reinterpret_cast<float4 *>(sm + SB_O + 8192 * m + rr * 128 + 16 * p8) = y;
                 else if (rr < Lc)
@@ -1053,10 +1070,6 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
 #pragma unroll
             for (int bx = 0; bx < 4; ++bx) tma_store_3d(&map_o, sm + SB_O + 8192 * bx, 32 * bx, h, tok0 + c0);
             bulk_commit();
-        }
-        if (GATED && j + 1 < nch) {          // this chunk's gate is consumed
-            if (t == 0) issue_gate(j + 1);
-            ++issued_gate;
         }
     }
     if (t == 0) bulk_wait();                 // o stores complete before the CTA exits
