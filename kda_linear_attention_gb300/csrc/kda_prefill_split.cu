@@ -50,6 +50,34 @@ using namespace tc;
 
 constexpr int C = 64;
 
+// 1 / x on the hardware reciprocal (about 1 ulp; 1 / 0 = inf)
+__device__ __forceinline__ float rcp_fast(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+// eight bf16 (one 16-byte chunk) <-> four channel pairs
+__device__ __forceinline__ void unpack_bf8x2(uint4 u, float2 (&x)[4]) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = __bfloat1622float2(h[e]);
+}
+__device__ __forceinline__ uint4 pack_bf8x2(const float2 (&x)[4]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 hv = __floats2bfloat162_rn(x[e].x, x[e].y);
+        w[e] = *reinterpret_cast<uint32_t *>(&hv);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ void ld_f2x4(const float *p, float2 (&x)[4]) {
+    const float4 a = *reinterpret_cast<const float4 *>(p);
+    const float4 b = *reinterpret_cast<const float4 *>(p + 4);
+    x[0] = make_float2(a.x, a.y); x[1] = make_float2(a.z, a.w);
+    x[2] = make_float2(b.x, b.y); x[3] = make_float2(b.z, b.w);
+}
+
 // ---- the per-(chunk, head) record ------------------------------------------
 // Each piece is stored in the shared-memory operand layout in which the state
 // pass feeds it to the tensor cores, so that one bulk copy places it.
@@ -334,66 +362,64 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             const int r = 16 * u + rb;
             uint8_t *pq = sm + SA_X + sw_chunk(r, cc, 16384);
             uint8_t *pk = sm + SA_X + sw_chunk(64 + r, cc, 16384);
-            float qv[8], kv[8];
-            unpack_bf8(*reinterpret_cast<const uint4 *>(pq), qv);
-            unpack_bf8(*reinterpret_cast<const uint4 *>(pk), kv);
-            float G[8], xq[8], xk[8], ep[8], el[8];
-            {
-                const float4 e0 = *reinterpret_cast<const float4 *>(s_ep + u * 128 + 8 * cc);
-                const float4 e1 = *reinterpret_cast<const float4 *>(s_ep + u * 128 + 8 * cc + 4);
-                const float4 l0 = *reinterpret_cast<const float4 *>(s_el + u * 128 + 8 * cc);
-                const float4 l1 = *reinterpret_cast<const float4 *>(s_el + u * 128 + 8 * cc + 4);
-                ep[0] = e0.x; ep[1] = e0.y; ep[2] = e0.z; ep[3] = e0.w;
-                ep[4] = e1.x; ep[5] = e1.y; ep[6] = e1.z; ep[7] = e1.w;
-                el[0] = l0.x; el[1] = l0.y; el[2] = l0.z; el[3] = l0.w;
-                el[4] = l1.x; el[5] = l1.y; el[6] = l1.z; el[7] = l1.w;
-            }
-            float dot = 0.f;
+            // channel pairs in packed fp32x2 arithmetic
+            float2 qv[4], kv[4], F2[4], G2[4], xq[4], xk[4], ep[4], el[4], kg[4];
+            unpack_bf8x2(*reinterpret_cast<const uint4 *>(pq), qv);
+            unpack_bf8x2(*reinterpret_cast<const uint4 *>(pk), kv);
+            ld_f2x4(s_ep + u * 128 + 8 * cc, ep);
+            ld_f2x4(s_el + u * 128 + 8 * cc, el);
+            float2 dot2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                dot = fmaf(qv[c], kv[c], dot);
-                const float Fc = F[u][c];
-                G[c] = (Fc > 0.f) ? __fdividef(1.f, Fc) : 0.f;
-                xq[c] = qv[c] * Fc;
-                xk[c] = kv[c] * Fc;
+            for (int m = 0; m < 4; ++m) {
+                F2[m] = make_float2(F[u][2 * m], F[u][2 * m + 1]);
+                dot2 = __ffma2_rn(qv[m], kv[m], dot2);
+                G2[m] = make_float2(F2[m].x > 0.f ? rcp_fast(F2[m].x) : 0.f,
+                                    F2[m].y > 0.f ? rcp_fast(F2[m].y) : 0.f);
+                xq[m] = __fmul2_rn(qv[m], F2[m]);
+                xk[m] = __fmul2_rn(kv[m], F2[m]);
+                kg[m] = __fmul2_rn(kv[m], G2[m]);
             }
-            dqp[u] = (r < Lc) ? dot : 0.f;
+            dqp[u] = (r < Lc) ? dot2.x + dot2.y : 0.f;
             // X in place: q rows 0..63, k rows 64..127
-            *reinterpret_cast<uint4 *>(pq) = pack_bf8(xq);
-            *reinterpret_cast<uint4 *>(pk) = pack_bf8(xk);
+            *reinterpret_cast<uint4 *>(pq) = pack_bf8x2(xq);
+            *reinterpret_cast<uint4 *>(pk) = pack_bf8x2(xk);
             // Khat stack: block pp >= u holds k_s e^{sigma_pp - b_s} at row 8pp(pp+1) + s
-            float kh[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) kh[c] = kv[c] * G[c];
+            float2 kh[4] = {kg[0], kg[1], kg[2], kg[3]};
 #pragma unroll
             for (int pp = 0; pp < 4; ++pp) {
                 if (pp >= u) {
                     if (pp > u) {
-                        const float4 da = *reinterpret_cast<const float4 *>(s_dd + pp * 128 + 8 * cc);
-                        const float4 db = *reinterpret_cast<const float4 *>(s_dd + pp * 128 + 8 * cc + 4);
-                        kh[0] *= da.x; kh[1] *= da.y; kh[2] *= da.z; kh[3] *= da.w;
-                        kh[4] *= db.x; kh[5] *= db.y; kh[6] *= db.z; kh[7] *= db.w;
+                        float2 dd[4];
+                        ld_f2x4(s_dd + pp * 128 + 8 * cc, dd);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) kh[m] = __fmul2_rn(kh[m], dd[m]);
                     }
                     *reinterpret_cast<uint4 *>(sm + SA_KH + sw_chunk(8 * pp * (pp + 1) + r, cc, 20480)) =
-                        pack_bf8(kh);
+                        pack_bf8x2(kh);
                 }
             }
             // Q0 = q e^{b} -> record rows 64..127 of [-W ; Q0];  K0 = k e^{b} -> smem
-            float q0[8], k0[8];
+            {
+                float2 q0[4], k0[4];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                q0[c] = xq[c] * ep[c];
-                k0[c] = xk[c] * ep[c];
+                for (int m = 0; m < 4; ++m) {
+                    q0[m] = __fmul2_rn(xq[m], ep[m]);
+                    k0[m] = __fmul2_rn(xk[m], ep[m]);
+                }
+                *reinterpret_cast<uint4 *>(rec + R_WQ + sw_chunk(64 + r, cc, 16384)) = pack_bf8x2(q0);
+                *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, cc, 8192)) = pack_bf8x2(k0);
             }
-            *reinterpret_cast<uint4 *>(rec + R_WQ + sw_chunk(64 + r, cc, 16384)) = pack_bf8(q0);
-            *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, cc, 8192)) = pack_bf8(k0);
             // Kbar^T tf32 K-major il [i][s]: a 4x4 transpose of channel pairs
             // inside each quad of lanes (4 consecutive rows) in two butterfly
             // stages leaves every lane 4 consecutive s for channels 2bq, 2bq+1
             {
                 float kb[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) kb[c] = kv[c] * G[c] * el[c];
+                for (int m = 0; m < 4; ++m) {
+                    const float2 kb2 = __fmul2_rn(kg[m], el[m]);
+                    kb[2 * m] = kb2.x;
+                    kb[2 * m + 1] = kb2.y;
+                }
                 const int bq = rb & 3;
                 const bool b0 = (bq & 1) != 0, b1 = (bq & 2) != 0;
                 // stage 1 (lanes bq, bq^2): keep pairs 2b1, 2b1+1 of this row and
