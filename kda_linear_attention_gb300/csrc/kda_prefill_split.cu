@@ -767,9 +767,10 @@ constexpr uint32_t SB_KB = 57344;         // Kbar^T
 constexpr uint32_t SB_VEC = 90112;        // 2 x 1 KB record vectors (double-buffered)
 constexpr uint32_t SB_V = 92160;          // 16 KB: v chunk sw (TMA) = V^T, MN-major operand
 constexpr uint32_t SB_S = 108544;         // 32 KB: S^T bf16 K-major il [j][i]
-constexpr uint32_t SB_O = 141312;         // 32 KB: o chunk, 4 x [64 r][32 j] fp32 (TMA store source)
+constexpr uint32_t SB_O = 141312;         // 32 KB: o of even chunks, 4 x [64 r][32 j] fp32 (TMA store source)
 constexpr uint32_t SB_GATE = 174080;      // 16 KB: gate chunk sw (TMA; gated variant only)
-constexpr uint32_t SB_MISC = 190464;      // 3 x u64 mbarriers, TMEM base; norm weight at +64
+constexpr uint32_t SB_O1 = 190464;        // 32 KB: o of odd chunks
+constexpr uint32_t SB_MISC = 223232;      // 3 x u64 mbarriers, TMEM base; norm weight at +64
 constexpr uint32_t SMEM_B_USED = SB_MISC + 64 + 512;
 constexpr uint32_t SMEM_B_ALLOC = SMEM_B_USED + 1024;
 static_assert(SB_T == R_T && SB_A == R_A && SB_KB == R_KB, "record pieces map onto shared memory");
@@ -908,6 +909,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         const int Lc = min(C, len - c0);
         const uint32_t par = (uint32_t)(j & 1);
         const float *vec = reinterpret_cast<const float *>(sm + SB_VEC + 1024 * par);
+        const uint32_t sbo = par ? SB_O1 : SB_O;   // this chunk's o staging buffer
 
         // ===== round 1: D_U = -(W S)^T + (T' V)^T, D_O = (Q0 S)^T ============
         if (!wait_all(bar_a, par)) { failed = true; break; }
@@ -993,6 +995,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         }
         issued_a += (j + 1 < nch);
         ++issued_mma;
+        // the o buffer of this chunk was last read by the store of chunk j - 2
+        if (t == 0) bulk_wait_read_but_last();
         // gated: while round 2 runs, each thread turns the 16 gate values of
         // the o elements it will normalise (row rr = t / 8, columns 32 m +
         // 4 (t % 8) .. + 3) into norm_w * sigmoid(gate), kept in registers
@@ -1031,9 +1035,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             tmem_ld16(tmem + lane_base + TMB_O + 16 * qt, ov);
             tmem_wait_ld();
             if (GATED || Lc == C) {
-                if (t == 0) bulk_wait_read();    // the previous chunk's stores have read SB_O
-                __syncthreads();
-                float *so = reinterpret_cast<float *>(sm + SB_O + 8192 * (ch >> 5)) + (ch & 31);
+                float *so = reinterpret_cast<float *>(sm + sbo + 8192 * (ch >> 5)) + (ch & 31);
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const int r = 16 * qt + k;
@@ -1070,7 +1072,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             float ss = 0.f;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                x[m] = *reinterpret_cast<const float4 *>(sm + SB_O + 8192 * m + rr * 128 + 16 * p8);
+                x[m] = *reinterpret_cast<const float4 *>(sm + sbo + 8192 * m + rr * 128 + 16 * p8);
                 ss = fmaf(x[m].x, x[m].x, fmaf(x[m].y, x[m].y, fmaf(x[m].z, x[m].z, fmaf(x[m].w, x[m].w, ss))));
             }
             ss += __shfl_xor_sync(0xffffffffu, ss, 1);
@@ -1085,7 +1087,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                 y.z = x[m].z * rs * gw[m].z;
                 y.w = x[m].w * rs * gw[m].w;
                 if (Lc == C)
-                    *reinterpret_cast<float4 *>(sm + SB_O + 8192 * m + rr * 128 + 16 * p8) = y;
+                    *reinterpret_cast<float4 *>(sm + sbo + 8192 * m + rr * 128 + 16 * p8) = y;
                 else if (rr < Lc)
                     *reinterpret_cast<float4 *>(o + ((size_t)(tok0 + c0 + rr) * H + h) * kDV + 32 * m + 4 * p8) = y;
             }
@@ -1094,7 +1096,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         sync_tc();
         if (t == 0 && Lc == C) {
 #pragma unroll
-            for (int bx = 0; bx < 4; ++bx) tma_store_3d(&map_o, sm + SB_O + 8192 * bx, 32 * bx, h, tok0 + c0);
+            for (int bx = 0; bx < 4; ++bx) tma_store_3d(&map_o, sm + sbo + 8192 * bx, 32 * bx, h, tok0 + c0);
             bulk_commit();
         }
     }

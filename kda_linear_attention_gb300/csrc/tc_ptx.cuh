@@ -216,6 +216,10 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// The same, leaving at most the most recently committed group pending.
+__device__ __forceinline__ void bulk_wait_read_but_last() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // Wait until the bulk stores committed by this thread are complete.
 __device__ __forceinline__ void bulk_wait() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
