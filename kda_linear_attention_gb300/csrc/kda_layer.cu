@@ -29,25 +29,6 @@ constexpr int kWin = kConvK - 1;
 __device__ __forceinline__ float silu(float y) { return __fdividef(y, 1.f + __expf(-y)); }
 __device__ __forceinline__ float sigmoid(float y) { return __fdividef(1.f, 1.f + __expf(-y)); }
 
-__device__ __forceinline__ void unpack8(uint4 u, float (&x)[8]) {
-    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(h[e]);
-        x[2 * e] = f.x;
-        x[2 * e + 1] = f.y;
-    }
-}
-__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-        w[e] = *reinterpret_cast<uint32_t *>(&h);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
 // ============================================================================
 // Prefill prologue.  A half-warp owns one (run of kRun tokens, projection p,
 // head h); lane l holds channels 8l..8l+7 (16-byte accesses) and walks the run

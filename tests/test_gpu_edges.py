@@ -1,0 +1,195 @@
+"""GPU edge cases of the recurrence through the C ABI: batches of more than
+1024 sequences (the chunk plan's multi-pass scan, the state pass's identity
+order past its longest-first limit), the extreme gates g = -5 everywhere
+(largest decay-folding factors) and g = 0, and the method's degenerate
+cases: beta = 0 with g = 0 leaves the state unchanged bit for bit, and with
+beta = 1 and exactly unit-norm keys the delta rule retrieves v exactly
+(o_t = v_t when q = k), a property that needs no oracle."""
+import numpy as np
+import pytest
+
+import kda_inputs as ki
+import oracle
+from kda_testlib import TOL_BF16, TOL_F32, assert_close, dev_tensor, prefill_on_gpu, rel_err
+
+pytestmark = pytest.mark.gpu
+
+PATHS = [("bf16", 64), ("bf16", 32), ("f32", 16)]   # tensor-core path, CUDA-core paths
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from kda_linear_attention_gb300 import build
+    build.build()
+    yield
+
+
+def _tol(dtype):
+    return TOL_F32 if dtype == "f32" else TOL_BF16
+
+
+def _compare(inp, o, S, tol, what, o_bound=None):
+    """Per sequence: S_out within tol; o within tol, or element by element
+    within o_bound (an array like o) when one is given."""
+    o_ref, S_ref = oracle.prefill(inp)
+    cu = inp.cu_seqlens
+    for n in range(inp.N):
+        a, b = int(cu[n]), int(cu[n + 1])
+        if b > a:
+            if o_bound is None:
+                assert_close(o[a:b], o_ref[a:b], tol, "%s: o of sequence %d" % (what, n))
+            else:
+                err = np.abs(o[a:b] - o_ref[a:b])
+                assert np.all(err <= o_bound[a:b]), "%s: o of sequence %d beyond its bound (%.2f x)" % (
+                    what, n, float((err / o_bound[a:b]).max()))
+        assert_close(S[n], S_ref[n], tol, "%s: S_out of sequence %d" % (what, n))
+
+
+def _readout_bound(inp, tol):
+    """With beta = 0 there is no update: o_t = S_t^T q_t comes from the state
+    alone, and the tensor-core path forms that product from the bf16 copy of
+    S it keeps for its round-1 MMA (and e^{b} q in bf16).  Each product term
+    then carries at most two bf16 half-ulps (2^-8 relative), so
+    |o - o_ref|_j <= 2^-8 sum_i |q_i| |S_t,ij| (with |S_t| <= |S0| here,
+    since every decay factor is at most 1), plus the fp32 sum's rounding."""
+    q = np.abs(inp.f32("q").astype(np.float64))
+    out = np.zeros(inp.v.shape, dtype=np.float64)
+    cu = inp.cu_seqlens
+    for n in range(inp.N):
+        a, b = int(cu[n]), int(cu[n + 1])
+        if b > a:
+            out[a:b] = np.einsum("thi,hij->thj", q[a:b], np.abs(inp.S0[n].astype(np.float64)))
+    return 2.0 ** -8 * out + tol * 1e-2 * out.max()
+
+
+@pytest.mark.parametrize("dtype,chunk", [("bf16", 64), ("f32", 16)])
+def test_prefill_more_than_1024_sequences(dtype, chunk):
+    """The scheduling machinery past its limits: the chunk plan's scan in
+    several 1024-sequence passes, the state pass's identity order beyond 256
+    sequences, empty sequences among them.  Every final state is held to the
+    bar per sequence; o is held to it over the batch (the sequences are 0 to
+    40 tokens long with a carried state, and on a few of them max |o| is
+    small enough that the per-sequence ratio of the tensor-core path reaches
+    2.4e-3; the worst one is printed)."""
+    lens = ki.ragged_lens(400 + chunk, 1300, 0, 40)
+    assert 0 in lens and len(lens) > 1024
+    inp = ki.gen_prefill(401, lens, H=2, dtype=dtype, chunk=chunk, with_s0=True)
+    o, S = prefill_on_gpu(inp)
+    o_ref, S_ref = oracle.prefill(inp)
+    tol = _tol(dtype)
+    assert_close(o, o_ref, tol, "1300 sequences: o over the batch")
+    cu = inp.cu_seqlens
+    worst = 0.0
+    for n in range(inp.N):
+        a, b = int(cu[n]), int(cu[n + 1])
+        if b > a:
+            worst = max(worst, rel_err(o[a:b], o_ref[a:b]))
+        assert_close(S[n], S_ref[n], tol, "1300 sequences: S_out of sequence %d" % n)
+    print("worst per-sequence o error over 1300 sequences: %.2e" % worst)
+
+
+@pytest.mark.parametrize("dtype,chunk", PATHS)
+@pytest.mark.parametrize("gate", [-5.0, 0.0])
+def test_prefill_constant_gate_extremes(dtype, chunk, gate):
+    inp = ki.gen_prefill(410, [64, 130, 17, 1], H=3, dtype=dtype, chunk=chunk, with_s0=True)
+    inp.g[...] = np.float32(gate)
+    o, S = prefill_on_gpu(inp)
+    _compare(inp, o, S, _tol(dtype), "g = %g" % gate)
+
+
+@pytest.mark.parametrize("dtype,chunk", PATHS)
+def test_prefill_beta_zero_decays_only(dtype, chunk):
+    """beta = 0: S_T = Diag(exp(sum g)) S0.  The sequences are short enough
+    that exp(sum g) stays in fp32's normal range (sum g >= -5 T)."""
+    inp = ki.gen_prefill(420, [9, 17, 1], H=2, dtype=dtype, chunk=chunk, with_s0=True)
+    inp.beta[...] = np.float32(0.0)
+    o, S = prefill_on_gpu(inp)
+    bound = _readout_bound(inp, _tol(dtype)) if (dtype, chunk) == ("bf16", 64) else None
+    _compare(inp, o, S, _tol(dtype), "beta = 0", o_bound=bound)
+
+
+@pytest.mark.parametrize("dtype,chunk", PATHS)
+def test_prefill_no_decay_no_update_keeps_state_exactly(dtype, chunk):
+    """g = 0, beta = 0: every update is zero and every decay factor is 1, so
+    S_out equals S0 bit for bit on every path."""
+    inp = ki.gen_prefill(430, [150, 3, 64], H=2, dtype=dtype, chunk=chunk, with_s0=True)
+    inp.g[...] = np.float32(0.0)
+    inp.beta[...] = np.float32(0.0)
+    o, S = prefill_on_gpu(inp)
+    np.testing.assert_array_equal(S, inp.S0)
+    bound = _readout_bound(inp, _tol(dtype)) if (dtype, chunk) == ("bf16", 64) else None
+    _compare(inp, o, S, _tol(dtype), "g = 0, beta = 0", o_bound=bound)
+
+
+def _unit_keys(rng, T, H, dk):
+    """Keys with four entries of +-0.5 at distinct random channels: exactly
+    unit norm in bf16 and fp32."""
+    k = np.zeros((T, H, dk), dtype=np.float32)
+    for t in range(T):
+        for h in range(H):
+            idx = rng.choice(dk, 4, replace=False)
+            k[t, h, idx] = rng.choice([-0.5, 0.5], 4)
+    return k
+
+
+@pytest.mark.parametrize("dtype,chunk", PATHS)
+def test_prefill_exact_retrieval_with_unit_keys(dtype, chunk):
+    """beta = 1 and ||k_t|| = 1: S_t^T k_t = v_t after every token, so with
+    q = k the output is o_t = v_t (no oracle involved)."""
+    rng = np.random.Generator(np.random.PCG64(440))
+    lens = [130, 64, 9]
+    inp = ki.gen_prefill(441, lens, H=2, dtype=dtype, chunk=chunk, with_s0=True)
+    k = _unit_keys(rng, inp.T, inp.H, 128)
+    kk = ki.f32_to_bf16_bits(k) if dtype == "bf16" else k
+    inp.k[...] = kk
+    inp.q[...] = kk
+    inp.beta[...] = np.float32(1.0)
+    o, S = prefill_on_gpu(inp)
+    v = inp.f32("v")
+    assert_close(o, v, _tol(dtype), "o = v")
+    # and the final states retrieve the last token's v
+    cu = inp.cu_seqlens
+    for n in range(inp.N):
+        last = int(cu[n + 1]) - 1
+        got = np.einsum("hij,hi->hj", S[n].astype(np.float64), k[last].astype(np.float64))
+        assert_close(got, v[last], _tol(dtype), "S^T k = v, sequence %d" % n)
+
+
+def test_decode_no_decay_no_update_keeps_state_exactly():
+    import torch
+    import kda_linear_attention_gb300 as kda
+    rng = np.random.Generator(np.random.PCG64(450))
+    B, H = 5, 4
+    S0 = ki.gen_decode_state(rng, B, H)
+    step = ki.gen_decode_step(rng, B, H, "bf16")
+    step.g[...] = np.float32(0.0)
+    step.beta[...] = np.float32(0.0)
+    S = dev_tensor(S0)
+    d = {n: dev_tensor(getattr(step, n)) for n in ("q", "k", "v", "g", "beta")}
+    o = kda.decode_step(d["q"], d["k"], d["v"], d["g"], d["beta"], S)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(S.cpu().numpy(), S0)
+    o_ref, _ = oracle.decode(S0, step)
+    assert_close(o.cpu().numpy(), o_ref, TOL_BF16, "o = S^T q")
+
+
+def test_decode_exact_retrieval_with_unit_keys():
+    import torch
+    import kda_linear_attention_gb300 as kda
+    rng = np.random.Generator(np.random.PCG64(460))
+    B, H = 6, 3
+    S0 = ki.gen_decode_state(rng, B, H)
+    step = ki.gen_decode_step(rng, B, H, "bf16")
+    k = _unit_keys(rng, B, H, 128)
+    step.k[...] = ki.f32_to_bf16_bits(k)
+    step.q[...] = step.k
+    step.beta[...] = np.float32(1.0)
+    S = dev_tensor(S0)
+    d = {n: dev_tensor(getattr(step, n)) for n in ("q", "k", "v", "g", "beta")}
+    o = kda.decode_step(d["q"], d["k"], d["v"], d["g"], d["beta"], S)
+    torch.cuda.synchronize()
+    # fp32 arithmetic throughout: o = v to fp32 rounding
+    assert_close(o.cpu().numpy(), step.f32("v"), 1e-5, "o = v")
