@@ -160,6 +160,145 @@ decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *_
     }
 }
 
+// ----------------------------------------------------------------------------
+// bf16-stored states: the state is kept packed (two bf16 per register) from
+// the load to the store and unpacked where it is used, so a thread keeps 128
+// bytes of state in flight with 32 registers.  One block per (b, h); thread
+// t holds columns 8 (t % 16) .. + 7 of rows t / 16 + 16 r, r < 8 (a 16-byte
+// load per row).  The decay is applied twice (once for the column sums, once
+// for the update), both times from the stored values.
+// ----------------------------------------------------------------------------
+constexpr int kPackedThreads = 256;
+
+__device__ __forceinline__ void unpack8_bf16(uint4 u, float (&x)[8]) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+    }
+}
+__device__ __forceinline__ uint4 pack8_bf16(const float (&x)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        w[e] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(kPackedThreads, 3)
+decode_bf16_state_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
+                         const float *__restrict__ g, const float *__restrict__ beta,
+                         __nv_bfloat16 *__restrict__ S, float *__restrict__ o,
+                         const int32_t *__restrict__ slots, int H, int P) {
+    constexpr int C8 = 16;                       // 8-column groups
+    constexpr int NRG = kPackedThreads / C8;     // 16 row groups
+    constexpr int RPT = kDK / NRG;               // 8 rows per thread
+    const int unit = blockIdx.x;                 // b * H + h
+    const int t = threadIdx.x;
+    const int c8 = t % C8, rg = t / C8;
+    const int col0 = 8 * c8;
+
+    int slot = unit / H;
+    if (slots) {
+        slot = slots[unit / H];
+        if (slot < 0 || slot >= P) {             // padding row (or an invalid slot)
+            if (slot >= P && t == 0) atomicOr(&g_kda_decode_error, 2u);
+            if (rg == 0) {
+                float4 *op = reinterpret_cast<float4 *>(o + (size_t)unit * kDV + col0);
+                op[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                op[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            return;
+        }
+    }
+    __nv_bfloat16 *Su = S + ((size_t)slot * H + unit % H) * kDK * kDV;
+    uint4 s[RPT];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r)
+        s[r] = __ldcs(reinterpret_cast<const uint4 *>(Su + (size_t)(rg + r * NRG) * kDV + col0));
+
+    __shared__ float sq[kDK], sk[kDK], sa[kDK];
+    __shared__ float red[16][NRG][C8];           // partials: k^T S (8 columns), q^T S (8 columns)
+    __shared__ float tot[16][C8];
+    __shared__ float s_qk[kDK / 32];
+    if (t < kDK) {
+        const float qi = load_in(q, (size_t)unit * kDK + t);
+        const float ki = load_in(k, (size_t)unit * kDK + t);
+        sq[t] = qi;
+        sk[t] = ki;
+        sa[t] = expf(g[(size_t)unit * kDK + t]);
+        float pq = qi * ki;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) pq += __shfl_xor_sync(0xffffffffu, pq, off);
+        if ((t & 31) == 0) s_qk[t >> 5] = pq;
+    }
+    __syncthreads();
+
+    float uk[8], uq[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) uk[c] = uq[c] = 0.f;
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        const int i = rg + r * NRG;
+        const float a = sa[i], ki = sk[i], qi = sq[i];
+        float x[8];
+        unpack8_bf16(s[r], x);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float xd = x[c] * a;
+            uk[c] = fmaf(ki, xd, uk[c]);
+            uq[c] = fmaf(qi, xd, uq[c]);
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        red[c][rg][c8] = uk[c];
+        red[8 + c][rg][c8] = uq[c];
+    }
+    __syncthreads();
+    {
+        // 256 threads: one (component, column group) sum each
+        const int comp = t / C8, cc = t % C8;
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < NRG; ++j) sum += red[comp][j][cc];
+        tot[comp][cc] = sum;
+    }
+    __syncthreads();
+    float qk = 0.f;
+#pragma unroll
+    for (int j = 0; j < kDK / 32; ++j) qk += s_qk[j];
+    const float bt = beta[unit];
+    const size_t vo = (size_t)unit * kDV + col0;
+    float w[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) w[c] = bt * (load_in(v, vo + c) - tot[c][c8]);
+
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        const int i = rg + r * NRG;
+        const float a = sa[i], ki = sk[i];
+        float x[8];
+        unpack8_bf16(s[r], x);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) x[c] = fmaf(ki, w[c], x[c] * a);
+        __stcs(reinterpret_cast<uint4 *>(Su + (size_t)i * kDV + col0), pack8_bf16(x));
+    }
+    if (rg == 0) {
+        float ov[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) ov[c] = tot[8 + c][c8] + qk * w[c];
+        float4 *op = reinterpret_cast<float4 *>(o + vo);
+        op[0] = make_float4(ov[0], ov[1], ov[2], ov[3]);
+        op[1] = make_float4(ov[4], ov[5], ov[6], ov[7]);
+    }
+}
+
 template <typename TIn, typename TS>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *g,
                          const float *beta, void *S, float *o, const int32_t *slots, int B, int H,
@@ -188,13 +327,23 @@ cudaError_t launch_decode_pool(const void *q, const void *k, const void *v, cons
                                const float *beta, void *S_pool, bool state_bf16,
                                const int32_t *slots, int P, float *o, int B, int H, bool bf16,
                                cudaStream_t stream) {
+    if (state_bf16) {
+        // the packed kernel: one block per state
+        const long long units = (long long)B * H;
+        if (bf16)
+            decode_bf16_state_kernel<__nv_bfloat16><<<(unsigned)units, kPackedThreads, 0, stream>>>(
+                static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+                static_cast<const __nv_bfloat16 *>(v), g, beta, static_cast<__nv_bfloat16 *>(S_pool), o,
+                slots, H, P);
+        else
+            decode_bf16_state_kernel<float><<<(unsigned)units, kPackedThreads, 0, stream>>>(
+                static_cast<const float *>(q), static_cast<const float *>(k), static_cast<const float *>(v),
+                g, beta, static_cast<__nv_bfloat16 *>(S_pool), o, slots, H, P);
+        return cudaGetLastError();
+    }
     if (bf16) {
-        if (state_bf16)
-            return launch_typed<__nv_bfloat16, __nv_bfloat16>(q, k, v, g, beta, S_pool, o, slots, B, H, P, stream);
         return launch_typed<__nv_bfloat16, float>(q, k, v, g, beta, S_pool, o, slots, B, H, P, stream);
     }
-    if (state_bf16)
-        return launch_typed<float, __nv_bfloat16>(q, k, v, g, beta, S_pool, o, slots, B, H, P, stream);
     return launch_typed<float, float>(q, k, v, g, beta, S_pool, o, slots, B, H, P, stream);
 }
 
