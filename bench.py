@@ -185,6 +185,23 @@ def _gpu_hold(torch, ms: float):
     torch.cuda._sleep(int(ms * 1e-3 * 2.0e9))
 
 
+def max_over_ranks(ms: float, ws: int, device) -> float:
+    """The slowest rank's time: every rank's timed region covers the same
+    per-rank work (a replica), so the job takes as long as its slowest rank."""
+    if ws <= 1:
+        return ms
+    import torch
+    tt = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_throughput(units_per_rank: float, ws: int, ms: float) -> float:
+    """Whole-job units per second: every rank processed units_per_rank in
+    the (max-over-ranks) time ms."""
+    return ws * units_per_rank / (ms / 1e3)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -286,13 +303,9 @@ def run_ours(args):
         clk.keep_busy(step, 1)
     barrier()
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
-    if ws > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), ws, dev)
     ms_per_step = ms / args.steps
-    value = ws * T / (ms_per_step / 1e3)
+    value = job_throughput(T, ws, ms_per_step)
     kern_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in ev_pre)
     if tc_path:
         part_ms = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev_pre) for i in range(3)]
@@ -696,13 +709,9 @@ def _e2e_leg(kda, torch, dev, stream, pre, dstep, args, barrier, ws):
     b.record(s_out)
     torch.cuda.synchronize()
     barrier()
-    ms = a.elapsed_time(b) / args.steps
-    if ws > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(a.elapsed_time(b) / args.steps, ws, dev)
     tc = pre.dtype == "bf16" and pre.chunk == 64 and T > 0
-    return {"value": round(ws * T / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+    return {"value": round(job_throughput(T, ws, ms), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "pipelined": "copy-in / compute / copy-out streams, two buffer sets",
             "gpu_launches": ((3 if tc else 1) + (dstep is not None)) * args.steps}
