@@ -539,7 +539,7 @@ def _layer_leg(kda, torch, dev, stream, peaks):
                                   "bytes_per_token_head": PROLOGUE_BYTES_PER_TOKEN_HEAD,
                                   "traffic": _traffic("conv_prologue_kernel", "kda_layer.cu")}},
         "gated_prefill": {"ms": round(t_gated, 4), "ungated_ms": round(t_plain, 4),
-                          "epilogue_cost": round(t_gated / t_plain - 1.0, 4)},
+                          "epilogue_overhead_frac": round(t_gated / t_plain - 1.0, 4)},
         "gpu_launches_per_call": 4,
     }
     del L, d, q, k, v, out
@@ -612,7 +612,8 @@ def _decode_pool_leg(kda, torch, dev, stream, peaks, S32, ins, B, H):
             "state_gbs": round(state_bytes / (med / 1e3) / 1e9, 1),
             "roofline": {"bound": "hbm", "achieved": round(gbs_all, 1), "peak": peaks["hbm"],
                          "unit": "GB/s", "frac": round(gbs_all / peaks["hbm"], 4),
-                         "algorithmic_bytes": int(all_bytes)},
+                         "algorithmic_bytes": int(all_bytes),
+                         "traffic": _traffic("decode_bf16_state_kernel", "kda_decode.cu")},
             "gpu_launches": len(ins)}
 
 
