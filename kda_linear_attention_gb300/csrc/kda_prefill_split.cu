@@ -757,9 +757,15 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
 }
 
 // ============================================================================
-// state pass: one CTA (512 threads) per (sequence, head)
+// state pass: one CTA per (sequence, head), warp-specialised: 16 epilogue
+// warps (512 threads, four per TMEM lane quarter), one warp that issues the
+// MMAs and one that issues the copies, so that neither issue stream waits
+// behind the other or behind the epilogues.
 // ============================================================================
-constexpr int NTB = 512;
+constexpr int NEPI = 512;                 // epilogue threads
+constexpr int T_MMA = NEPI;               // the MMA-issuing thread (warp 16)
+constexpr int T_TMA = NEPI + 32;          // the copy-issuing thread (warp 17)
+constexpr int NTB = NEPI + 64;
 constexpr uint32_t SB_WQ = 0;             // [-W ; Q0] (bulk copy 1, with T')
 constexpr uint32_t SB_T = 32768;          // T'
 constexpr uint32_t SB_A = 40960;          // A' (bulk copy 2, with Kbar^T)
@@ -770,23 +776,52 @@ constexpr uint32_t SB_S = 108544;         // 32 KB: S^T bf16 K-major il [j][i]
 constexpr uint32_t SB_O = 141312;         // 32 KB: o of even chunks, 4 x [64 r][32 j] fp32 (TMA store source)
 constexpr uint32_t SB_GATE = 174080;      // 16 KB: gate chunk sw (TMA; gated variant only)
 constexpr uint32_t SB_O1 = 190464;        // 32 KB: o of odd chunks
-constexpr uint32_t SB_MISC = 223232;      // 3 x u64 mbarriers, TMEM base; norm weight at +64
-constexpr uint32_t SMEM_B_USED = SB_MISC + 64 + 512;
+constexpr uint32_t SB_MISC = 223232;      // 4 x u64 mbarriers, TMEM base; norm weight at +64
+constexpr uint32_t SB_EB = SB_MISC + 576; // 2 x 512 B: e^{b_L} of the chunk after next (by parity)
+constexpr uint32_t SMEM_B_USED = SB_EB + 1024;
 constexpr uint32_t SMEM_B_ALLOC = SMEM_B_USED + 1024;
 static_assert(SB_T == R_T && SB_A == R_A && SB_KB == R_KB, "record pieces map onto shared memory");
+static_assert(SB_KB == SB_A + 16384, "A' and Kbar^T form one N = 192 operand");
 static_assert(SMEM_B_ALLOC <= 232448, "dynamic shared memory limit (227 KB)");
-constexpr uint32_t TMB_S = 0;             // S^T master fp32 (lane j, column i), 128 columns
-constexpr uint32_t TMB_U = 128;           // U^T, 64 columns
-constexpr uint32_t TMB_O = 192;           // O^T, 64 columns (N = 128 with TMB_U in the first round)
+static_assert(SB_EB % 16 == 0, "bulk copy destination alignment");
+// TMEM columns: U^T | O^T | S^T master.  Round 1 writes [U | O] (N = 128),
+// round 2 accumulates [O | S] (N = 192) from the contiguous [A' ; Kbar^T].
+constexpr uint32_t TMB_U = 0;             // U^T, 64 columns
+constexpr uint32_t TMB_O = 64;            // O^T, 64 columns
+constexpr uint32_t TMB_S = 128;           // S^T master fp32 (lane j, column i), 128 columns
 constexpr uint32_t COPY1 = R_A - R_WQ;    // bytes of [-W ; Q0] + T'
 constexpr uint32_t COPY2 = R_VEC - R_A;   // bytes of A' + Kbar^T
+
+// 16 consecutive floats of a record vector (16-byte aligned) in four
+// broadcast 16-byte shared-memory loads
+__device__ __forceinline__ void ld_vec16(const float *p, float (&x)[16]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const float4 f = reinterpret_cast<const float4 *>(p)[c];
+        x[4 * c] = f.x;
+        x[4 * c + 1] = f.y;
+        x[4 * c + 2] = f.z;
+        x[4 * c + 3] = f.w;
+    }
+}
+
+// barrier among the 512 epilogue threads only
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
 // 1 / (1 + e^-x) with the fast exponential and division (a few ulp)
 __device__ __forceinline__ float gate_sigmoid(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
 // GATED: the layer's output epilogue ("Colibri Kimi K3 Metal backend",
 // section 8.4) on every row of o before it is stored: o / sqrt(mean_j o_j^2
-// + eps) * norm_w_j * sigmoid(gate_j), the gate chunk arriving by TMA beside v.
+// + eps) * norm_w_j * sigmoid(gate_j), the gate chunk arriving by TMA.
+//
+// Per chunk j (the block meets at two barriers, "mid" and "end"):
+//   MMA warp:  wait record A(j) -> round 1 | mid | wait record B(j) -> round 2 | end
+//   epilogue:  u = D_U + beta v in TMEM | mid | stage o(j-1) (gated:
+//              normalise it) while round 2 runs; o(j) into registers, bf16
+//              copy of S and S <- Diag(e^{b_L(j+1)}) S for the next chunk | end
+//   copy warp: store o(j-2), request the gate of chunk j-1; after round 1,
+//              record A(j+1) | mid | v(j+1); after round 2, record B(j+1) | end
 template <bool GATED>
 __global__ void __launch_bounds__(NTB, 1)
 state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -799,7 +834,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bar_a = reinterpret_cast<uint64_t *>(sm + SB_MISC);
     uint64_t *bar_b = bar_a + 1;
-    uint64_t *bar_mma = bar_a + 2;
+    uint64_t *bar_mma = bar_a + 2;            // round 1 completes phases of parity 0, round 2 parity 1
     uint64_t *bar_gate = bar_a + 3;           // gated variant: the gate chunk
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SB_MISC + 32);
     float *s_normw = reinterpret_cast<float *>(sm + SB_MISC + 64);
@@ -807,8 +842,9 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
 
     const int t = threadIdx.x;
     const int warp = t >> 5;
-    const int ch = t & 127;
-    const int qt = t >> 7;
+    const bool epi = t < NEPI;
+    const int ch = t & 127;                   // epilogue: TMEM lane j = ch
+    const int qt = (t >> 7) & 3;              // epilogue: column quarter
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
 
     const int h = blockIdx.x % H;
@@ -841,7 +877,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
     const uint32_t tmem = *s_tmem;
 
     // ---- initial state: S^T master in TMEM (lane j, column i) + bf16 copy
-    {
+    if (epi) {
         float sv[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -871,16 +907,21 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
     auto rec_at = [&](int j) -> const uint8_t * {
         return recs + ((size_t)(cbase + j) * H + h) * REC_BYTES;
     };
+    // record A of chunk j and e^{b_L} of chunk j + 1 (for the scaling of S at
+    // the end of chunk j), with the byte count of v, which issue_v requests
+    // once the previous chunk's v is consumed
     auto issue_a = [&](int j) {
         const uint8_t *r = rec_at(j);
-        mbar_arrive_expect_tx(bar_a, COPY1 + 1024 + 16384);
+        const bool next = j + 1 < nch;
+        mbar_arrive_expect_tx(bar_a, COPY1 + 1024 + 16384 + (next ? 512 : 0));
         bulk_load(sm + SB_WQ, r + R_WQ, COPY1, bar_a);
         bulk_load(sm + SB_VEC + 1024 * (j & 1), r + R_VEC, 1024, bar_a);
+        if (next) bulk_load(sm + SB_EB + 512 * ((j + 1) & 1), rec_at(j + 1) + R_VEC + 512, 512, bar_a);
+    };
+    auto issue_v = [&](int j) {
         tma_load_3d(sm + SB_V, &map_v, bar_a, 0, h, tok0 + j * C);
         tma_load_3d(sm + SB_V + 8192, &map_v, bar_a, 64, h, tok0 + j * C);
     };
-    // the gate chunk has a barrier of its own: it is read in the epilogue,
-    // after the next chunk's round-1 operands have been requested
     auto issue_gate = [&](int j) {
         mbar_arrive_expect_tx(bar_gate, 16384);
         tma_load_3d(sm + SB_GATE, &map_gate, bar_gate, 0, h, tok0 + j * C);
@@ -890,120 +931,49 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         mbar_arrive_expect_tx(bar_b, COPY2);
         bulk_load(sm + SB_A, rec_at(j) + R_A, COPY2, bar_b);
     };
-    if (t == 0 && nch > 0) {
+    auto prefetch2 = [&](int j) {            // chunk j toward L2
+        bulk_prefetch_l2(rec_at(j), REC_BYTES);
+        tma_prefetch_l2_3d(&map_v, 0, h, tok0 + j * C);
+        tma_prefetch_l2_3d(&map_v, 64, h, tok0 + j * C);
+    };
+    if (t == T_TMA && nch > 0) {
         issue_a(0);
+        issue_v(0);
         issue_b(0);
         if (GATED) issue_gate(0);
-        if (nch > 1) {
-            bulk_prefetch_l2(rec_at(1), REC_BYTES);
-            tma_prefetch_l2_3d(&map_v, 0, h, tok0 + C);
-            tma_prefetch_l2_3d(&map_v, 64, h, tok0 + C);
-        }
+        if (nch > 1) prefetch2(1);
     }
+    // bookkeeping of the issuing threads, which wait for everything in flight
+    // if a bounded wait gives up
     int issued_a = nch > 0, issued_b = nch > 0, issued_mma = 0;
     int issued_gate = (GATED && nch > 0) ? 1 : 0;
-    uint32_t mma_phase = 0;
+    bool bad = false;
+    float po[16];                             // epilogue: o of the previous chunk
 
-    for (int j = 0; j < nch && !failed; ++j) {
-        const int c0 = j * C;
-        const int Lc = min(C, len - c0);
-        const uint32_t par = (uint32_t)(j & 1);
-        const float *vec = reinterpret_cast<const float *>(sm + SB_VEC + 1024 * par);
-        const uint32_t sbo = par ? SB_O1 : SB_O;   // this chunk's o staging buffer
-
-        // ===== round 1: D_U = -(W S)^T + (T' V)^T, D_O = (Q0 S)^T ============
-        if (!wait_all(bar_a, par)) { failed = true; break; }
-        if (t == 0) {
-            const uint32_t id1 = instr_desc(kFmtBF16, 128, 128, 0, 0);
-            const uint32_t idv = instr_desc(kFmtBF16, 128, 64, 1, 0);
+    // stage o of chunk jp from po (gated: normalise the rows); epilogue threads
+    auto stage_o = [&](int jp) {
+        const int Lp = min(C, len - jp * C);
+        const uint32_t sbp = (jp & 1) ? SB_O1 : SB_O;
+        const size_t row0 = (size_t)(tok0 + jp * C);
+        if (GATED || Lp == C) {
+            float *so = reinterpret_cast<float *>(sm + sbp + 8192 * (ch >> 5)) + (ch & 31);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t as = smem_desc(smem_u32(sm + SB_S + 256 * kk), 128, 2048, kSwizzleNone);
-                const uint64_t bw = smem_desc(
-                    smem_u32(sm + SB_WQ + (uint32_t)(kk >> 2) * 16384 + (uint32_t)(kk & 3) * 32), 16,
-                    1024, kSwizzle128B);
-                mma_bf16_ss(tmem + TMB_U, as, bw, id1, kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t av = smem_desc(smem_u32(sm + SB_V + 2048 * kk), 8192, 1024, kSwizzle128B);
-                const uint64_t bt = smem_desc(smem_u32(sm + SB_T + 256 * kk), 128, 1024, kSwizzleNone);
-                mma_bf16_ss(tmem + TMB_U, av, bt, idv, 1);
-            }
-            mma_commit(bar_mma);
-        }
-        ++issued_mma;
-        // S <- Diag(e^{b_L}) S in TMEM while the MMAs run (they read shared memory only)
-        {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const uint32_t col = 32 * qt + 16 * hh;
-                float sv[16];
-                tmem_ld16(tmem + lane_base + TMB_S + col, sv);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 16; ++c) sv[c] *= vec[128 + col + c];
-                tmem_st16(tmem + lane_base + TMB_S + col, sv);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-        }
-        if (!wait_all(bar_mma, mma_phase)) { failed = true; break; }
-        mma_phase ^= 1;
-        tc_fence_after();
-
-        // ===== u = D_U + beta v, rounded to tf32 in place in TMEM =============
-        float uv[16];
-        {
-            tmem_ld16(tmem + lane_base + TMB_U + 16 * qt, uv);
-            tmem_wait_ld();
-            float ut[16];
+            for (int k = 0; k < 16; ++k) so[(16 * qt + k) * 32] = po[k];
+        } else {
+            // the last, partial chunk of a sequence goes out row by row so
+            // that the next sequence's rows are never written
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 const int r = 16 * qt + k;
-                uv[k] = fmaf(vec[r], bf(sm + SB_V + sw_elem64(r, ch)), uv[k]);
-                ut[k] = __uint_as_float(to_tf32(uv[k]));
+                if (r < Lp) o[((row0 + r) * H + h) * kDV + ch] = po[k];
             }
-            tmem_st16(tmem + lane_base + TMB_U + 16 * qt, ut);
-            tmem_wait_st();
         }
-        tc_fence_before();
-        if (!wait_all(bar_b, par)) { failed = true; break; }
-        tc_fence_after();
-
-        // ===== round 2: D_O += (A' U)^T, S^T += (Kbar^T U)^T (tf32, U^T from TMEM)
-        if (t == 0) {
-            // round-1 operands and v are consumed: fetch the next chunk's, and
-            // start the chunk after it toward L2 (the records are single-
-            // buffered in shared memory; this hides most of their DRAM latency)
-            if (j + 1 < nch) issue_a(j + 1);
-            if (j + 2 < nch) {
-                bulk_prefetch_l2(rec_at(j + 2), REC_BYTES);
-                tma_prefetch_l2_3d(&map_v, 0, h, tok0 + (j + 2) * C);
-                tma_prefetch_l2_3d(&map_v, 64, h, tok0 + (j + 2) * C);
-            }
-            const uint32_t ido = instr_desc(kFmtTF32, 128, 64, 0, 0);
-            const uint32_t ids = instr_desc(kFmtTF32, 128, 128, 0, 0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t ba = smem_desc(smem_u32(sm + SB_A + 256 * kk), 128, 2048, kSwizzleNone);
-                const uint64_t bk = smem_desc(smem_u32(sm + SB_KB + 256 * kk), 128, 2048, kSwizzleNone);
-                mma_tf32_ts(tmem + TMB_O, tmem + TMB_U + 8 * kk, ba, ido, 1);
-                mma_tf32_ts(tmem + TMB_S, tmem + TMB_U + 8 * kk, bk, ids, 1);
-            }
-            mma_commit(bar_mma);
-        }
-        issued_a += (j + 1 < nch);
-        ++issued_mma;
-        // the o buffer of this chunk was last read by the store of chunk j - 2
-        if (t == 0) bulk_wait_read_but_last();
-        // gated: while round 2 runs, each thread turns the 16 gate values of
-        // the o elements it will normalise (row rr = t / 8, columns 32 m +
-        // 4 (t % 8) .. + 3) into norm_w * sigmoid(gate), kept in registers
-        float4 gw[4];
         if (GATED) {
-            if (!wait_all(bar_gate, par)) { failed = true; break; }
+            // per row: RMSNorm over the 128 columns times the weighted gate.
+            // Thread: row rr, columns 32 m + 4 p8 .. +3 of the four boxes m.
             const int rr = t >> 3, p8 = t & 7;
+            float4 gw[4];
+            if (!mbar_wait(bar_gate, (uint32_t)(jp & 1), kWaitLimit)) bad = true;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int cg = (m & 1) * 4 + (p8 >> 1);          // 16-byte chunk of the gate row
@@ -1015,38 +985,169 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                 gw[m] = make_float4(wv.x * gate_sigmoid(ga.x), wv.y * gate_sigmoid(ga.y),
                                     wv.z * gate_sigmoid(gb.x), wv.w * gate_sigmoid(gb.y));
             }
+            epi_sync();                          // every row of o is staged
+            float4 x[4];
+            float ss = 0.f;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                x[m] = *reinterpret_cast<const float4 *>(sm + sbp + 8192 * m + rr * 128 + 16 * p8);
+                ss = fmaf(x[m].x, x[m].x, fmaf(x[m].y, x[m].y, fmaf(x[m].z, x[m].z, fmaf(x[m].w, x[m].w, ss))));
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+            const float rs = rsqrtf(ss * (1.f / 128.f) + norm_eps);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                float4 y;
+                y.x = x[m].x * rs * gw[m].x;
+                y.y = x[m].y * rs * gw[m].y;
+                y.z = x[m].z * rs * gw[m].z;
+                y.w = x[m].w * rs * gw[m].w;
+                if (Lp == C)
+                    *reinterpret_cast<float4 *>(sm + sbp + 8192 * m + rr * 128 + 16 * p8) = y;
+                else if (rr < Lp)
+                    *reinterpret_cast<float4 *>(o + ((row0 + rr) * H + h) * kDV + 32 * m + 4 * p8) = y;
+            }
         }
-        if (!wait_all(bar_mma, mma_phase)) { failed = true; break; }
-        mma_phase ^= 1;
-        tc_fence_after();
-        if (t == 0 && j + 1 < nch) issue_b(j + 1);
-        issued_b += (j + 1 < nch);
-        if (GATED && j + 1 < nch) {          // every thread has read this chunk's gate
-            if (t == 0) issue_gate(j + 1);
-            ++issued_gate;
+        fence_proxy_async_smem();
+    };
+    auto store_o = [&](int jp) {             // copy thread, after the barrier that follows stage_o
+        if (min(C, len - jp * C) == C) {
+            const uint32_t sbp = (jp & 1) ? SB_O1 : SB_O;
+#pragma unroll
+            for (int bx = 0; bx < 4; ++bx) tma_store_3d(&map_o, sm + sbp + 8192 * bx, 32 * bx, h, tok0 + jp * C);
+            bulk_commit();
         }
+    };
 
-        // ===== o = D_O + (q.k) u;  bf16 copy of the new S^T ====================
-        // A full chunk of o goes out through shared memory and four TMA stores;
-        // the last, partial chunk of a sequence is stored row by row so that
-        // the next sequence's rows are never written.
-        {
-            float ov[16];
-            tmem_ld16(tmem + lane_base + TMB_O + 16 * qt, ov);
-            tmem_wait_ld();
-            if (GATED || Lc == C) {
-                float *so = reinterpret_cast<float *>(sm + sbo + 8192 * (ch >> 5)) + (ch & 31);
+    for (int j = 0; j < nch; ++j) {
+        const uint32_t par = (uint32_t)(j & 1);
+        const float *vec = reinterpret_cast<const float *>(sm + SB_VEC + 1024 * par);
+
+        // ===== round 1: D_U = -(W S)^T + (T' V)^T, D_O = (Q0 S)^T ============
+        if (t == T_MMA) {
+            if (mbar_wait(bar_a, par, kWaitLimit)) {
+                tc_fence_after();
+                const uint32_t id1 = instr_desc(kFmtBF16, 128, 128, 0, 0);
+                const uint32_t idv = instr_desc(kFmtBF16, 128, 64, 1, 0);
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int r = 16 * qt + k;
-                    so[r * 32] = fmaf(vec[64 + r], uv[k], ov[k]);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t as = smem_desc(smem_u32(sm + SB_S + 256 * kk), 128, 2048, kSwizzleNone);
+                    const uint64_t bw = smem_desc(
+                        smem_u32(sm + SB_WQ + (uint32_t)(kk >> 2) * 16384 + (uint32_t)(kk & 3) * 32), 16,
+                        1024, kSwizzle128B);
+                    mma_bf16_ss(tmem + TMB_U, as, bw, id1, kk > 0);
                 }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t av = smem_desc(smem_u32(sm + SB_V + 2048 * kk), 8192, 1024, kSwizzle128B);
+                    const uint64_t bt = smem_desc(smem_u32(sm + SB_T + 256 * kk), 128, 1024, kSwizzleNone);
+                    mma_bf16_ss(tmem + TMB_U, av, bt, idv, 1);
+                }
+                mma_commit(bar_mma);
+                ++issued_mma;
             } else {
+                bad = true;
+            }
+        }
+        if (t == T_TMA) {
+            // o of chunk j - 2 was staged before the last barrier
+            if (j >= 2) store_o(j - 2);
+            // the buffer o(j - 1) is staged into was last read by the store of chunk j - 3
+            bulk_wait_read_but_last();
+            if (GATED && j >= 2) issue_gate(j - 1);
+            // once round 1 has read them: the next chunk's round-1 operands
+            if (!mbar_wait(bar_mma, 0u, kWaitLimit)) bad = true;
+            if (j + 1 < nch) issue_a(j + 1);
+        }
+        float uv[16];
+        if (epi) {
+            if (!mbar_wait(bar_a, par, kWaitLimit)) bad = true;   // vec and v of this chunk
+            __syncwarp();
+            if (j == 0) {
+                // S <- Diag(e^{b_L}) S for the first chunk (later chunks get
+                // it at the end of the chunk before)
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int r = 16 * qt + k;
-                    if (r < Lc) o[((size_t)(tok0 + c0 + r) * H + h) * kDV + ch] = fmaf(vec[64 + r], uv[k], ov[k]);
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint32_t col = 32 * qt + 16 * hh;
+                    float sv[16], eb[16];
+                    tmem_ld16(tmem + lane_base + TMB_S + col, sv);
+                    ld_vec16(vec + 128 + col, eb);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) sv[c] *= eb[c];
+                    tmem_st16(tmem + lane_base + TMB_S + col, sv);
                 }
+            }
+            // ===== u = D_U + beta v, rounded to tf32 in place in TMEM =========
+            float bt[16], vv[16];
+            ld_vec16(vec + 16 * qt, bt);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) vv[k] = bf(sm + SB_V + sw_elem64(16 * qt + k, ch));
+            if (!mbar_wait(bar_mma, 0u, kWaitLimit)) bad = true;
+            __syncwarp();
+            tc_fence_after();
+            tmem_ld16(tmem + lane_base + TMB_U + 16 * qt, uv);
+            tmem_wait_ld();
+            float ut[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                uv[k] = fmaf(bt[k], vv[k], uv[k]);
+                ut[k] = __uint_as_float(to_tf32(uv[k]));
+            }
+            tmem_st16(tmem + lane_base + TMB_U + 16 * qt, ut);
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        if (__syncthreads_or(bad)) { failed = true; break; }   // ---- mid
+        tc_fence_after();
+
+        // ===== round 2: [D_O | S^T] += U^T [A' ; Kbar^T]^T (tf32, U^T from TMEM, N = 192)
+        if (t == T_MMA) {
+            if (mbar_wait(bar_b, par, kWaitLimit)) {
+                const uint32_t id2 = instr_desc(kFmtTF32, 128, 192, 0, 0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t bak = smem_desc(smem_u32(sm + SB_A + 256 * kk), 128, 2048, kSwizzleNone);
+                    mma_tf32_ts(tmem + TMB_O, tmem + TMB_U + 8 * kk, bak, id2, 1);
+                }
+                mma_commit(bar_mma);
+                ++issued_mma;
+            } else {
+                bad = true;
+            }
+        }
+        if (t == T_TMA) {
+            // v is consumed: the next chunk's, and the chunk after it toward
+            // L2 (the records are single-buffered in shared memory)
+            if (j + 1 < nch) issue_v(j + 1);
+            if (j + 2 < nch) prefetch2(j + 2);
+            if (!mbar_wait(bar_mma, 1u, kWaitLimit)) bad = true;
+            if (j + 1 < nch) issue_b(j + 1);   // A' and Kbar^T are consumed
+        }
+        issued_a += (j + 1 < nch);
+        issued_b += (j + 1 < nch);
+        issued_gate += (GATED && j >= 2);
+
+        // ===== the previous chunk's o is staged while round 2 runs; then
+        // o = D_O + (q.k) u into registers, the bf16 copy of the new S^T, and
+        // S <- Diag(e^{b_L}) S for the next chunk
+        if (epi) {
+            if (j > 0) stage_o(j - 1);
+            float qk[16];
+            ld_vec16(vec + 64 + 16 * qt, qk);
+            const bool next = j + 1 < nch;
+            const float *ebn = reinterpret_cast<const float *>(sm + SB_EB + 512 * (par ^ 1u));
+            if (!mbar_wait(bar_mma, 1u, kWaitLimit)) bad = true;
+            __syncwarp();
+            tc_fence_after();
+            {
+                float ov[16];
+                tmem_ld16(tmem + lane_base + TMB_O + 16 * qt, ov);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 16; ++k) po[k] = fmaf(qk[k], uv[k], ov[k]);
             }
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -1061,56 +1162,47 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                     for (int u = 0; u < 8; ++u) x8[u] = sv[8 * c8 + u];
                     *reinterpret_cast<uint4 *>(sm + SB_S + km_bf16(ch, col + 8 * c8, 2048)) = pack_bf8(x8);
                 }
-            }
-        }
-        if (GATED) {
-            // per row: RMSNorm over the 128 columns times the weighted gate.
-            // Thread: row rr, columns 32 m + 4 p8 .. +3 of the four boxes m.
-            __syncthreads();                     // every row of o is staged
-            const int rr = t >> 3, p8 = t & 7;
-            float4 x[4];
-            float ss = 0.f;
+                if (next) {
+                    float eb[16];
+                    ld_vec16(ebn + col, eb);
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                x[m] = *reinterpret_cast<const float4 *>(sm + sbo + 8192 * m + rr * 128 + 16 * p8);
-                ss = fmaf(x[m].x, x[m].x, fmaf(x[m].y, x[m].y, fmaf(x[m].z, x[m].z, fmaf(x[m].w, x[m].w, ss))));
+                    for (int c = 0; c < 16; ++c) sv[c] *= eb[c];
+                    tmem_st16(tmem + lane_base + TMB_S + col, sv);
+                }
             }
-            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-            const float rs = rsqrtf(ss * (1.f / 128.f) + norm_eps);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                float4 y;
-                y.x = x[m].x * rs * gw[m].x;
-                y.y = x[m].y * rs * gw[m].y;
-                y.z = x[m].z * rs * gw[m].z;
-                y.w = x[m].w * rs * gw[m].w;
-                if (Lc == C)
-                    *reinterpret_cast<float4 *>(sm + sbo + 8192 * m + rr * 128 + 16 * p8) = y;
-                else if (rr < Lc)
-                    *reinterpret_cast<float4 *>(o + ((size_t)(tok0 + c0 + rr) * H + h) * kDV + 32 * m + 4 * p8) = y;
-            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
-        sync_tc();
-        if (t == 0 && Lc == C) {
-#pragma unroll
-            for (int bx = 0; bx < 4; ++bx) tma_store_3d(&map_o, sm + sbo + 8192 * bx, 32 * bx, h, tok0 + c0);
-            bulk_commit();
-        }
+        tc_fence_before();
+        if (__syncthreads_or(bad)) { failed = true; break; }   // ---- end
     }
-    if (t == 0) bulk_wait();                 // o stores complete before the CTA exits
+    // the last two chunks' o
+    if (!failed && nch > 0) {
+        if (t == T_TMA) {
+            if (nch >= 2) store_o(nch - 2);
+            bulk_wait_read_but_last();
+            if (GATED && nch >= 2) issue_gate(nch - 1);
+        }
+        issued_gate += (GATED && nch >= 2);
+        __syncthreads();
+        if (epi) stage_o(nch - 1);
+        if (__syncthreads_or(bad)) failed = true;
+        else if (t == T_TMA) store_o(nch - 1);
+    }
+    if (t == T_TMA) bulk_wait();             // o stores complete before the CTA exits
 
     if (failed) {
-        if (t == 0) atomicOr(&g_kda_device_error, 1u);
+        if (t == T_TMA || t == 0) atomicOr(&g_kda_device_error, 1u);
         // let copies and MMAs in flight finish (bounded) before freeing TMEM
-        if (issued_a) mbar_wait(bar_a, (uint32_t)(issued_a - 1) & 1u, kWaitLimit);
-        if (issued_b) mbar_wait(bar_b, (uint32_t)(issued_b - 1) & 1u, kWaitLimit);
-        if (issued_mma) mbar_wait(bar_mma, (uint32_t)(issued_mma - 1) & 1u, kWaitLimit);
-        if (issued_gate) mbar_wait(bar_gate, (uint32_t)(issued_gate - 1) & 1u, kWaitLimit);
-    } else {
+        if (t == T_TMA) {
+            if (issued_a) mbar_wait(bar_a, (uint32_t)(issued_a - 1) & 1u, kWaitLimit);
+            if (issued_b) mbar_wait(bar_b, (uint32_t)(issued_b - 1) & 1u, kWaitLimit);
+            if (issued_gate) mbar_wait(bar_gate, (uint32_t)(issued_gate - 1) & 1u, kWaitLimit);
+        }
+        if (t == T_MMA && issued_mma) mbar_wait(bar_mma, (uint32_t)(issued_mma - 1) & 1u, kWaitLimit);
+    } else if (epi) {
         // ---- final state: S_out[i][j] from the TMEM master (lane j, column i)
+        tc_fence_after();
         float sv[32];
         tmem_ld32(tmem + lane_base + TMB_S + 32 * qt, sv);
 #pragma unroll
