@@ -772,7 +772,7 @@ constexpr uint32_t SB_A = 40960;          // A' (bulk copy 2, with Kbar^T)
 constexpr uint32_t SB_KB = 57344;         // Kbar^T
 constexpr uint32_t SB_VEC = 90112;        // 2 x 1 KB record vectors (double-buffered)
 constexpr uint32_t SB_V = 92160;          // 16 KB: v chunk sw (TMA) = V^T, MN-major operand
-constexpr uint32_t SB_S = 108544;         // 32 KB: S^T bf16 K-major il [j][i]
+constexpr uint32_t SB_S = 108544;         // 32 KB: unused (the bf16 copy of S^T lives in TMEM)
 constexpr uint32_t SB_O = 141312;         // 32 KB: o of even chunks, 4 x [64 r][32 j] fp32 (TMA store source)
 constexpr uint32_t SB_GATE = 174080;      // 16 KB: gate chunk sw (TMA; gated variant only)
 constexpr uint32_t SB_O1 = 190464;        // 32 KB: o of odd chunks
@@ -784,11 +784,14 @@ static_assert(SB_T == R_T && SB_A == R_A && SB_KB == R_KB, "record pieces map on
 static_assert(SB_KB == SB_A + 16384, "A' and Kbar^T form one N = 192 operand");
 static_assert(SMEM_B_ALLOC <= 232448, "dynamic shared memory limit (227 KB)");
 static_assert(SB_EB % 16 == 0, "bulk copy destination alignment");
-// TMEM columns: U^T | O^T | S^T master.  Round 1 writes [U | O] (N = 128),
-// round 2 accumulates [O | S] (N = 192) from the contiguous [A' ; Kbar^T].
+// TMEM columns: U^T | O^T | S^T master | S^T bf16.  Round 1 writes [U | O]
+// (N = 128) with S^T bf16 as its A operand, round 2 accumulates [O | S]
+// (N = 192) from the contiguous [A' ; Kbar^T].
 constexpr uint32_t TMB_U = 0;             // U^T, 64 columns
 constexpr uint32_t TMB_O = 64;            // O^T, 64 columns
 constexpr uint32_t TMB_S = 128;           // S^T master fp32 (lane j, column i), 128 columns
+constexpr uint32_t TMB_SB = 256;          // S^T bf16 (lane j, column i / 2: pairs i, i + 1), 64 columns
+constexpr uint32_t TMEM_COLS_B = 512;
 constexpr uint32_t COPY1 = R_A - R_WQ;    // bytes of [-W ; Q0] + T'
 constexpr uint32_t COPY2 = R_VEC - R_A;   // bytes of A' + Kbar^T
 
@@ -820,8 +823,9 @@ __device__ __forceinline__ float gate_sigmoid(float x) { return __fdividef(1.f, 
 //   epilogue:  u = D_U + beta v in TMEM | mid | stage o(j-1) (gated:
 //              normalise it) while round 2 runs; o(j) into registers, bf16
 //              copy of S and S <- Diag(e^{b_L(j+1)}) S for the next chunk | end
-//   copy warp: store o(j-2), request the gate of chunk j-1; after round 1,
-//              record A(j+1) | mid | v(j+1); after round 2, record B(j+1) | end
+//   copy warp: request the gate of chunk j-1; after round 1, record A(j+1)
+//              | mid | v(j+1); once staged, store o(j-1); after round 2,
+//              record B(j+1) | end
 template <bool GATED>
 __global__ void __launch_bounds__(NTB, 1)
 state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -836,6 +840,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
     uint64_t *bar_b = bar_a + 1;
     uint64_t *bar_mma = bar_a + 2;            // round 1 completes phases of parity 0, round 2 parity 1
     uint64_t *bar_gate = bar_a + 3;           // gated variant: the gate chunk
+    uint64_t *bar_ost = bar_a + 5;            // o of a chunk is staged (512 arrivals)
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SB_MISC + 32);
     float *s_normw = reinterpret_cast<float *>(sm + SB_MISC + 64);
     __shared__ int s_seq;
@@ -861,12 +866,13 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         failed = true;
     }
 
-    if (warp == 0) tmem_alloc(s_tmem, 256);
+    if (warp == 0) tmem_alloc(s_tmem, TMEM_COLS_B);
     if (t == 0) {
         mbar_init(bar_a, 1);
         mbar_init(bar_b, 1);
         mbar_init(bar_mma, 1);
         mbar_init(bar_gate, 1);
+        mbar_init(bar_ost, NEPI);
         fence_mbar_init();
         prefetch_tmap(&map_v);
         prefetch_tmap(&map_o);
@@ -892,13 +898,10 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         }
         tmem_st16(tmem + lane_base + TMB_S + 32 * qt, a);
         tmem_st16(tmem + lane_base + TMB_S + 32 * qt + 16, b2);
+        float pk[16];
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-            float x8[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) x8[u] = sv[8 * c8 + u];
-            *reinterpret_cast<uint4 *>(sm + SB_S + km_bf16(ch, 32 * qt + 8 * c8, 2048)) = pack_bf8(x8);
-        }
+        for (int c = 0; c < 16; ++c) pk[c] = __uint_as_float(pack_bf2(sv[2 * c], sv[2 * c + 1]));
+        tmem_st16(tmem + lane_base + TMB_SB + 16 * qt, pk);
         tmem_wait_st();
     }
     fence_proxy_async_smem();
@@ -1033,11 +1036,10 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                 const uint32_t idv = instr_desc(kFmtBF16, 128, 64, 1, 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t as = smem_desc(smem_u32(sm + SB_S + 256 * kk), 128, 2048, kSwizzleNone);
                     const uint64_t bw = smem_desc(
                         smem_u32(sm + SB_WQ + (uint32_t)(kk >> 2) * 16384 + (uint32_t)(kk & 3) * 32), 16,
                         1024, kSwizzle128B);
-                    mma_bf16_ss(tmem + TMB_U, as, bw, id1, kk > 0);
+                    mma_bf16_ts(tmem + TMB_U, tmem + TMB_SB + 8 * kk, bw, id1, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
@@ -1052,8 +1054,6 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             }
         }
         if (t == T_TMA) {
-            // o of chunk j - 2 was staged before the last barrier
-            if (j >= 2) store_o(j - 2);
             // the buffer o(j - 1) is staged into was last read by the store of chunk j - 3
             bulk_wait_read_but_last();
             if (GATED && j >= 2) issue_gate(j - 1);
@@ -1123,6 +1123,10 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             // L2 (the records are single-buffered in shared memory)
             if (j + 1 < nch) issue_v(j + 1);
             if (j + 2 < nch) prefetch2(j + 2);
+            if (j > 0) {                     // o of the previous chunk, once staged
+                if (mbar_wait(bar_ost, (uint32_t)((j - 1) & 1), kWaitLimit)) store_o(j - 1);
+                else bad = true;
+            }
             if (!mbar_wait(bar_mma, 1u, kWaitLimit)) bad = true;
             if (j + 1 < nch) issue_b(j + 1);   // A' and Kbar^T are consumed
         }
@@ -1134,7 +1138,10 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         // o = D_O + (q.k) u into registers, the bf16 copy of the new S^T, and
         // S <- Diag(e^{b_L}) S for the next chunk
         if (epi) {
-            if (j > 0) stage_o(j - 1);
+            if (j > 0) {
+                stage_o(j - 1);
+                mbar_arrive(bar_ost);        // the copy thread stores it now
+            }
             float qk[16];
             ld_vec16(vec + 64 + 16 * qt, qk);
             const bool next = j + 1 < nch;
@@ -1149,29 +1156,24 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
 #pragma unroll
                 for (int k = 0; k < 16; ++k) po[k] = fmaf(qk[k], uv[k], ov[k]);
             }
+            {
+                float sv[32], pk[16];
+                tmem_ld32(tmem + lane_base + TMB_S + 32 * qt, sv);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const uint32_t col = 32 * qt + 16 * hh;
-                float sv[16];
-                tmem_ld16(tmem + lane_base + TMB_S + col, sv);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c8 = 0; c8 < 2; ++c8) {
-                    float x8[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) x8[u] = sv[8 * c8 + u];
-                    *reinterpret_cast<uint4 *>(sm + SB_S + km_bf16(ch, col + 8 * c8, 2048)) = pack_bf8(x8);
-                }
+                for (int c = 0; c < 16; ++c) pk[c] = __uint_as_float(pack_bf2(sv[2 * c], sv[2 * c + 1]));
+                tmem_st16(tmem + lane_base + TMB_SB + 16 * qt, pk);
                 if (next) {
-                    float eb[16];
-                    ld_vec16(ebn + col, eb);
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) sv[c] *= eb[c];
-                    tmem_st16(tmem + lane_base + TMB_S + col, sv);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float eb[16], x[16];
+                        ld_vec16(ebn + 32 * qt + 16 * hh, eb);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) x[c] = sv[16 * hh + c] * eb[c];
+                        tmem_st16(tmem + lane_base + TMB_S + 32 * qt + 16 * hh, x);
+                    }
                 }
             }
             tmem_wait_st();
-            fence_proxy_async_smem();
         }
         tc_fence_before();
         if (__syncthreads_or(bad)) { failed = true; break; }   // ---- end
@@ -1179,7 +1181,6 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
     // the last two chunks' o
     if (!failed && nch > 0) {
         if (t == T_TMA) {
-            if (nch >= 2) store_o(nch - 2);
             bulk_wait_read_but_last();
             if (GATED && nch >= 2) issue_gate(nch - 1);
         }
@@ -1212,7 +1213,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         }
     }
     sync_tc();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS_B);
 }
 
 // ---- workspace: a library-owned stream-ordered pool per device that keeps
