@@ -31,26 +31,12 @@ namespace {
 
 constexpr int kDecodeThreads = 256;
 
-// four consecutive state values <-> registers
+// four consecutive fp32 state values <-> registers (streaming)
 __device__ __forceinline__ float4 load_state4(const float *p) {
     return __ldcs(reinterpret_cast<const float4 *>(p));
 }
-__device__ __forceinline__ float4 load_state4(const __nv_bfloat16 *p) {
-    const uint2 u = __ldcs(reinterpret_cast<const uint2 *>(p));
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-    return make_float4(a.x, a.y, b.x, b.y);
-}
 __device__ __forceinline__ void store_state4(float *p, float4 x) {
     __stcs(reinterpret_cast<float4 *>(p), x);
-}
-__device__ __forceinline__ void store_state4(__nv_bfloat16 *p, float4 x) {
-    const __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y);
-    const __nv_bfloat162 b = __floats2bfloat162_rn(x.z, x.w);
-    uint2 u;
-    u.x = *reinterpret_cast<const uint32_t *>(&a);
-    u.y = *reinterpret_cast<const uint32_t *>(&b);
-    __stcs(reinterpret_cast<uint2 *>(p), u);
 }
 
 template <typename TIn, typename TS, int COLS>

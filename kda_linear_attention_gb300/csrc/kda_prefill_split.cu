@@ -772,7 +772,7 @@ constexpr uint32_t SB_A = 40960;          // A' (bulk copy 2, with Kbar^T)
 constexpr uint32_t SB_KB = 57344;         // Kbar^T
 constexpr uint32_t SB_VEC = 90112;        // 2 x 1 KB record vectors (double-buffered)
 constexpr uint32_t SB_V = 92160;          // 16 KB: v chunk sw (TMA) = V^T, MN-major operand
-constexpr uint32_t SB_S = 108544;         // 32 KB: unused (the bf16 copy of S^T lives in TMEM)
+                                          // 108544..141312 free: the bf16 copy of S^T lives in TMEM
 constexpr uint32_t SB_O = 141312;         // 32 KB: o of even chunks, 4 x [64 r][32 j] fp32 (TMA store source)
 constexpr uint32_t SB_GATE = 174080;      // 16 KB: gate chunk sw (TMA; gated variant only)
 constexpr uint32_t SB_O1 = 190464;        // 32 KB: o of odd chunks
