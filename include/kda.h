@@ -161,6 +161,36 @@ int kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v,
                                 int dtype, void *stream);
 
 /*
+ * Bytes of caller-owned workspace that kda_prefill_chunked_ws needs for these
+ * sizes: the records of the tensor-core path (bf16, chunk 64, T > 0),
+ * 1024 * ceil(4 (N + 1) / 1024) + (ceil(T / 64) + N) * H * 91136; 0 for every
+ * other combination (the CUDA-core kernel needs none) and for invalid sizes.
+ * Host-only, no CUDA call.
+ */
+size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chunk, int dtype);
+
+/*
+ * kda_prefill_chunked with a workspace the caller owns (for instance a
+ * buffer from the caller's own allocator), so that the library allocates
+ * nothing.  Same operation, arguments, layouts and results as
+ * kda_prefill_chunked, plus:
+ *   workspace  device memory of ws_bytes bytes, 256-byte aligned
+ *              (KDA_ERR_ALIGN otherwise), read and written by the call's
+ *              kernels on `stream` (the caller keeps it alive and unshared
+ *              until they finish); NULL is accepted where
+ *              kda_prefill_workspace_bytes gives 0
+ *   ws_bytes   at least kda_prefill_workspace_bytes(...) (KDA_ERR_WORKSPACE
+ *              otherwise, before anything is launched)
+ * Nothing in the workspace has to be initialised or cleared between calls.
+ * Returns KDA_OK or a kda_status_t.
+ */
+int kda_prefill_chunked_ws(const void *q, const void *k, const void *v,
+                           const float *g, const float *beta, const float *S0,
+                           float *o, float *S_out, const int32_t *cu_seqlens,
+                           int N, int64_t T, int H, int dk, int dv, int chunk,
+                           int dtype, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * One decode token for each of B sequences, state updated IN PLACE.
  *
  * Operation: the recurrence above applied once per (b, h) with

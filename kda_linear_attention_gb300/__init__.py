@@ -8,6 +8,8 @@ calls raise if the library has not been built.
 
     o, S_out = prefill_chunked(q, k, v, g, beta, cu_seqlens, S0=None, chunk=64)
     o, S_out = prefill_chunked_noalloc(...)      # same, no device allocation
+    ws = torch.empty(prefill_workspace_bytes(N, T, H), dtype=torch.uint8, device="cuda")
+    o, S_out = prefill_chunked(..., workspace=ws) # same, in a workspace the caller owns
     o = decode_step(q, k, v, g, beta, S)          # S updated in place
 
 The layer around the recurrence (conv1d + SiLU + L2 norm before it, gated
@@ -29,7 +31,8 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["prefill_chunked", "prefill_chunked_noalloc", "prefill_chunked_events", "decode_step",
+__all__ = ["prefill_chunked", "prefill_chunked_noalloc", "prefill_chunked_events",
+           "prefill_workspace_bytes", "decode_step",
            "decode_step_pool", "conv_prologue", "prefill_chunked_gated", "prefill_layer",
            "decode_layer_step", "device_error", "lib",
            "KDAError", "KDA_BF16", "KDA_F32", "library_path"]
@@ -77,6 +80,11 @@ def lib() -> ctypes.CDLL:
         L.kda_prefill_chunked_events.argtypes = L.kda_prefill_chunked.argtypes + [
             ctypes.POINTER(ctypes.c_void_p)]
         L.kda_prefill_chunked_events.restype = i32
+        L.kda_prefill_chunked_ws.argtypes = L.kda_prefill_chunked.argtypes[:-1] + [
+            vp, ctypes.c_size_t, vp]
+        L.kda_prefill_chunked_ws.restype = i32
+        L.kda_prefill_workspace_bytes.argtypes = [i32, i64, i32, i32, i32, i32, i32]
+        L.kda_prefill_workspace_bytes.restype = ctypes.c_size_t
         L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
         L.kda_decode_step.restype = i32
         L.kda_decode_step_pool.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32,
@@ -129,7 +137,7 @@ def _stream(device: torch.device, stream) -> ctypes.c_void_p:
 
 
 def _prefill(fn_name: str, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_out, stream, extra=(),
-             gated=None):
+             gated=None, ws=None):
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("inputs must be CUDA tensors")
@@ -155,6 +163,10 @@ def _prefill(fn_name: str, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_out, st
         rc = getattr(lib(), fn_name)(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(gate),
                                      _p(norm_w), float(eps), _p(o), _p(S_out), _p(cu_seqlens), N,
                                      T, H, DK, DV, int(chunk), dt, _stream(dev, stream))
+    elif ws is not None:
+        rc = getattr(lib(), fn_name)(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(o),
+                                     _p(S_out), _p(cu_seqlens), N, T, H, DK, DV, int(chunk), dt,
+                                     ws[0], ctypes.c_size_t(ws[1]), _stream(dev, stream))
     else:
         rc = getattr(lib(), fn_name)(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(o),
                                      _p(S_out), _p(cu_seqlens), N, T, H, DK, DV, int(chunk), dt,
@@ -164,16 +176,33 @@ def _prefill(fn_name: str, q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_out, st
     return o, S_out
 
 
+def prefill_workspace_bytes(N: int, T: int, H: int, chunk: int = 64, dtype: int = None) -> int:
+    """Bytes of workspace ``prefill_chunked(..., workspace=...)`` needs
+    (``kda_prefill_workspace_bytes``); 0 where the call needs none."""
+    dt = KDA_BF16 if dtype is None else int(dtype)
+    return int(lib().kda_prefill_workspace_bytes(int(N), int(T), int(H), DK, DV, int(chunk), dt))
+
+
 def prefill_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
                     beta: torch.Tensor, cu_seqlens: torch.Tensor,
                     S0: Optional[torch.Tensor] = None, chunk: int = 64,
                     o: Optional[torch.Tensor] = None, S_out: Optional[torch.Tensor] = None,
-                    stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+                    stream: Optional[torch.cuda.Stream] = None,
+                    workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Chunked KDA prefill over packed varlen sequences (``kda_prefill_chunked``).
 
     Returns (o [T, H, 128] fp32, S_out [N, H, 128, 128] fp32).  ``S_out`` may
-    be ``S0`` itself to update the states in place.
+    be ``S0`` itself to update the states in place.  With ``workspace`` (a
+    contiguous CUDA tensor of at least ``prefill_workspace_bytes`` bytes) the
+    call runs in that buffer (``kda_prefill_chunked_ws``) instead of the
+    library's own pool.
     """
+    if workspace is not None:
+        if workspace.device != q.device or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+        nbytes = workspace.numel() * workspace.element_size()
+        return _prefill("kda_prefill_chunked_ws", q, k, v, g, beta, cu_seqlens, S0, chunk, o,
+                        S_out, stream, ws=(_p(workspace), nbytes))
     return _prefill("kda_prefill_chunked", q, k, v, g, beta, cu_seqlens, S0, chunk, o, S_out,
                     stream)
 

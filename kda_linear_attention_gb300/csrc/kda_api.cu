@@ -104,6 +104,41 @@ int kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v, con
                                                 chunk, dtype == KDA_BF16, s));
 }
 
+size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chunk, int dtype) {
+    if (dtype != KDA_BF16 && dtype != KDA_F32) return 0;
+    if (dk != kda::kDK || dv != kda::kDV || N < 1 || H < 1 || T <= 0 || T >= (int64_t(1) << 31))
+        return 0;
+    if (dtype != KDA_BF16 || chunk != 64) return 0;
+    return kda::prefill_split_workspace_bytes(N, T, H);
+}
+
+int kda_prefill_chunked_ws(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, const float *S0, float *o, float *S_out,
+                           const int32_t *cu_seqlens, int N, int64_t T, int H, int dk, int dv,
+                           int chunk, int dtype, void *workspace, size_t ws_bytes, void *stream) {
+    if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_DTYPE;
+    if (dk != kda::kDK || dv != kda::kDV || N < 1 || H < 1 || T < 0 || T >= (int64_t(1) << 31))
+        return KDA_ERR_DIM;
+    if ((int64_t)N * H * (kda::kDV / 32) >= (int64_t(1) << 31)) return KDA_ERR_DIM;
+    if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_CHUNK;
+    if (!S_out || !cu_seqlens) return KDA_ERR_NULL;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_NULL;
+    const void *ptrs[] = {q, k, v, g, beta, S0, o, S_out, cu_seqlens};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == KDA_BF16 && chunk == 64 && T > 0) {
+        const size_t need = kda::prefill_split_workspace_bytes(N, T, H);
+        if (!workspace || ws_bytes < need) return KDA_ERR_WORKSPACE;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KDA_ERR_ALIGN;
+        return cuda_status(kda::launch_prefill_split_ws(q, k, v, g, beta, S0, o, S_out, cu_seqlens,
+                                                        N, T, H, workspace, s));
+    }
+    // the CUDA-core kernel needs no workspace
+    return cuda_status(kda::launch_prefill_simt(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, H,
+                                                chunk, dtype == KDA_BF16, s));
+}
+
 int kda_decode_step(const void *q, const void *k, const void *v, const float *g,
                     const float *beta, float *S_inout, float *o, int B, int H, int dk, int dv,
                     int dtype, void *stream) {

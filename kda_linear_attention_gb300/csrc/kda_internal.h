@@ -53,6 +53,14 @@ cudaError_t launch_prefill_split_noalloc(const void *q, const void *k, const voi
                                          float *o, float *S_out, const int32_t *cu_seqlens, int N,
                                          int64_t T, int H, cudaStream_t stream);
 
+// The same prefill with a workspace the caller owns (at least
+// prefill_split_workspace_bytes(N, T, H) bytes, 256-byte aligned); nothing is
+// allocated and nothing in it has to be cleared between calls.
+cudaError_t launch_prefill_split_ws(const void *q, const void *k, const void *v, const float *g,
+                                    const float *beta, const float *S0, float *o, float *S_out,
+                                    const int32_t *cu_seqlens, int N, int64_t T, int H, void *ws,
+                                    cudaStream_t stream);
+
 // Read (and optionally clear) the device-side error word that the
 // tensor-core kernels set when a bounded wait gives up.
 cudaError_t read_device_error(unsigned int *code, bool reset);

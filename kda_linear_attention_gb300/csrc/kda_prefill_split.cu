@@ -1363,6 +1363,14 @@ std::mutex g_scratch_mu;
 void *g_scratch_addr[kMaxDevices] = {};
 }  // namespace
 
+cudaError_t launch_prefill_split_ws(const void *q, const void *k, const void *v, const float *g,
+                                    const float *beta, const float *S0, float *o, float *S_out,
+                                    const int32_t *cu_seqlens, int N, int64_t T, int H, void *ws,
+                                    cudaStream_t stream) {
+    if (!grid_fits(N, T, H) || !ws) return cudaErrorInvalidValue;
+    return run_split(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, T, H, ws, stream);
+}
+
 cudaError_t launch_prefill_split_noalloc(const void *q, const void *k, const void *v,
                                          const float *g, const float *beta, const float *S0,
                                          float *o, float *S_out, const int32_t *cu_seqlens, int N,

@@ -111,6 +111,45 @@ def test_prefill_variants_reject_bad_arguments(L, fn, kw, status):
     assert getattr(L, fn)(*args) == status
 
 
+def _prefill_ws(L, ws=GOOD, ws_bytes=None, **kw):
+    a = dict(q=GOOD, k=GOOD, v=GOOD, g=GOOD, beta=GOOD, S0=None, o=GOOD, S_out=GOOD, cu=GOOD,
+             N=1, T=64, H=2, dk=128, dv=128, chunk=64, dtype=0, stream=None)
+    a.update(kw)
+    if ws_bytes is None:
+        ws_bytes = L.kda_prefill_workspace_bytes(a["N"], a["T"], a["H"], a["dk"], a["dv"],
+                                                 a["chunk"], a["dtype"])
+    return L.kda_prefill_chunked_ws(a["q"], a["k"], a["v"], a["g"], a["beta"], a["S0"], a["o"],
+                                    a["S_out"], a["cu"], a["N"], a["T"], a["H"], a["dk"], a["dv"],
+                                    a["chunk"], a["dtype"], ws, ctypes.c_size_t(ws_bytes),
+                                    a["stream"])
+
+
+def test_prefill_workspace_bytes(L):
+    """The caller-owned workspace of the tensor-core path: the chunk-offset
+    table (4 (N + 1) bytes rounded up to 1 KB) and one 91,136-byte record per
+    (chunk, head), with one spare chunk per sequence for a partial tail; no
+    workspace for the CUDA-core path or for invalid sizes."""
+    for N, T, H in [(1, 64, 2), (1, 4096, 96), (3, 130, 5), (300, 4096, 4)]:
+        want = 1024 * (-(-4 * (N + 1) // 1024)) + (-(-T // 64) + N) * H * 91136
+        assert L.kda_prefill_workspace_bytes(N, T, H, 128, 128, 64, 0) == want
+    assert L.kda_prefill_workspace_bytes(1, 64, 2, 128, 128, 64, 1) == 0    # fp32 inputs
+    assert L.kda_prefill_workspace_bytes(1, 64, 2, 128, 128, 32, 0) == 0    # chunk 32
+    assert L.kda_prefill_workspace_bytes(1, 0, 2, 128, 128, 64, 0) == 0     # no tokens
+    assert L.kda_prefill_workspace_bytes(0, 64, 2, 128, 128, 64, 0) == 0    # no sequences
+    assert L.kda_prefill_workspace_bytes(1, 64, 2, 64, 128, 64, 0) == 0     # unsupported dk
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=64), 2), (dict(N=0), 2), (dict(chunk=48), 3), (dict(dtype=7), 5),
+    (dict(q=None), 1), (dict(S_out=None), 1), (dict(q=ctypes.c_void_p(0x10004)), 4),
+    (dict(ws=None), 6),                                  # the tensor-core path needs one
+    (dict(ws_bytes=1024), 6),                            # too small
+    (dict(ws=ctypes.c_void_p(0x10010)), 4),              # not 256-byte aligned
+])
+def test_prefill_ws_rejects_bad_arguments(L, kw, status):
+    assert _prefill_ws(L, **kw) == status
+
+
 def test_prefill_events_needs_events_and_the_tensor_core_path(L):
     def call(evs, dtype=0, chunk=64):
         return L.kda_prefill_chunked_events(GOOD, GOOD, GOOD, GOOD, GOOD, None, GOOD, GOOD, GOOD,
