@@ -146,6 +146,32 @@ def test_gated_prefill_ragged(dtype, chunk, with_s0):
         assert_close(S[n], S_ref[n], tol, "S_out, sequence %d" % n)
 
 
+@pytest.mark.parametrize("dtype,chunk", [("bf16", 64), ("f32", 16)])
+def test_gated_prefill_saturated_gates(dtype, chunk):
+    """Gates far in both tails: sigmoid saturates to 1 or underflows to 0
+    (e^{-x} overflows), and a zero weight silences its channel."""
+    lens = [70, 64, 5]
+    inp = ki.gen_prefill(120 + chunk, lens, H=2, dtype=dtype, chunk=chunk, with_s0=True)
+    rng = np.random.Generator(np.random.PCG64(121))
+    vals = np.array([-200.0, -90.0, -20.0, -1.0, 0.0, 1.0, 20.0, 90.0, 200.0], np.float32)
+    gate = ki.f32_to_bf16_bits(rng.choice(vals, size=(inp.T, 2, 128)).astype(np.float32))
+    norm_w = (1.0 + 0.1 * rng.standard_normal(128)).astype(np.float32)
+    norm_w[::7] = 0.0
+    out, S = _gated_gpu(inp, gate, norm_w, chunk)
+    assert np.isfinite(out).all()
+    assert (out[:, :, ::7] == 0).all()
+    o_ref, S_ref = oracle.prefill(inp)
+    gf = olayer._f64(gate)
+    out_ref = olayer.gated_rmsnorm(o_ref, gf, norm_w)
+    tol = TOL_F32 if dtype == "f32" else TOL_BF16
+    cu = inp.cu_seqlens
+    for n in range(inp.N):
+        a, b = int(cu[n]), int(cu[n + 1])
+        assert_gated_close(out[a:b], out_ref[a:b], o_ref[a:b], gf[a:b], norm_w, tol,
+                           "gated out, sequence %d" % n)
+        assert_close(S[n], S_ref[n], tol, "S_out, sequence %d" % n)
+
+
 def test_gated_prefill_4k_full():
     """The full 4K bf16 prefill (H = 96, chunk 64), every output."""
     inp = ki.workload_prefill("prefill_4k")
