@@ -57,18 +57,27 @@ DECODE_BYTES_PER_STATE = 2 * STATE_BYTES + 3 * 256 + 512 + 4 + 512
 FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12   # fp32 FMA lanes x 2 flop x max SM clock
 
 
+def code_sha(source_file):
+    """sha256 prefix of a kernel source's code: comments removed and
+    whitespace collapsed, so that edits to comments keep a capture valid."""
+    import hashlib
+    import re
+    src = open(os.path.join(ROOT, "kda_linear_attention_gb300", "csrc", source_file)).read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return hashlib.sha256(" ".join(src.split()).encode()).hexdigest()[:16]
+
+
 def _traffic(kernel, source_file):
     """DRAM bytes per launch from profiles/dram_traffic.md, if that capture was
-    taken on the current kernel source (sha256 prefix), else None."""
-    import hashlib
+    taken on the current kernel code (code_sha), else None."""
     try:
-        src = os.path.join(ROOT, "kda_linear_attention_gb300", "csrc", source_file)
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        sha = code_sha(source_file)
         for line in open(os.path.join(ROOT, "profiles", "dram_traffic.md")):
             f = line.split()
             if len(f) >= 4 and f[0] == "traffic:" and f[1] == kernel:
                 kv = dict(x.split("=", 1) for x in f[2:] if "=" in x)
-                if kv.get("sha256") == sha:
+                if kv.get("code_sha256") == sha:
                     return int(kv["bytes"])
     except Exception:
         pass

@@ -776,7 +776,7 @@ constexpr uint32_t SB_V = 92160;          // 16 KB: v chunk sw (TMA) = V^T, MN-m
 constexpr uint32_t SB_O = 141312;         // 32 KB: o of even chunks, 4 x [64 r][32 j] fp32 (TMA store source)
 constexpr uint32_t SB_GATE = 174080;      // 16 KB: gate chunk sw (TMA; gated variant only)
 constexpr uint32_t SB_O1 = 190464;        // 32 KB: o of odd chunks
-constexpr uint32_t SB_MISC = 223232;      // 4 x u64 mbarriers, TMEM base; norm weight at +64
+constexpr uint32_t SB_MISC = 223232;      // mbarriers at +0, +8, +16, +24, +40; TMEM base at +32; norm weight at +64
 constexpr uint32_t SB_EB = SB_MISC + 576; // 2 x 512 B: e^{b_L} of the chunk after next (by parity)
 constexpr uint32_t SMEM_B_USED = SB_EB + 1024;
 constexpr uint32_t SMEM_B_ALLOC = SMEM_B_USED + 1024;
