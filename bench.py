@@ -422,6 +422,7 @@ def _decode_leg(kda, torch, dev, stream, peaks, args):
     B, H, n_steps = w["B"], w["H"], w["steps"]
     S_np, steps = ki.workload_decode("decode_b64")
     S = _to_dev(S_np, dev)
+    cpu = None if args.no_cpu_baseline else _decode_cpu_baseline(S_np, steps[0], B, H)
     del S_np
     ins = [{n: _to_dev(getattr(st, n), dev) for n in ("q", "k", "v", "g", "beta")} for st in steps]
     o = torch.empty((B, H, DV), dtype=torch.float32, device=dev)
@@ -470,8 +471,34 @@ def _decode_leg(kda, torch, dev, stream, peaks, args):
                      "algorithmic_bytes": int(all_bytes)},
         "gpu_launches": n_steps,
         "clocks": clk.summary(),
+        "cpu_baseline": cpu,
         "pool_bf16": _decode_pool_leg(kda, torch, dev, stream, peaks, S, ins, B, H),
     }
+
+
+def _decode_cpu_baseline(S_np, step, B, H):
+    """The fp64 oracle on one whole decode step (every state), timed on the
+    host cores, in the decode metric (state bytes read and written / s)."""
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    oracle.decode(S_np[:1], _first_rows(step, 1), threads=threads)     # warm
+    t = time.perf_counter()
+    oracle.decode(S_np, step, threads=threads)
+    dt = time.perf_counter() - t
+    state_bytes = 2 * STATE_BYTES * B * H
+    return {"value": round(state_bytes / dt / 1e9, 3), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": "one whole decode step (%d states) of the fp64 oracle, %.2f s" % (B * H, dt)}
+
+
+def _first_rows(step, b):
+    """The first b sequences of a decode step (same type, sliced fields)."""
+    import copy
+    st = copy.copy(step)
+    for n in ("q", "k", "v", "g", "beta"):
+        setattr(st, n, getattr(step, n)[:b])
+    return st
 
 
 def _timed(torch, stream, fn, reps=10, warm=3):
