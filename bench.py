@@ -25,6 +25,7 @@ sample of the same workload and prints the same line with "impl": "reference".
 from __future__ import annotations
 
 import argparse
+import itertools
 import json
 import os
 import statistics
@@ -422,9 +423,12 @@ def _decode_leg(kda, torch, dev, stream, peaks, args):
     B, H, n_steps = w["B"], w["H"], w["steps"]
     S_np, steps = ki.workload_decode("decode_b64")
     S = _to_dev(S_np, dev)
-    cpu = None if args.no_cpu_baseline else _decode_cpu_baseline(S_np, steps[0], B, H)
+    steps = iter(steps)
+    first = next(steps)
+    cpu = None if args.no_cpu_baseline else _decode_cpu_baseline(S_np, first, B, H)
     del S_np
-    ins = [{n: _to_dev(getattr(st, n), dev) for n in ("q", "k", "v", "g", "beta")} for st in steps]
+    ins = [{n: _to_dev(getattr(st, n), dev) for n in ("q", "k", "v", "g", "beta")}
+           for st in itertools.chain([first], steps)]
     o = torch.empty((B, H, DV), dtype=torch.float32, device=dev)
     for i in range(3):
         x = ins[i]
