@@ -1100,7 +1100,13 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             tmem_wait_st();
         }
         tc_fence_before();
-        if (__syncthreads_or(bad)) { failed = true; break; }   // ---- mid
+        if (__syncthreads_or(bad)) {                            // ---- mid
+            // the copy thread has already requested this chunk's record A and gate
+            issued_a += (j + 1 < nch);
+            issued_gate += (GATED && j >= 2);
+            failed = true;
+            break;
+        }
         tc_fence_after();
 
         // ===== round 2: [D_O | S^T] += U^T [A' ; Kbar^T]^T (tf32, U^T from TMEM, N = 192)
