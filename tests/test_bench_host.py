@@ -3,7 +3,6 @@ recorded DRAM traffic (insensitive to comments and whitespace, sensitive to
 code), the traffic lookup, and the decode leg's CPU baseline on a small step
 taken from a generator the way the leg takes it."""
 import itertools
-import os
 
 import numpy as np
 

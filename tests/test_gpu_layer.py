@@ -10,7 +10,7 @@ import kda_inputs as ki
 import oracle
 from oracle import layer as olayer
 
-from kda_testlib import TOL_BF16, TOL_F32, assert_close, dev_tensor, rel_err
+from kda_testlib import TOL_BF16, TOL_F32, assert_close, dev_tensor
 
 pytestmark = pytest.mark.gpu
 

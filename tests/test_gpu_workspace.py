@@ -3,7 +3,6 @@ torch tensor here).  It must match the pool-backed entry point on the same
 inputs, need no clearing between calls (the buffer starts as 0xFF bytes and
 is reused), and work for the CUDA-core configurations that need no
 workspace at all; the oracle ties the results to the method."""
-import numpy as np
 import pytest
 
 import kda_inputs as ki
