@@ -16,11 +16,13 @@
  * Conventions shared by every call
  *   - Pointers are DEVICE pointers unless marked "host"; the caller owns all
  *     memory it passes.  The tensor-core prefill (bf16, chunk 64) also needs
- *     a scratch workspace of about 89 KB per (64-token chunk, head); it takes
- *     it from a library-owned stream-ordered memory pool on the current
- *     device, which keeps that memory for later calls.  That pool and the
- *     device error word (kda_device_error) are the library's only global
- *     state.
+ *     a scratch workspace of about 89 KB per (64-token chunk, head):
+ *     kda_prefill_chunked takes it from a library-owned stream-ordered memory
+ *     pool on the current device, which keeps that memory for later calls;
+ *     kda_prefill_chunked_ws runs in a buffer the caller passes, and
+ *     kda_prefill_chunked_noalloc in a fixed array in the library's device
+ *     image.  That pool, that array and the device error word
+ *     (kda_device_error) are the library's only global state.
  *   - Layouts are token-major and dense (C order):
  *         q, k, g : [T, H, dk]      v, o : [T, H, dv]      beta : [T, H]
  *         S       : [N, H, dk, dv]  with S[n][h][i][j], i = key channel,
@@ -56,7 +58,7 @@ typedef enum {
     KDA_ERR_CHUNK = 3,       /* chunk not in {16, 32, 64} */
     KDA_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
     KDA_ERR_DTYPE = 5,       /* dtype not a kda_dtype_t */
-    KDA_ERR_WORKSPACE = 6,   /* the prefill's scratch workspace could not be allocated */
+    KDA_ERR_WORKSPACE = 6,   /* the prefill's scratch workspace could not be allocated, or the caller's is too small */
     KDA_ERR_CUDA = 7,        /* the CUDA runtime reported an error at launch */
     KDA_ERR_VALUE = 8        /* a scalar argument is out of range, or buffers alias */
 } kda_status_t;

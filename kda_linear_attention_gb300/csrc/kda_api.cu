@@ -7,7 +7,7 @@
 
 namespace {
 
-constexpr int kVersion = 100;   // 0.1.0
+constexpr int kVersion = 200;   // 0.2.0: caller-owned prefill workspace
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -27,7 +27,7 @@ const char *kda_status_string(int status) {
         case KDA_ERR_CHUNK: return "chunk must be 16, 32 or 64";
         case KDA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
         case KDA_ERR_DTYPE: return "dtype must be KDA_BF16 or KDA_F32";
-        case KDA_ERR_WORKSPACE: return "workspace error";
+        case KDA_ERR_WORKSPACE: return "workspace could not be allocated or is too small";
         case KDA_ERR_CUDA: return "CUDA launch error";
         case KDA_ERR_VALUE: return "a scalar argument is out of range (eps >= 0, finite q_scale)";
         default: return "unknown status";
