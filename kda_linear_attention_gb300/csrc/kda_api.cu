@@ -54,7 +54,7 @@ int kda_prefill_chunked(const void *q, const void *k, const void *v, const float
                                                         N, T, H, s);
         return e == cudaErrorMemoryAllocation ? KDA_ERR_WORKSPACE : cuda_status(e);
     }
-    return cuda_status(kda::launch_prefill_simt(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, H,
+    return cuda_status(kda::launch_prefill_simt(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, T, H,
                                                 chunk, dtype == KDA_BF16, s));
 }
 
@@ -100,7 +100,7 @@ int kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v, con
                                                              cu_seqlens, N, T, H, s));
     }
     // the CUDA-core kernel needs no workspace
-    return cuda_status(kda::launch_prefill_simt(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, H,
+    return cuda_status(kda::launch_prefill_simt(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, T, H,
                                                 chunk, dtype == KDA_BF16, s));
 }
 
@@ -135,7 +135,7 @@ int kda_prefill_chunked_ws(const void *q, const void *k, const void *v, const fl
                                                         N, T, H, workspace, s));
     }
     // the CUDA-core kernel needs no workspace
-    return cuda_status(kda::launch_prefill_simt(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, H,
+    return cuda_status(kda::launch_prefill_simt(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, T, H,
                                                 chunk, dtype == KDA_BF16, s));
 }
 
@@ -214,7 +214,7 @@ int kda_prefill_chunked_gated(const void *q, const void *k, const void *v, const
         return e == cudaErrorMemoryAllocation ? KDA_ERR_WORKSPACE : cuda_status(e);
     }
     // CUDA-core prefill into `out`, then the gated norm in place
-    cudaError_t e = kda::launch_prefill_simt(q, k, v, g, beta, S0, out, S_out, cu_seqlens, N, H,
+    cudaError_t e = kda::launch_prefill_simt(q, k, v, g, beta, S0, out, S_out, cu_seqlens, N, T, H,
                                              chunk, dtype == KDA_BF16, s);
     if (e == cudaSuccess) e = kda::launch_gated_norm(out, gate, norm_w, eps, T * H, s);
     return cuda_status(e);

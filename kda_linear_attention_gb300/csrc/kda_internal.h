@@ -28,7 +28,7 @@ cudaError_t read_decode_error(unsigned int *code, bool reset);
 // bf16 or fp32 inputs.
 cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, const float *g,
                                 const float *beta, const float *S0, float *o, float *S_out,
-                                const int32_t *cu_seqlens, int N, int H, int chunk, bool bf16,
+                                const int32_t *cu_seqlens, int N, int64_t T, int H, int chunk, bool bf16,
                                 cudaStream_t stream);
 
 // Two-kernel tensor-core chunked prefill (kda_prefill_split.cu): bf16 q/k/v,

@@ -39,7 +39,7 @@ prefill_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
                     const TIn *__restrict__ v, const float *__restrict__ g,
                     const float *__restrict__ beta, const float *__restrict__ S0,
                     float *__restrict__ o, float *S_out, const int32_t *__restrict__ cu,
-                    int N, int H) {
+                    int N, int H, int T) {
     using L = SimtSmem<C, DVS>;
     constexpr int LD = L::LD, LU = L::LU;
     constexpr int NSL = kDV / DVS;
@@ -64,8 +64,10 @@ prefill_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
     const int h = (blockIdx.x / NSL) % H;
     const int rank = blockIdx.x / (NSL * H);
     const int n = lpt_sequence(cu, N, rank, &s_seq);
-    const int tok0 = cu[n];
-    const int len = cu[n + 1] - tok0;
+    // tokens clamped to [0, T): an inconsistent cu_seqlens (cu[N] != T, a
+    // caller error) never makes the kernel read or write past the buffers
+    const int tok0 = min(max(cu[n], 0), T);
+    const int len = min(max(cu[n + 1], tok0), T) - tok0;
     const int col0 = slice * DVS;
     const size_t st_off = ((size_t)n * H + h) * kDK * kDV + col0;
 
@@ -221,7 +223,7 @@ prefill_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
 template <typename TIn, int C>
 cudaError_t launch_c(const void *q, const void *k, const void *v, const float *g,
                      const float *beta, const float *S0, float *o, float *S_out,
-                     const int32_t *cu, int N, int H, cudaStream_t stream) {
+                     const int32_t *cu, int N, int H, int T, cudaStream_t stream) {
     constexpr int DVS = 32;
     using L = SimtSmem<C, DVS>;
     auto kern = prefill_simt_kernel<TIn, C, DVS>;
@@ -231,18 +233,18 @@ cudaError_t launch_c(const void *q, const void *k, const void *v, const float *g
     const long long blocks = (long long)N * H * (kDV / DVS);
     kern<<<(unsigned)blocks, kSimtThreads, L::bytes, stream>>>(
         static_cast<const TIn *>(q), static_cast<const TIn *>(k), static_cast<const TIn *>(v), g,
-        beta, S0, o, S_out, cu, N, H);
+        beta, S0, o, S_out, cu, N, H, T);
     return cudaGetLastError();
 }
 
 template <typename TIn>
 cudaError_t launch_t(int chunk, const void *q, const void *k, const void *v, const float *g,
                      const float *beta, const float *S0, float *o, float *S_out,
-                     const int32_t *cu, int N, int H, cudaStream_t stream) {
+                     const int32_t *cu, int N, int H, int T, cudaStream_t stream) {
     switch (chunk) {
-        case 16: return launch_c<TIn, 16>(q, k, v, g, beta, S0, o, S_out, cu, N, H, stream);
-        case 32: return launch_c<TIn, 32>(q, k, v, g, beta, S0, o, S_out, cu, N, H, stream);
-        default: return launch_c<TIn, 64>(q, k, v, g, beta, S0, o, S_out, cu, N, H, stream);
+        case 16: return launch_c<TIn, 16>(q, k, v, g, beta, S0, o, S_out, cu, N, H, T, stream);
+        case 32: return launch_c<TIn, 32>(q, k, v, g, beta, S0, o, S_out, cu, N, H, T, stream);
+        default: return launch_c<TIn, 64>(q, k, v, g, beta, S0, o, S_out, cu, N, H, T, stream);
     }
 }
 
@@ -250,12 +252,12 @@ cudaError_t launch_t(int chunk, const void *q, const void *k, const void *v, con
 
 cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, const float *g,
                                 const float *beta, const float *S0, float *o, float *S_out,
-                                const int32_t *cu_seqlens, int N, int H, int chunk, bool bf16,
-                                cudaStream_t stream) {
+                                const int32_t *cu_seqlens, int N, int64_t T, int H, int chunk,
+                                bool bf16, cudaStream_t stream) {
     if (bf16)
         return launch_t<__nv_bfloat16>(chunk, q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, H,
-                                       stream);
-    return launch_t<float>(chunk, q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, H, stream);
+                                       (int)T, stream);
+    return launch_t<float>(chunk, q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, H, (int)T, stream);
 }
 
 }  // namespace kda

@@ -90,19 +90,32 @@ constexpr uint32_t REC_BYTES = 91136;
 static_assert(REC_BYTES % 1024 == 0, "records stay 1 KB aligned");
 
 // ============================================================================
-// chunk plan: chunk_off[n] = sum_{m<n} ceil(len_m / 64), chunk_off[N] = total
+// chunk plan: chunk_off[n] = sum_{m<n} ceil(len_m / 64), chunk_off[N] = total.
+// cu_seqlens must start at or above 0, never decrease and end at or below T
+// (the call's precondition, which the host cannot read); otherwise the plan
+// is emptied (every offset 0) and the device error word set, so that the
+// intra-chunk kernel has no jobs and the state pass, finding the chunk
+// counts inconsistent, skips every non-empty sequence: nothing is read or
+// written past the buffers sized for T.
 // ============================================================================
-__global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t *__restrict__ cu, int N,
+__global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t *__restrict__ cu, int N, int T,
                                                           int32_t *__restrict__ chunk_off) {
     __shared__ int32_t s_scan[1024];
     __shared__ int32_t s_carry;
+    __shared__ int s_bad;
     const int t = threadIdx.x;
-    if (t == 0) s_carry = 0;
+    if (t == 0) {
+        s_carry = 0;
+        s_bad = (cu[0] < 0 || cu[N] > T) ? 1 : 0;
+    }
     __syncthreads();
     for (int base = 0; base < N; base += 1024) {
         const int n = base + t;
         int v = 0;
-        if (n < N) v = (max(cu[n + 1] - cu[n], 0) + C - 1) / C;
+        if (n < N) {
+            if (cu[n + 1] < cu[n]) s_bad = 1;
+            v = (max(cu[n + 1] - cu[n], 0) + C - 1) / C;
+        }
         s_scan[t] = v;
         __syncthreads();
         for (int off = 1; off < 1024; off <<= 1) {
@@ -117,7 +130,11 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t *__restr
         if (t == 1023) s_carry = carry + s_scan[1023];
         __syncthreads();
     }
-    if (t == 0) chunk_off[N] = s_carry;
+    if (t == 0) chunk_off[N] = s_bad ? 0 : s_carry;
+    if (s_bad) {
+        for (int n = t; n < N; n += 1024) chunk_off[n] = 0;
+        if (t == 0) atomicOr(&g_kda_device_error, 1u);
+    }
 }
 
 // ============================================================================
@@ -1304,7 +1321,7 @@ cudaError_t run_split(const void *q, const void *k, const void *v, const float *
     uint8_t *recs = static_cast<uint8_t *>(ws) +
                     (((size_t)(N + 1) * sizeof(int32_t) + 1023) & ~(size_t)1023);
     if (ev) cudaEventRecord(ev[0], stream);
-    chunk_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, chunk_off);
+    chunk_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, (int)T, chunk_off);
     if (ev) cudaEventRecord(ev[1], stream);
     intra_chunk_kernel<<<intra_grid(max_chunks * H), NTA, SMEM_A_ALLOC, stream>>>(
         mq, mk, mg, beta, cu_seqlens, chunk_off, N, H, recs);

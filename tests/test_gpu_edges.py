@@ -193,3 +193,30 @@ def test_decode_exact_retrieval_with_unit_keys():
     torch.cuda.synchronize()
     # fp32 arithmetic throughout: o = v to fp32 rounding
     assert_close(o.cpu().numpy(), step.f32("v"), 1e-5, "o = v")
+
+
+@pytest.mark.parametrize("dtype,chunk", [("bf16", 64), ("f32", 16)])
+def test_cu_seqlens_past_T_is_contained(dtype, chunk):
+    """cu_seqlens ending past T breaks the call's precondition (the host
+    cannot read the device array to check it).  The tensor-core path empties
+    its chunk plan and raises the device error flag; the CUDA-core path
+    clamps the tokens to [0, T).  Neither reads or writes past the buffers,
+    and the next valid call is unaffected."""
+    import torch
+    import kda_linear_attention_gb300 as kda
+    inp = ki.gen_prefill(470, [60, 40], H=2, dtype=dtype, chunk=chunk, with_s0=True)   # T = 100
+    d = {n: dev_tensor(getattr(inp, n)) for n in ("q", "k", "v", "g", "beta")}
+    s0 = dev_tensor(inp.S0)
+    bad_cu = dev_tensor(np.array([0, 60, 130], dtype=np.int32))
+    kda.device_error(reset=True)
+    kda.prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], bad_cu, S0=s0, chunk=chunk)
+    torch.cuda.synchronize()
+    err = kda.device_error(reset=True)
+    if (dtype, chunk) == ("bf16", 64):
+        assert err & 1, "the inconsistent plan was not flagged"
+    else:
+        assert err == 0
+    o, S = prefill_on_gpu(inp)                  # a valid call afterwards
+    o_ref, S_ref = oracle.prefill(inp)
+    assert_close(o, o_ref, _tol(dtype), "o after the flagged call")
+    assert_close(S, S_ref, _tol(dtype), "S_out after the flagged call")
