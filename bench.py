@@ -5,13 +5,18 @@
 
 A step is one call of the hot path on one batch of seeded synthetic input
 already resident in HBM:
-  prefill_4k         kda_prefill_chunked, H=96, T=4096, bf16 q/k/v, chunk 64 (default)
-  prefill_32k_carry  kda_prefill_chunked, H=96, T=32768 with S0
   varlen_64k         kda_prefill_chunked over 8 packed sequences (65536 tokens)
-                     with S0, then kda_decode_step for all 8
-The JSON line's value is prefill tokens/s.  The metric's second half, decode
-state GB/s, is measured on the batched decode workload (B=64, H=96, 100
-consecutive in-place steps) and reported under "decode".
+                     with S0, then kda_decode_step for all 8 (default: the
+                     largest workload)
+  prefill_32k_carry  kda_prefill_chunked, H=96, T=32768 with S0
+  prefill_4k         kda_prefill_chunked, H=96, T=4096, bf16 q/k/v, chunk 64
+  tiny_fp32          kda_prefill_chunked, H=2, T=64, fp32 q/k/v, chunk 16
+                     (the CUDA-core path)
+The JSON line's value is prefill tokens/s of the headline workload; the
+other prefill workloads are reported under "legs", each with its roofline.
+The metric's second half, decode state GB/s, is measured on the batched
+decode workload (B=64, H=96, 100 consecutive in-place steps) and reported
+under "decode".
 
 Inputs (and outputs) exceed the 129 MB L2, so no L2 flush is done between
 steps.  Timing: CUDA events on the launching stream, W untimed warm-up steps,
@@ -69,20 +74,48 @@ def code_sha(source_file):
     return hashlib.sha256(" ".join(src.split()).encode()).hexdigest()[:16]
 
 
+TRAFFIC_FILE = os.path.join("profiles", "dram_traffic.json")
+
+
 def _traffic(kernel, source_file):
-    """DRAM bytes per launch from profiles/dram_traffic.md, if that capture was
-    taken on the current kernel code (code_sha), else None."""
+    """DRAM bytes per launch of `kernel` as stored from an ncu capture in
+    profiles/dram_traffic.json, if that capture was taken on the current
+    kernel code (code_sha), else None.  A stored capture, not a number
+    measured by this run."""
+    rec = _traffic_record(kernel, source_file)
+    return None if rec is None else int(rec["bytes"])
+
+
+def _traffic_record(kernel, source_file):
     try:
         sha = code_sha(source_file)
-        for line in open(os.path.join(ROOT, "profiles", "dram_traffic.md")):
-            f = line.split()
-            if len(f) >= 4 and f[0] == "traffic:" and f[1] == kernel:
-                kv = dict(x.split("=", 1) for x in f[2:] if "=" in x)
-                if kv.get("code_sha256") == sha:
-                    return int(kv["bytes"])
+        with open(os.path.join(ROOT, TRAFFIC_FILE)) as f:
+            data = json.load(f)
+        for rec in data.get("captures", []):
+            if rec.get("kernel") == kernel and rec.get("code_sha256") == sha:
+                return rec
     except Exception:
         pass
     return None
+
+
+def _prefill_traffic(units):
+    """DRAM bytes of one tensor-core prefill call over `units` (chunk, head)
+    pairs, from the stored captures of its two kernels scaled by units (both
+    kernels' traffic is per (chunk, head): records, q/k/g/beta/v in, o out),
+    with a note of where the number comes from; (None, reason) if there is
+    no capture on the current code."""
+    recs = [_traffic_record(k, "kda_prefill_split.cu") for k in ("intra_chunk_kernel", "state_pass_kernel")]
+    if None in recs:
+        return None, "no stored capture on the current kernel code"
+    tot = 0.0
+    for r in recs:
+        tot += r["bytes"] * units / r["units"]
+    src = "stored ncu capture (%s, %s), dram__bytes_read.sum + dram__bytes_write.sum" % (
+        TRAFFIC_FILE, recs[0].get("workload"))
+    if units != recs[0]["units"]:
+        src += ", scaled by (chunk, head) units %d -> %d" % (recs[0]["units"], units)
+    return int(round(tot)), src
 
 
 def _peaks():
@@ -235,6 +268,154 @@ def _pinned(a):
     return t.pin_memory()
 
 
+PREFILL_WORKLOADS = ["varlen_64k", "prefill_32k_carry", "prefill_4k", "tiny_fp32"]
+REC_BYTES = 91136          # per-(chunk, head) record of the two-kernel tensor-core prefill
+
+
+class PrefillCase:
+    """One prefill workload resident on the device, ready to be stepped."""
+
+    def __init__(self, kda, torch, dev, wl):
+        self.kda, self.torch, self.wl = kda, torch, wl
+        if wl == "varlen_64k":
+            pre, dstep = ki.workload_varlen_with_decode(wl)
+        else:
+            pre, dstep = ki.workload_prefill(wl), None
+        self.pre, self.dstep = pre, dstep
+        self.T, self.H, self.N, self.C = pre.T, pre.H, pre.N, pre.chunk
+        self.d = {n: _to_dev(getattr(pre, n), dev) for n in ("q", "k", "v", "g", "beta")}
+        self.cu = _to_dev(pre.cu_seqlens, dev)
+        self.S0 = None if pre.S0 is None else _to_dev(pre.S0, dev)
+        self.o = torch.empty((self.T, self.H, DV), dtype=torch.float32, device=dev)
+        self.S_out = torch.empty((self.N, self.H, DK, DV), dtype=torch.float32, device=dev)
+        if dstep is not None:
+            self.dd = {n: _to_dev(getattr(dstep, n), dev) for n in ("q", "k", "v", "g", "beta")}
+            self.od = torch.empty((self.N, self.H, DV), dtype=torch.float32, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        # tensor-core path: chunk plan + intra-chunk kernel + state pass per call
+        self.tc = pre.dtype == "bf16" and self.C == 64 and self.T > 0
+        self.launches = (3 if self.tc else 1) + (1 if dstep is not None else 0)
+        self.ev = []
+
+    def step(self, record=False):
+        kda, torch, d = self.kda, self.torch, self.d
+        if record and self.tc:
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            kda.prefill_chunked_events(d["q"], d["k"], d["v"], d["g"], d["beta"], self.cu, evs,
+                                       S0=self.S0, o=self.o, S_out=self.S_out)
+            self.ev.append(evs)
+        else:
+            if record:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(self.stream)
+            kda.prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], self.cu, S0=self.S0,
+                                chunk=self.C, o=self.o, S_out=self.S_out)
+            if record:
+                b.record(self.stream)
+                self.ev.append([a, b])
+        if self.dstep is not None:
+            x = self.dd
+            kda.decode_step(x["q"], x["k"], x["v"], x["g"], x["beta"], self.S_out, o=self.od)
+
+    def kernel_ms(self):
+        """Mean prefill time per call (first to last event) and, on the
+        tensor-core path, per kernel (plan, intra-chunk, state pass)."""
+        kern = statistics.mean(e[0].elapsed_time(e[-1]) for e in self.ev)
+        parts = None
+        if self.tc:
+            parts = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in self.ev) for i in range(3)]
+        return kern, parts
+
+    def roofline(self, peaks):
+        pre, T, H, N, C = self.pre, self.T, self.H, self.N, self.C
+        kern_ms, part_ms = self.kernel_ms()
+        tok_heads = T * H
+        n_state = N * H
+        per_th = PREFILL_BYTES_PER_TOKEN_HEAD_BF16 if pre.dtype == "bf16" else (3 * 512 + 512 + 4 + 512)
+        alg_bytes = tok_heads * per_th + n_state * STATE_BYTES * (2 if self.S0 is not None else 1)
+        alg_flops = tok_heads * prefill_flops_per_token_head(C)
+        achieved_gbs = alg_bytes / (kern_ms / 1e3) / 1e9
+        achieved_tflops = alg_flops / (kern_ms / 1e3) / 1e12
+        hbm_frac = achieved_gbs / peaks["hbm"]
+        tc_frac = achieved_tflops / peaks["bf16"]
+        if self.tc:
+            # Designed against the HBM roofline (arithmetic intensity ~100
+            # flop/B, below the bf16 ridge point).  One call = chunk plan +
+            # intra-chunk kernel + state pass; its roofline is the call's
+            # (algorithmic bytes / call time: the per-chunk records the two
+            # kernels exchange count against it), and each kernel is reported
+            # with the bytes it moves in this design.
+            lens = np.diff(pre.cu_seqlens)
+            nchunk = int(sum((int(x) + 63) // 64 for x in lens))
+            intra_bytes = nchunk * H * (2 * 64 * 256 + 64 * 512 + 64 * 4 + REC_BYTES)
+            state_bytes = nchunk * H * (REC_BYTES + 64 * 256) + T * H * 512 + n_state * STATE_BYTES * (
+                2 if self.S0 is not None else 1)
+            kernels = {}
+            for kname, ms_k, mb in (("chunk_plan_kernel", part_ms[0], None),
+                                    ("intra_chunk_kernel", part_ms[1], intra_bytes),
+                                    ("state_pass_kernel", part_ms[2], state_bytes)):
+                kd = {"ms": round(ms_k, 4), "share": round(ms_k / kern_ms, 4)}
+                if mb is not None:
+                    kd.update({"moved_bytes": int(mb), "gbs": round(mb / (ms_k / 1e3) / 1e9, 1),
+                               "frac_hbm": round(mb / (ms_k / 1e3) / 1e9 / peaks["hbm"], 4)})
+                kernels[kname] = kd
+            traffic, tsrc = _prefill_traffic(nchunk * H)
+            roof = {
+                "kernel": "prefill call: chunk_plan_kernel + intra_chunk_kernel + state_pass_kernel "
+                          "(tcgen05/TMEM/TMA); dominant: intra_chunk_kernel",
+                "bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm"],
+                "unit": "GB/s", "frac": round(hbm_frac, 4), "of": peaks["source"],
+                "traffic": traffic, "traffic_source": tsrc,
+                "kernels": kernels,
+            }
+        else:
+            roof = {
+                "kernel": "prefill_simt_kernel (fp32 CUDA-core chunked prefill)",
+                "bound": "alu", "achieved": round(achieved_tflops, 4),
+                "peak": round(FFMA_PEAK_TFLOPS, 1), "unit": "TFLOP/s",
+                "frac": round(achieved_tflops / FFMA_PEAK_TFLOPS, 5),
+                "of": "derived: 152 SMs x 128 FMA lanes x 2 flop x 2.07 GHz", "traffic": None,
+            }
+        roof.update({
+            "tensor": {"achieved_tflops": round(achieved_tflops, 2), "peak_tflops": peaks["bf16"],
+                       "frac": round(tc_frac, 5), "of": peaks["source"]},
+            "hbm": {"achieved_gbs": round(achieved_gbs, 1), "peak_gbs": peaks["hbm"],
+                    "frac": round(hbm_frac, 5), "of": peaks["source"]},
+            "kernel_ms": round(kern_ms, 4),
+            "algorithmic_bytes": int(alg_bytes), "algorithmic_flops": int(alg_flops),
+            "bytes_per_token_head": per_th, "flops_per_token_head": prefill_flops_per_token_head(C),
+        })
+        return roof
+
+    def config(self):
+        pre = self.pre
+        return {"workload": self.wl, "H": self.H, "T": self.T, "N": self.N, "chunk": self.C,
+                "dk": DK, "dv": DV, "qkv": pre.dtype, "S0": self.S0 is not None,
+                "lens": [int(x) for x in np.diff(pre.cu_seqlens)] if self.N > 1 else None,
+                "then_decode": self.dstep is not None}
+
+
+def _leg(case, peaks, reps):
+    """A secondary prefill workload: `reps` calls back to back behind a GPU
+    hold (median call time and per-kernel times from CUDA events), with its
+    roofline."""
+    torch = case.torch
+    for _ in range(3):
+        case.step()
+    torch.cuda.synchronize()
+    case.ev = []
+    _gpu_hold(torch, 3.0 * reps)
+    for _ in range(reps):
+        case.step(record=True)
+    torch.cuda.synchronize()
+    med = statistics.median(e[0].elapsed_time(e[-1]) for e in case.ev)
+    roof = case.roofline(peaks)
+    return {"config": case.config(), "ms_per_call": round(med, 4),
+            "tokens_per_s": round(case.T / (med / 1e3), 1), "calls": reps,
+            "gpu_launches_per_call": case.launches, "roofline": roof}
+
+
 def run_ours(args):
     import torch
     import kda_linear_attention_gb300 as kda
@@ -256,128 +437,46 @@ def run_ours(args):
             torch.distributed.barrier()
 
     wl = args.workload
-    if wl == "varlen_64k":
-        pre, dstep = ki.workload_varlen_with_decode(wl)
-    else:
-        pre, dstep = ki.workload_prefill(wl), None
-    T, H, N, C = pre.T, pre.H, pre.N, pre.chunk
-    d = {n: _to_dev(getattr(pre, n), dev) for n in ("q", "k", "v", "g", "beta")}
-    cu = _to_dev(pre.cu_seqlens, dev)
-    S0 = None if pre.S0 is None else _to_dev(pre.S0, dev)
-    o = torch.empty((T, H, DV), dtype=torch.float32, device=dev)
-    S_out = torch.empty((N, H, DK, DV), dtype=torch.float32, device=dev)
-    if dstep is not None:
-        dd = {n: _to_dev(getattr(dstep, n), dev) for n in ("q", "k", "v", "g", "beta")}
-        od = torch.empty((N, H, DV), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    tc_path = pre.dtype == "bf16" and C == 64 and T > 0
-    # tensor-core path: chunk plan + intra-chunk kernel + state pass per call
-    launches_per_step = (3 if tc_path else 1) + (1 if dstep is not None else 0)
-
-    ev_pre = []   # per call: (start, end) of the prefill, or the four kernel-boundary events
-
-    def step(record=False):
-        if record and tc_path:
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-            kda.prefill_chunked_events(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, evs,
-                                       S0=S0, o=o, S_out=S_out)
-            ev_pre.append(evs)
-        else:
-            if record:
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-            kda.prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, S0=S0, chunk=C,
-                                o=o, S_out=S_out)
-            if record:
-                b.record(stream)
-                ev_pre.append([a, b])
-        if dstep is not None:
-            kda.decode_step(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], S_out, o=od)
-
+    case = PrefillCase(kda, torch, dev, wl)
+    stream = case.stream
     for _ in range(args.warmup):
-        step()
+        case.step()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
-        clk.keep_busy(step, 2)             # untimed load until the sampler reports
+        clk.keep_busy(case.step, 2)        # untimed load until the sampler reports
         barrier()
         torch.cuda.synchronize()
-        _gpu_hold(torch, 2.0 * args.steps)
+        _gpu_hold(torch, 3.0 * args.steps * max(1.0, case.T / 4096))
         t0.record(stream)
         for _ in range(args.steps):
-            step(record=True)
+            case.step(record=True)
         t1.record(stream)
         torch.cuda.synchronize()
-        clk.keep_busy(step, 1)
+        clk.keep_busy(case.step, 1)
     barrier()
     torch.cuda.synchronize()
     ms = max_over_ranks(t0.elapsed_time(t1), ws, dev)
     ms_per_step = ms / args.steps
-    value = job_throughput(T, ws, ms_per_step)
-    kern_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in ev_pre)
-    if tc_path:
-        part_ms = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev_pre) for i in range(3)]
-
+    value = job_throughput(case.T, ws, ms_per_step)
     peaks = _peaks()
-    tok_heads = T * H
-    n_state = N * H
-    alg_bytes = tok_heads * (PREFILL_BYTES_PER_TOKEN_HEAD_BF16 if pre.dtype == "bf16" else
-                             (3 * 512 + 512 + 4 + 512)) + n_state * STATE_BYTES * (2 if S0 is not None else 1)
-    alg_flops = tok_heads * prefill_flops_per_token_head(C)
-    achieved_gbs = alg_bytes / (kern_ms / 1e3) / 1e9
-    achieved_tflops = alg_flops / (kern_ms / 1e3) / 1e12
-    hbm_frac = achieved_gbs / peaks["hbm"]
-    tc_frac = achieved_tflops / peaks["bf16"]
-    if tc_path:
-        # The tensor-core prefill is designed against the HBM roofline (its
-        # arithmetic intensity, ~100 flop/B, is below the bf16 ridge point).
-        # One call = chunk plan + intra-chunk kernel + state pass; the
-        # roofline is that of the call (algorithmic bytes / call time: the
-        # per-chunk records the two kernels exchange count against it), and
-        # each kernel is reported with the bytes it moves in this design.
-        lens = np.diff(pre.cu_seqlens)
-        nchunk = int(sum((int(x) + 63) // 64 for x in lens))
-        rec = 91136
-        intra_bytes = nchunk * H * (2 * 64 * 256 + 64 * 512 + 64 * 4 + rec)
-        state_bytes = nchunk * H * (rec + 64 * 256) + T * H * 512 + n_state * STATE_BYTES * (
-            2 if S0 is not None else 1)
-        tr = [_traffic(kname, "kda_prefill_split.cu") for kname in ("intra_chunk_kernel", "state_pass_kernel")]
-        kernels = {}
-        for kname, ms_k, mb in (("chunk_plan_kernel", part_ms[0], None),
-                                ("intra_chunk_kernel", part_ms[1], intra_bytes),
-                                ("state_pass_kernel", part_ms[2], state_bytes)):
-            kd = {"ms": round(ms_k, 4), "share": round(ms_k / kern_ms, 4)}
-            if mb is not None:
-                kd.update({"moved_bytes": int(mb), "gbs": round(mb / (ms_k / 1e3) / 1e9, 1),
-                           "frac_hbm": round(mb / (ms_k / 1e3) / 1e9 / peaks["hbm"], 4)})
-            kernels[kname] = kd
-        roofline = {
-            "kernel": "prefill call: chunk_plan_kernel + intra_chunk_kernel + state_pass_kernel "
-                      "(tcgen05/TMEM/TMA); dominant: intra_chunk_kernel",
-            "bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm"],
-            "unit": "GB/s", "frac": round(hbm_frac, 4), "of": peaks["source"],
-            "traffic": (tr[0] + tr[1]) if (wl == "prefill_4k" and None not in tr) else None,
-            "kernels": kernels,
-        }
-    else:
-        roofline = {
-            "kernel": "prefill_simt_kernel (fp32 CUDA-core chunked prefill)",
-            "bound": "alu", "achieved": round(achieved_tflops, 3),
-            "peak": round(FFMA_PEAK_TFLOPS, 1), "unit": "TFLOP/s",
-            "frac": round(achieved_tflops / FFMA_PEAK_TFLOPS, 4),
-            "of": "derived: 152 SMs x 128 FMA lanes x 2 flop x 2.07 GHz", "traffic": None,
-        }
-    roofline.update({
-        "tensor": {"achieved_tflops": round(achieved_tflops, 2), "peak_tflops": peaks["bf16"],
-                   "frac": round(tc_frac, 5), "of": peaks["source"]},
-        "hbm": {"achieved_gbs": round(achieved_gbs, 1), "peak_gbs": peaks["hbm"],
-                "frac": round(hbm_frac, 4), "of": peaks["source"]},
-        "kernel_ms": round(kern_ms, 4),
-        "algorithmic_bytes": int(alg_bytes), "algorithmic_flops": int(alg_flops),
-        "bytes_per_token_head": 1796, "flops_per_token_head": prefill_flops_per_token_head(C),
-    })
+    roofline = case.roofline(peaks)
+    config = case.config()
+    config.update({"l2": "inputs larger than L2 (no flush)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"})
+    dstep = case.dstep
+
+    # ---- the other prefill workloads, each with its roofline --------------
+    legs = {}
+    if not args.no_legs:
+        for other in PREFILL_WORKLOADS:
+            if other == wl:
+                continue
+            c2 = PrefillCase(kda, torch, dev, other)
+            legs[other] = _leg(c2, peaks, reps=max(5, args.steps))
+            del c2
+            torch.cuda.empty_cache()
 
     # ---- decode leg: B=64, H=96, 100 consecutive in-place steps ----------
     decode = None
@@ -390,28 +489,25 @@ def run_ours(args):
         layer = _layer_leg(kda, torch, dev, stream, peaks)
 
     # ---- end to end through the public API with host buffers -------------
-    e2e = None if args.no_e2e else _e2e_leg(kda, torch, dev, stream, pre, dstep, args, barrier, ws)
+    e2e = None if args.no_e2e else _e2e_leg(kda, torch, dev, stream, case.pre, dstep, args, barrier, ws)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 in, fp32 state/accumulate" if pre.dtype == "bf16" else "f32",
+        "dtype": "bf16 in, fp32 state/accumulate" if case.pre.dtype == "bf16" else "f32",
         "data": "synthetic (seeded; shapes and distributions of the model's KDA layer)",
-        "config": {"workload": wl, "H": H, "T": T, "N": N, "chunk": C, "dk": DK, "dv": DV,
-                   "qkv": pre.dtype, "S0": S0 is not None,
-                   "lens": [int(x) for x in np.diff(pre.cu_seqlens)] if N > 1 else None,
-                   "l2": "inputs larger than L2 (no flush)",
-                   "parallelism": "replicas" if ws > 1 else "single GPU"},
-        "gpu_launches": launches_per_step * args.steps,
+        "config": config,
+        "gpu_launches": case.launches * args.steps,
         "roofline": roofline,
+        "legs": legs or None,
         "decode": decode,
         "layer": layer,
         "e2e": e2e,
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = _cpu_baseline(pre, args)
+        line["cpu_baseline"] = _cpu_baseline(case.pre, args)
     if ws > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
@@ -775,15 +871,65 @@ def _sample_heads(pre, args):
     return max(1, min(pre.H, args.cpu_heads or int(round(4e5 / max(1, pre.T)))))
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the
+    platform string)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _single_core_anchor(args):
+    """The oracle on one core over 16 heads of the 4K prefill: the scaling
+    anchor of the multi-core numbers (tokens/s counting the sampled
+    token-heads as full-width tokens)."""
+    import oracle
+    pre = ki.workload_prefill("prefill_4k")
+    heads = 16
+    units = [(0, h) for h in range(heads)]
+    oracle.build()
+    t = time.perf_counter()
+    oracle.prefill(pre, units=units, threads=1)
+    dt = time.perf_counter() - t
+    return {"workload": "prefill_4k", "value": round(pre.T * heads / pre.H / dt, 2), "unit": UNIT,
+            "cores": 1, "sample": "%d of %d heads (%d token-heads), %.2f s" % (heads, pre.H, pre.T * heads, dt)}
+
+
 def _cpu_baseline(pre, args):
     heads = _sample_heads(pre, args)
     dt, threads, units = _oracle_sample(pre, heads)
     tokens_equiv = pre.T * heads / pre.H      # sampled token-heads as full-width tokens
-    return {"value": round(tokens_equiv / dt, 2), "unit": UNIT, "cores": threads,
-            "kind": "oracle",
-            "sample": "fp64 sequential oracle on %d of %d heads of every sequence (%d token-heads, "
-                      "%.1f s); value counts the sampled token-heads as %.0f full-width tokens"
-                      % (heads, pre.H, pre.T * heads, dt, tokens_equiv)}
+    out = {"value": round(tokens_equiv / dt, 2), "unit": UNIT, "cores": threads,
+           "kind": "oracle", "cpu_model": cpu_model(),
+           "threads": "%d worker threads (one (sequence, head) unit each at a time; the C oracle "
+                      "itself is single-threaded, OMP_NUM_THREADS=%s is not used)"
+                      % (threads, os.environ.get("OMP_NUM_THREADS", "unset")),
+           "host_cores": _host_cores(),
+           "sample": "fp64 sequential oracle on %d of %d heads of every sequence (%d token-heads, "
+                     "%.1f s); value counts the sampled token-heads as %.0f full-width tokens"
+                     % (heads, pre.H, pre.T * heads, dt, tokens_equiv)}
+    if not args.no_anchor:
+        out["single_core_anchor"] = _single_core_anchor(args)
+    return out
+
+
+def _host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
 
 
 def run_reference(args):
@@ -811,10 +957,15 @@ def run_reference(args):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl, "H": pre.H, "T": pre.T, "N": pre.N, "chunk": pre.chunk},
+        "config": {"workload": wl, "H": pre.H, "T": pre.T, "N": pre.N, "chunk": pre.chunk,
+                   "dk": DK, "dv": DV, "qkv": pre.dtype, "S0": pre.S0 is not None,
+                   "lens": [int(x) for x in np.diff(pre.cu_seqlens)] if pre.N > 1 else None,
+                   "then_decode": wl == "varlen_64k"},
         "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": threads,
-                         "kind": "oracle",
-                         "sample": "%d of %d heads of every sequence per step" % (heads, pre.H)},
+                         "kind": "oracle", "cpu_model": cpu_model(),
+                         "sample": "%d of %d heads of every sequence per step (the prefill; "
+                                   "value counts the sampled token-heads as full-width tokens)"
+                                   % (heads, pre.H)},
         "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -828,8 +979,12 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="prefill_4k",
-                    choices=["prefill_4k", "prefill_32k_carry", "varlen_64k"])
+    ap.add_argument("--workload", default="varlen_64k", choices=PREFILL_WORKLOADS,
+                    help="headline workload (default: the largest, the 65,536-token varlen "
+                         "batch then one decode step); the others run as legs")
+    ap.add_argument("--no-legs", action="store_true", help="skip the other prefill workloads")
+    ap.add_argument("--no-anchor", action="store_true",
+                    help="skip the single-core oracle anchor of the CPU baseline")
     ap.add_argument("--cpu-heads", type=int, default=0,
                     help="heads per sequence in the oracle sample (default: ~4e5 token-heads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -38,7 +38,11 @@ __all__ = ["prefill_chunked", "prefill_chunked_noalloc", "prefill_chunked_events
            "KDAError", "KDA_BF16", "KDA_F32", "library_path"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_PKG, "libkda_gb300.so")
+# KDA_GB300_DEBUG=1 loads the debug build (python -m kda_linear_attention_gb300.build
+# --debug): the same kernels with index checks that flag bit 3 of the device
+# error word instead of touching memory outside a buffer.
+_LIB_PATH = os.path.join(_PKG, "libkda_gb300_debug.so" if os.environ.get("KDA_GB300_DEBUG") == "1"
+                         else "libkda_gb300.so")
 _lib = None
 
 KDA_BF16 = 0
@@ -64,8 +68,9 @@ def lib() -> ctypes.CDLL:
     if _lib is None:
         if not os.path.exists(_LIB_PATH):
             raise RuntimeError(
-                "libkda_gb300.so is not built (python -m kda_linear_attention_gb300.build); "
-                "this package has no CPU fallback")
+                "%s is not built (python -m kda_linear_attention_gb300.build%s); "
+                "this package has no CPU fallback"
+                % (os.path.basename(_LIB_PATH), " --debug" if "debug" in _LIB_PATH else ""))
         L = ctypes.CDLL(_LIB_PATH)
         vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
         L.kda_version.argtypes = []

@@ -245,12 +245,14 @@ int kda_decode_layer_step(const void *xq, const void *xk, const void *xv, const 
 
 int kda_device_error(unsigned int *code, int reset) {
     if (!code) return KDA_ERR_NULL;
-    unsigned int a = 0, b = 0, c = 0;
+    unsigned int a = 0, b = 0, c = 0, d = 0;
     const cudaError_t e1 = kda::read_device_error(&a, reset != 0);
     const cudaError_t e2 = kda::read_decode_error(&b, reset != 0);
     const cudaError_t e3 = kda::read_layer_error(&c, reset != 0);
-    *code = a | b | c;
-    return cuda_status(e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3));
+    const cudaError_t e4 = kda::read_simt_error(&d, reset != 0);
+    *code = a | b | c | d;
+    const cudaError_t e = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : (e3 != cudaSuccess ? e3 : e4));
+    return cuda_status(e);
 }
 
 }  // extern "C"

@@ -69,6 +69,7 @@ decode_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *_
             return;
         }
     }
+    slot = KDA_DBG_INDEX(g_kda_decode_error, slot, 0, P);
     TS *Su = S + ((size_t)slot * H + unit % H) * kDK * kDV;
 
     // Issue the state loads first; they are independent of everything else.
@@ -202,6 +203,7 @@ decode_bf16_state_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k, c
             return;
         }
     }
+    slot = KDA_DBG_INDEX(g_kda_decode_error, slot, 0, P);
     __nv_bfloat16 *Su = S + ((size_t)slot * H + unit % H) * kDK * kDV;
     uint4 s[RPT];
 #pragma unroll

@@ -10,6 +10,37 @@ namespace kda {
 constexpr int kDK = 128;
 constexpr int kDV = 128;
 
+// Bits of the device error word (kda_device_error).
+constexpr unsigned kErrWait = 1u;        // a bounded wait gave up, or cu_seqlens broke the call's precondition
+constexpr unsigned kErrSlot = 2u;        // a pool slot index past the end of the pool
+constexpr unsigned kErrGateRange = 4u;   // the tensor-core prefill saw a gate g outside [-5, 0] (or NaN)
+constexpr unsigned kErrBounds = 8u;      // debug builds (KDA_DEBUG): an index check failed; the access was skipped
+// Lower bound of the log-decay gate that the decay folding of the
+// tensor-core prefill is sized for (the model's gate lower bound).
+constexpr float kGateMin = -5.0f;
+
+// Debug builds (nvcc -DKDA_DEBUG; python -m kda_linear_attention_gb300.build
+// --debug): index checks on the kernels' global-memory addressing, in place
+// of a memory checker.  A failed check sets kErrBounds in the kernel's error
+// word and replaces the index by the first value of its range, so the access
+// stays inside the buffer (the outputs are then invalid, and flagged);
+// nothing traps and no control flow changes.  Release builds compile the
+// checks out.
+#ifdef KDA_DEBUG
+__device__ __forceinline__ long long dbg_index(unsigned int *word, long long i, long long lo,
+                                               long long hi) {
+    if (i < lo || i >= hi) {
+        atomicOr(word, kErrBounds);
+        return lo;
+    }
+    return i;
+}
+#define KDA_DBG_INDEX(word, i, lo, hi) \
+    ((decltype(i))::kda::dbg_index(&(word), (long long)(i), (long long)(lo), (long long)(hi)))
+#else
+#define KDA_DBG_INDEX(word, i, lo, hi) (i)
+#endif
+
 // Fused decode step (kda_decode.cu).  Returns the launch error.
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *S, float *o, int B, int H, bool bf16,
@@ -30,6 +61,9 @@ cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, con
                                 const float *beta, const float *S0, float *o, float *S_out,
                                 const int32_t *cu_seqlens, int N, int64_t T, int H, int chunk, bool bf16,
                                 cudaStream_t stream);
+// Error word of the CUDA-core prefill (bit 0: cu_seqlens outside [0, T] or
+// decreasing; its tokens were clamped to [0, T)).
+cudaError_t read_simt_error(unsigned int *code, bool reset);
 
 // Two-kernel tensor-core chunked prefill (kda_prefill_split.cu): bf16 q/k/v,
 // chunk 64, T >= 1.  Takes its workspace (see prefill_split_workspace_bytes)

@@ -126,8 +126,12 @@ conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *
     }
     const int t0 = active ? j * kRun : T;
     const int t_end = min(t0 + kRun, T);
-    auto row = [&](int t) -> size_t { return ((size_t)t * H + h) * 128 + c0; };
+    auto row = [&](int t) -> size_t {
+        return ((size_t)KDA_DBG_INDEX(g_kda_layer_error, t, 0, T) * H + h) * 128 + c0;
+    };
     auto win_at = [&](int n, int slot) -> size_t {
+        n = KDA_DBG_INDEX(g_kda_layer_error, n, 0, N);
+        slot = KDA_DBG_INDEX(g_kda_layer_error, slot, 0, kWin);
         return (((size_t)n * 3 + p) * kWin + slot) * win_row + (size_t)h * 128 + c0;
     };
 
@@ -140,18 +144,25 @@ conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *
         for (int s2 = 0; s2 < kWin; ++s2) {
             const int tau = tt - kWin + s2;
             uint4 u = make_uint4(0, 0, 0, 0);
-            if (tau >= start) u = *reinterpret_cast<const uint4 *>(x + row(tau));
-            else if (conv_in) u = *reinterpret_cast<const uint4 *>(conv_in + win_at(n, kWin + (tau - start)));
+            if (tau >= start) {
+                // tau < 0 only when cu_seqlens starts below 0 (a caller error,
+                // flagged below): zeros instead of a read before the buffer
+                if (tau >= 0) u = *reinterpret_cast<const uint4 *>(x + row(tau));
+            } else if (conv_in) {
+                u = *reinterpret_cast<const uint4 *>(conv_in + win_at(n, kWin + (tau - start)));
+            }
             win[s2][0] = bf2_to_f2(u.x);
             win[s2][1] = bf2_to_f2(u.y);
             win[s2][2] = bf2_to_f2(u.z);
             win[s2][3] = bf2_to_f2(u.w);
         }
     };
+    bool bad_cu = false;                       // cu_seqlens outside [0, T] or decreasing
     if (t0 < t_end) {
         n = seq_of(cu, N, t0);
         start = cu[n];
         end = cu[n + 1];
+        bad_cu |= start < 0 || end < start || end > T;
         load_window(t0);
     } else {
 #pragma unroll
@@ -161,8 +172,9 @@ conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *
     }
 
     const size_t rstride = (size_t)H * 128;    // elements between consecutive tokens
-    const __nv_bfloat16 *xp = x + row(t0 < T ? t0 : 0);
-    __nv_bfloat16 *yp = y_out + row(t0 < T ? t0 : 0);
+    const size_t base0 = ((size_t)(t0 < T ? t0 : 0) * H + h) * 128 + c0;   // not dereferenced when t0 = T
+    const __nv_bfloat16 *xp = x + base0;
+    __nv_bfloat16 *yp = y_out + base0;
 #pragma unroll 1
     for (int i = 0; i < kRun; i += kBatch) {
         uint4 xr[kBatch];
@@ -181,6 +193,7 @@ conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *
                 } while (n < N - 1 && cu[n + 1] <= t);
                 start = cu[n];
                 end = cu[n + 1];
+                bad_cu |= start < 0 || end < start || end > T;
                 load_window(t);
             }
             const float2 xn[4] = {bf2_to_f2(xr[u].x), bf2_to_f2(xr[u].y), bf2_to_f2(xr[u].z),
@@ -222,6 +235,7 @@ conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *
             }
         }
     }
+    if (bad_cu) atomicOr(&g_kda_layer_error, kErrWait);
 }
 
 // ============================================================================

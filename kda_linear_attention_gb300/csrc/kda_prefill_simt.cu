@@ -20,6 +20,11 @@
 #include "kda_internal.h"
 
 namespace kda {
+
+// Set (bit 0) when a block finds its sequence's cu_seqlens entries outside
+// [0, T] or decreasing: its tokens are then clamped to [0, T).
+__device__ unsigned int g_kda_simt_error = 0;
+
 namespace {
 
 constexpr int kSimtThreads = 256;
@@ -68,6 +73,7 @@ prefill_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
     // caller error) never makes the kernel read or write past the buffers
     const int tok0 = min(max(cu[n], 0), T);
     const int len = min(max(cu[n + 1], tok0), T) - tok0;
+    if (t == 0 && (cu[n] != tok0 || cu[n + 1] != tok0 + len)) atomicOr(&g_kda_simt_error, kErrWait);
     const int col0 = slice * DVS;
     const size_t st_off = ((size_t)n * H + h) * kDK * kDV + col0;
 
@@ -193,7 +199,9 @@ prefill_simt_kernel(const TIn *__restrict__ q, const TIn *__restrict__ k,
 #pragma unroll
             for (int m = 0; m < C / 8; ++m) {
                 const int r = warp + 8 * m;
-                if (r < Lc) o[((size_t)(tok0 + c0 + r) * H + h) * kDV + col0 + lane] = acc[m];
+                if (r < Lc)
+                    o[((size_t)KDA_DBG_INDEX(g_kda_simt_error, tok0 + c0 + r, 0, T) * H + h) * kDV + col0 +
+                      lane] = acc[m];
             }
         }
         __syncthreads();
@@ -258,6 +266,13 @@ cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, con
         return launch_t<__nv_bfloat16>(chunk, q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, H,
                                        (int)T, stream);
     return launch_t<float>(chunk, q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, H, (int)T, stream);
+}
+
+cudaError_t read_simt_error(unsigned int *code, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_kda_simt_error, sizeof(unsigned int));
+    if (e != cudaSuccess || !reset) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_kda_simt_error, &zero, sizeof(unsigned int));
 }
 
 }  // namespace kda

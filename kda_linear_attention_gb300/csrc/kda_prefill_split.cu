@@ -15,7 +15,8 @@
 // one chunk only; the intra-chunk kernel computes it for all chunks of all
 // sequences in parallel and writes one record per (chunk, head).  The state
 // pass then does, per chunk, two rounds of MMAs and two epilogues:
-//   D_U[j][r] = -(W S)^T + (T' V)^T,   D_O[j][r] = (Q0 S)^T      (bf16)
+//   D_U[j][r] = -(W S)^T + (T' V)^T,   D_O[j][r] = (Q0 S)^T      (bf16;
+//                                                   S as hi + lo pieces)
 //   u = D_U + beta v  (fp32, rounded to tf32 in TMEM)
 //   D_O += (A' U)^T,   S^T += (Kbar^T U)^T                        (tf32)
 // with S^T kept in fp32 in TMEM for the whole sequence (lane j, column i) and
@@ -28,9 +29,11 @@
 // key side a stack of four operands k_s e^{sigma_p - b_s} (160 rows), and one
 // M=128, N=160 MMA gives both Gram matrices.
 //
-// Precision: bf16 operands for the products that carry state-side or Gram
-// terms; tf32 (software round-to-nearest) for A' U and Kbar^T U; the diagonal
-// terms (beta_r v_r, beta_r K0_r, (q_r.k_r) u_r) in fp32 outside the MMAs.
+// Precision: bf16 operands for the Gram matrices, W, Q0 and T'; the state
+// enters round 1 as two bf16 pieces (hi + lo, 16 significant bits), so the
+// products with S lose only the bf16 rounding of W and Q0; tf32 (software
+// round-to-nearest) for A' U and Kbar^T U; the diagonal terms (beta_r v_r,
+// beta_r K0_r, (q_r.k_r) u_r) in fp32 outside the MMAs.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -54,6 +57,17 @@ constexpr int C = 64;
 __device__ __forceinline__ float rcp_fast(float x) {
     float r;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+// min / max that return NaN when either operand is NaN
+__device__ __forceinline__ float fmin_nan(float a, float b) {
+    float r;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
     return r;
 }
 // eight bf16 (one 16-byte chunk) <-> four channel pairs
@@ -153,17 +167,17 @@ constexpr uint32_t SA_Y = SA_KH + 17408;  //   solve temporaries (4 KB)
 constexpr uint32_t SA_T = SA_KH + 24576;  //   T Diag(beta) bf16 il [r][s], rows 0..63 twice
                                           //   (16 KB: the M = 128 A operand of the W product)
 constexpr uint32_t SA_K0 = 73728;         // 16 KB: K0 [64 s][128 i] sw (MN-major B of the W product)
-constexpr uint32_t SA_MISC = 90112;
+constexpr uint32_t SA_KLO = 90112;        // 16 KB: low bf16 parts of the diagonal key rows [64 s][128 i] sw
+constexpr uint32_t SA_MISC = 106496;
 constexpr uint32_t MA_BETA = 0;           // float[64]
 constexpr uint32_t MA_GAM = 256;          // float[128]  e^{b_L}
 constexpr uint32_t MA_DQ = 768;           // float[64]   q_r . k_r
 constexpr uint32_t MA_TOT = 1024;         // float[4][128] sub-block totals, then carry - sigma_u
 constexpr uint32_t MA_SIG = 3072;         // float[4][128] first-half scan totals, then e^{b_L - sigma_u}
 constexpr uint32_t MA_DD = 5120;          // float[4][128] e^{sigma_0}, e^{sigma_w - sigma_{w-1}}
-constexpr uint32_t MA_EP = 7168;          // float[4][128] e^{sigma_u}
-constexpr uint32_t MA_BAR = 9216;         // 3 x u64: q|k, g, MMA
-constexpr uint32_t MA_TMEM = 9240;
-constexpr uint32_t SMEM_A_USED = SA_MISC + 9248;
+constexpr uint32_t MA_BAR = 7168;         // 3 x u64: q|k, g, MMA
+constexpr uint32_t MA_TMEM = 7192;
+constexpr uint32_t SMEM_A_USED = SA_MISC + 7200;
 constexpr uint32_t SMEM_A_ALLOC = SMEM_A_USED + 1024;
 static_assert(2 * (SMEM_A_ALLOC + 1024) <= 233472, "two intra-chunk CTAs per SM");
 static_assert(SA_T + 16384 <= SA_K0 && SA_Y + 4096 <= SA_T, "solve space inside the Khat region");
@@ -171,6 +185,7 @@ static_assert(SA_Y + 32 * 40 * 4 <= SA_T, "the 32 x 32 solve temporary fits");
 constexpr int MLD = 68;                   // row stride (floats) of M / T
 constexpr int YLD = 40;                   // row stride (floats) of the 32x32 solve temporary
 constexpr uint32_t TMA_G = 0;             // Gram D, 160 columns
+constexpr uint32_t TMA_C = 160;           // correction of its diagonal q blocks, 64 columns
 constexpr uint32_t TMA_W = 0;             // W, 128 columns (after the Gram epilogue)
 
 struct Job {
@@ -181,7 +196,7 @@ __global__ void __launch_bounds__(NTA, 2)
 intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_g, const float *__restrict__ beta,
                    const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N,
-                   int H, uint8_t *__restrict__ recs) {
+                   int H, uint8_t *__restrict__ recs, int T, int max_chunks) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float *s_beta = reinterpret_cast<float *>(sm + SA_MISC + MA_BETA);
@@ -190,7 +205,6 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     float *s_tot = reinterpret_cast<float *>(sm + SA_MISC + MA_TOT);
     float *s_sig = reinterpret_cast<float *>(sm + SA_MISC + MA_SIG);
     float *s_dd = reinterpret_cast<float *>(sm + SA_MISC + MA_DD);
-    float *s_ep = reinterpret_cast<float *>(sm + SA_MISC + MA_EP);
     float *s_el = s_sig;
     uint64_t *bar_qk = reinterpret_cast<uint64_t *>(sm + SA_MISC + MA_BAR);
     uint64_t *bar_g = bar_qk + 1;
@@ -220,6 +234,10 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         }
         J.tok = cu[lo] + (J.gc - chunk_off[lo]) * C;
         J.Lc = min(C, cu[lo + 1] - J.tok);
+        // debug builds: the job's record and tokens inside the buffers
+        J.gc = KDA_DBG_INDEX(g_kda_device_error, J.gc, 0, max_chunks);
+        J.tok = KDA_DBG_INDEX(g_kda_device_error, J.tok, 0, T);
+        J.Lc = KDA_DBG_INDEX(g_kda_device_error, J.Lc, 1, T - J.tok + 1);
         return J;
     };
     // q and k land as the two 64-row halves of X (rows 0..63 q, 64..127 k)
@@ -292,13 +310,21 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             for (int rr = 0; rr < 8; ++rr)
                 x[rr] = *reinterpret_cast<const float4 *>(colp + rr * 128 + (((qd & 7) ^ rr) << 4));
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float glo = 0.f, ghi = 0.f;       // smallest and largest gate (NaN-propagating)
 #pragma unroll
             for (int rr = 0; rr < 8; ++rr) {
                 if (16 * u + 8 * hf + rr < Lc) {  // rows past the end add nothing
+                    glo = fmin_nan(glo, fmin_nan(fmin_nan(x[rr].x, x[rr].y), fmin_nan(x[rr].z, x[rr].w)));
+                    ghi = fmax_nan(ghi, fmax_nan(fmax_nan(x[rr].x, x[rr].y), fmax_nan(x[rr].z, x[rr].w)));
                     acc.x += x[rr].x; acc.y += x[rr].y; acc.z += x[rr].z; acc.w += x[rr].w;
                 }
                 x[rr] = acc;
             }
+            // the decay folding below needs every gate in [-5, 0]: a gate
+            // below that would overflow the folding factors, so it is reported
+            // (as is a NaN, which fails both comparisons)
+            const bool g_out = !(glo >= kGateMin && ghi <= 0.f);
+            if (__any_sync(0xffffffffu, g_out) && lane == 0) atomicOr(&g_kda_device_error, kErrGateRange);
             float4 *half_tot = reinterpret_cast<float4 *>(s_sig) + u * 32 + qd;
             if (hf == 0) *half_tot = acc;
             __syncthreads();
@@ -338,10 +364,6 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             s_dd[256 + t] = d2;
             s_dd[384 + t] = d3;
             const float e1 = d0 * d1, e2 = e1 * d2, e3 = e2 * d3;
-            s_ep[t] = d0;
-            s_ep[128 + t] = e1;
-            s_ep[256 + t] = e2;
-            s_ep[384 + t] = e3;
             const float l2 = d3, l1 = d2 * d3, l0 = d1 * l1;
             s_el[t] = l0;
             s_el[128 + t] = l1;
@@ -383,7 +405,16 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             float2 qv[4], kv[4], F2[4], G2[4], xq[4], xk[4], ep[4], el[4], kg[4];
             unpack_bf8x2(*reinterpret_cast<const uint4 *>(pq), qv);
             unpack_bf8x2(*reinterpret_cast<const uint4 *>(pk), kv);
-            ld_f2x4(s_ep + u * 128 + 8 * cc, ep);
+            // e^{sigma_u} = e^{sigma_0} e^{sigma_1 - sigma_0} ... (the products
+            // that also give e^{b_L})
+            ld_f2x4(s_dd + 8 * cc, ep);
+#pragma unroll
+            for (int w = 1; w <= u; ++w) {
+                float2 dw[4];
+                ld_f2x4(s_dd + w * 128 + 8 * cc, dw);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) ep[m] = __fmul2_rn(ep[m], dw[m]);
+            }
             ld_f2x4(s_el + u * 128 + 8 * cc, el);
             float2 dot2 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -414,6 +445,18 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     *reinterpret_cast<uint4 *>(sm + SA_KH + sw_chunk(8 * pp * (pp + 1) + r, cc, 20480)) =
                         pack_bf8x2(kh);
                 }
+            }
+            // the low part of the diagonal block's keys (block u of the stack
+            // holds kg itself): lo(kg) = kg - bf16(kg), rounded to bf16, at row r
+            // of the Klo tile (see the correction MMA after the Gram)
+            {
+                float2 kl[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float2 kh2 = __bfloat1622float2(__floats2bfloat162_rn(kg[m].x, kg[m].y));
+                    kl[m] = make_float2(kg[m].x - kh2.x, kg[m].y - kh2.y);
+                }
+                *reinterpret_cast<uint4 *>(sm + SA_KLO + sw_chunk(r, cc, 8192)) = pack_bf8x2(kl);
             }
             // Q0 = q e^{b} -> record rows 64..127 of [-W ; Q0];  K0 = k e^{b} -> smem
             {
@@ -489,6 +532,20 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 const uint64_t bk = smem_desc(smem_u32(sm + SA_KH + ko * 20480 + kb2), 16, 1024, kSwizzle128B);
                 mma_bf16_ss(tmem + TMA_G, ax, bk, idg, kk > 0);
             }
+            // the diagonal q blocks of the Gram in more than bf16 precision:
+            // D_C = X Klo^T (N = 64: every q row against every diagonal key
+            // row; row r of sub-block p uses columns 16p .. 16p + 15), added to
+            // hi(xq) hi(kg) in the epilogue.  A' of a short sequence lives in
+            // these blocks, where the bf16 rounding of the keys alone would
+            // cost o up to 2^-9 of each product term.
+            const uint32_t idc = instr_desc(kFmtBF16, 128, 64, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t ko = (uint32_t)(kk >> 2), kb2 = (uint32_t)(kk & 3) * 32u;
+                const uint64_t ax = smem_desc(smem_u32(sm + SA_X + ko * 16384 + kb2), 16, 1024, kSwizzle128B);
+                const uint64_t bl = smem_desc(smem_u32(sm + SA_KLO + ko * 8192 + kb2), 16, 1024, kSwizzle128B);
+                mma_bf16_ss(tmem + TMA_C, ax, bl, idc, kk > 0);
+            }
             mma_commit(bar_mma);
         }
         {
@@ -528,19 +585,25 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 const int qt = 2 * (t >> 7) + qq;
                 const uint32_t col_lo = (uint32_t)min(8 * plo * (plo + 1) + 16 * qt, 144);
                 const uint32_t col_hi = (uint32_t)min(8 * (plo + 1) * (plo + 2) + 16 * qt, 144);
-                float va[16], vb[16];
+                float va[16], vb[16], ca[16], cb[16];
                 tmem_ld16(tmem + lane_base + TMA_G + col_lo, va);
                 tmem_ld16(tmem + lane_base + TMA_G + col_hi, vb);
+                if (qside) {                   // the diagonal correction of sub-blocks plo, plo + 1
+                    tmem_ld16(tmem + lane_base + TMA_C + 16 * plo, ca);
+                    tmem_ld16(tmem + lane_base + TMA_C + 16 * plo + 16, cb);
+                }
                 tmem_wait_ld();
                 const bool use_hi = p != plo;
                 const bool have = qt <= p && r < Lc;
+                const bool diag = qside && qt == p;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     float x4[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int s = 16 * qt + 4 * j + e;
-                        const float val = use_hi ? vb[4 * j + e] : va[4 * j + e];
+                        float val = use_hi ? vb[4 * j + e] : va[4 * j + e];
+                        if (diag) val += use_hi ? cb[4 * j + e] : ca[4 * j + e];
                         x4[e] = (have && s < r) ? val : 0.f;
                     }
                     if (qside) {
@@ -789,7 +852,7 @@ constexpr uint32_t SB_A = 40960;          // A' (bulk copy 2, with Kbar^T)
 constexpr uint32_t SB_KB = 57344;         // Kbar^T
 constexpr uint32_t SB_VEC = 90112;        // 2 x 1 KB record vectors (double-buffered)
 constexpr uint32_t SB_V = 92160;          // 16 KB: v chunk sw (TMA) = V^T, MN-major operand
-                                          // 108544..141312 free: the bf16 copy of S^T lives in TMEM
+                                          // 108544..141312 free: the bf16 pieces of S^T live in TMEM
 constexpr uint32_t SB_O = 141312;         // 32 KB: o of even chunks, 4 x [64 r][32 j] fp32 (TMA store source)
 constexpr uint32_t SB_GATE = 174080;      // 16 KB: gate chunk sw (TMA; gated variant only)
 constexpr uint32_t SB_O1 = 190464;        // 32 KB: o of odd chunks
@@ -801,13 +864,15 @@ static_assert(SB_T == R_T && SB_A == R_A && SB_KB == R_KB, "record pieces map on
 static_assert(SB_KB == SB_A + 16384, "A' and Kbar^T form one N = 192 operand");
 static_assert(SMEM_B_ALLOC <= 232448, "dynamic shared memory limit (227 KB)");
 static_assert(SB_EB % 16 == 0, "bulk copy destination alignment");
-// TMEM columns: U^T | O^T | S^T master | S^T bf16.  Round 1 writes [U | O]
-// (N = 128) with S^T bf16 as its A operand, round 2 accumulates [O | S]
-// (N = 192) from the contiguous [A' ; Kbar^T].
+// TMEM columns: U^T | O^T | S^T master | S^T as two bf16 pieces.  Round 1
+// writes [U | O] (N = 128) with the two pieces of S^T as A operands (one
+// MMA chain each, same accumulator), round 2 accumulates [O | S] (N = 192)
+// from the contiguous [A' ; Kbar^T].
 constexpr uint32_t TMB_U = 0;             // U^T, 64 columns
 constexpr uint32_t TMB_O = 64;            // O^T, 64 columns
 constexpr uint32_t TMB_S = 128;           // S^T master fp32 (lane j, column i), 128 columns
-constexpr uint32_t TMB_SB = 256;          // S^T bf16 (lane j, column i / 2: pairs i, i + 1), 64 columns
+constexpr uint32_t TMB_SB = 256;          // S^T high bf16 piece (lane j, column i / 2: pairs i, i + 1), 64 columns
+constexpr uint32_t TMB_SL = 320;          // S^T low bf16 piece, same layout, 64 columns
 constexpr uint32_t TMEM_COLS_B = 512;
 constexpr uint32_t COPY1 = R_A - R_WQ;    // bytes of [-W ; Q0] + T'
 constexpr uint32_t COPY2 = R_VEC - R_A;   // bytes of A' + Kbar^T
@@ -825,6 +890,19 @@ __device__ __forceinline__ void ld_vec16(const float *p, float (&x)[16]) {
     }
 }
 
+// 16 fp32 values (channel pairs 2c, 2c + 1) as two bf16 pieces: hi = bf16(x),
+// lo = bf16(x - hi).  hi + lo keeps 16 significant bits of each value, so a
+// product with a bf16 operand loses no more than that operand's own rounding.
+__device__ __forceinline__ void split_bf16_pairs(const float (&x)[16], float (&hi)[8], float (&lo)[8]) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * c], x[2 * c + 1]);
+        const float2 hf = __bfloat1622float2(h);
+        hi[c] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&h));
+        lo[c] = __uint_as_float(pack_bf2(x[2 * c] - hf.x, x[2 * c + 1] - hf.y));
+    }
+}
+
 // barrier among the 512 epilogue threads only
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
@@ -839,7 +917,7 @@ __device__ __forceinline__ float gate_sigmoid(float x) { return __fdividef(1.f, 
 //   MMA warp:  wait record A(j) -> round 1 | mid | wait record B(j) -> round 2 | end
 //   epilogue:  u = D_U + beta v in TMEM | mid | stage o(j-1) (gated:
 //              normalise it) while round 2 runs; o(j) into registers, bf16
-//              copy of S and S <- Diag(e^{b_L(j+1)}) S for the next chunk | end
+//              pieces of S and S <- Diag(e^{b_L(j+1)}) S for the next chunk | end
 //   copy warp: request the gate of chunk j-1; after round 1, record A(j+1)
 //              | mid | v(j+1); once staged, store o(j-1); after round 2,
 //              record B(j+1) | end
@@ -850,7 +928,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                   float *__restrict__ o, float *__restrict__ S_out, const int32_t *__restrict__ cu,
                   const int32_t *__restrict__ chunk_off, int N, int H, int max_chunks,
                   const uint8_t *__restrict__ recs, const __grid_constant__ CUtensorMap map_gate,
-                  const float *__restrict__ norm_w, float norm_eps) {
+                  const float *__restrict__ norm_w, float norm_eps, int T) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bar_a = reinterpret_cast<uint64_t *>(sm + SB_MISC);
@@ -899,7 +977,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
     sync_tc();
     const uint32_t tmem = *s_tmem;
 
-    // ---- initial state: S^T master in TMEM (lane j, column i) + bf16 copy
+    // ---- initial state: S^T master in TMEM (lane j, column i) + its two bf16 pieces
     if (epi) {
         float sv[32];
 #pragma unroll
@@ -915,17 +993,24 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         }
         tmem_st16(tmem + lane_base + TMB_S + 32 * qt, a);
         tmem_st16(tmem + lane_base + TMB_S + 32 * qt + 16, b2);
-        float pk[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) pk[c] = __uint_as_float(pack_bf2(sv[2 * c], sv[2 * c + 1]));
-        tmem_st16(tmem + lane_base + TMB_SB + 16 * qt, pk);
+        for (int hh = 0; hh < 2; ++hh) {
+            float hi[8], lo[8];
+            split_bf16_pairs(hh ? b2 : a, hi, lo);
+            tmem_st8(tmem + lane_base + TMB_SB + 16 * qt + 8 * hh, hi);
+            tmem_st8(tmem + lane_base + TMB_SL + 16 * qt + 8 * hh, lo);
+        }
         tmem_wait_st();
     }
     fence_proxy_async_smem();
     sync_tc();
 
+    // requests made by the copy thread, counted where they are made, so that
+    // if a bounded wait gives up it waits for exactly what is in flight
+    int issued_a = 0, issued_b = 0, issued_gate = 0, issued_mma = 0;
     auto rec_at = [&](int j) -> const uint8_t * {
-        return recs + ((size_t)(cbase + j) * H + h) * REC_BYTES;
+        const int gc = KDA_DBG_INDEX(g_kda_device_error, cbase + j, 0, max_chunks);
+        return recs + ((size_t)gc * H + h) * REC_BYTES;
     };
     // record A of chunk j and e^{b_L} of chunk j + 1 (for the scaling of S at
     // the end of chunk j), with the byte count of v, which issue_v requests
@@ -934,6 +1019,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         const uint8_t *r = rec_at(j);
         const bool next = j + 1 < nch;
         mbar_arrive_expect_tx(bar_a, COPY1 + 1024 + 16384 + (next ? 512 : 0));
+        ++issued_a;
         bulk_load(sm + SB_WQ, r + R_WQ, COPY1, bar_a);
         bulk_load(sm + SB_VEC + 1024 * (j & 1), r + R_VEC, 1024, bar_a);
         if (next) bulk_load(sm + SB_EB + 512 * ((j + 1) & 1), rec_at(j + 1) + R_VEC + 512, 512, bar_a);
@@ -944,11 +1030,13 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
     };
     auto issue_gate = [&](int j) {
         mbar_arrive_expect_tx(bar_gate, 16384);
+        ++issued_gate;
         tma_load_3d(sm + SB_GATE, &map_gate, bar_gate, 0, h, tok0 + j * C);
         tma_load_3d(sm + SB_GATE + 8192, &map_gate, bar_gate, 64, h, tok0 + j * C);
     };
     auto issue_b = [&](int j) {
         mbar_arrive_expect_tx(bar_b, COPY2);
+        ++issued_b;
         bulk_load(sm + SB_A, rec_at(j) + R_A, COPY2, bar_b);
     };
     auto prefetch2 = [&](int j) {            // chunk j toward L2
@@ -963,10 +1051,6 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         if (GATED) issue_gate(0);
         if (nch > 1) prefetch2(1);
     }
-    // bookkeeping of the issuing threads, which wait for everything in flight
-    // if a bounded wait gives up
-    int issued_a = nch > 0, issued_b = nch > 0, issued_mma = 0;
-    int issued_gate = (GATED && nch > 0) ? 1 : 0;
     bool bad = false;
     float po[16];                             // epilogue: o of the previous chunk
 
@@ -985,7 +1069,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 const int r = 16 * qt + k;
-                if (r < Lp) o[((row0 + r) * H + h) * kDV + ch] = po[k];
+                if (r < Lp) o[((size_t)KDA_DBG_INDEX(g_kda_device_error, (long long)(row0 + r), 0, T) * H + h) * kDV + ch] = po[k];
             }
         }
         if (GATED) {
@@ -1027,7 +1111,9 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                 if (Lp == C)
                     *reinterpret_cast<float4 *>(sm + sbp + 8192 * m + rr * 128 + 16 * p8) = y;
                 else if (rr < Lp)
-                    *reinterpret_cast<float4 *>(o + ((row0 + rr) * H + h) * kDV + 32 * m + 4 * p8) = y;
+                    *reinterpret_cast<float4 *>(
+                        o + ((size_t)KDA_DBG_INDEX(g_kda_device_error, (long long)(row0 + rr), 0, T) * H + h) * kDV +
+                        32 * m + 4 * p8) = y;
             }
         }
         fence_proxy_async_smem();
@@ -1057,6 +1143,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                         smem_u32(sm + SB_WQ + (uint32_t)(kk >> 2) * 16384 + (uint32_t)(kk & 3) * 32), 16,
                         1024, kSwizzle128B);
                     mma_bf16_ts(tmem + TMB_U, tmem + TMB_SB + 8 * kk, bw, id1, kk > 0);
+                    mma_bf16_ts(tmem + TMB_U, tmem + TMB_SL + 8 * kk, bw, id1, 1);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
@@ -1075,8 +1162,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             bulk_wait_read_but_last();
             if (GATED && j >= 2) issue_gate(j - 1);
             // once round 1 has read them: the next chunk's round-1 operands
-            if (!mbar_wait(bar_mma, 0u, kWaitLimit)) bad = true;
-            if (j + 1 < nch) issue_a(j + 1);
+            if (!mbar_wait(bar_mma, 0u, kWaitLimit)) bad = true;   // round 1 may still read them
+            else if (j + 1 < nch) issue_a(j + 1);
         }
         float uv[16];
         if (epi) {
@@ -1118,9 +1205,6 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         }
         tc_fence_before();
         if (__syncthreads_or(bad)) {                            // ---- mid
-            // the copy thread has already requested this chunk's record A and gate
-            issued_a += (j + 1 < nch);
-            issued_gate += (GATED && j >= 2);
             failed = true;
             break;
         }
@@ -1150,15 +1234,12 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                 if (mbar_wait(bar_ost, (uint32_t)((j - 1) & 1), kWaitLimit)) store_o(j - 1);
                 else bad = true;
             }
-            if (!mbar_wait(bar_mma, 1u, kWaitLimit)) bad = true;
-            if (j + 1 < nch) issue_b(j + 1);   // A' and Kbar^T are consumed
+            if (!mbar_wait(bar_mma, 1u, kWaitLimit)) bad = true;   // round 2 may still read them
+            else if (j + 1 < nch) issue_b(j + 1);                    // A' and Kbar^T are consumed
         }
-        issued_a += (j + 1 < nch);
-        issued_b += (j + 1 < nch);
-        issued_gate += (GATED && j >= 2);
 
         // ===== the previous chunk's o is staged while round 2 runs; then
-        // o = D_O + (q.k) u into registers, the bf16 copy of the new S^T, and
+        // o = D_O + (q.k) u into registers, the bf16 pieces of the new S^T, and
         // S <- Diag(e^{b_L}) S for the next chunk
         if (epi) {
             if (j > 0) {
@@ -1180,19 +1261,20 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                 for (int k = 0; k < 16; ++k) po[k] = fmaf(qk[k], uv[k], ov[k]);
             }
             {
-                float sv[32], pk[16];
-                tmem_ld32(tmem + lane_base + TMB_S + 32 * qt, sv);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) pk[c] = __uint_as_float(pack_bf2(sv[2 * c], sv[2 * c + 1]));
-                tmem_st16(tmem + lane_base + TMB_SB + 16 * qt, pk);
-                if (next) {
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        float eb[16], x[16];
+                for (int hh = 0; hh < 2; ++hh) {
+                    float sv[16], hi[8], lo[8];
+                    tmem_ld16(tmem + lane_base + TMB_S + 32 * qt + 16 * hh, sv);
+                    tmem_wait_ld();
+                    split_bf16_pairs(sv, hi, lo);
+                    tmem_st8(tmem + lane_base + TMB_SB + 16 * qt + 8 * hh, hi);
+                    tmem_st8(tmem + lane_base + TMB_SL + 16 * qt + 8 * hh, lo);
+                    if (next) {
+                        float eb[16];
                         ld_vec16(ebn + 32 * qt + 16 * hh, eb);
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) x[c] = sv[16 * hh + c] * eb[c];
-                        tmem_st16(tmem + lane_base + TMB_S + 32 * qt + 16 * hh, x);
+                        for (int c = 0; c < 16; ++c) sv[c] *= eb[c];
+                        tmem_st16(tmem + lane_base + TMB_S + 32 * qt + 16 * hh, sv);
                     }
                 }
             }
@@ -1207,7 +1289,6 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             bulk_wait_read_but_last();
             if (GATED && nch >= 2) issue_gate(nch - 1);
         }
-        issued_gate += (GATED && nch >= 2);
         __syncthreads();
         if (epi) stage_o(nch - 1);
         if (__syncthreads_or(bad)) failed = true;
@@ -1239,38 +1320,82 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS_B);
 }
 
-// ---- workspace: a library-owned stream-ordered pool per device that keeps
-// its memory between calls (release threshold = max), so only the first call
-// of a given size reaches the driver's allocator.
+// ---- per-device state the library keeps between calls --------------------
+// Everything cached here belongs to one CUDA context of the device: a
+// cudaDeviceReset destroys it (the pool, the kernel attributes, the scratch
+// array's address), so each entry remembers the context it was made in and
+// is made again when the current context differs.
 constexpr int kMaxDevices = 64;
+
+// Unique (for the process's lifetime) identity of the calling thread's
+// current context; 0 when none is current or the driver cannot say.
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (!get_cur || !get_id) return 0;
+    CUcontext c = nullptr;
+    if (get_cur(&c) != CUDA_SUCCESS || !c) return 0;
+    unsigned long long id = 0;
+    return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+int current_device_checked(cudaError_t *e) {
+    int dev = 0;
+    *e = cudaGetDevice(&dev);
+    if (*e == cudaSuccess && (dev < 0 || dev >= kMaxDevices)) *e = cudaErrorInvalidDevice;
+    return dev;
+}
+
+// The workspace pool: a library-owned stream-ordered pool per device that
+// keeps its memory between calls (release threshold = max), so only the
+// first call of a given size reaches the driver's allocator.
 std::mutex g_pool_mu;
-cudaMemPool_t g_pool[kMaxDevices] = {};
+struct {
+    unsigned long long ctx;
+    cudaMemPool_t pool;
+} g_pool[kMaxDevices] = {};
 
 cudaError_t ws_alloc(void **p, size_t bytes, cudaStream_t s) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e;
+    const int dev = current_device_checked(&e);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     cudaMemPool_t pool;
     {
         std::lock_guard<std::mutex> lk(g_pool_mu);
-        if (!g_pool[dev]) {
+        const unsigned long long ctx = current_context_id();
+        if (!g_pool[dev].pool || (ctx != 0 && ctx != g_pool[dev].ctx)) {
             cudaMemPoolProps props = {};
             props.allocType = cudaMemAllocationTypePinned;
             props.location.type = cudaMemLocationTypeDevice;
             props.location.id = dev;
-            e = cudaMemPoolCreate(&g_pool[dev], &props);
-            if (e != cudaSuccess) {
-                g_pool[dev] = nullptr;
-                return e;
-            }
+            cudaMemPool_t np = nullptr;
+            e = cudaMemPoolCreate(&np, &props);
+            if (e != cudaSuccess) return e;
             uint64_t thr = ~0ull;
-            cudaMemPoolSetAttribute(g_pool[dev], cudaMemPoolAttrReleaseThreshold, &thr);
+            cudaMemPoolSetAttribute(np, cudaMemPoolAttrReleaseThreshold, &thr);
+            g_pool[dev].pool = np;
+            g_pool[dev].ctx = current_context_id();
         }
-        pool = g_pool[dev];
+        pool = g_pool[dev].pool;
     }
     return cudaMallocFromPoolAsync(p, bytes, pool, s);
 }
+
+// The kernels' dynamic shared-memory limits, set once per device context.
+std::mutex g_attr_mu;
+unsigned long long g_attr_ctx[kMaxDevices] = {};
 
 }  // namespace
 
@@ -1304,19 +1429,33 @@ cudaError_t run_split(const void *q, const void *k, const void *v, const float *
                       const void *gate = nullptr, const float *norm_w = nullptr,
                       float norm_eps = 0.f) {
     const int64_t max_chunks = (T + C - 1) / C + N;
+    static MapCache maps;
     CUtensorMap mq, mk, mv, mg, mo, mgate;
-    if (!make_map_bf16(&mq, q, T, H, 64, true) || !make_map_bf16(&mk, k, T, H, 64, true) ||
-        !make_map_bf16(&mv, v, T, H, 64, true) || !make_map_f32(&mg, g, T, H) ||
-        !make_map_f32_plain(&mo, o, T, H))
+    if (!maps.get(&mq, kMapBf16Sw, q, T, H) || !maps.get(&mk, kMapBf16Sw, k, T, H) ||
+        !maps.get(&mv, kMapBf16Sw, v, T, H) || !maps.get(&mg, kMapF32Sw, g, T, H) ||
+        !maps.get(&mo, kMapF32Plain, o, T, H))
         return cudaErrorInvalidValue;
-    if (gate && !make_map_bf16(&mgate, gate, T, H, 64, true)) return cudaErrorInvalidValue;
+    if (gate && !maps.get(&mgate, kMapBf16Sw, gate, T, H)) return cudaErrorInvalidValue;
     if (!gate) mgate = mv;                   // unused by the ungated kernel
-    cudaError_t e = cudaFuncSetAttribute(intra_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_A_ALLOC);
+    cudaError_t e;
+    const int dev = current_device_checked(&e);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gate ? state_pass_kernel<true> : state_pass_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_B_ALLOC);
-    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lk(g_attr_mu);
+        const unsigned long long ctx = current_context_id();
+        if (ctx == 0 || ctx != g_attr_ctx[dev]) {
+            e = cudaFuncSetAttribute(intra_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)SMEM_A_ALLOC);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(state_pass_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_B_ALLOC);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(state_pass_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_B_ALLOC);
+            if (e != cudaSuccess) return e;
+            g_attr_ctx[dev] = current_context_id();
+        }
+    }
     int32_t *chunk_off = static_cast<int32_t *>(ws);
     uint8_t *recs = static_cast<uint8_t *>(ws) +
                     (((size_t)(N + 1) * sizeof(int32_t) + 1023) & ~(size_t)1023);
@@ -1324,16 +1463,16 @@ cudaError_t run_split(const void *q, const void *k, const void *v, const float *
     chunk_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, (int)T, chunk_off);
     if (ev) cudaEventRecord(ev[1], stream);
     intra_chunk_kernel<<<intra_grid(max_chunks * H), NTA, SMEM_A_ALLOC, stream>>>(
-        mq, mk, mg, beta, cu_seqlens, chunk_off, N, H, recs);
+        mq, mk, mg, beta, cu_seqlens, chunk_off, N, H, recs, (int)T, (int)max_chunks);
     if (ev) cudaEventRecord(ev[2], stream);
     if (gate)
         state_pass_kernel<true><<<(unsigned)((int64_t)N * H), NTB, SMEM_B_ALLOC, stream>>>(
             mv, mo, S0, o, S_out, cu_seqlens, chunk_off, N, H, (int)max_chunks, recs, mgate, norm_w,
-            norm_eps);
+            norm_eps, (int)T);
     else
         state_pass_kernel<false><<<(unsigned)((int64_t)N * H), NTB, SMEM_B_ALLOC, stream>>>(
             mv, mo, S0, o, S_out, cu_seqlens, chunk_off, N, H, (int)max_chunks, recs, mgate, nullptr,
-            0.f);
+            0.f, (int)T);
     if (ev) cudaEventRecord(ev[3], stream);
     return cudaGetLastError();
 }
@@ -1383,7 +1522,10 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 
 namespace {
 std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices] = {};
+struct {
+    unsigned long long ctx;
+    void *addr;
+} g_scratch[kMaxDevices] = {};
 }  // namespace
 
 cudaError_t launch_prefill_split_ws(const void *q, const void *k, const void *v, const float *g,
@@ -1400,21 +1542,23 @@ cudaError_t launch_prefill_split_noalloc(const void *q, const void *k, const voi
                                          int64_t T, int H, cudaStream_t stream) {
     if (!grid_fits(N, T, H) || prefill_split_workspace_bytes(N, T, H) > kNoAllocScratchBytes)
         return cudaErrorInvalidValue;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e;
+    const int dev = current_device_checked(&e);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     void *ws = nullptr;
     {
-        // first call on a device: look up the array's address once
+        // first call on a device (and again after a device reset made a new
+        // context): look up the array's address, with the device current
         std::lock_guard<std::mutex> lk(g_scratch_mu);
-        if (!g_scratch_addr[dev]) {
+        const unsigned long long ctx = current_context_id();
+        if (!g_scratch[dev].addr || ctx == 0 || ctx != g_scratch[dev].ctx) {
             void *addr = nullptr;
             e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
             if (e != cudaSuccess) return e;
-            g_scratch_addr[dev] = addr;
+            g_scratch[dev].addr = addr;
+            g_scratch[dev].ctx = current_context_id();
         }
-        ws = g_scratch_addr[dev];
+        ws = g_scratch[dev].addr;
     }
     return run_split(q, k, v, g, beta, S0, o, S_out, cu_seqlens, N, T, H, ws, stream);
 }

@@ -6,6 +6,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "tc_ptx.cuh"
 
 namespace kda {
@@ -144,6 +146,49 @@ inline bool make_map_f32_plain(CUtensorMap *m, const void *base, int64_t T, int 
                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+
+// ---- host: a small cache of encoded maps ----------------------------------
+// A serving loop calls the prefill again and again on the same buffers;
+// encoding a map is pure host work but not free, so the last few maps are
+// kept, keyed on everything that goes into them.
+enum MapKind : int { kMapBf16Sw = 0, kMapF32Sw = 1, kMapF32Plain = 2 };
+
+struct MapCache {
+    struct Entry {
+        const void *base = nullptr;
+        int64_t T = -1;
+        int H = 0, kind = -1;
+        CUtensorMap map;
+    };
+    static constexpr int kEntries = 32;
+    std::mutex mu;
+    Entry e[kEntries];
+    int next = 0;
+
+    bool get(CUtensorMap *m, int kind, const void *base, int64_t T, int H) {
+        {
+            std::lock_guard<std::mutex> lk(mu);
+            for (const Entry &x : e)
+                if (x.kind == kind && x.base == base && x.T == T && x.H == H) {
+                    *m = x.map;
+                    return true;
+                }
+        }
+        bool ok = kind == kMapBf16Sw   ? make_map_bf16(m, base, T, H, 64, true)
+                  : kind == kMapF32Sw  ? make_map_f32(m, base, T, H)
+                                       : make_map_f32_plain(m, base, T, H);
+        if (!ok) return false;
+        std::lock_guard<std::mutex> lk(mu);
+        Entry &x = e[next];
+        next = (next + 1) % kEntries;
+        x.base = base;
+        x.T = T;
+        x.H = H;
+        x.kind = kind;
+        x.map = *m;
+        return true;
+    }
+};
 
 }  // namespace tc
 }  // namespace kda

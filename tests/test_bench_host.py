@@ -30,16 +30,41 @@ def test_code_sha_ignores_comments_and_whitespace(tmp_path, monkeypatch):
 
 
 def test_traffic_lookup_follows_the_code(tmp_path, monkeypatch):
+    import json
     b = _with_source(tmp_path, monkeypatch, "__global__ void k() {}\n")
     prof = tmp_path / "profiles"
     prof.mkdir()
     sha = b.code_sha("k.cu")
-    (prof / "dram_traffic.md").write_text(
-        "# notes\n\ntraffic: k_kernel code_sha256=%s bytes=12345 workload=w\n"
-        "traffic: other code_sha256=0000000000000000 bytes=1 workload=w\n" % sha)
+    (prof / "dram_traffic.json").write_text(json.dumps({"captures": [
+        {"kernel": "k_kernel", "code_sha256": sha, "bytes": 12345, "workload": "w"},
+        {"kernel": "other", "code_sha256": "0000000000000000", "bytes": 1, "workload": "w"}]}))
     assert b._traffic("k_kernel", "k.cu") == 12345
     assert b._traffic("other", "k.cu") is None          # captured on other code
     assert b._traffic("missing", "k.cu") is None
+
+
+def test_prefill_traffic_scales_by_units(tmp_path, monkeypatch):
+    import json
+    b = _with_source(tmp_path, monkeypatch, "__global__ void k() {}\n")
+    import os
+    os.rename(tmp_path / "kda_linear_attention_gb300" / "csrc" / "k.cu",
+              tmp_path / "kda_linear_attention_gb300" / "csrc" / "kda_prefill_split.cu")
+    sha = b.code_sha("kda_prefill_split.cu")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "dram_traffic.json").write_text(json.dumps({"captures": [
+        {"kernel": "intra_chunk_kernel", "code_sha256": sha, "bytes": 1000, "units": 10, "workload": "w"},
+        {"kernel": "state_pass_kernel", "code_sha256": sha, "bytes": 500, "units": 10, "workload": "w"}]}))
+    t, src = b._prefill_traffic(10)
+    assert t == 1500 and "stored" in src
+    t, src = b._prefill_traffic(40)
+    assert t == 6000 and "scaled" in src
+
+
+def test_cpu_model_is_a_string():
+    import bench
+    m = bench.cpu_model()
+    assert isinstance(m, str) and m
 
 
 def test_decode_cpu_baseline_on_a_generated_step():

@@ -334,3 +334,29 @@ def test_decode_layer_b64_full():
     assert_close(out, out_ref, 1e-4, "layer step out")
     assert_close(S_dev.cpu().numpy(), S_ref, 1e-5, "pool")
     assert np.array_equal(_bf16_np(conv_dev), conv_ref)
+
+
+def test_conv_prologue_negative_cu_start_is_contained():
+    """cu_seqlens starting below 0 breaks the call's precondition (the host
+    cannot read the device array).  The prologue takes zeros for the window
+    slots before token 0 instead of reading before the input buffer, raises
+    bit 0 of the device error word, and a valid call afterwards is clean and
+    matches the oracle."""
+    import torch
+    kda = _kda()
+    L = ki.gen_layer(490, [50, 50], H=2, with_conv0=True)
+    d = dev_tensor
+    cin = d(L.conv0).view(torch.bfloat16)
+    kda.device_error(reset=True)
+    kda.conv_prologue(d(L.xq), d(L.xk), d(L.xv), d(L.conv_w), d(np.array([-3, 50, 100], np.int32)),
+                      conv_in=cin, q_scale=QS)
+    torch.cuda.synchronize()
+    assert kda.device_error(reset=True) & 1, "the negative sequence start was not flagged"
+    q, k, v, co = _prologue_gpu(L)
+    _check_no_device_error()
+    f = olayer._f64
+    rq, rk, rv, rco = olayer.prologue(f(L.xq), f(L.xk), f(L.xv), L.conv_w, f(L.conv0),
+                                      L.cu_seqlens, QS)
+    for name, x, r in (("q", q, rq), ("k", k, rk), ("v", v, rv)):
+        _assert_bf16_rounding_of(_bf16_np(x), r, "prologue " + name)
+    assert np.array_equal(_bf16_np(co), rco)

@@ -1,8 +1,9 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle on
-the same seeded inputs.  Small cases are compared element by element over
-every output; the full-size workloads are compared on sampled (sequence,
-head) units that the oracle computes one by one, plus properties that hold
-at any size."""
+the same seeded inputs, element by element over every output: the small
+ragged cases and all five full-size workloads (the all-fp32 prefill, the
+4K prefill, the 100-step batched decode, the 32K prefill with carried
+state, and the 65,536-token varlen batch with its decode step), plus
+properties that hold at any size."""
 import numpy as np
 import pytest
 
@@ -42,31 +43,21 @@ def test_decode_small(dtype, B, H):
     assert_close(Sd.cpu().numpy(), S_ref, _tol(dtype), "decode S")
 
 
-def test_decode_b64_100_steps_sampled():
-    """Batched decode, B=64, H=96, 100 consecutive in-place steps; 24 sampled
-    (b, h) states are followed by the oracle in fp64 along the whole run."""
-    w = ki.WORKLOADS["decode_b64"]
+def test_decode_b64_100_steps_full():
+    """Batched decode, B=64, H=96, 100 consecutive in-place steps: every
+    state is followed by the oracle in fp64 along the whole run; o of every
+    step and every final state against it."""
     S, steps = ki.workload_decode("decode_b64")
-    r = np.random.Generator(np.random.PCG64(77))
-    units = sorted({(int(b), int(h)) for b, h in zip(r.integers(0, w["B"], 24),
-                                                      r.integers(0, w["H"], 24))})
-    units += [(0, 0), (w["B"] - 1, w["H"] - 1)]
-    S_ref = {u: S[u].astype(np.float64) for u in units}
+    S_ref = S.astype(np.float64)
     Sd = dev_tensor(S)
+    worst = 0.0
     for it, step in enumerate(steps):
         o = decode_on_gpu(Sd, step)
-        got, want = [], []
-        for u in units:
-            o_u, S_u = oracle.run_unit(step.q, step.k, step.v, step.g, step.beta, S_ref[u],
-                                       u[0], u[0] + 1, u[1])
-            S_ref[u] = S_u
-            got.append(o[u])
-            want.append(o_u[0])
-        assert_close(np.stack(got), np.stack(want), TOL_BF16, "decode o at step %d" % it)
+        o_ref, S_ref = oracle.decode(S_ref, step)
+        worst = max(worst, assert_close(o, o_ref, TOL_BF16, "decode o at step %d" % it))
     S_fin = Sd.cpu().numpy()
-    assert_close(np.stack([S_fin[u] for u in units]), np.stack([S_ref[u] for u in units]),
-                 TOL_BF16, "decode S after 100 steps")
-    assert np.isfinite(S_fin).all()
+    e = assert_close(S_fin, S_ref, TOL_BF16, "decode S after 100 steps")
+    print("decode B=64 x 100 steps: worst o %.2e, final S %.2e" % (worst, e))
 
 
 # ---------------------------------------------------------------- prefill, small
@@ -209,41 +200,65 @@ def test_prefill_4k_full():
     assert_close(S, S_ref, TOL_BF16, "S_out")
 
 
-def test_prefill_32k_carry_sampled():
-    """bf16 prefill, H=96, T=32768, S0 ~ N(0, 0.02^2): sampled heads vs the oracle."""
+def _oracle_heads(inp, n, heads):
+    """The oracle's o [len_n, len(heads), dv] and S [len(heads), dk, dv] of
+    sequence n on the given heads."""
+    ref = oracle.prefill(inp, units=[(n, h) for h in heads])
+    o = np.stack([ref[(n, h)][0] for h in heads], axis=1)
+    S = np.stack([ref[(n, h)][1] for h in heads])
+    return o, S
+
+
+def test_prefill_32k_carry_full():
+    """bf16 prefill, H=96, T=32768, S0 ~ N(0, 0.02^2): every head, every
+    element of o and of the final state against the oracle (the long chain
+    of carried fp32 state is where accumulated error would show).  The
+    oracle runs 16 heads at a time to bound host memory; the bar applies to
+    the whole tensor."""
     inp = ki.workload_prefill("prefill_32k_carry")
     o, S = prefill_on_gpu(inp)
     assert np.isfinite(o).all() and np.isfinite(S).all()
-    heads = [0, 37, 95]
-    ref = oracle.prefill(inp, units=[(0, h) for h in heads])
-    for h in heads:
-        o_r, S_r = ref[(0, h)]
-        assert_close(o[:, h], o_r, TOL_BF16, "o head %d" % h)
-        assert_close(S[0, h], S_r, TOL_BF16, "S_out head %d" % h)
+    o_ref_max = S_ref_max = 0.0
+    o_err = S_err = 0.0
+    for h0 in range(0, inp.H, 16):
+        heads = list(range(h0, min(inp.H, h0 + 16)))
+        o_r, S_r = _oracle_heads(inp, 0, heads)
+        o_err = max(o_err, float(np.abs(o[:, heads].astype(np.float64) - o_r).max()))
+        S_err = max(S_err, float(np.abs(S[0, heads].astype(np.float64) - S_r).max()))
+        o_ref_max = max(o_ref_max, float(np.abs(o_r).max()))
+        S_ref_max = max(S_ref_max, float(np.abs(S_r).max()))
+    print("32K carry: o %.2e, S %.2e" % (o_err / o_ref_max, S_err / S_ref_max))
+    assert o_err <= TOL_BF16 * o_ref_max, "o: max rel err %.3e" % (o_err / o_ref_max)
+    assert S_err <= TOL_BF16 * S_ref_max, "S_out: max rel err %.3e" % (S_err / S_ref_max)
 
 
-def test_varlen_64k_then_decode_sampled():
-    """Varlen packed prefill (8 sequences, 65536 tokens) with per-sequence S0,
-    then one decode step for all 8 from the prefill's final states."""
-    import torch
+def test_varlen_64k_then_decode_full():
+    """Varlen packed prefill (8 sequences, 65536 tokens) with per-sequence
+    S0, then one decode step for all 8 from the final states: every
+    (sequence, head) unit against the oracle, the bar applied per sequence
+    (o and S_out of each sequence over all its heads), and the decode step's
+    o and states against the oracle's decode from the oracle's own final
+    states."""
     pre, step = ki.workload_varlen_with_decode("varlen_64k")
     o, S = prefill_on_gpu(pre)
     assert np.isfinite(o).all() and np.isfinite(S).all()
-    units = [(7, 0), (7, 95), (5, 12), (0, 3), (3, 50), (6, 64)]
-    ref = oracle.prefill(pre, units=units)
-    cu = pre.cu_seqlens
-    for (n, h) in units:
-        o_r, S_r = ref[(n, h)]
-        assert_close(o[cu[n]:cu[n + 1], h], o_r, TOL_BF16, "o seq %d head %d" % (n, h))
-        assert_close(S[n, h], S_r, TOL_BF16, "S_out seq %d head %d" % (n, h))
     Sd = dev_tensor(S)
     od = decode_on_gpu(Sd, step)
     Sd_np = Sd.cpu().numpy()
-    for (n, h) in units:
-        o_r, S_r = oracle.run_unit(step.q, step.k, step.v, step.g, step.beta, ref[(n, h)][1],
-                                   n, n + 1, h)
-        assert_close(od[n, h], o_r[0], TOL_BF16, "decode o seq %d head %d" % (n, h))
-        assert_close(Sd_np[n, h], S_r, TOL_BF16, "decode S seq %d head %d" % (n, h))
+    cu = pre.cu_seqlens
+    heads = list(range(pre.H))
+    S_ref = np.empty((pre.N, pre.H, 128, 128), dtype=np.float64)
+    worst = 0.0
+    for n in range(pre.N):
+        o_r, S_ref[n] = _oracle_heads(pre, n, heads)
+        worst = max(worst, assert_close(o[cu[n]:cu[n + 1]], o_r, TOL_BF16, "o of sequence %d" % n))
+        assert_close(S[n], S_ref[n], TOL_BF16, "S_out of sequence %d" % n)
+        del o_r
+    od_ref, Sd_ref = oracle.decode(S_ref, step)
+    for n in range(pre.N):
+        assert_close(od[n], od_ref[n], TOL_BF16, "decode o of sequence %d" % n)
+        assert_close(Sd_np[n], Sd_ref[n], TOL_BF16, "decode S of sequence %d" % n)
+    print("varlen 64K: worst per-sequence o error %.2e" % worst)
 
 
 # ---------------------------------------------------------------- state pools

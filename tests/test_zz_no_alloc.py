@@ -1,16 +1,18 @@
 """kda_prefill_chunked_noalloc: the prefill with its workspace in the
 library's fixed device array.  Two calls in a row must match the pool-backed
-entry point; inputs that need more scratch than the array holds are rejected
-before any launch.  (This file is collected last on purpose: it must pass
-both alone and after every other test.)"""
+entry point and, on their own, the fp64 oracle within the bf16 bar; inputs
+that need more scratch than the array holds are rejected before any launch.
+(This file is collected last on purpose: it must pass both alone and after
+every other test.)"""
 import ctypes
 
 import numpy as np
 import pytest
 
 import kda_inputs as ki
+import oracle
 
-from kda_testlib import dev_tensor, rel_err
+from kda_testlib import TOL_BF16, assert_close, dev_tensor, rel_err
 
 KDA_ERR_WORKSPACE = 6
 SCRATCH = 64 << 20
@@ -49,6 +51,7 @@ def test_noalloc_matches_pool_entry_point_twice(lens, H, with_s0):
     s0 = None if inp.S0 is None else dev_tensor(inp.S0)
     o_ref, S_ref = kda.prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, S0=s0)
     o_ref, S_ref = o_ref.cpu().numpy(), S_ref.cpu().numpy()
+    o_or, S_or = oracle.prefill(inp)
     T, N = sum(lens), len(lens)
     o = torch.empty((T, H, 128), dtype=torch.float32, device="cuda")
     S = torch.empty((N, H, 128, 128), dtype=torch.float32, device="cuda")
@@ -64,3 +67,5 @@ def test_noalloc_matches_pool_entry_point_twice(lens, H, with_s0):
         # same kernels and inputs; only the order of a shared-memory sum may differ
         assert rel_err(on, o_ref) <= 1e-5, "call %d: o differs from kda_prefill_chunked" % call
         assert rel_err(Sn, S_ref) <= 1e-5, "call %d: S differs from kda_prefill_chunked" % call
+        assert_close(on, o_or, TOL_BF16, "call %d: o against the oracle" % call)
+        assert_close(Sn, S_or, TOL_BF16, "call %d: S against the oracle" % call)
