@@ -32,9 +32,11 @@
  *     always fp32.  g is the log-decay (decay = exp(g)); beta is already in
  *     [0, 1] (any sigmoid is applied by the caller); q is used as given (any
  *     1/sqrt(dk) scale is folded in by the caller).
- *   - Supported sizes: dk = dv = 128.  Preconditions not checked at run time:
- *     -5 <= g <= 0 (the model's gate bound; the chunked kernels' decay
- *     folding relies on it), finite inputs.
+ *   - Supported sizes: dk = dv = 128.  Preconditions: -5 <= g <= 0 (the
+ *     model's gate bound; the tensor-core prefill's decay folding relies on
+ *     it and raises bit 2 of the device error word when it sees a gate
+ *     outside that range, or a NaN, in a prefill's input), finite inputs
+ *     (not checked elsewhere).
  *   - Every pointer must be 16-byte aligned (KDA_ERR_ALIGN otherwise).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream); they never synchronise.  Arguments are validated on
@@ -96,7 +98,12 @@ const char *kda_status_string(int status);
  *   o          [T, H, dv]  fp32, written
  *   S_out      [N, H, dk, dv] fp32, written; may alias S0 exactly (in place)
  *   cu_seqlens [N + 1]     int32 DEVICE array, cu_seqlens[0] = 0,
- *                          non-decreasing, cu_seqlens[N] = T (not checked)
+ *                          non-decreasing, cu_seqlens[N] = T.  The host
+ *                          cannot read it; the kernels check it on the
+ *                          device: entries below 0, above T or decreasing
+ *                          raise bit 0 of the device error word, and no
+ *                          kernel then reads or writes outside the buffers
+ *                          sized for T (the outputs are invalid)
  *   N          number of sequences (>= 1); T total tokens (>= 0, < 2^31)
  *   H          heads (>= 1); dk, dv must be 128
  *   chunk      16, 32 or 64.  bf16 inputs with chunk 64 run on the
@@ -151,7 +158,10 @@ int kda_prefill_chunked_events(const void *q, const void *k, const void *v,
  *
  * First call on each device: the library looks up the array's address
  * (cudaGetSymbolAddress, which may load the library's device image); make
- * that first call before any stream capture begins.  The array is shared by
+ * that first call before any stream capture begins.  The address is cached
+ * with the identity of the device's context; after a cudaDeviceReset the
+ * next call looks it up again (so that call, too, should come before any
+ * capture).  The array is shared by
  * all calls on a device: two calls whose executions overlap (different
  * streams, or different host threads) race on it and must be serialised by
  * the caller.  Returns KDA_OK or a kda_status_t.
@@ -337,14 +347,24 @@ int kda_decode_layer_step(const void *xq, const void *xk, const void *xv, const 
                           void *stream);
 
 /*
- * Device-side error word of the library.  Bit 0: the tensor-core prefill
- * kernels never wait without bound: if one of their waits on an asynchronous copy or
- * on the tensor cores runs past its iteration limit they set a bit here,
- * release their tensor memory and exit (the outputs are then invalid).  The
- * state pass also sets it when a sequence's chunk count does not match the
- * workspace it was sized for (cu_seqlens inconsistent with T).  Bit 1: a
- * kda_decode_step_pool or kda_decode_layer_step slot index was past the end
- * of the pool.
+ * Device-side error word of the library.  The outputs of a call that raised
+ * a bit are invalid.
+ *   Bit 0: the tensor-core prefill kernels never wait without bound: if one
+ *          of their waits on an asynchronous copy or on the tensor cores
+ *          runs past its iteration limit they set this bit, release their
+ *          tensor memory and exit.  Also set when cu_seqlens breaks its
+ *          precondition (an entry below 0 or above T, or a decrease), by
+ *          the prefill paths and the conv prologue, which then touch no
+ *          memory outside their buffers.
+ *   Bit 1: a kda_decode_step_pool or kda_decode_layer_step slot index was
+ *          past the end of the pool.
+ *   Bit 2: the tensor-core prefill saw a gate g outside [-5, 0] or a NaN
+ *          (its decay folding is sized for the model's gate bound).
+ *   Bit 3: debug builds only (libkda_gb300_debug.so, built with
+ *          python -m kda_linear_attention_gb300.build --debug and loaded by
+ *          the Python binding when KDA_GB300_DEBUG=1): an index check on a
+ *          kernel's global-memory addressing failed; the access was kept
+ *          inside its buffer.
  *
  *   code   host pointer, receives the word (0 = no error since the last reset)
  *   reset  nonzero: clear the word after reading it
