@@ -16,7 +16,7 @@
  * Conventions shared by every call
  *   - Pointers are DEVICE pointers unless marked "host"; the caller owns all
  *     memory it passes.  The tensor-core prefill (bf16, chunk 64) also needs
- *     a scratch workspace of about 89 KB per (64-token chunk, head):
+ *     a scratch workspace of 65 KB per (64-token chunk, head):
  *     kda_prefill_chunked takes it from a library-owned stream-ordered memory
  *     pool on the current device, which keeps that memory for later calls;
  *     kda_prefill_chunked_ws runs in a buffer the caller passes, and
@@ -35,8 +35,10 @@
  *   - Supported sizes: dk = dv = 128.  Preconditions: -5 <= g <= 0 (the
  *     model's gate bound; the tensor-core prefill's decay folding relies on
  *     it and raises bit 2 of the device error word when it sees a gate
- *     outside that range, or a NaN, in a prefill's input), finite inputs
- *     (not checked elsewhere).
+ *     outside that range, or a NaN, in a prefill's input); for the
+ *     tensor-core prefill, |q| |k| and |v| far below 65504 (q and k are
+ *     L2-normalised in the model, as the layer's prologue makes them; u is
+ *     checked, bit 4 below); finite inputs (not checked elsewhere).
  *   - Every pointer must be 16-byte aligned (KDA_ERR_ALIGN otherwise).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream); they never synchronise.  Arguments are validated on
@@ -150,9 +152,9 @@ int kda_prefill_chunked_events(const void *q, const void *k, const void *v,
  *
  * The tensor-core path (bf16, chunk 64, T > 0) takes its workspace from a
  * fixed 64 MiB array in the library's device image instead of the pool.  It
- * needs 1024 * ceil(4 (N + 1) / 1024) + (ceil(T / 64) + N) * H * 91136
+ * needs 1024 * ceil(4 (N + 1) / 1024) + (ceil(T / 64) + N) * H * 66560
  * bytes; larger inputs are rejected with KDA_ERR_WORKSPACE before anything
- * is launched (for H = 96 and one sequence: T <= 384).  Every other dtype /
+ * is launched (for H = 96 and one sequence: T <= 576).  Every other dtype /
  * chunk combination runs the CUDA-core kernel, which needs no workspace.
  * Nothing in the array has to be cleared between calls.
  *
@@ -175,7 +177,7 @@ int kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v,
 /*
  * Bytes of caller-owned workspace that kda_prefill_chunked_ws needs for these
  * sizes: the records of the tensor-core path (bf16, chunk 64, T > 0),
- * 1024 * ceil(4 (N + 1) / 1024) + (ceil(T / 64) + N) * H * 91136; 0 for every
+ * 1024 * ceil(4 (N + 1) / 1024) + (ceil(T / 64) + N) * H * 66560; 0 for every
  * other combination (the CUDA-core kernel needs none) and for invalid sizes.
  * Host-only, no CUDA call.
  */
@@ -365,6 +367,10 @@ int kda_decode_layer_step(const void *xq, const void *xk, const void *xv, const 
  *          the Python binding when KDA_GB300_DEBUG=1): an index check on a
  *          kernel's global-memory addressing failed; the access was kept
  *          inside its buffer.
+ *   Bit 4: the tensor-core prefill's intermediate u = beta (v - ...) (the
+ *          delta-rule correction of each token, carried into its second
+ *          state-pass product in fp16) reached 65504 in magnitude or NaN:
+ *          v far outside a model's activation range.
  *
  *   code   host pointer, receives the word (0 = no error since the last reset)
  *   reset  nonzero: clear the word after reading it

@@ -14,7 +14,8 @@ constexpr int kDV = 128;
 constexpr unsigned kErrWait = 1u;        // a bounded wait gave up, or cu_seqlens broke the call's precondition
 constexpr unsigned kErrSlot = 2u;        // a pool slot index past the end of the pool
 constexpr unsigned kErrGateRange = 4u;   // the tensor-core prefill saw a gate g outside [-5, 0] (or NaN)
-constexpr unsigned kErrBounds = 8u;      // debug builds (KDA_DEBUG): an index check failed; the access was skipped
+constexpr unsigned kErrBounds = 8u;      // debug builds (KDA_DEBUG): an index check failed; the access was kept in bounds
+constexpr unsigned kErrFp16Range = 16u;  // the tensor-core prefill's u left fp16's finite range (|u| >= 65504 or NaN)
 // Lower bound of the log-decay gate that the decay folding of the
 // tensor-core prefill is sized for (the model's gate lower bound).
 constexpr float kGateMin = -5.0f;

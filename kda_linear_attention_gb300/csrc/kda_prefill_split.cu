@@ -17,8 +17,8 @@
 // pass then does, per chunk, two rounds of MMAs and two epilogues:
 //   D_U[j][r] = -(W S)^T + (T' V)^T,   D_O[j][r] = (Q0 S)^T      (bf16;
 //                                                   S as hi + lo pieces)
-//   u = D_U + beta v  (fp32, rounded to tf32 in TMEM)
-//   D_O += (A' U)^T,   S^T += (Kbar^T U)^T                        (tf32)
+//   u = D_U + beta v  (fp32; its fp16 copy in TMEM is round 2's operand)
+//   D_O += (A' U)^T,   S^T += (Kbar^T U)^T                        (fp16)
 // with S^T kept in fp32 in TMEM for the whole sequence (lane j, column i) and
 // pre-scaled by e^{b_L} while the first round runs.
 //
@@ -29,10 +29,12 @@
 // key side a stack of four operands k_s e^{sigma_p - b_s} (160 rows), and one
 // M=128, N=160 MMA gives both Gram matrices.
 //
-// Precision: bf16 operands for the Gram matrices, W, Q0 and T'; the state
-// enters round 1 as two bf16 pieces (hi + lo, 16 significant bits), so the
-// products with S lose only the bf16 rounding of W and Q0; tf32 (software
-// round-to-nearest) for A' U and Kbar^T U; the diagonal terms (beta_r v_r,
+// Precision: bf16 operands for the Gram matrices, W, Q0 and T', with the
+// diagonal blocks of the query-side Gram corrected by the keys' bf16 low
+// parts; the state enters round 1 as two bf16 pieces (hi + lo, 16
+// significant bits), so the products with S lose only the bf16 rounding of
+// W and Q0; fp16 (11 significant bits, every operand bounded: |A'|, |Kbar|
+// <= 1 for unit q, k) for A' U and Kbar^T U; the diagonal terms (beta_r v_r,
 // beta_r K0_r, (q_r.k_r) u_r) in fp32 outside the MMAs.
 #include <cuda_runtime.h>
 
@@ -97,10 +99,10 @@ __device__ __forceinline__ void ld_f2x4(const float *p, float2 (&x)[4]) {
 // pass feeds it to the tensor cores, so that one bulk copy places it.
 constexpr uint32_t R_WQ = 0;        // [-W ; Q0] bf16, 128 rows x 128, K-major sw (two 16 KB halves)
 constexpr uint32_t R_T = 32768;     // T' bf16 K-major il [r][s], 8 KB
-constexpr uint32_t R_A = 40960;     // A' tf32 K-major il [r][s], 16 KB
-constexpr uint32_t R_KB = 57344;    // Kbar^T tf32 K-major il [i][s], 32 KB
-constexpr uint32_t R_VEC = 90112;   // beta[64], q.k[64], e^{b_L}[128] (fp32)
-constexpr uint32_t REC_BYTES = 91136;
+constexpr uint32_t R_A = 40960;     // A' fp16 K-major il [r][s], 8 KB
+constexpr uint32_t R_KB = 49152;    // Kbar^T fp16 K-major il [i][s], 16 KB
+constexpr uint32_t R_VEC = 65536;   // beta[64], q.k[64], e^{b_L}[128] (fp32)
+constexpr uint32_t REC_BYTES = 66560;
 static_assert(REC_BYTES % 1024 == 0, "records stay 1 KB aligned");
 
 // ============================================================================
@@ -469,7 +471,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 *reinterpret_cast<uint4 *>(rec + R_WQ + sw_chunk(64 + r, cc, 16384)) = pack_bf8x2(q0);
                 *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, cc, 8192)) = pack_bf8x2(k0);
             }
-            // Kbar^T tf32 K-major il [i][s]: a 4x4 transpose of channel pairs
+            // Kbar^T fp16 K-major il [i][s]: a 4x4 transpose of channel pairs
             // inside each quad of lanes (4 consecutive rows) in two butterfly
             // stages leaves every lane 4 consecutive s for channels 2bq, 2bq+1
             {
@@ -509,8 +511,8 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     const float w2 = b0 ? v[3][f] : v[2][f], w3 = b0 ? v[2][f] : v[3][f];
                     const float y0 = b1 ? w2 : w0, y1 = b1 ? w3 : w1;
                     const float y2 = b1 ? w0 : w2, y3 = b1 ? w1 : w3;
-                    *reinterpret_cast<uint4 *>(rec + R_KB + km_tf32(i0 + f, s0r, 2048)) =
-                        make_uint4(to_tf32(y0), to_tf32(y1), to_tf32(y2), to_tf32(y3));
+                    *reinterpret_cast<uint2 *>(rec + R_KB + km_bf16(i0 + f, s0r, 1024)) =
+                        make_uint2(pack_h2(y0, y1), pack_h2(y2, y3));
                 }
             }
         }
@@ -571,7 +573,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         tc_fence_after();
         // X is consumed: the next job's q and k
         if (t == 0 && has_next) issue_qk(Jn);
-        // ===== Gram epilogue -> A' (tf32, record) and M = Diag(beta) G^kk (fp32)
+        // ===== Gram epilogue -> A' (fp16, record) and M = Diag(beta) G^kk (fp32)
         float *Mm = reinterpret_cast<float *>(sm + SA_M);
         {
             const int ch = t & 127;
@@ -607,8 +609,8 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                         x4[e] = (have && s < r) ? val : 0.f;
                     }
                     if (qside) {
-                        *reinterpret_cast<uint4 *>(rec + R_A + km_tf32(r, 16 * qt + 4 * j, 2048)) =
-                            make_uint4(to_tf32(x4[0]), to_tf32(x4[1]), to_tf32(x4[2]), to_tf32(x4[3]));
+                        *reinterpret_cast<uint2 *>(rec + R_A + km_bf16(r, 16 * qt + 4 * j, 1024)) =
+                            make_uint2(pack_h2(x4[0], x4[1]), pack_h2(x4[2], x4[3]));
                     } else {
                         *reinterpret_cast<float4 *>(Mm + r * MLD + 16 * qt + 4 * j) =
                             make_float4(br * x4[0], br * x4[1], br * x4[2], br * x4[3]);
@@ -849,8 +851,8 @@ constexpr int NTB = NEPI + 64;
 constexpr uint32_t SB_WQ = 0;             // [-W ; Q0] (bulk copy 1, with T')
 constexpr uint32_t SB_T = 32768;          // T'
 constexpr uint32_t SB_A = 40960;          // A' (bulk copy 2, with Kbar^T)
-constexpr uint32_t SB_KB = 57344;         // Kbar^T
-constexpr uint32_t SB_VEC = 90112;        // 2 x 1 KB record vectors (double-buffered)
+constexpr uint32_t SB_KB = 49152;         // Kbar^T
+constexpr uint32_t SB_VEC = 65536;        // 2 x 1 KB record vectors (double-buffered)
 constexpr uint32_t SB_V = 92160;          // 16 KB: v chunk sw (TMA) = V^T, MN-major operand
                                           // 108544..141312 free: the bf16 pieces of S^T live in TMEM
 constexpr uint32_t SB_O = 141312;         // 32 KB: o of even chunks, 4 x [64 r][32 j] fp32 (TMA store source)
@@ -861,7 +863,8 @@ constexpr uint32_t SB_EB = SB_MISC + 576; // 2 x 512 B: e^{b_L} of the chunk aft
 constexpr uint32_t SMEM_B_USED = SB_EB + 1024;
 constexpr uint32_t SMEM_B_ALLOC = SMEM_B_USED + 1024;
 static_assert(SB_T == R_T && SB_A == R_A && SB_KB == R_KB, "record pieces map onto shared memory");
-static_assert(SB_KB == SB_A + 16384, "A' and Kbar^T form one N = 192 operand");
+static_assert(SB_KB == SB_A + 8192, "A' and Kbar^T form one N = 192 operand");
+static_assert(SB_VEC + 2048 <= SB_V, "record vectors before v");
 static_assert(SMEM_B_ALLOC <= 232448, "dynamic shared memory limit (227 KB)");
 static_assert(SB_EB % 16 == 0, "bulk copy destination alignment");
 // TMEM columns: U^T | O^T | S^T master | S^T as two bf16 pieces.  Round 1
@@ -873,6 +876,7 @@ constexpr uint32_t TMB_O = 64;            // O^T, 64 columns
 constexpr uint32_t TMB_S = 128;           // S^T master fp32 (lane j, column i), 128 columns
 constexpr uint32_t TMB_SB = 256;          // S^T high bf16 piece (lane j, column i / 2: pairs i, i + 1), 64 columns
 constexpr uint32_t TMB_SL = 320;          // S^T low bf16 piece, same layout, 64 columns
+constexpr uint32_t TMB_UP = 384;          // U^T as fp16 pairs (s, s + 1 per column): round 2's A, 32 columns
 constexpr uint32_t TMEM_COLS_B = 512;
 constexpr uint32_t COPY1 = R_A - R_WQ;    // bytes of [-W ; Q0] + T'
 constexpr uint32_t COPY2 = R_VEC - R_A;   // bytes of A' + Kbar^T
@@ -1017,12 +1021,10 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
     // once the previous chunk's v is consumed
     auto issue_a = [&](int j) {
         const uint8_t *r = rec_at(j);
-        const bool next = j + 1 < nch;
-        mbar_arrive_expect_tx(bar_a, COPY1 + 1024 + 16384 + (next ? 512 : 0));
+        mbar_arrive_expect_tx(bar_a, COPY1 + 1024 + 16384);
         ++issued_a;
         bulk_load(sm + SB_WQ, r + R_WQ, COPY1, bar_a);
         bulk_load(sm + SB_VEC + 1024 * (j & 1), r + R_VEC, 1024, bar_a);
-        if (next) bulk_load(sm + SB_EB + 512 * ((j + 1) & 1), rec_at(j + 1) + R_VEC + 512, 512, bar_a);
     };
     auto issue_v = [&](int j) {
         tma_load_3d(sm + SB_V, &map_v, bar_a, 0, h, tok0 + j * C);
@@ -1169,9 +1171,9 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         if (epi) {
             if (!mbar_wait(bar_a, par, kWaitLimit)) bad = true;   // vec and v of this chunk
             __syncwarp();
-            if (j == 0) {
-                // S <- Diag(e^{b_L}) S for the first chunk (later chunks get
-                // it at the end of the chunk before)
+            {
+                // S <- Diag(e^{b_L}) S for this chunk's round 2, while round 1
+                // runs (it reads only the bf16 pieces): off the serial chain
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const uint32_t col = 32 * qt + 16 * hh;
@@ -1184,7 +1186,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                     tmem_st16(tmem + lane_base + TMB_S + col, sv);
                 }
             }
-            // ===== u = D_U + beta v, rounded to tf32 in place in TMEM =========
+            // ===== u = D_U + beta v; round 2's A operand U^T as fp16 pairs =====
             float bt[16], vv[16];
             ld_vec16(vec + 16 * qt, bt);
 #pragma unroll
@@ -1194,13 +1196,17 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             tc_fence_after();
             tmem_ld16(tmem + lane_base + TMB_U + 16 * qt, uv);
             tmem_wait_ld();
-            float ut[16];
+            float up[8];
+            bool u_big = false;               // |u| beyond fp16's finite range (or NaN)
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 uv[k] = fmaf(bt[k], vv[k], uv[k]);
-                ut[k] = __uint_as_float(to_tf32(uv[k]));
+                u_big |= !(fabsf(uv[k]) < 65504.f);
             }
-            tmem_st16(tmem + lane_base + TMB_U + 16 * qt, ut);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) up[c] = __uint_as_float(pack_h2(uv[2 * c], uv[2 * c + 1]));
+            tmem_st8(tmem + lane_base + TMB_UP + 8 * qt, up);
+            if (__any_sync(0xffffffffu, u_big) && (t & 31) == 0) atomicOr(&g_kda_device_error, kErrFp16Range);
             tmem_wait_st();
         }
         tc_fence_before();
@@ -1210,14 +1216,14 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         }
         tc_fence_after();
 
-        // ===== round 2: [D_O | S^T] += U^T [A' ; Kbar^T]^T (tf32, U^T from TMEM, N = 192)
+        // ===== round 2: [D_O | S^T] += U^T [A' ; Kbar^T]^T (fp16, U^T from TMEM, N = 192)
         if (t == T_MMA) {
             if (mbar_wait(bar_b, par, kWaitLimit)) {
-                const uint32_t id2 = instr_desc(kFmtTF32, 128, 192, 0, 0);
+                const uint32_t id2 = instr_desc(kFmtF16, 128, 192, 0, 0);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bak = smem_desc(smem_u32(sm + SB_A + 256 * kk), 128, 2048, kSwizzleNone);
-                    mma_tf32_ts(tmem + TMB_O, tmem + TMB_U + 8 * kk, bak, id2, 1);
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t bak = smem_desc(smem_u32(sm + SB_A + 256 * kk), 128, 1024, kSwizzleNone);
+                    mma_bf16_ts(tmem + TMB_O, tmem + TMB_UP + 8 * kk, bak, id2, 1);
                 }
                 mma_commit(bar_mma);
                 ++issued_mma;
@@ -1249,7 +1255,6 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             float qk[16];
             ld_vec16(vec + 64 + 16 * qt, qk);
             const bool next = j + 1 < nch;
-            const float *ebn = reinterpret_cast<const float *>(sm + SB_EB + 512 * (par ^ 1u));
             if (!mbar_wait(bar_mma, 1u, kWaitLimit)) bad = true;
             __syncwarp();
             tc_fence_after();
@@ -1261,20 +1266,15 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                 for (int k = 0; k < 16; ++k) po[k] = fmaf(qk[k], uv[k], ov[k]);
             }
             {
+                if (next) {
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float sv[16], hi[8], lo[8];
-                    tmem_ld16(tmem + lane_base + TMB_S + 32 * qt + 16 * hh, sv);
-                    tmem_wait_ld();
-                    split_bf16_pairs(sv, hi, lo);
-                    tmem_st8(tmem + lane_base + TMB_SB + 16 * qt + 8 * hh, hi);
-                    tmem_st8(tmem + lane_base + TMB_SL + 16 * qt + 8 * hh, lo);
-                    if (next) {
-                        float eb[16];
-                        ld_vec16(ebn + 32 * qt + 16 * hh, eb);
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) sv[c] *= eb[c];
-                        tmem_st16(tmem + lane_base + TMB_S + 32 * qt + 16 * hh, sv);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float sv[16], hi[8], lo[8];
+                        tmem_ld16(tmem + lane_base + TMB_S + 32 * qt + 16 * hh, sv);
+                        tmem_wait_ld();
+                        split_bf16_pairs(sv, hi, lo);
+                        tmem_st8(tmem + lane_base + TMB_SB + 16 * qt + 8 * hh, hi);
+                        tmem_st8(tmem + lane_base + TMB_SL + 16 * qt + 8 * hh, lo);
                     }
                 }
             }

@@ -5,6 +5,7 @@
 
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <mutex>
 
@@ -47,6 +48,10 @@ __device__ __forceinline__ float bf(const uint8_t *p) {
 }
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
 }
 __device__ __forceinline__ uint4 pack_bf8(const float (&x)[8]) {
