@@ -15,8 +15,8 @@
 // one chunk only; the intra-chunk kernel computes it for all chunks of all
 // sequences in parallel and writes one record per (chunk, head).  The state
 // pass then does, per chunk, two rounds of MMAs and two epilogues:
-//   D_U[j][r] = -(W S)^T + (T' V)^T,   D_O[j][r] = (Q0 S)^T      (bf16;
-//                                                   S as hi + lo pieces)
+//   D_U[j][r] = -(W S)^T + (T' V)^T,   D_O[j][r] = (Q0 S)^T
+//                                      (fp16 S, W, Q0; bf16 T', V)
 //   u = D_U + beta v  (fp32; its fp16 copy in TMEM is round 2's operand)
 //   D_O += (A' U)^T,   S^T += (Kbar^T U)^T                        (fp16)
 // with S^T kept in fp32 in TMEM for the whole sequence (lane j, column i) and
@@ -29,13 +29,16 @@
 // key side a stack of four operands k_s e^{sigma_p - b_s} (160 rows), and one
 // M=128, N=160 MMA gives both Gram matrices.
 //
-// Precision: bf16 operands for the Gram matrices, W, Q0 and T', with the
-// diagonal blocks of the query-side Gram corrected by the keys' bf16 low
-// parts; the state enters round 1 as two bf16 pieces (hi + lo, 16
-// significant bits), so the products with S lose only the bf16 rounding of
-// W and Q0; fp16 (11 significant bits, every operand bounded: |A'|, |Kbar|
-// <= 1 for unit q, k) for A' U and Kbar^T U; the diagonal terms (beta_r v_r,
-// beta_r K0_r, (q_r.k_r) u_r) in fp32 outside the MMAs.
+// Precision: bf16 operands for the Gram matrices and T' (whose partner V
+// arrives in bf16), with the diagonal blocks of the query-side Gram
+// corrected by the keys' bf16 low parts; fp16 (11 significant bits) for
+// every product with the state and its inputs: S's copy, W, Q0 and the W
+// product's T Diag(beta) and K0 in round 1, A', Kbar^T and U in round 2.
+// Each of those is bounded (|q|, |k| <= 1 after the L2 norm; the decay
+// factors <= 1; S and u of the order of v), well inside fp16's range; u
+// (and through it an overflowing state copy) is checked.  The diagonal
+// terms (beta_r v_r, beta_r K0_r, (q_r.k_r) u_r) stay in fp32 outside the
+// MMAs, and the state itself is fp32 in TMEM for the whole sequence.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -97,7 +100,7 @@ __device__ __forceinline__ void ld_f2x4(const float *p, float2 (&x)[4]) {
 // ---- the per-(chunk, head) record ------------------------------------------
 // Each piece is stored in the shared-memory operand layout in which the state
 // pass feeds it to the tensor cores, so that one bulk copy places it.
-constexpr uint32_t R_WQ = 0;        // [-W ; Q0] bf16, 128 rows x 128, K-major sw (two 16 KB halves)
+constexpr uint32_t R_WQ = 0;        // [-W ; Q0] fp16, 128 rows x 128, K-major sw (two 16 KB halves)
 constexpr uint32_t R_T = 32768;     // T' bf16 K-major il [r][s], 8 KB
 constexpr uint32_t R_A = 40960;     // A' fp16 K-major il [r][s], 8 KB
 constexpr uint32_t R_KB = 49152;    // Kbar^T fp16 K-major il [i][s], 16 KB
@@ -166,9 +169,9 @@ constexpr uint32_t SA_X = 0;              // 32 KB: q|k (TMA) -> X [128][128] sw
 constexpr uint32_t SA_KH = 32768;         // 40 KB: g (TMA) -> Khat [160][128] sw (B of the Gram)
 constexpr uint32_t SA_M = SA_KH;          //   after the Gram: M / T fp32 [64][68] (17408 B)
 constexpr uint32_t SA_Y = SA_KH + 17408;  //   solve temporaries (4 KB)
-constexpr uint32_t SA_T = SA_KH + 24576;  //   T Diag(beta) bf16 il [r][s], rows 0..63 twice
+constexpr uint32_t SA_T = SA_KH + 24576;  //   T Diag(beta) fp16 il [r][s], rows 0..63 twice
                                           //   (16 KB: the M = 128 A operand of the W product)
-constexpr uint32_t SA_K0 = 73728;         // 16 KB: K0 [64 s][128 i] sw (MN-major B of the W product)
+constexpr uint32_t SA_K0 = 73728;         // 16 KB: K0 [64 s][128 i] fp16 sw (MN-major B of the W product)
 constexpr uint32_t SA_KLO = 90112;        // 16 KB: low bf16 parts of the diagonal key rows [64 s][128 i] sw
 constexpr uint32_t SA_MISC = 106496;
 constexpr uint32_t MA_BETA = 0;           // float[64]
@@ -468,8 +471,8 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     q0[m] = __fmul2_rn(xq[m], ep[m]);
                     k0[m] = __fmul2_rn(xk[m], ep[m]);
                 }
-                *reinterpret_cast<uint4 *>(rec + R_WQ + sw_chunk(64 + r, cc, 16384)) = pack_bf8x2(q0);
-                *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, cc, 8192)) = pack_bf8x2(k0);
+                *reinterpret_cast<uint4 *>(rec + R_WQ + sw_chunk(64 + r, cc, 16384)) = pack_h8x2(q0);
+                *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, cc, 8192)) = pack_h8x2(k0);
             }
             // Kbar^T fp16 K-major il [i][s]: a 4x4 transpose of channel pairs
             // inside each quad of lanes (4 consecutive rows) in two butterfly
@@ -759,7 +762,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             *reinterpret_cast<uint4 *>(rec + R_T + km_bf16(r, s0, 1024)) = pack_bf8(w8);
             // rows 64..127 of the M = 128 operand repeat rows 0..63, so that every
             // TMEM lane quarter of the W accumulator holds real rows
-            const uint4 pd = pack_bf8(d8);
+            const uint4 pd = pack_h8(d8);
             *reinterpret_cast<uint4 *>(sm + SA_T + km_bf16(r, s0, 1024)) = pd;
             *reinterpret_cast<uint4 *>(sm + SA_T + km_bf16(64 + r, s0, 1024)) = pd;
         }
@@ -769,7 +772,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         // ===== W = T Diag(beta) K0: D_W[r][i] (M = 128, rows 64..127 a copy),
         // A = T Diag(beta) (K-major), B = K0 (MN-major)
         if (t == 0) {
-            const uint32_t idw = instr_desc(kFmtBF16, 128, 128, 0, 1);
+            const uint32_t idw = instr_desc(kFmtF16, 128, 128, 0, 1);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t a = smem_desc(smem_u32(sm + SA_T + 256 * kk), 128, 1024, kSwizzleNone);
@@ -801,7 +804,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x8[e] = -d[8 * c8 + e];
                     *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, 4 * cq + 2 * q2 + c8, 8192)) =
-                        pack_bf8(x8);
+                        pack_h8(x8);
                 }
             }
         }
@@ -854,7 +857,7 @@ constexpr uint32_t SB_A = 40960;          // A' (bulk copy 2, with Kbar^T)
 constexpr uint32_t SB_KB = 49152;         // Kbar^T
 constexpr uint32_t SB_VEC = 65536;        // 2 x 1 KB record vectors (double-buffered)
 constexpr uint32_t SB_V = 92160;          // 16 KB: v chunk sw (TMA) = V^T, MN-major operand
-                                          // 108544..141312 free: the bf16 pieces of S^T live in TMEM
+                                          // 108544..141312 free: the fp16 copy of S^T lives in TMEM
 constexpr uint32_t SB_O = 141312;         // 32 KB: o of even chunks, 4 x [64 r][32 j] fp32 (TMA store source)
 constexpr uint32_t SB_GATE = 174080;      // 16 KB: gate chunk sw (TMA; gated variant only)
 constexpr uint32_t SB_O1 = 190464;        // 32 KB: o of odd chunks
@@ -867,16 +870,15 @@ static_assert(SB_KB == SB_A + 8192, "A' and Kbar^T form one N = 192 operand");
 static_assert(SB_VEC + 2048 <= SB_V, "record vectors before v");
 static_assert(SMEM_B_ALLOC <= 232448, "dynamic shared memory limit (227 KB)");
 static_assert(SB_EB % 16 == 0, "bulk copy destination alignment");
-// TMEM columns: U^T | O^T | S^T master | S^T as two bf16 pieces.  Round 1
+// TMEM columns: U^T | O^T | S^T master | S^T in fp16 | U^T in fp16.  Round 1
 // writes [U | O] (N = 128) with the two pieces of S^T as A operands (one
 // MMA chain each, same accumulator), round 2 accumulates [O | S] (N = 192)
 // from the contiguous [A' ; Kbar^T].
 constexpr uint32_t TMB_U = 0;             // U^T, 64 columns
 constexpr uint32_t TMB_O = 64;            // O^T, 64 columns
 constexpr uint32_t TMB_S = 128;           // S^T master fp32 (lane j, column i), 128 columns
-constexpr uint32_t TMB_SB = 256;          // S^T high bf16 piece (lane j, column i / 2: pairs i, i + 1), 64 columns
-constexpr uint32_t TMB_SL = 320;          // S^T low bf16 piece, same layout, 64 columns
-constexpr uint32_t TMB_UP = 384;          // U^T as fp16 pairs (s, s + 1 per column): round 2's A, 32 columns
+constexpr uint32_t TMB_SB = 256;          // S^T in fp16 (lane j, column i / 2: pairs i, i + 1), 64 columns
+constexpr uint32_t TMB_UP = 320;          // U^T as fp16 pairs (s, s + 1 per column): round 2's A, 32 columns
 constexpr uint32_t TMEM_COLS_B = 512;
 constexpr uint32_t COPY1 = R_A - R_WQ;    // bytes of [-W ; Q0] + T'
 constexpr uint32_t COPY2 = R_VEC - R_A;   // bytes of A' + Kbar^T
@@ -891,19 +893,6 @@ __device__ __forceinline__ void ld_vec16(const float *p, float (&x)[16]) {
         x[4 * c + 1] = f.y;
         x[4 * c + 2] = f.z;
         x[4 * c + 3] = f.w;
-    }
-}
-
-// 16 fp32 values (channel pairs 2c, 2c + 1) as two bf16 pieces: hi = bf16(x),
-// lo = bf16(x - hi).  hi + lo keeps 16 significant bits of each value, so a
-// product with a bf16 operand loses no more than that operand's own rounding.
-__device__ __forceinline__ void split_bf16_pairs(const float (&x)[16], float (&hi)[8], float (&lo)[8]) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * c], x[2 * c + 1]);
-        const float2 hf = __bfloat1622float2(h);
-        hi[c] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&h));
-        lo[c] = __uint_as_float(pack_bf2(x[2 * c] - hf.x, x[2 * c + 1] - hf.y));
     }
 }
 
@@ -981,7 +970,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
     sync_tc();
     const uint32_t tmem = *s_tmem;
 
-    // ---- initial state: S^T master in TMEM (lane j, column i) + its two bf16 pieces
+    // ---- initial state: S^T master in TMEM (lane j, column i) + its fp16 copy
     if (epi) {
         float sv[32];
 #pragma unroll
@@ -997,13 +986,10 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         }
         tmem_st16(tmem + lane_base + TMB_S + 32 * qt, a);
         tmem_st16(tmem + lane_base + TMB_S + 32 * qt + 16, b2);
+        float pk[16];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            float hi[8], lo[8];
-            split_bf16_pairs(hh ? b2 : a, hi, lo);
-            tmem_st8(tmem + lane_base + TMB_SB + 16 * qt + 8 * hh, hi);
-            tmem_st8(tmem + lane_base + TMB_SL + 16 * qt + 8 * hh, lo);
-        }
+        for (int c = 0; c < 16; ++c) pk[c] = __uint_as_float(pack_h2(sv[2 * c], sv[2 * c + 1]));
+        tmem_st16(tmem + lane_base + TMB_SB + 16 * qt, pk);
         tmem_wait_st();
     }
     fence_proxy_async_smem();
@@ -1137,7 +1123,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         if (t == T_MMA) {
             if (mbar_wait(bar_a, par, kWaitLimit)) {
                 tc_fence_after();
-                const uint32_t id1 = instr_desc(kFmtBF16, 128, 128, 0, 0);
+                const uint32_t id1 = instr_desc(kFmtF16, 128, 128, 0, 0);
                 const uint32_t idv = instr_desc(kFmtBF16, 128, 64, 1, 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -1145,7 +1131,6 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                         smem_u32(sm + SB_WQ + (uint32_t)(kk >> 2) * 16384 + (uint32_t)(kk & 3) * 32), 16,
                         1024, kSwizzle128B);
                     mma_bf16_ts(tmem + TMB_U, tmem + TMB_SB + 8 * kk, bw, id1, kk > 0);
-                    mma_bf16_ts(tmem + TMB_U, tmem + TMB_SL + 8 * kk, bw, id1, 1);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
@@ -1173,7 +1158,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             __syncwarp();
             {
                 // S <- Diag(e^{b_L}) S for this chunk's round 2, while round 1
-                // runs (it reads only the bf16 pieces): off the serial chain
+                // runs (it reads only the fp16 copy): off the serial chain
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const uint32_t col = 32 * qt + 16 * hh;
@@ -1245,7 +1230,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         }
 
         // ===== the previous chunk's o is staged while round 2 runs; then
-        // o = D_O + (q.k) u into registers, the bf16 pieces of the new S^T, and
+        // o = D_O + (q.k) u into registers, the fp16 copy of the new S^T, and
         // S <- Diag(e^{b_L}) S for the next chunk
         if (epi) {
             if (j > 0) {
@@ -1267,15 +1252,11 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             }
             {
                 if (next) {
+                    float sv[32], pk[16];
+                    tmem_ld32(tmem + lane_base + TMB_S + 32 * qt, sv);
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        float sv[16], hi[8], lo[8];
-                        tmem_ld16(tmem + lane_base + TMB_S + 32 * qt + 16 * hh, sv);
-                        tmem_wait_ld();
-                        split_bf16_pairs(sv, hi, lo);
-                        tmem_st8(tmem + lane_base + TMB_SB + 16 * qt + 8 * hh, hi);
-                        tmem_st8(tmem + lane_base + TMB_SL + 16 * qt + 8 * hh, lo);
-                    }
+                    for (int c = 0; c < 16; ++c) pk[c] = __uint_as_float(pack_h2(sv[2 * c], sv[2 * c + 1]));
+                    tmem_st16(tmem + lane_base + TMB_SB + 16 * qt, pk);
                 }
             }
             tmem_wait_st();

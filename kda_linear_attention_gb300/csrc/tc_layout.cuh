@@ -54,6 +54,13 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
 }
+__device__ __forceinline__ uint4 pack_h8(const float (&x)[8]) {
+    return make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]), pack_h2(x[4], x[5]), pack_h2(x[6], x[7]));
+}
+__device__ __forceinline__ uint4 pack_h8x2(const float2 (&x)[4]) {
+    return make_uint4(pack_h2(x[0].x, x[0].y), pack_h2(x[1].x, x[1].y), pack_h2(x[2].x, x[2].y),
+                      pack_h2(x[3].x, x[3].y));
+}
 __device__ __forceinline__ uint4 pack_bf8(const float (&x)[8]) {
     return make_uint4(pack_bf2(x[0], x[1]), pack_bf2(x[2], x[3]), pack_bf2(x[4], x[5]),
                       pack_bf2(x[6], x[7]));
