@@ -33,7 +33,7 @@
 // arrives in bf16), with the diagonal blocks of the query-side Gram
 // corrected by the keys' bf16 low parts; fp16 (11 significant bits) for
 // every product with the state and its inputs: S's copy, W, Q0 and the W
-// product's T Diag(beta) and K0 in round 1, A', Kbar^T and U in round 2.
+// product's T Diag(beta) and K0 in round 1, A', Kbar and U in round 2.
 // Each of those is bounded (|q|, |k| <= 1 after the L2 norm; the decay
 // factors <= 1; S and u of the order of v), well inside fp16's range; u
 // (and through it an overflowing state copy) is checked.  The diagonal
@@ -103,7 +103,7 @@ __device__ __forceinline__ void ld_f2x4(const float *p, float2 (&x)[4]) {
 constexpr uint32_t R_WQ = 0;        // [-W ; Q0] fp16, 128 rows x 128, K-major sw (two 16 KB halves)
 constexpr uint32_t R_T = 32768;     // T' bf16 K-major il [r][s], 8 KB
 constexpr uint32_t R_A = 40960;     // A' fp16 K-major il [r][s], 8 KB
-constexpr uint32_t R_KB = 49152;    // Kbar^T fp16 K-major il [i][s], 16 KB
+constexpr uint32_t R_KB = 49152;    // Kbar fp16 [s][i] sw (two 8 KB halves of 64 channels), 16 KB
 constexpr uint32_t R_VEC = 65536;   // beta[64], q.k[64], e^{b_L}[128] (fp32)
 constexpr uint32_t REC_BYTES = 66560;
 static_assert(REC_BYTES % 1024 == 0, "records stay 1 KB aligned");
@@ -474,49 +474,13 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 *reinterpret_cast<uint4 *>(rec + R_WQ + sw_chunk(64 + r, cc, 16384)) = pack_h8x2(q0);
                 *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, cc, 8192)) = pack_h8x2(k0);
             }
-            // Kbar^T fp16 K-major il [i][s]: a 4x4 transpose of channel pairs
-            // inside each quad of lanes (4 consecutive rows) in two butterfly
-            // stages leaves every lane 4 consecutive s for channels 2bq, 2bq+1
+            // Kbar = e^{b_L - b} k, fp16, row s, in the 128B-swizzled [s][i]
+            // layout of K0: round 2 reads it as an MN-major operand
             {
-                float kb[8];
+                float2 kb[4];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float2 kb2 = __fmul2_rn(kg[m], el[m]);
-                    kb[2 * m] = kb2.x;
-                    kb[2 * m + 1] = kb2.y;
-                }
-                const int bq = rb & 3;
-                const bool b0 = (bq & 1) != 0, b1 = (bq & 2) != 0;
-                // stage 1 (lanes bq, bq^2): keep pairs 2b1, 2b1+1 of this row and
-                // receive the same pairs of row bq^2
-                float kp[4], rp[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    kp[e] = b1 ? kb[4 + e] : kb[e];
-                    rp[e] = __shfl_xor_sync(0xffffffffu, b1 ? kb[e] : kb[4 + e], 2);
-                }
-                // stage 2 (lanes bq, bq^1): keep pair bq of rows bq, bq^2 and
-                // receive it for rows bq^1, bq^3; v[m] = row bq ^ m
-                float v[4][2];
-#pragma unroll
-                for (int f = 0; f < 2; ++f) {
-                    v[0][f] = b0 ? kp[2 + f] : kp[f];
-                    v[2][f] = b0 ? rp[2 + f] : rp[f];
-                    v[1][f] = __shfl_xor_sync(0xffffffffu, b0 ? kp[f] : kp[2 + f], 1);
-                    v[3][f] = __shfl_xor_sync(0xffffffffu, b0 ? rp[f] : rp[2 + f], 1);
-                }
-                const int s0r = 16 * u + (rb & ~3);
-                const int i0 = 8 * cc + 2 * bq;
-#pragma unroll
-                for (int f = 0; f < 2; ++f) {
-                    // y[r] = v[r ^ bq]
-                    const float w0 = b0 ? v[1][f] : v[0][f], w1 = b0 ? v[0][f] : v[1][f];
-                    const float w2 = b0 ? v[3][f] : v[2][f], w3 = b0 ? v[2][f] : v[3][f];
-                    const float y0 = b1 ? w2 : w0, y1 = b1 ? w3 : w1;
-                    const float y2 = b1 ? w0 : w2, y3 = b1 ? w1 : w3;
-                    *reinterpret_cast<uint2 *>(rec + R_KB + km_bf16(i0 + f, s0r, 1024)) =
-                        make_uint2(pack_h2(y0, y1), pack_h2(y2, y3));
-                }
+                for (int m = 0; m < 4; ++m) kb[m] = __fmul2_rn(kg[m], el[m]);
+                *reinterpret_cast<uint4 *>(rec + R_KB + sw_chunk(r, cc, 8192)) = pack_h8x2(kb);
             }
         }
 #pragma unroll
@@ -853,8 +817,8 @@ constexpr int T_TMA = NEPI + 32;          // the copy-issuing thread (warp 17)
 constexpr int NTB = NEPI + 64;
 constexpr uint32_t SB_WQ = 0;             // [-W ; Q0] (bulk copy 1, with T')
 constexpr uint32_t SB_T = 32768;          // T'
-constexpr uint32_t SB_A = 40960;          // A' (bulk copy 2, with Kbar^T)
-constexpr uint32_t SB_KB = 49152;         // Kbar^T
+constexpr uint32_t SB_A = 40960;          // A' (bulk copy 2, with Kbar)
+constexpr uint32_t SB_KB = 49152;         // Kbar (MN-major, 128B swizzle: 1 KB aligned)
 constexpr uint32_t SB_VEC = 65536;        // 2 x 1 KB record vectors (double-buffered)
 constexpr uint32_t SB_V = 92160;          // 16 KB: v chunk sw (TMA) = V^T, MN-major operand
                                           // 108544..141312 free: the fp16 copy of S^T lives in TMEM
@@ -862,18 +826,16 @@ constexpr uint32_t SB_O = 141312;         // 32 KB: o of even chunks, 4 x [64 r]
 constexpr uint32_t SB_GATE = 174080;      // 16 KB: gate chunk sw (TMA; gated variant only)
 constexpr uint32_t SB_O1 = 190464;        // 32 KB: o of odd chunks
 constexpr uint32_t SB_MISC = 223232;      // mbarriers at +0, +8, +16, +24, +40; TMEM base at +32; norm weight at +64
-constexpr uint32_t SB_EB = SB_MISC + 576; // 2 x 512 B: e^{b_L} of the chunk after next (by parity)
-constexpr uint32_t SMEM_B_USED = SB_EB + 1024;
+constexpr uint32_t SMEM_B_USED = SB_MISC + 576;
 constexpr uint32_t SMEM_B_ALLOC = SMEM_B_USED + 1024;
 static_assert(SB_T == R_T && SB_A == R_A && SB_KB == R_KB, "record pieces map onto shared memory");
-static_assert(SB_KB == SB_A + 8192, "A' and Kbar^T form one N = 192 operand");
+static_assert(SB_KB == SB_A + 8192 && SB_KB % 1024 == 0, "A' then Kbar in one bulk copy; Kbar swizzle atoms aligned");
 static_assert(SB_VEC + 2048 <= SB_V, "record vectors before v");
 static_assert(SMEM_B_ALLOC <= 232448, "dynamic shared memory limit (227 KB)");
-static_assert(SB_EB % 16 == 0, "bulk copy destination alignment");
 // TMEM columns: U^T | O^T | S^T master | S^T in fp16 | U^T in fp16.  Round 1
-// writes [U | O] (N = 128) with the two pieces of S^T as A operands (one
-// MMA chain each, same accumulator), round 2 accumulates [O | S] (N = 192)
-// from the contiguous [A' ; Kbar^T].
+// writes [U | O] (N = 128) with the fp16 copy of S^T as its A operand;
+// round 2 accumulates O (N = 64, B = A') and S (N = 128, B = Kbar) with the
+// fp16 U^T as A.
 constexpr uint32_t TMB_U = 0;             // U^T, 64 columns
 constexpr uint32_t TMB_O = 64;            // O^T, 64 columns
 constexpr uint32_t TMB_S = 128;           // S^T master fp32 (lane j, column i), 128 columns
@@ -881,7 +843,7 @@ constexpr uint32_t TMB_SB = 256;          // S^T in fp16 (lane j, column i / 2: 
 constexpr uint32_t TMB_UP = 320;          // U^T as fp16 pairs (s, s + 1 per column): round 2's A, 32 columns
 constexpr uint32_t TMEM_COLS_B = 512;
 constexpr uint32_t COPY1 = R_A - R_WQ;    // bytes of [-W ; Q0] + T'
-constexpr uint32_t COPY2 = R_VEC - R_A;   // bytes of A' + Kbar^T
+constexpr uint32_t COPY2 = R_VEC - R_A;   // bytes of A' + Kbar
 
 // 16 consecutive floats of a record vector (16-byte aligned) in four
 // broadcast 16-byte shared-memory loads
@@ -1201,14 +1163,18 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         }
         tc_fence_after();
 
-        // ===== round 2: [D_O | S^T] += U^T [A' ; Kbar^T]^T (fp16, U^T from TMEM, N = 192)
+        // ===== round 2: D_O += U^T A'^T (N = 64, A' K-major), S^T += U^T Kbar
+        // (N = 128, Kbar MN-major); fp16, U^T from TMEM
         if (t == T_MMA) {
             if (mbar_wait(bar_b, par, kWaitLimit)) {
-                const uint32_t id2 = instr_desc(kFmtF16, 128, 192, 0, 0);
+                const uint32_t ida = instr_desc(kFmtF16, 128, 64, 0, 0);
+                const uint32_t idk = instr_desc(kFmtF16, 128, 128, 0, 1);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t bak = smem_desc(smem_u32(sm + SB_A + 256 * kk), 128, 1024, kSwizzleNone);
-                    mma_bf16_ts(tmem + TMB_O, tmem + TMB_UP + 8 * kk, bak, id2, 1);
+                    const uint64_t ba = smem_desc(smem_u32(sm + SB_A + 256 * kk), 128, 1024, kSwizzleNone);
+                    const uint64_t bk = smem_desc(smem_u32(sm + SB_KB + 2048 * kk), 8192, 1024, kSwizzle128B);
+                    mma_bf16_ts(tmem + TMB_O, tmem + TMB_UP + 8 * kk, ba, ida, 1);
+                    mma_bf16_ts(tmem + TMB_S, tmem + TMB_UP + 8 * kk, bk, idk, 1);
                 }
                 mma_commit(bar_mma);
                 ++issued_mma;
@@ -1226,7 +1192,7 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                 else bad = true;
             }
             if (!mbar_wait(bar_mma, 1u, kWaitLimit)) bad = true;   // round 2 may still read them
-            else if (j + 1 < nch) issue_b(j + 1);                    // A' and Kbar^T are consumed
+            else if (j + 1 < nch) issue_b(j + 1);                    // A' and Kbar are consumed
         }
 
         // ===== the previous chunk's o is staged while round 2 runs; then
