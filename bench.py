@@ -269,7 +269,7 @@ def _pinned(a):
 
 
 PREFILL_WORKLOADS = ["varlen_64k", "prefill_32k_carry", "prefill_4k", "tiny_fp32"]
-REC_BYTES = 66560          # per-(chunk, head) record of the two-kernel tensor-core prefill
+REC_BYTES = 60416          # per-(chunk, head) record of the two-kernel tensor-core prefill
 
 
 class PrefillCase:

@@ -16,7 +16,7 @@
  * Conventions shared by every call
  *   - Pointers are DEVICE pointers unless marked "host"; the caller owns all
  *     memory it passes.  The tensor-core prefill (bf16, chunk 64) also needs
- *     a scratch workspace of 65 KB per (64-token chunk, head):
+ *     a scratch workspace of 59 KB per (64-token chunk, head):
  *     kda_prefill_chunked takes it from a library-owned stream-ordered memory
  *     pool on the current device, which keeps that memory for later calls;
  *     kda_prefill_chunked_ws runs in a buffer the caller passes, and
@@ -152,9 +152,9 @@ int kda_prefill_chunked_events(const void *q, const void *k, const void *v,
  *
  * The tensor-core path (bf16, chunk 64, T > 0) takes its workspace from a
  * fixed 64 MiB array in the library's device image instead of the pool.  It
- * needs 1024 * ceil(4 (N + 1) / 1024) + (ceil(T / 64) + N) * H * 66560
+ * needs 1024 * ceil(4 (N + 1) / 1024) + (ceil(T / 64) + N) * H * 60416
  * bytes; larger inputs are rejected with KDA_ERR_WORKSPACE before anything
- * is launched (for H = 96 and one sequence: T <= 576).  Every other dtype /
+ * is launched (for H = 96 and one sequence: T <= 640).  Every other dtype /
  * chunk combination runs the CUDA-core kernel, which needs no workspace.
  * Nothing in the array has to be cleared between calls.
  *
@@ -177,7 +177,7 @@ int kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v,
 /*
  * Bytes of caller-owned workspace that kda_prefill_chunked_ws needs for these
  * sizes: the records of the tensor-core path (bf16, chunk 64, T > 0),
- * 1024 * ceil(4 (N + 1) / 1024) + (ceil(T / 64) + N) * H * 66560; 0 for every
+ * 1024 * ceil(4 (N + 1) / 1024) + (ceil(T / 64) + N) * H * 60416; 0 for every
  * other combination (the CUDA-core kernel needs none) and for invalid sizes.
  * Host-only, no CUDA call.
  */

@@ -101,12 +101,29 @@ __device__ __forceinline__ void ld_f2x4(const float *p, float2 (&x)[4]) {
 // Each piece is stored in the shared-memory operand layout in which the state
 // pass feeds it to the tensor cores, so that one bulk copy places it.
 constexpr uint32_t R_WQ = 0;        // [-W ; Q0] fp16, 128 rows x 128, K-major sw (two 16 KB halves)
-constexpr uint32_t R_T = 32768;     // T' bf16 K-major il [r][s], 8 KB
-constexpr uint32_t R_A = 40960;     // A' fp16 K-major il [r][s], 8 KB
-constexpr uint32_t R_KB = 49152;    // Kbar fp16 [s][i] sw (two 8 KB halves of 64 channels), 16 KB
-constexpr uint32_t R_VEC = 65536;   // beta[64], q.k[64], e^{b_L}[128] (fp32)
-constexpr uint32_t REC_BYTES = 66560;
-static_assert(REC_BYTES % 1024 == 0, "records stay 1 KB aligned");
+constexpr uint32_t R_T = 32768;     // T' bf16, strictly lower 64 x 64 packed by K-step (tri_off), 5 KB
+constexpr uint32_t R_A = 37888;     // A' fp16, the same packing, 5 KB
+constexpr uint32_t R_KB = 43008;    // Kbar fp16 [s][i] sw (two 8 KB halves of 64 channels), 16 KB
+constexpr uint32_t R_VEC = 59392;   // beta[64], q.k[64], e^{b_L}[128] (fp32)
+constexpr uint32_t REC_BYTES = 60416;
+static_assert(REC_BYTES % 1024 == 0 && R_KB % 1024 == 0, "records and their swizzled piece 1 KB aligned");
+
+// The strictly lower triangular 64 x 64 tiles T' [r][s] and A' [r][s] are
+// stored by K-step kk (columns s = 16 kk .. 16 kk + 15) with only the row
+// groups that can be nonzero there, g = r / 8 >= 2 kk: block kk holds groups
+// 2 kk .. 7, two 128-byte chunks each (8 rows x 8 columns, the interleaved
+// K-major layout of the MMA operands: group stride 256 B, chunk stride
+// 128 B), at tri_base(kk); 5120 bytes in all instead of 8192.  The state
+// pass multiplies block kk with N = 64 - 16 kk into columns 16 kk ..
+__host__ __device__ constexpr uint32_t tri_base(int kk) { return 256u * (uint32_t)(8 * kk - kk * (kk - 1)); }
+constexpr uint32_t kTriBytes = tri_base(4);
+static_assert(kTriBytes == 5120, "packed triangle size");
+// element (r, s), for r / 8 >= 2 (s / 16) only
+__device__ __forceinline__ uint32_t tri_off(int r, int s) {
+    const int kk = s >> 4;
+    return tri_base(kk) + (uint32_t)((r >> 3) - 2 * kk) * 256u + (uint32_t)((s >> 3) & 1) * 128u +
+           (uint32_t)(r & 7) * 16u + (uint32_t)(s & 7) * 2u;
+}
 
 // ============================================================================
 // chunk plan: chunk_off[n] = sum_{m<n} ceil(len_m / 64), chunk_off[N] = total.
@@ -576,8 +593,9 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                         x4[e] = (have && s < r) ? val : 0.f;
                     }
                     if (qside) {
-                        *reinterpret_cast<uint2 *>(rec + R_A + km_bf16(r, 16 * qt + 4 * j, 1024)) =
-                            make_uint2(pack_h2(x4[0], x4[1]), pack_h2(x4[2], x4[3]));
+                        if ((r >> 3) >= 2 * qt)      // a row group that block qt of the packing holds
+                            *reinterpret_cast<uint2 *>(rec + R_A + tri_off(r, 16 * qt + 4 * j)) =
+                                make_uint2(pack_h2(x4[0], x4[1]), pack_h2(x4[2], x4[3]));
                     } else {
                         *reinterpret_cast<float4 *>(Mm + r * MLD + 16 * qt + 4 * j) =
                             make_float4(br * x4[0], br * x4[1], br * x4[2], br * x4[3]);
@@ -723,7 +741,8 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 w8[u] = (s3 < r) ? tv[u] * bs : 0.f;
                 d8[u] = (s3 == r) ? bs : w8[u];
             }
-            *reinterpret_cast<uint4 *>(rec + R_T + km_bf16(r, s0, 1024)) = pack_bf8(w8);
+            if ((r >> 3) >= 2 * (s0 >> 4))     // a row group that the packing holds
+                *reinterpret_cast<uint4 *>(rec + R_T + tri_off(r, s0)) = pack_bf8(w8);
             // rows 64..127 of the M = 128 operand repeat rows 0..63, so that every
             // TMEM lane quarter of the W accumulator holds real rows
             const uint4 pd = pack_h8(d8);
@@ -816,10 +835,10 @@ constexpr int T_MMA = NEPI;               // the MMA-issuing thread (warp 16)
 constexpr int T_TMA = NEPI + 32;          // the copy-issuing thread (warp 17)
 constexpr int NTB = NEPI + 64;
 constexpr uint32_t SB_WQ = 0;             // [-W ; Q0] (bulk copy 1, with T')
-constexpr uint32_t SB_T = 32768;          // T'
-constexpr uint32_t SB_A = 40960;          // A' (bulk copy 2, with Kbar)
-constexpr uint32_t SB_KB = 49152;         // Kbar (MN-major, 128B swizzle: 1 KB aligned)
-constexpr uint32_t SB_VEC = 65536;        // 2 x 1 KB record vectors (double-buffered)
+constexpr uint32_t SB_T = 32768;          // T' (packed triangle)
+constexpr uint32_t SB_A = 37888;          // A' (packed triangle; bulk copy 2, with Kbar)
+constexpr uint32_t SB_KB = 43008;         // Kbar (MN-major, 128B swizzle: 1 KB aligned)
+constexpr uint32_t SB_VEC = 59392;        // 2 x 1 KB record vectors (double-buffered)
 constexpr uint32_t SB_V = 92160;          // 16 KB: v chunk sw (TMA) = V^T, MN-major operand
                                           // 108544..141312 free: the fp16 copy of S^T lives in TMEM
 constexpr uint32_t SB_O = 141312;         // 32 KB: o of even chunks, 4 x [64 r][32 j] fp32 (TMA store source)
@@ -829,7 +848,7 @@ constexpr uint32_t SB_MISC = 223232;      // mbarriers at +0, +8, +16, +24, +40;
 constexpr uint32_t SMEM_B_USED = SB_MISC + 576;
 constexpr uint32_t SMEM_B_ALLOC = SMEM_B_USED + 1024;
 static_assert(SB_T == R_T && SB_A == R_A && SB_KB == R_KB, "record pieces map onto shared memory");
-static_assert(SB_KB == SB_A + 8192 && SB_KB % 1024 == 0, "A' then Kbar in one bulk copy; Kbar swizzle atoms aligned");
+static_assert(SB_KB == SB_A + kTriBytes && SB_KB % 1024 == 0, "A' then Kbar in one bulk copy; Kbar swizzle atoms aligned");
 static_assert(SB_VEC + 2048 <= SB_V, "record vectors before v");
 static_assert(SMEM_B_ALLOC <= 232448, "dynamic shared memory limit (227 KB)");
 // TMEM columns: U^T | O^T | S^T master | S^T in fp16 | U^T in fp16.  Round 1
@@ -1086,7 +1105,6 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             if (mbar_wait(bar_a, par, kWaitLimit)) {
                 tc_fence_after();
                 const uint32_t id1 = instr_desc(kFmtF16, 128, 128, 0, 0);
-                const uint32_t idv = instr_desc(kFmtBF16, 128, 64, 1, 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t bw = smem_desc(
@@ -1094,11 +1112,13 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                         1024, kSwizzle128B);
                     mma_bf16_ts(tmem + TMB_U, tmem + TMB_SB + 8 * kk, bw, id1, kk > 0);
                 }
+                // (T' V)^T: K-step kk meets only rows r >= 16 kk of the packed T'
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t idv = instr_desc(kFmtBF16, 128, 64 - 16 * kk, 1, 0);
                     const uint64_t av = smem_desc(smem_u32(sm + SB_V + 2048 * kk), 8192, 1024, kSwizzle128B);
-                    const uint64_t bt = smem_desc(smem_u32(sm + SB_T + 256 * kk), 128, 1024, kSwizzleNone);
-                    mma_bf16_ss(tmem + TMB_U, av, bt, idv, 1);
+                    const uint64_t bt = smem_desc(smem_u32(sm + SB_T + tri_base(kk)), 128, 256, kSwizzleNone);
+                    mma_bf16_ss(tmem + TMB_U + 16 * kk, av, bt, idv, 1);
                 }
                 mma_commit(bar_mma);
                 ++issued_mma;
@@ -1167,13 +1187,14 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         // (N = 128, Kbar MN-major); fp16, U^T from TMEM
         if (t == T_MMA) {
             if (mbar_wait(bar_b, par, kWaitLimit)) {
-                const uint32_t ida = instr_desc(kFmtF16, 128, 64, 0, 0);
                 const uint32_t idk = instr_desc(kFmtF16, 128, 128, 0, 1);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ba = smem_desc(smem_u32(sm + SB_A + 256 * kk), 128, 1024, kSwizzleNone);
+                    // K-step kk meets only rows r >= 16 kk of the packed A'
+                    const uint32_t ida = instr_desc(kFmtF16, 128, 64 - 16 * kk, 0, 0);
+                    const uint64_t ba = smem_desc(smem_u32(sm + SB_A + tri_base(kk)), 128, 256, kSwizzleNone);
                     const uint64_t bk = smem_desc(smem_u32(sm + SB_KB + 2048 * kk), 8192, 1024, kSwizzle128B);
-                    mma_bf16_ts(tmem + TMB_O, tmem + TMB_UP + 8 * kk, ba, ida, 1);
+                    mma_bf16_ts(tmem + TMB_O + 16 * kk, tmem + TMB_UP + 8 * kk, ba, ida, 1);
                     mma_bf16_ts(tmem + TMB_S, tmem + TMB_UP + 8 * kk, bk, idk, 1);
                 }
                 mma_commit(bar_mma);

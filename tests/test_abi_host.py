@@ -130,7 +130,7 @@ def test_prefill_workspace_bytes(L):
     (chunk, head), with one spare chunk per sequence for a partial tail; no
     workspace for the CUDA-core path or for invalid sizes."""
     for N, T, H in [(1, 64, 2), (1, 4096, 96), (3, 130, 5), (300, 4096, 4)]:
-        want = 1024 * (-(-4 * (N + 1) // 1024)) + (-(-T // 64) + N) * H * 66560
+        want = 1024 * (-(-4 * (N + 1) // 1024)) + (-(-T // 64) + N) * H * 60416
         assert L.kda_prefill_workspace_bytes(N, T, H, 128, 128, 64, 0) == want
     assert L.kda_prefill_workspace_bytes(1, 64, 2, 128, 128, 64, 1) == 0    # fp32 inputs
     assert L.kda_prefill_workspace_bytes(1, 64, 2, 128, 128, 32, 0) == 0    # chunk 32

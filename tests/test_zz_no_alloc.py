@@ -16,7 +16,7 @@ from kda_testlib import TOL_BF16, assert_close, dev_tensor, rel_err
 
 KDA_ERR_WORKSPACE = 6
 SCRATCH = 64 << 20
-REC = 66560
+REC = 60416
 
 
 def _needed(N, T, H):
@@ -32,15 +32,15 @@ def test_noalloc_rejects_oversize_before_launch():
     L = kda.lib()
     fake = ctypes.c_void_p(1 << 20)
     N, H = 1, 96
-    T = 640                                   # (10 + 1) * 96 records > 64 MiB
-    assert _needed(N, T, H) > SCRATCH and _needed(N, 576, H) <= SCRATCH
+    T = 704                                   # (11 + 1) * 96 records > 64 MiB
+    assert _needed(N, T, H) > SCRATCH and _needed(N, 640, H) <= SCRATCH
     rc = L.kda_prefill_chunked_noalloc(fake, fake, fake, fake, fake, None, fake, fake, fake,
                                       N, T, H, 128, 128, 64, 0, None)
     assert rc == KDA_ERR_WORKSPACE
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("lens,H,with_s0", [([576], 96, False), ([70, 33, 129, 0, 64], 8, True)])
+@pytest.mark.parametrize("lens,H,with_s0", [([640], 96, False), ([70, 33, 129, 0, 64], 8, True)])
 def test_noalloc_matches_pool_entry_point_twice(lens, H, with_s0):
     import torch
     import kda_linear_attention_gb300 as kda
