@@ -623,6 +623,10 @@ def _timed(torch, stream, fn, reps=10, warm=3):
 
 # algorithmic bytes of the layer's kernels
 PROLOGUE_BYTES_PER_TOKEN_HEAD = 3 * 256 + 3 * 256        # raw q/k/v in, q/k/v out (bf16)
+# layer prefill per token-head: raw q/k/v and gate in (bf16), g, beta in,
+# the gated output out (fp32); per (sequence, head) the state in and out and
+# the conv window in and out
+LAYER_PREFILL_BYTES_PER_TOKEN_HEAD = 3 * 256 + 256 + 512 + 4 + 512
 # decode layer step per (b, h): state read + write, raw q/k/v, gate (bf16),
 # conv window read + write (3 x 3 x 128 bf16 each), g, beta, out (fp32)
 DECODE_LAYER_BYTES_PER_STATE = 2 * STATE_BYTES + 3 * 256 + 256 + 2 * 2304 + 512 + 4 + 512
@@ -654,19 +658,34 @@ def _layer_leg(kda, torch, dev, stream, peaks):
     def plain():
         kda.prefill_chunked(q, k, v, d["g"], d["beta"], d["cu_seqlens"], o=out, S_out=S_out)
 
-    def whole():
+    def two_calls():
         prologue()
         gated()
+
+    def fused():
+        kda.prefill_layer(d["xq"], d["xk"], d["xv"], d["conv_w"], d["g"], d["beta"], d["gate"],
+                          d["norm_w"], d["cu_seqlens"], conv_in=d["conv0"], out=out, S_out=S_out,
+                          conv_out=conv_out)
 
     t_pro = _timed(torch, stream, prologue)
     t_gated = _timed(torch, stream, gated)
     t_plain = _timed(torch, stream, plain)
-    t_all = _timed(torch, stream, whole)
+    t_two = _timed(torch, stream, two_calls)
+    t_all = _timed(torch, stream, fused)
     pro_bytes = T * H * PROLOGUE_BYTES_PER_TOKEN_HEAD
     pro_gbs = pro_bytes / (t_pro / 1e3) / 1e9
+    lay_bytes = T * H * LAYER_PREFILL_BYTES_PER_TOKEN_HEAD + H * (STATE_BYTES + 2 * 2304)
+    lay_gbs = lay_bytes / (t_all / 1e3) / 1e9
     prefill = {
         "workload": "layer prefill, H=96, T=4096, chunk 64, bf16 raw projections, carried windows",
+        "call": "kda_layer_prefill (prologue fused into the intra-chunk kernel)",
         "ms": round(t_all, 4), "tokens_per_s": round(T / (t_all / 1e3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(lay_gbs, 1), "peak": peaks["hbm"],
+                     "unit": "GB/s", "frac": round(lay_gbs / peaks["hbm"], 4),
+                     "algorithmic_bytes": int(lay_bytes),
+                     "bytes_per_token_head": LAYER_PREFILL_BYTES_PER_TOKEN_HEAD, "traffic": None},
+        "vs_gated_prefill_alone": round(t_all / t_gated, 4),
+        "two_calls_ms": round(t_two, 4),
         "prologue": {"kernel": "conv_prologue_kernel", "ms": round(t_pro, 4),
                      "roofline": {"bound": "hbm", "achieved": round(pro_gbs, 1),
                                   "peak": peaks["hbm"], "unit": "GB/s",
@@ -676,7 +695,7 @@ def _layer_leg(kda, torch, dev, stream, peaks):
                                   "traffic": _traffic("conv_prologue_kernel", "kda_layer.cu")}},
         "gated_prefill": {"ms": round(t_gated, 4), "ungated_ms": round(t_plain, 4),
                           "epilogue_overhead_frac": round(t_gated / t_plain - 1.0, 4)},
-        "gpu_launches_per_call": 4,
+        "gpu_launches_per_call": 3,
     }
     del L, d, q, k, v, out
 

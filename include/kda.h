@@ -319,6 +319,35 @@ int kda_prefill_chunked_gated(const void *q, const void *k, const void *v, const
                               int chunk, int dtype, void *stream);
 
 /*
+ * The whole layer's prefill in one call ("Colibri Kimi K3 Metal backend",
+ * sections 8.3 and 8.4: the conv + L2-norm prologue feeds the recurrence, the
+ * gated RMSNorm follows it): kda_conv_prologue followed by
+ * kda_prefill_chunked_gated, with the prologue computed inside the prefill's
+ * intra-chunk kernel, so the normalised q, k, v never go through HBM.  The
+ * results equal those two calls' (the same arithmetic and roundings: q, k, v
+ * rounded to bf16 before the recurrence).  Tensor-core path only (chunk 64).
+ *
+ *   xq, xk, xv [T, H, 128] bf16 raw projections
+ *   conv_w     [3, H, 128, 4] fp32 taps
+ *   conv_in    [N, 3, 3, H, 128] bf16 windows before each sequence, or NULL
+ *   conv_out   [N, 3, 3, H, 128] bf16, written, or NULL; not conv_in
+ *   g, beta, S0, S_out, cu_seqlens   as for kda_prefill_chunked
+ *   gate       [T, H, 128] bf16; norm_w [128] fp32
+ *   out        [T, H, 128] fp32, written: the gated RMSNorm of o
+ *   q_scale    finite; l2_eps, norm_eps >= 0
+ *   dk, dv     must be 128
+ * The workspace (one 76,800-byte record per (chunk, head): the record of
+ * kda_prefill_chunked plus the chunk's v) comes from the library's pool
+ * (KDA_ERR_WORKSPACE if it cannot grow).  Returns KDA_OK or a kda_status_t.
+ */
+int kda_layer_prefill(const void *xq, const void *xk, const void *xv, const float *conv_w,
+                      const void *conv_in, void *conv_out, const float *g, const float *beta,
+                      const float *S0, const void *gate, const float *norm_w, float q_scale,
+                      float l2_eps, float norm_eps, float *out, float *S_out,
+                      const int32_t *cu_seqlens, int N, int64_t T, int H, int dk, int dv,
+                      void *stream);
+
+/*
  * One token of the whole layer for each of B sequences on slot-indexed
  * pools, in one kernel: conv1d + SiLU + L2 norm of the raw projections (the
  * window of pool row state_indices[b] is read and shifted in place), the

@@ -102,6 +102,9 @@ def lib() -> ctypes.CDLL:
         L.kda_prefill_chunked_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp,
                                                 i32, i64, i32, i32, i32, i32, i32, vp]
         L.kda_prefill_chunked_gated.restype = i32
+        L.kda_layer_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, f32, f32,
+                                        vp, vp, vp, i32, i64, i32, i32, i32, vp]
+        L.kda_layer_prefill.restype = i32
         L.kda_decode_layer_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32,
                                             vp, i32, i32, i32, i32, f32, f32, f32, vp]
         L.kda_decode_layer_step.restype = i32
@@ -383,14 +386,55 @@ def prefill_chunked_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: 
 def prefill_layer(xq, xk, xv, conv_w, g, beta, gate, norm_w, cu_seqlens,
                   conv_in: Optional[torch.Tensor] = None, S0: Optional[torch.Tensor] = None,
                   q_scale: float = Q_SCALE, l2_eps: float = L2_EPS, norm_eps: float = NORM_EPS,
+                  out: Optional[torch.Tensor] = None, S_out: Optional[torch.Tensor] = None,
+                  conv_out: Optional[torch.Tensor] = None, fused: bool = True,
                   stream: Optional[torch.cuda.Stream] = None):
-    """The layer's prefill from raw projections: ``conv_prologue`` (q, k, v
-    in bf16) then ``prefill_chunked_gated``, on one stream.  Returns
-    (out [T, H, 128] fp32, S_out [N, H, 128, 128] fp32, conv_out)."""
-    q, k, v, conv_out = conv_prologue(xq, xk, xv, conv_w, cu_seqlens, conv_in=conv_in,
-                                      q_scale=q_scale, eps=l2_eps, stream=stream)
-    out, S_out = prefill_chunked_gated(q, k, v, g, beta, cu_seqlens, gate, norm_w, S0=S0,
-                                       eps=norm_eps, stream=stream)
+    """The layer's prefill from raw projections (``kda_layer_prefill``: the
+    conv + SiLU + L2-norm prologue inside the prefill's intra-chunk kernel,
+    the gated RMSNorm in its state pass).  fused=False runs the same layer as
+    two calls, ``conv_prologue`` (q, k, v through HBM in bf16) then
+    ``prefill_chunked_gated``.  Returns (out [T, H, 128] fp32,
+    S_out [N, H, 128, 128] fp32, conv_out [N, 3, 3, H, 128] bf16)."""
+    if not fused:
+        q, k, v, conv_out = conv_prologue(xq, xk, xv, conv_w, cu_seqlens, conv_in=conv_in,
+                                          conv_out=conv_out, q_scale=q_scale, eps=l2_eps,
+                                          stream=stream)
+        out, S_out = prefill_chunked_gated(q, k, v, g, beta, cu_seqlens, gate, norm_w, S0=S0,
+                                           eps=norm_eps, out=out, S_out=S_out, stream=stream)
+        return out, S_out, conv_out
+    dev = xq.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    T, H = xq.shape[0], xq.shape[1]
+    N = cu_seqlens.numel() - 1
+    bf = torch.bfloat16
+    for n, t in (("xq", xq), ("xk", xk), ("xv", xv), ("gate", gate)):
+        _check(n, t, bf, (T, H, DK), dev)
+    _check("conv_w", conv_w, torch.float32, (3, H, DK, CONV_K), dev)
+    _check("g", g, torch.float32, (T, H, DK), dev)
+    _check("beta", beta, torch.float32, (T, H), dev)
+    _check("norm_w", norm_w, torch.float32, (DV,), dev)
+    _check("cu_seqlens", cu_seqlens, torch.int32, (N + 1,), dev)
+    wshape = (N, 3, CONV_K - 1, H, DK)
+    if conv_in is not None:
+        _check("conv_in", conv_in, bf, wshape, dev)
+    if conv_out is None:
+        conv_out = torch.empty(wshape, dtype=bf, device=dev)
+    _check("conv_out", conv_out, bf, wshape, dev)
+    if S0 is not None:
+        _check("S0", S0, torch.float32, (N, H, DK, DV), dev)
+    if out is None:
+        out = torch.empty((T, H, DV), dtype=torch.float32, device=dev)
+    if S_out is None:
+        S_out = torch.empty((N, H, DK, DV), dtype=torch.float32, device=dev)
+    _check("out", out, torch.float32, (T, H, DV), dev)
+    _check("S_out", S_out, torch.float32, (N, H, DK, DV), dev)
+    rc = lib().kda_layer_prefill(_p(xq), _p(xk), _p(xv), _p(conv_w), _p(conv_in), _p(conv_out),
+                                 _p(g), _p(beta), _p(S0), _p(gate), _p(norm_w), float(q_scale),
+                                 float(l2_eps), float(norm_eps), _p(out), _p(S_out),
+                                 _p(cu_seqlens), N, T, H, DK, DV, _stream(dev, stream))
+    if rc != 0:
+        raise KDAError(rc, "kda_layer_prefill")
     return out, S_out, conv_out
 
 

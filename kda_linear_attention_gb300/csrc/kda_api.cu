@@ -220,6 +220,43 @@ int kda_prefill_chunked_gated(const void *q, const void *k, const void *v, const
     return cuda_status(e);
 }
 
+int kda_layer_prefill(const void *xq, const void *xk, const void *xv, const float *conv_w,
+                      const void *conv_in, void *conv_out, const float *g, const float *beta,
+                      const float *S0, const void *gate, const float *norm_w, float q_scale,
+                      float l2_eps, float norm_eps, float *out, float *S_out,
+                      const int32_t *cu_seqlens, int N, int64_t T, int H, int dk, int dv,
+                      void *stream) {
+    if (dk != kda::kDK || dv != kda::kDV || N < 1 || H < 1 || T < 0 || T >= (int64_t(1) << 31))
+        return KDA_ERR_DIM;
+    if ((int64_t)N * H * (kda::kDV / 32) >= (int64_t(1) << 31)) return KDA_ERR_DIM;
+    if (!(l2_eps >= 0.f) || !(norm_eps >= 0.f) || !(q_scale == q_scale) || q_scale - q_scale != 0.f)
+        return KDA_ERR_VALUE;
+    if (conv_in && conv_in == conv_out) return KDA_ERR_VALUE;
+    if (!S_out || !cu_seqlens) return KDA_ERR_NULL;
+    if (T > 0 && (!xq || !xk || !xv || !conv_w || !g || !beta || !gate || !norm_w || !out))
+        return KDA_ERR_NULL;
+    const void *ptrs[] = {xq, xk, xv, conv_w, conv_in, conv_out, g, beta, S0, gate, norm_w, out,
+                          S_out, cu_seqlens};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {   // every sequence empty: windows and states pass through
+        cudaError_t e = cudaSuccess;
+        if (conv_out)
+            e = kda::launch_conv_prologue(xq, xk, xv, conv_w, conv_in, conv_out, nullptr, nullptr,
+                                          nullptr, cu_seqlens, N, T, H, q_scale, l2_eps, s);
+        if (e == cudaSuccess)
+            e = kda::launch_prefill_simt(nullptr, nullptr, nullptr, g, beta, S0, out, S_out,
+                                         cu_seqlens, N, T, H, 64, true, s);
+        return cuda_status(e);
+    }
+    const cudaError_t e = kda::launch_prefill_split_layer(xq, xk, xv, conv_w, conv_in, conv_out, g,
+                                                          beta, S0, gate, norm_w, q_scale, l2_eps,
+                                                          norm_eps, out, S_out, cu_seqlens, N, T,
+                                                          H, s);
+    return e == cudaErrorMemoryAllocation ? KDA_ERR_WORKSPACE : cuda_status(e);
+}
+
 int kda_decode_layer_step(const void *xq, const void *xk, const void *xv, const float *conv_w,
                           void *conv_pool, const float *g, const float *beta, const void *gate,
                           const float *norm_w, void *S_pool, int state_dtype,

@@ -57,26 +57,6 @@ __device__ __forceinline__ int seq_of(const int32_t *cu, int N, int t) {
     return lo;
 }
 
-// bf16 pair (low half = even channel) -> float2, exactly
-__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
-    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
-}
-__device__ __forceinline__ uint32_t f2_to_bf2(float2 v) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-// 1 / x on the hardware reciprocal (about 1 ulp); 1 / inf = 0
-__device__ __forceinline__ float rcp_approx(float x) {
-    float r;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-    return r;
-}
-// SiLU of a channel pair: y / (1 + e^-y)
-__device__ __forceinline__ float2 silu2(float2 y) {
-    const float2 d = __fadd2_rn(make_float2(1.f, 1.f), make_float2(__expf(-y.x), __expf(-y.y)));
-    return __fmul2_rn(y, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
-}
-
 __global__ void __launch_bounds__(kPrologueThreads, 2)
 conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *__restrict__ xk,
                      const __nv_bfloat16 *__restrict__ xv, const float *__restrict__ conv_w,

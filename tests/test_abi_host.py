@@ -244,3 +244,27 @@ def test_decode_layer_rejects_bad_arguments(L, kw, status):
 
 def test_decode_layer_with_slots_allows_small_pool_and_empty_batch(L):
     assert _layer_step(L, B=0, xq=None, S=None) == 0
+
+
+def _layer_prefill(L, **kw):
+    a = dict(xq=GOOD, xk=GOOD, xv=GOOD, w=GOOD, cin=None, cout=GOOD, g=GOOD, beta=GOOD, S0=None,
+             gate=GOOD, nw=GOOD, qs=0.088, l2=1e-6, ne=1e-6, out=GOOD, S_out=GOOD, cu=GOOD, N=1,
+             T=64, H=2, dk=128, dv=128, stream=None)
+    a.update(kw)
+    return L.kda_layer_prefill(a["xq"], a["xk"], a["xv"], a["w"], a["cin"], a["cout"], a["g"],
+                               a["beta"], a["S0"], a["gate"], a["nw"], a["qs"], a["l2"], a["ne"],
+                               a["out"], a["S_out"], a["cu"], a["N"], a["T"], a["H"], a["dk"],
+                               a["dv"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=64), 2), (dict(dv=256), 2), (dict(N=0), 2), (dict(H=0), 2), (dict(T=-1), 2),
+    (dict(T=1 << 31), 2), (dict(l2=-1.0), 8), (dict(ne=float("nan")), 8),
+    (dict(qs=float("inf")), 8), (dict(cin=GOOD, cout=GOOD), 8),
+    (dict(xq=None), 1), (dict(w=None), 1), (dict(g=None), 1), (dict(gate=None), 1),
+    (dict(nw=None), 1), (dict(out=None), 1), (dict(S_out=None), 1), (dict(cu=None), 1),
+    (dict(xv=ctypes.c_void_p(0x10004)), 4), (dict(S0=ctypes.c_void_p(0x10008)), 4),
+    (dict(cout=ctypes.c_void_p(0x10002)), 4),
+])
+def test_layer_prefill_rejects_bad_arguments(L, kw, status):
+    assert _layer_prefill(L, **kw) == status

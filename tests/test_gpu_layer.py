@@ -186,18 +186,29 @@ def test_gated_prefill_4k_full():
     assert_close(S, S_ref, TOL_BF16, "S_out")
 
 
-@pytest.mark.parametrize("lens,H,with_s0", [([0, 1, 70, 3, 129], 3, True), ([4096], 96, False)])
-def test_prefill_layer_against_the_layer_oracle(lens, H, with_s0):
-    """Prologue (q, k, v stored in bf16) then the gated tensor-core prefill,
-    against the oracle's layer prefill with q, k, v rounded to bf16."""
+LAYER_CASES = [([0, 1, 70, 3, 129], 3, True, True),
+               (RAGGED, 2, True, False),
+               ([2, 1, 66, 0, 3, 190], 3, False, True),
+               ([4096], 96, False, True)]
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "two_calls"])
+@pytest.mark.parametrize("lens,H,with_s0,with_conv0", LAYER_CASES)
+def test_prefill_layer_against_the_layer_oracle(lens, H, with_s0, with_conv0, fused):
+    """The layer prefill from raw projections, fused (``kda_layer_prefill``:
+    the prologue inside the intra-chunk kernel) and as two calls (prologue,
+    then the gated tensor-core prefill), against the oracle's layer prefill
+    with q, k, v rounded to bf16.  Sequences of 1 and 2 tokens carry part of
+    the window before them into the window after them."""
     import torch
     kda = _kda()
-    L = ki.gen_layer(120 + H, lens, H=H, with_s0=with_s0)
+    L = ki.gen_layer(120 + H, lens, H=H, with_s0=with_s0, with_conv0=with_conv0)
     d = dev_tensor
     s0 = None if L.S0 is None else d(L.S0)
+    cin = d(L.conv0).view(torch.bfloat16) if with_conv0 else None
     out, S, co = kda.prefill_layer(d(L.xq), d(L.xk), d(L.xv), d(L.conv_w), d(L.g), d(L.beta),
                                    d(L.gate), d(L.norm_w), d(L.cu_seqlens),
-                                   conv_in=d(L.conv0).view(torch.bfloat16), S0=s0)
+                                   conv_in=cin, S0=s0, fused=fused)
     torch.cuda.synchronize()
     _check_no_device_error()
     out_ref, o_ref, S_ref, co_ref = olayer.prefill_layer(L, QS, round_qkv_bf16=True)
@@ -211,6 +222,27 @@ def test_prefill_layer_against_the_layer_oracle(lens, H, with_s0):
                                "layer out, sequence %d" % n)
         assert_close(S[n], S_ref[n], TOL_BF16, "layer S_out, sequence %d" % n)
     assert np.array_equal(_bf16_np(co), co_ref)
+
+
+@pytest.mark.parametrize("lens,H", [(RAGGED, 2), ([4096], 96)])
+def test_fused_layer_prefill_equals_the_two_calls(lens, H):
+    """The fused layer prefill computes the prologue with the separate
+    prologue kernel's arithmetic and feeds the same bf16 q, k, v to the same
+    recurrence, so its outputs, final states and windows are the two-call
+    path's bit for bit."""
+    import torch
+    kda = _kda()
+    L = ki.gen_layer(150 + H, lens, H=H, with_s0=True)
+    d = dev_tensor
+    args = (d(L.xq), d(L.xk), d(L.xv), d(L.conv_w), d(L.g), d(L.beta), d(L.gate), d(L.norm_w),
+            d(L.cu_seqlens))
+    cin = d(L.conv0).view(torch.bfloat16)
+    a = kda.prefill_layer(*args, conv_in=cin, S0=d(L.S0), fused=True)
+    b = kda.prefill_layer(*args, conv_in=cin, S0=d(L.S0), fused=False)
+    torch.cuda.synchronize()
+    _check_no_device_error()
+    for x, y, what in zip(a, b, ("out", "S_out", "conv_out")):
+        assert torch.equal(x, y), what
 
 
 def _pools(rng, P, H, state_bf16):
