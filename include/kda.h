@@ -322,10 +322,9 @@ int kda_prefill_chunked_gated(const void *q, const void *k, const void *v, const
  * The whole layer's prefill in one call ("Colibri Kimi K3 Metal backend",
  * sections 8.3 and 8.4: the conv + L2-norm prologue feeds the recurrence, the
  * gated RMSNorm follows it): kda_conv_prologue followed by
- * kda_prefill_chunked_gated, with the prologue computed inside the prefill's
- * intra-chunk kernel, so the normalised q, k, v never go through HBM.  The
- * results equal those two calls' (the same arithmetic and roundings: q, k, v
- * rounded to bf16 before the recurrence).  Tensor-core path only (chunk 64).
+ * kda_prefill_chunked_gated on the tensor-core path, with q, k, v kept in the
+ * call's workspace, so a caller needs no buffers for them.  The results are
+ * those two calls' bit for bit.
  *
  *   xq, xk, xv [T, H, 128] bf16 raw projections
  *   conv_w     [3, H, 128, 4] fp32 taps
@@ -336,9 +335,9 @@ int kda_prefill_chunked_gated(const void *q, const void *k, const void *v, const
  *   out        [T, H, 128] fp32, written: the gated RMSNorm of o
  *   q_scale    finite; l2_eps, norm_eps >= 0
  *   dk, dv     must be 128
- * The workspace (one 76,800-byte record per (chunk, head): the record of
- * kda_prefill_chunked plus the chunk's v) comes from the library's pool
- * (KDA_ERR_WORKSPACE if it cannot grow).  Returns KDA_OK or a kda_status_t.
+ * The workspace (q, k, v in bf16, 768 bytes per token-head, and the records
+ * of kda_prefill_chunked) comes from the library's pool (KDA_ERR_WORKSPACE if
+ * it cannot grow).  Returns KDA_OK or a kda_status_t.
  */
 int kda_layer_prefill(const void *xq, const void *xk, const void *xv, const float *conv_w,
                       const void *conv_in, void *conv_out, const float *g, const float *beta,

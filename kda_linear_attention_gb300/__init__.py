@@ -387,15 +387,16 @@ def prefill_layer(xq, xk, xv, conv_w, g, beta, gate, norm_w, cu_seqlens,
                   conv_in: Optional[torch.Tensor] = None, S0: Optional[torch.Tensor] = None,
                   q_scale: float = Q_SCALE, l2_eps: float = L2_EPS, norm_eps: float = NORM_EPS,
                   out: Optional[torch.Tensor] = None, S_out: Optional[torch.Tensor] = None,
-                  conv_out: Optional[torch.Tensor] = None, fused: bool = True,
+                  conv_out: Optional[torch.Tensor] = None, one_call: bool = True,
                   stream: Optional[torch.cuda.Stream] = None):
-    """The layer's prefill from raw projections (``kda_layer_prefill``: the
-    conv + SiLU + L2-norm prologue inside the prefill's intra-chunk kernel,
-    the gated RMSNorm in its state pass).  fused=False runs the same layer as
-    two calls, ``conv_prologue`` (q, k, v through HBM in bf16) then
-    ``prefill_chunked_gated``.  Returns (out [T, H, 128] fp32,
-    S_out [N, H, 128, 128] fp32, conv_out [N, 3, 3, H, 128] bf16)."""
-    if not fused:
+    """The layer's prefill from raw projections in one C call
+    (``kda_layer_prefill``: the conv + SiLU + L2-norm prologue, then the
+    gated prefill, q, k, v in the library's workspace).  one_call=False runs
+    the same layer as the two public calls, ``conv_prologue`` (q, k, v in
+    tensors of this binding) then ``prefill_chunked_gated``.  Returns
+    (out [T, H, 128] fp32, S_out [N, H, 128, 128] fp32,
+    conv_out [N, 3, 3, H, 128] bf16)."""
+    if not one_call:
         q, k, v, conv_out = conv_prologue(xq, xk, xv, conv_w, cu_seqlens, conv_in=conv_in,
                                           conv_out=conv_out, q_scale=q_scale, eps=l2_eps,
                                           stream=stream)

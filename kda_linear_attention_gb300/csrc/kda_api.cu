@@ -250,10 +250,9 @@ int kda_layer_prefill(const void *xq, const void *xk, const void *xv, const floa
                                          cu_seqlens, N, T, H, 64, true, s);
         return cuda_status(e);
     }
-    const cudaError_t e = kda::launch_prefill_split_layer(xq, xk, xv, conv_w, conv_in, conv_out, g,
-                                                          beta, S0, gate, norm_w, q_scale, l2_eps,
-                                                          norm_eps, out, S_out, cu_seqlens, N, T,
-                                                          H, s);
+    const cudaError_t e = kda::launch_prefill_layer(xq, xk, xv, conv_w, conv_in, conv_out, g, beta,
+                                                    S0, gate, norm_w, q_scale, l2_eps, norm_eps,
+                                                    out, S_out, cu_seqlens, N, T, H, s);
     return e == cudaErrorMemoryAllocation ? KDA_ERR_WORKSPACE : cuda_status(e);
 }
 

@@ -77,7 +77,7 @@ cudaError_t launch_prefill_split(const void *q, const void *k, const void *v, co
                                  const float *beta, const float *S0, float *o, float *S_out,
                                  const int32_t *cu_seqlens, int N, int64_t T, int H,
                                  cudaStream_t stream, cudaEvent_t const *events = nullptr);
-size_t prefill_split_workspace_bytes(int N, int64_t T, int H, bool layer = false);
+size_t prefill_split_workspace_bytes(int N, int64_t T, int H);
 
 // The same prefill with its workspace in a fixed file-scope device array of
 // kNoAllocScratchBytes (no allocation during the call); cudaErrorInvalidValue
@@ -110,17 +110,15 @@ cudaError_t launch_prefill_split_gated(const void *q, const void *k, const void 
                                        int64_t T, int H, cudaStream_t stream,
                                        cudaEvent_t const *events = nullptr);
 
-// The layer prefill in the tensor-core kernels: the conv1d + SiLU + L2-norm
-// prologue runs inside the intra-chunk kernel on the raw projections (bf16
-// [T, H, 128]), v's conv reaches the state pass in the record, and the state
-// pass applies the gated RMSNorm; windows as for launch_conv_prologue.
-cudaError_t launch_prefill_split_layer(const void *xq, const void *xk, const void *xv,
-                                       const float *conv_w, const void *conv_in, void *conv_out,
-                                       const float *g, const float *beta, const float *S0,
-                                       const void *gate, const float *norm_w, float q_scale,
-                                       float l2_eps, float norm_eps, float *out, float *S_out,
-                                       const int32_t *cu_seqlens, int N, int64_t T, int H,
-                                       cudaStream_t stream, cudaEvent_t const *events = nullptr);
+// The layer prefill on the tensor-core path: the conv prologue's q, k, v in
+// a pool workspace (bf16), then the gated prefill on them (kda_layer.cu's
+// prologue kernel, then this file's three launches).
+cudaError_t launch_prefill_layer(const void *xq, const void *xk, const void *xv, const float *conv_w,
+                                 const void *conv_in, void *conv_out, const float *g,
+                                 const float *beta, const float *S0, const void *gate,
+                                 const float *norm_w, float q_scale, float l2_eps, float norm_eps,
+                                 float *out, float *S_out, const int32_t *cu_seqlens, int N,
+                                 int64_t T, int H, cudaStream_t stream);
 
 // The layer around the recurrence (kda_layer.cu).
 // conv1d + SiLU on xq/xk/xv, L2 norm of q (times q_scale) and k; windows in
@@ -144,7 +142,7 @@ cudaError_t read_layer_error(unsigned int *code, bool reset);
 // The conv prologue's arithmetic, shared by the prologue kernel and the
 // layer prefill that fuses it: bf16 pairs (low half = even channel) to and
 // from float2 (exact / round to nearest even), and the SiLU of a channel
-// pair, y / (1 + e^-y), with the fast exponential and the hardware
+// pair, y / (1 + e^-y), with e^-y as a power of two and the hardware
 // reciprocal (a few ulp; its results are rounded to bf16).
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
@@ -158,8 +156,17 @@ __device__ __forceinline__ float rcp_approx(float x) {   // 1 / x, about 1 ulp; 
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
 }
+// 2^x on the special-function unit (ex2.approx, a few ulp; results below
+// 2^-126 flush to 0, 2^x for x >= 128 is inf)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+// e^-y = 2^(-y log2 e), the pair's scaling in one packed multiply
 __device__ __forceinline__ float2 silu2(float2 y) {
-    const float2 d = __fadd2_rn(make_float2(1.f, 1.f), make_float2(__expf(-y.x), __expf(-y.y)));
+    const float2 a = __fmul2_rn(y, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+    const float2 d = __fadd2_rn(make_float2(1.f, 1.f), make_float2(ex2_approx(a.x), ex2_approx(a.y)));
     return __fmul2_rn(y, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
 }
 

@@ -107,11 +107,6 @@ constexpr uint32_t R_KB = 43008;    // Kbar fp16 [s][i] sw (two 8 KB halves of 6
 constexpr uint32_t R_VEC = 59392;   // beta[64], q.k[64], e^{b_L}[128] (fp32)
 constexpr uint32_t REC_BYTES = 60416;
 static_assert(REC_BYTES % 1024 == 0 && R_KB % 1024 == 0, "records and their swizzled piece 1 KB aligned");
-// The layer prefill (the conv prologue fused into the intra-chunk kernel)
-// adds v = SiLU(conv(x_v)) of the chunk to the record, bf16 in the
-// 128B-swizzled [s][j] layout of the state pass's V tile.
-constexpr uint32_t R_V = REC_BYTES;
-constexpr uint32_t REC_BYTES_LAYER = R_V + 16384;
 
 // The strictly lower triangular 64 x 64 tiles T' [r][s] and A' [r][s] are
 // stored by K-step kk (columns s = 16 kk .. 16 kk + 15) with only the row
@@ -140,9 +135,7 @@ __device__ __forceinline__ uint32_t tri_off(int r, int s) {
 // written past the buffers sized for T.
 // ============================================================================
 __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t *__restrict__ cu, int N, int T,
-                                                          int32_t *__restrict__ chunk_off,
-                                                          const __nv_bfloat16 *__restrict__ conv_in,
-                                                          __nv_bfloat16 *__restrict__ conv_out, int H) {
+                                                          int32_t *__restrict__ chunk_off) {
     __shared__ int32_t s_scan[1024];
     __shared__ int32_t s_carry;
     __shared__ int s_bad;
@@ -177,19 +170,6 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t *__restr
     if (s_bad) {
         for (int n = t; n < N; n += 1024) chunk_off[n] = 0;
         if (t == 0) atomicOr(&g_kda_device_error, 1u);
-        return;
-    }
-    // layer prefill: an empty sequence's window passes through unchanged (the
-    // intra-chunk kernel writes every other sequence's at its last chunk)
-    if (conv_out) {
-        const long long per_seq = 3LL * 3 * H * 16;          // 16-byte pieces
-        for (long long i = t; i < (long long)N * per_seq; i += 1024) {
-            const int n = (int)(i / per_seq);
-            if (cu[n + 1] != cu[n]) continue;
-            const size_t off = (size_t)n * 3 * 3 * H * 128 + (size_t)(i % per_seq) * 8;
-            const uint4 w = conv_in ? *reinterpret_cast<const uint4 *>(conv_in + off) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(conv_out + off) = w;
-        }
     }
 }
 
@@ -233,29 +213,13 @@ constexpr uint32_t TMA_W = 0;             // W, 128 columns (after the Gram epil
 
 struct Job {
     int h, gc, tok, Lc;
-    int n;                  // sequence
-    bool first, last;       // the sequence's first / last chunk
 };
 
-// The layer prefill's conv prologue, fused into the intra-chunk kernel: raw
-// projections [T, H, 128] bf16 (xq, xk reach the kernel through its q, k
-// tensor maps), taps [3, H, 128, 4] fp32, windows [N, 3, 3, H, 128] bf16 in
-// (or null: zeros) and out (or null).
-struct LayerArgs {
-    const __nv_bfloat16 *xq, *xk, *xv;
-    const float *conv_w;
-    const __nv_bfloat16 *conv_in;
-    __nv_bfloat16 *conv_out;
-    float q_scale, l2_eps;
-};
-
-template <bool LAYER>
 __global__ void __launch_bounds__(NTA, 2)
 intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_g, const float *__restrict__ beta,
                    const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N,
-                   int H, uint8_t *__restrict__ recs, int T, int max_chunks, const LayerArgs la) {
-    constexpr uint32_t kRec = LAYER ? REC_BYTES_LAYER : REC_BYTES;
+                   int H, uint8_t *__restrict__ recs, int T, int max_chunks) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float *s_beta = reinterpret_cast<float *>(sm + SA_MISC + MA_BETA);
@@ -292,9 +256,6 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         }
         J.tok = cu[lo] + (J.gc - chunk_off[lo]) * C;
         J.Lc = min(C, cu[lo + 1] - J.tok);
-        J.n = lo;
-        J.first = J.gc == chunk_off[lo];
-        J.last = J.tok + J.Lc == cu[lo + 1];
         // debug builds: the job's record and tokens inside the buffers
         J.gc = KDA_DBG_INDEX(g_kda_device_error, J.gc, 0, max_chunks);
         J.tok = KDA_DBG_INDEX(g_kda_device_error, J.tok, 0, T);
@@ -317,112 +278,6 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     };
     auto load_beta = [&](const Job &J) -> float {
         return (t < J.Lc) ? beta[(size_t)(J.tok + t) * H + J.h] : 0.f;
-    };
-    // ===== the layer's conv prologue ("Colibri Kimi K3 Metal backend",
-    // section 8.3): per channel a causal conv of width 4 over the raw
-    // projection (tap m on the input m - 3 tokens back from the newest), SiLU,
-    // then per (token, head) the L2 norm of q (times q_scale) and of k.  q and
-    // k are rounded to bf16, as the separate prologue stores them, and
-    // replace the raw rows in X; v goes to the record.  Half-warp hw takes
-    // rows 4 hw .. 4 hw + 3 of the chunk, lane l channels 8 l .. 8 l + 7, and
-    // reads the three rows before its first from the chunk, from the chunk
-    // before (same sequence) or from the carried window (first chunk).
-    auto layer_prologue = [&](const Job &J, uint8_t *rec) {
-        const int hw = t >> 4, l = t & 15;
-        const size_t rstride = (size_t)H * 128;
-        const size_t col = (size_t)J.h * 128 + 8 * l;
-        // projection pi = v (to the record), then q and k (in place in X: all
-        // of a projection's raw rows are read before any is overwritten)
-#pragma unroll 1
-        for (int pi = 0; pi < 3; ++pi) {
-            const int p = pi == 0 ? 2 : pi - 1;
-            const __nv_bfloat16 *xp = p == 0 ? la.xq : (p == 1 ? la.xk : la.xv);
-            float2 wt[4][4];                  // (channel pair m, tap)
-            {
-                const float4 *wp = reinterpret_cast<const float4 *>(la.conv_w + (((size_t)p * H + J.h) * 128 + 8 * l) * 4);
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float4 a = wp[2 * m], b = wp[2 * m + 1];
-                    wt[m][0] = make_float2(a.x, b.x);
-                    wt[m][1] = make_float2(a.y, b.y);
-                    wt[m][2] = make_float2(a.z, b.z);
-                    wt[m][3] = make_float2(a.w, b.w);
-                }
-            }
-            uint4 xr[7];                      // raw rows 4 hw - 3 .. 4 hw + 3
-#pragma unroll
-            for (int i = 0; i < 7; ++i) {
-                const int row = 4 * hw - 3 + i;
-                uint4 u = make_uint4(0, 0, 0, 0);
-                if (row >= 0) {
-                    if (row < J.Lc) {
-                        if (p < 2) u = *reinterpret_cast<const uint4 *>(sm + SA_X + sw_chunk(64 * p + row, l, 16384));
-                        else u = *reinterpret_cast<const uint4 *>(xp + (size_t)(J.tok + row) * rstride + col);
-                    }
-                } else if (J.first) {
-                    if (la.conv_in)
-                        u = *reinterpret_cast<const uint4 *>(la.conv_in + (((size_t)J.n * 3 + p) * 3 + (3 + row)) * rstride + col);
-                } else {
-                    u = *reinterpret_cast<const uint4 *>(xp + (size_t)(J.tok + row) * rstride + col);
-                }
-                xr[i] = u;
-            }
-            // the window after the sequence's last token: its last three raw
-            // inputs, each written by the half-warp whose rows hold it
-            if (J.last && la.conv_out) {
-#pragma unroll
-                for (int s2 = 0; s2 < 3; ++s2) {
-                    const int row = J.Lc - 3 + s2;
-                    if (hw == (row >= 0 ? row >> 2 : 0)) {
-                        const int i = row - (4 * hw - 3);
-#pragma unroll
-                        for (int ii = 0; ii < 7; ++ii)
-                            if (ii == i)
-                                *reinterpret_cast<uint4 *>(la.conv_out + (((size_t)J.n * 3 + p) * 3 + s2) * rstride + col) = xr[ii];
-                    }
-                }
-            }
-            uint4 out[4];
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                float2 z[4];
-                float2 ss2 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const uint32_t w0 = (&xr[rr].x)[m], w1 = (&xr[rr + 1].x)[m];
-                    const uint32_t w2 = (&xr[rr + 2].x)[m], w3 = (&xr[rr + 3].x)[m];
-                    float2 y = __fmul2_rn(wt[m][3], bf2_to_f2(w3));
-                    y = __ffma2_rn(wt[m][2], bf2_to_f2(w2), y);
-                    y = __ffma2_rn(wt[m][1], bf2_to_f2(w1), y);
-                    y = __ffma2_rn(wt[m][0], bf2_to_f2(w0), y);
-                    z[m] = silu2(y);
-                    ss2 = __ffma2_rn(z[m], z[m], ss2);
-                }
-                float f = 1.f;
-                if (p < 2) {                  // the L2 norm over the row's 128 channels (this half-warp)
-                    float ss = ss2.x + ss2.y;
-#pragma unroll
-                    for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, 16);
-                    f = (p == 0 ? la.q_scale : 1.f) * rsqrtf(ss + la.l2_eps);
-                }
-                const float2 f2 = make_float2(f, f);
-                out[rr] = make_uint4(f2_to_bf2(__fmul2_rn(z[0], f2)), f2_to_bf2(__fmul2_rn(z[1], f2)),
-                                     f2_to_bf2(__fmul2_rn(z[2], f2)), f2_to_bf2(__fmul2_rn(z[3], f2)));
-            }
-            if (p == 2) {                     // rows past the sequence stay zero (finite)
-#pragma unroll
-                for (int rr = 0; rr < 4; ++rr) {
-                    const int row = 4 * hw + rr;
-                    *reinterpret_cast<uint4 *>(rec + R_V + sw_chunk(row, l, 8192)) =
-                        row < J.Lc ? out[rr] : make_uint4(0, 0, 0, 0);
-                }
-            } else {
-                __syncthreads();              // every raw row of this projection is read
-#pragma unroll
-                for (int rr = 0; rr < 4; ++rr)
-                    *reinterpret_cast<uint4 *>(sm + SA_X + sw_chunk(64 * p + 4 * hw + rr, l, 16384)) = out[rr];
-            }
-        }
     };
 
     int job = blockIdx.x;
@@ -453,14 +308,12 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
 
     for (int it = 0; !failed; ++it) {
     const int h = J.h, Lc = J.Lc;
-    uint8_t *rec = recs + ((size_t)J.gc * H + h) * kRec;
+    uint8_t *rec = recs + ((size_t)J.gc * H + h) * REC_BYTES;
     if (t < C) s_beta[t] = bnext;
     const int job_next = job + gridDim.x;
     const bool has_next = job_next < total;
     Job Jn = J;
-    if (!wait_all(bar_qk, it & 1)) { failed = true; fail_at = 1; fail_it = it; fail_next = has_next; break; }
-    if constexpr (LAYER) layer_prologue(J, rec);
-    if (!wait_all(bar_g, it & 1)) { failed = true; fail_at = 1; fail_it = it; fail_next = has_next; break; }
+    if (!wait_all(bar_qk, it & 1) || !wait_all(bar_g, it & 1)) { failed = true; fail_at = 1; fail_it = it; fail_next = has_next; break; }
 
     {
         // ===== decay prefix sums: column scan in place in the g tile =========
@@ -1046,7 +899,7 @@ __device__ __forceinline__ float gate_sigmoid(float x) { return __fdividef(1.f, 
 //   copy warp: request the gate of chunk j-1; after round 1, record A(j+1)
 //              | mid | v(j+1); once staged, store o(j-1); after round 2,
 //              record B(j+1) | end
-template <bool GATED, bool VREC>
+template <bool GATED>
 __global__ void __launch_bounds__(NTB, 1)
 state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
                   const float *__restrict__ S0,
@@ -1130,12 +983,12 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
     // requests made by the copy thread, counted where they are made, so that
     // if a bounded wait gives up it waits for exactly what is in flight
     int issued_a = 0, issued_b = 0, issued_gate = 0, issued_mma = 0;
-    constexpr uint32_t kRec = VREC ? REC_BYTES_LAYER : REC_BYTES;
     auto rec_at = [&](int j) -> const uint8_t * {
         const int gc = KDA_DBG_INDEX(g_kda_device_error, cbase + j, 0, max_chunks);
-        return recs + ((size_t)gc * H + h) * kRec;
+        return recs + ((size_t)gc * H + h) * REC_BYTES;
     };
-    // record A of chunk j, with the byte count of v, which issue_v requests
+    // record A of chunk j and e^{b_L} of chunk j + 1 (for the scaling of S at
+    // the end of chunk j), with the byte count of v, which issue_v requests
     // once the previous chunk's v is consumed
     auto issue_a = [&](int j) {
         const uint8_t *r = rec_at(j);
@@ -1145,12 +998,8 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         bulk_load(sm + SB_VEC + 1024 * (j & 1), r + R_VEC, 1024, bar_a);
     };
     auto issue_v = [&](int j) {
-        if (VREC) {                          // the layer prefill: v is part of the record
-            bulk_load(sm + SB_V, rec_at(j) + R_V, 16384, bar_a);
-        } else {
-            tma_load_3d(sm + SB_V, &map_v, bar_a, 0, h, tok0 + j * C);
-            tma_load_3d(sm + SB_V + 8192, &map_v, bar_a, 64, h, tok0 + j * C);
-        }
+        tma_load_3d(sm + SB_V, &map_v, bar_a, 0, h, tok0 + j * C);
+        tma_load_3d(sm + SB_V + 8192, &map_v, bar_a, 64, h, tok0 + j * C);
     };
     auto issue_gate = [&](int j) {
         mbar_arrive_expect_tx(bar_gate, 16384);
@@ -1164,11 +1013,9 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
         bulk_load(sm + SB_A, rec_at(j) + R_A, COPY2, bar_b);
     };
     auto prefetch2 = [&](int j) {            // chunk j toward L2
-        bulk_prefetch_l2(rec_at(j), kRec);
-        if (!VREC) {
-            tma_prefetch_l2_3d(&map_v, 0, h, tok0 + j * C);
-            tma_prefetch_l2_3d(&map_v, 64, h, tok0 + j * C);
-        }
+        bulk_prefetch_l2(rec_at(j), REC_BYTES);
+        tma_prefetch_l2_3d(&map_v, 0, h, tok0 + j * C);
+        tma_prefetch_l2_3d(&map_v, 64, h, tok0 + j * C);
     };
     if (t == T_TMA && nch > 0) {
         issue_a(0);
@@ -1524,10 +1371,10 @@ unsigned long long g_attr_ctx[kMaxDevices] = {};
 
 }  // namespace
 
-size_t prefill_split_workspace_bytes(int N, int64_t T, int H, bool layer) {
+size_t prefill_split_workspace_bytes(int N, int64_t T, int H) {
     const int64_t max_chunks = (T + C - 1) / C + N;
     const size_t off_bytes = ((size_t)(N + 1) * sizeof(int32_t) + 1023) & ~(size_t)1023;
-    return off_bytes + (size_t)max_chunks * (size_t)H * (layer ? REC_BYTES_LAYER : REC_BYTES);
+    return off_bytes + (size_t)max_chunks * (size_t)H * REC_BYTES;
 }
 
 namespace {
@@ -1545,16 +1392,14 @@ unsigned intra_grid(int64_t jobs) {
 }
 
 // The three launches of one prefill, with the workspace at `ws` (at least
-// prefill_split_workspace_bytes(N, T, H, layer != nullptr) bytes).  With a
-// gate, the state pass writes the gated RMSNorm of o to `o` instead of o
-// itself.  With `layer` (the layer prefill: gated) q, k, v are the raw
-// projections and the intra-chunk kernel runs the conv prologue on them.
+// prefill_split_workspace_bytes(N, T, H) bytes).  With a gate, the state pass
+// writes the gated RMSNorm of o to `o` instead of o itself.
 cudaError_t run_split(const void *q, const void *k, const void *v, const float *g,
                       const float *beta, const float *S0, float *o, float *S_out,
                       const int32_t *cu_seqlens, int N, int64_t T, int H, void *ws,
                       cudaStream_t stream, cudaEvent_t const *ev = nullptr,
                       const void *gate = nullptr, const float *norm_w = nullptr,
-                      float norm_eps = 0.f, const LayerArgs *layer = nullptr) {
+                      float norm_eps = 0.f) {
     const int64_t max_chunks = (T + C - 1) / C + N;
     static MapCache maps;
     CUtensorMap mq, mk, mv, mg, mo, mgate;
@@ -1571,20 +1416,14 @@ cudaError_t run_split(const void *q, const void *k, const void *v, const float *
         std::lock_guard<std::mutex> lk(g_attr_mu);
         const unsigned long long ctx = current_context_id();
         if (ctx == 0 || ctx != g_attr_ctx[dev]) {
-            e = cudaFuncSetAttribute(intra_chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(intra_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)SMEM_A_ALLOC);
             if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(intra_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_A_ALLOC);
+                e = cudaFuncSetAttribute(state_pass_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_B_ALLOC);
             if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(state_pass_kernel<true, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_B_ALLOC);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(state_pass_kernel<false, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_B_ALLOC);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(state_pass_kernel<true, true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_B_ALLOC);
+                e = cudaFuncSetAttribute(state_pass_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_B_ALLOC);
             if (e != cudaSuccess) return e;
             g_attr_ctx[dev] = current_context_id();
         }
@@ -1593,29 +1432,17 @@ cudaError_t run_split(const void *q, const void *k, const void *v, const float *
     uint8_t *recs = static_cast<uint8_t *>(ws) +
                     (((size_t)(N + 1) * sizeof(int32_t) + 1023) & ~(size_t)1023);
     if (ev) cudaEventRecord(ev[0], stream);
-    chunk_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, (int)T, chunk_off,
-                                               layer ? layer->conv_in : nullptr,
-                                               layer ? layer->conv_out : nullptr, H);
+    chunk_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, (int)T, chunk_off);
     if (ev) cudaEventRecord(ev[1], stream);
-    const unsigned grid_a = intra_grid(max_chunks * H);
-    if (layer)
-        intra_chunk_kernel<true><<<grid_a, NTA, SMEM_A_ALLOC, stream>>>(
-            mq, mk, mg, beta, cu_seqlens, chunk_off, N, H, recs, (int)T, (int)max_chunks, *layer);
-    else
-        intra_chunk_kernel<false><<<grid_a, NTA, SMEM_A_ALLOC, stream>>>(
-            mq, mk, mg, beta, cu_seqlens, chunk_off, N, H, recs, (int)T, (int)max_chunks, LayerArgs{});
+    intra_chunk_kernel<<<intra_grid(max_chunks * H), NTA, SMEM_A_ALLOC, stream>>>(
+        mq, mk, mg, beta, cu_seqlens, chunk_off, N, H, recs, (int)T, (int)max_chunks);
     if (ev) cudaEventRecord(ev[2], stream);
-    const unsigned grid_b = (unsigned)((int64_t)N * H);
-    if (layer)
-        state_pass_kernel<true, true><<<grid_b, NTB, SMEM_B_ALLOC, stream>>>(
-            mv, mo, S0, o, S_out, cu_seqlens, chunk_off, N, H, (int)max_chunks, recs, mgate, norm_w,
-            norm_eps, (int)T);
-    else if (gate)
-        state_pass_kernel<true, false><<<grid_b, NTB, SMEM_B_ALLOC, stream>>>(
+    if (gate)
+        state_pass_kernel<true><<<(unsigned)((int64_t)N * H), NTB, SMEM_B_ALLOC, stream>>>(
             mv, mo, S0, o, S_out, cu_seqlens, chunk_off, N, H, (int)max_chunks, recs, mgate, norm_w,
             norm_eps, (int)T);
     else
-        state_pass_kernel<false, false><<<grid_b, NTB, SMEM_B_ALLOC, stream>>>(
+        state_pass_kernel<false><<<(unsigned)((int64_t)N * H), NTB, SMEM_B_ALLOC, stream>>>(
             mv, mo, S0, o, S_out, cu_seqlens, chunk_off, N, H, (int)max_chunks, recs, mgate, nullptr,
             0.f, (int)T);
     if (ev) cudaEventRecord(ev[3], stream);
@@ -1658,23 +1485,25 @@ cudaError_t launch_prefill_split_gated(const void *q, const void *k, const void 
     return e != cudaSuccess ? e : ef;
 }
 
-cudaError_t launch_prefill_split_layer(const void *xq, const void *xk, const void *xv,
-                                       const float *conv_w, const void *conv_in, void *conv_out,
-                                       const float *g, const float *beta, const float *S0,
-                                       const void *gate, const float *norm_w, float q_scale,
-                                       float l2_eps, float norm_eps, float *out, float *S_out,
-                                       const int32_t *cu_seqlens, int N, int64_t T, int H,
-                                       cudaStream_t stream, cudaEvent_t const *events) {
+// The layer prefill: the conv prologue writes q, k, v (bf16) into the front
+// of one pool allocation, the gated prefill's records follow them.
+cudaError_t launch_prefill_layer(const void *xq, const void *xk, const void *xv, const float *conv_w,
+                                 const void *conv_in, void *conv_out, const float *g,
+                                 const float *beta, const float *S0, const void *gate,
+                                 const float *norm_w, float q_scale, float l2_eps, float norm_eps,
+                                 float *out, float *S_out, const int32_t *cu_seqlens, int N,
+                                 int64_t T, int H, cudaStream_t stream) {
     if (!grid_fits(N, T, H)) return cudaErrorInvalidValue;
-    const LayerArgs la{static_cast<const __nv_bfloat16 *>(xq), static_cast<const __nv_bfloat16 *>(xk),
-                       static_cast<const __nv_bfloat16 *>(xv), conv_w,
-                       static_cast<const __nv_bfloat16 *>(conv_in), static_cast<__nv_bfloat16 *>(conv_out),
-                       q_scale, l2_eps};
+    const size_t qkv_bytes = ((size_t)T * H * kDK * 2 + 1023) & ~(size_t)1023;
     void *ws = nullptr;
-    cudaError_t e = ws_alloc(&ws, prefill_split_workspace_bytes(N, T, H, true), stream);
+    cudaError_t e = ws_alloc(&ws, 3 * qkv_bytes + prefill_split_workspace_bytes(N, T, H), stream);
     if (e != cudaSuccess) return e;
-    e = run_split(xq, xk, xv, g, beta, S0, out, S_out, cu_seqlens, N, T, H, ws, stream, events, gate,
-                  norm_w, norm_eps, &la);
+    uint8_t *q = static_cast<uint8_t *>(ws);
+    e = launch_conv_prologue(xq, xk, xv, conv_w, conv_in, conv_out, q, q + qkv_bytes,
+                             q + 2 * qkv_bytes, cu_seqlens, N, T, H, q_scale, l2_eps, stream);
+    if (e == cudaSuccess)
+        e = run_split(q, q + qkv_bytes, q + 2 * qkv_bytes, g, beta, S0, out, S_out, cu_seqlens, N,
+                      T, H, q + 3 * qkv_bytes, stream, nullptr, gate, norm_w, norm_eps);
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     return e != cudaSuccess ? e : ef;
 }

@@ -192,14 +192,14 @@ LAYER_CASES = [([0, 1, 70, 3, 129], 3, True, True),
                ([4096], 96, False, True)]
 
 
-@pytest.mark.parametrize("fused", [True, False], ids=["fused", "two_calls"])
+@pytest.mark.parametrize("one_call", [True, False], ids=["one_call", "two_calls"])
 @pytest.mark.parametrize("lens,H,with_s0,with_conv0", LAYER_CASES)
-def test_prefill_layer_against_the_layer_oracle(lens, H, with_s0, with_conv0, fused):
-    """The layer prefill from raw projections, fused (``kda_layer_prefill``:
-    the prologue inside the intra-chunk kernel) and as two calls (prologue,
-    then the gated tensor-core prefill), against the oracle's layer prefill
-    with q, k, v rounded to bf16.  Sequences of 1 and 2 tokens carry part of
-    the window before them into the window after them."""
+def test_prefill_layer_against_the_layer_oracle(lens, H, with_s0, with_conv0, one_call):
+    """The layer prefill from raw projections, in one call
+    (``kda_layer_prefill``) and as two calls (prologue, then the gated
+    tensor-core prefill), against the oracle's layer prefill with q, k, v
+    rounded to bf16.  Sequences of 1 and 2 tokens carry part of the window
+    before them into the window after them."""
     import torch
     kda = _kda()
     L = ki.gen_layer(120 + H, lens, H=H, with_s0=with_s0, with_conv0=with_conv0)
@@ -208,7 +208,7 @@ def test_prefill_layer_against_the_layer_oracle(lens, H, with_s0, with_conv0, fu
     cin = d(L.conv0).view(torch.bfloat16) if with_conv0 else None
     out, S, co = kda.prefill_layer(d(L.xq), d(L.xk), d(L.xv), d(L.conv_w), d(L.g), d(L.beta),
                                    d(L.gate), d(L.norm_w), d(L.cu_seqlens),
-                                   conv_in=cin, S0=s0, fused=fused)
+                                   conv_in=cin, S0=s0, one_call=one_call)
     torch.cuda.synchronize()
     _check_no_device_error()
     out_ref, o_ref, S_ref, co_ref = olayer.prefill_layer(L, QS, round_qkv_bf16=True)
@@ -225,10 +225,10 @@ def test_prefill_layer_against_the_layer_oracle(lens, H, with_s0, with_conv0, fu
 
 
 @pytest.mark.parametrize("lens,H", [(RAGGED, 2), ([4096], 96)])
-def test_fused_layer_prefill_equals_the_two_calls(lens, H):
-    """The fused layer prefill computes the prologue with the separate
-    prologue kernel's arithmetic and feeds the same bf16 q, k, v to the same
-    recurrence, so its outputs, final states and windows are the two-call
+def test_layer_prefill_equals_the_two_calls(lens, H):
+    """kda_layer_prefill runs the prologue and the gated prefill on the same
+    bf16 q, k, v as the two public calls, and every prefill kernel sums in a
+    fixed order, so its outputs, final states and windows are the two-call
     path's bit for bit."""
     import torch
     kda = _kda()
@@ -237,8 +237,8 @@ def test_fused_layer_prefill_equals_the_two_calls(lens, H):
     args = (d(L.xq), d(L.xk), d(L.xv), d(L.conv_w), d(L.g), d(L.beta), d(L.gate), d(L.norm_w),
             d(L.cu_seqlens))
     cin = d(L.conv0).view(torch.bfloat16)
-    a = kda.prefill_layer(*args, conv_in=cin, S0=d(L.S0), fused=True)
-    b = kda.prefill_layer(*args, conv_in=cin, S0=d(L.S0), fused=False)
+    a = kda.prefill_layer(*args, conv_in=cin, S0=d(L.S0), one_call=True)
+    b = kda.prefill_layer(*args, conv_in=cin, S0=d(L.S0), one_call=False)
     torch.cuda.synchronize()
     _check_no_device_error()
     for x, y, what in zip(a, b, ("out", "S_out", "conv_out")):
