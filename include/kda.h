@@ -152,8 +152,8 @@ int kda_prefill_chunked_events(const void *q, const void *k, const void *v,
  *
  * The tensor-core path (bf16, chunk 64, T > 0) takes its workspace from a
  * fixed 64 MiB array in the library's device image instead of the pool.  It
- * needs 1024 * ceil(4 (N + 1) / 1024) + (ceil(T / 64) + N) * H * 60416
- * bytes; larger inputs are rejected with KDA_ERR_WORKSPACE before anything
+ * needs kda_prefill_workspace_bytes(N, T, H, ...) bytes (about
+ * (ceil(T / 64) + N) * H * 60416); larger inputs are rejected with KDA_ERR_WORKSPACE before anything
  * is launched (for H = 96 and one sequence: T <= 640).  Every other dtype /
  * chunk combination runs the CUDA-core kernel, which needs no workspace.
  * Nothing in the array has to be cleared between calls.
@@ -176,9 +176,11 @@ int kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v,
 
 /*
  * Bytes of caller-owned workspace that kda_prefill_chunked_ws needs for these
- * sizes: the records of the tensor-core path (bf16, chunk 64, T > 0),
- * 1024 * ceil(4 (N + 1) / 1024) + (ceil(T / 64) + N) * H * 60416; 0 for every
- * other combination (the CUDA-core kernel needs none) and for invalid sizes.
+ * sizes on the tensor-core path (bf16, chunk 64, T > 0): with
+ * C = ceil(T / 64) + N chunks (one spare per sequence for a partial tail),
+ * 1024 * ceil(4 (N + 1) / 1024) + 1024 * ceil(8 C / 1024) + C * H * 60416
+ * (the chunk offsets, the chunk table, one record per (chunk, head)); 0 for
+ * every other combination (the CUDA-core kernel needs none) and for invalid sizes.
  * Host-only, no CUDA call.
  */
 size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chunk, int dtype);

@@ -126,7 +126,9 @@ __device__ __forceinline__ uint32_t tri_off(int r, int s) {
 }
 
 // ============================================================================
-// chunk plan: chunk_off[n] = sum_{m<n} ceil(len_m / 64), chunk_off[N] = total.
+// chunk plan: chunk_off[n] = sum_{m<n} ceil(len_m / 64), chunk_off[N] = total,
+// and per global chunk gc its first token and row count, tab[gc] = (tok, Lc),
+// so that the intra-chunk kernel finds a job's chunk with one 8-byte load.
 // cu_seqlens must start at or above 0, never decrease and end at or below T
 // (the call's precondition, which the host cannot read); otherwise the plan
 // is emptied (every offset 0) and the device error word set, so that the
@@ -135,7 +137,8 @@ __device__ __forceinline__ uint32_t tri_off(int r, int s) {
 // written past the buffers sized for T.
 // ============================================================================
 __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t *__restrict__ cu, int N, int T,
-                                                          int32_t *__restrict__ chunk_off) {
+                                                          int32_t *__restrict__ chunk_off,
+                                                          int2 *__restrict__ tab) {
     __shared__ int32_t s_scan[1024];
     __shared__ int32_t s_carry;
     __shared__ int s_bad;
@@ -170,6 +173,19 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t *__restr
     if (s_bad) {
         for (int n = t; n < N; n += 1024) chunk_off[n] = 0;
         if (t == 0) atomicOr(&g_kda_device_error, 1u);
+        return;
+    }
+    __syncthreads();                       // chunk_off is complete (this block wrote it)
+    const int total = s_carry;
+    for (int gc = t; gc < total; gc += 1024) {
+        int lo = 0, hi = N - 1;            // the sequence: the last n with chunk_off[n] <= gc
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (chunk_off[mid] <= gc) lo = mid;
+            else hi = mid - 1;
+        }
+        const int tok = cu[lo] + (gc - chunk_off[lo]) * C;
+        tab[gc] = make_int2(tok, min(C, cu[lo + 1] - tok));
     }
 }
 
@@ -183,17 +199,19 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t *__restr
 // ============================================================================
 constexpr int NTA = 256;
 constexpr uint32_t SA_X = 0;              // 32 KB: q|k (TMA) -> X [128][128] sw (A of the Gram)
-constexpr uint32_t SA_KH = 32768;         // 40 KB: g (TMA) -> Khat [160][128] sw (B of the Gram)
+constexpr uint32_t SA_KH = 32768;         // 56 KB: g (TMA) -> Khat [160][128] and below it Klo
+                                          //   [64][128], one [224][128] sw B operand of the Gram
 constexpr uint32_t SA_M = SA_KH;          //   after the Gram: M / T fp32 [64][68] (17408 B)
 constexpr uint32_t SA_Y = SA_KH + 17408;  //   solve temporaries (4 KB)
 constexpr uint32_t SA_T = SA_KH + 24576;  //   T Diag(beta) fp16 il [r][s], rows 0..63 twice
                                           //   (16 KB: the M = 128 A operand of the W product)
-constexpr uint32_t SA_K0 = 73728;         // 16 KB: K0 [64 s][128 i] fp16 sw (MN-major B of the W product)
-constexpr uint32_t SA_KLO = 90112;        // 16 KB: low bf16 parts of the diagonal key rows [64 s][128 i] sw
+constexpr uint32_t KH_HALF = 224 * 128;  // one 64-channel half of the Khat | Klo operand
+constexpr uint32_t SA_K0 = 90112;         // 16 KB: K0 [64 s][128 i] fp16 sw (MN-major B of the W product)
 constexpr uint32_t SA_MISC = 106496;
 constexpr uint32_t MA_BETA = 0;           // float[64]
 constexpr uint32_t MA_GAM = 256;          // float[128]  e^{b_L}
-                                          // (768..1023 free)
+constexpr uint32_t MA_TAB = 768;          // int2[2]: chunk-table entries of the next two jobs
+                                          // (784..1023 free)
 constexpr uint32_t MA_TOT = 1024;         // float[4][128] sub-block totals, then carry - sigma_u,
                                           //   then the warps' q . k partials [8][64]
 constexpr uint32_t MA_SIG = 3072;         // float[4][128] first-half scan totals, then e^{b_L - sigma_u}
@@ -204,11 +222,12 @@ constexpr uint32_t SMEM_A_USED = SA_MISC + 7200;
 constexpr uint32_t SMEM_A_ALLOC = SMEM_A_USED + 1024;
 static_assert(2 * (SMEM_A_ALLOC + 1024) <= 233472, "two intra-chunk CTAs per SM");
 static_assert(SA_T + 16384 <= SA_K0 && SA_Y + 4096 <= SA_T, "solve space inside the Khat region");
+static_assert(SA_KH + 2 * KH_HALF == SA_K0 && (SA_KH + KH_HALF) % 1024 == 0, "Khat | Klo operand");
 static_assert(SA_Y + 32 * 40 * 4 <= SA_T, "the 32 x 32 solve temporary fits");
 constexpr int MLD = 68;                   // row stride (floats) of M / T
 constexpr int YLD = 40;                   // row stride (floats) of the 32x32 solve temporary
-constexpr uint32_t TMA_G = 0;             // Gram D, 160 columns
-constexpr uint32_t TMA_C = 160;           // correction of its diagonal q blocks, 64 columns
+constexpr uint32_t TMA_G = 0;             // Gram D, 160 columns, then
+constexpr uint32_t TMA_C = 160;           //   the correction of its diagonal q blocks, 64 columns
 constexpr uint32_t TMA_W = 0;             // W, 128 columns (after the Gram epilogue)
 
 struct Job {
@@ -218,7 +237,7 @@ struct Job {
 __global__ void __launch_bounds__(NTA, 2)
 intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_g, const float *__restrict__ beta,
-                   const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N,
+                   const int2 *__restrict__ tab, const int32_t *__restrict__ chunk_off, int N,
                    int H, uint8_t *__restrict__ recs, int T, int max_chunks) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -243,19 +262,24 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     // which the state pass reads first, are the most recently written and
     // still in L2 when it starts.
     const int total = chunk_off[N] * H;
-    auto decode = [&](int job) -> Job {
+    // A job's chunk-table entry is copied into shared memory (s_tab, slot
+    // k & 1 for the CTA's k-th job) two jobs ahead, so that no decode waits
+    // on a global load.
+    int2 *s_tab = reinterpret_cast<int2 *>(sm + SA_MISC + MA_TAB);
+    auto gc_of = [&](int job) -> int { return (total - 1 - job) / H; };
+    auto prefetch_entry = [&](int job, int slot) {
+        if (job < total) {
+            cp_async8(s_tab + slot, tab + KDA_DBG_INDEX(g_kda_device_error, gc_of(job), 0, max_chunks));
+            cp_async_commit();
+        }
+    };
+    auto decode = [&](int job, int2 e) -> Job {
         Job J;
         const int jr = total - 1 - job;
         J.h = jr % H;
         J.gc = jr / H;
-        int lo = 0, hi = N - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (chunk_off[mid] <= J.gc) lo = mid;
-            else hi = mid - 1;
-        }
-        J.tok = cu[lo] + (J.gc - chunk_off[lo]) * C;
-        J.Lc = min(C, cu[lo + 1] - J.tok);
+        J.tok = e.x;
+        J.Lc = e.y;
         // debug builds: the job's record and tokens inside the buffers
         J.gc = KDA_DBG_INDEX(g_kda_device_error, J.gc, 0, max_chunks);
         J.tok = KDA_DBG_INDEX(g_kda_device_error, J.tok, 0, T);
@@ -282,7 +306,8 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
 
     int job = blockIdx.x;
     if (job >= total) return;
-    Job J = decode(job);
+    Job J = decode(job, tab[KDA_DBG_INDEX(g_kda_device_error, gc_of(job), 0, max_chunks)]);
+    if (t == 0) prefetch_entry(job + (int)gridDim.x, 1);
     if (warp == 0) tmem_alloc(s_tmem, 256);
     if (t == 0) {
         mbar_init(bar_qk, 1);
@@ -313,6 +338,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     const int job_next = job + gridDim.x;
     const bool has_next = job_next < total;
     Job Jn = J;
+    if (t == 0) cp_async_wait_all();   // the next job's table entry (published by the barrier)
     if (!wait_all(bar_qk, it & 1) || !wait_all(bar_g, it & 1)) { failed = true; fail_at = 1; fail_it = it; fail_next = has_next; break; }
 
     {
@@ -461,13 +487,13 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
 #pragma unroll
                         for (int m = 0; m < 4; ++m) kh[m] = __fmul2_rn(kh[m], dd[m]);
                     }
-                    *reinterpret_cast<uint4 *>(sm + SA_KH + sw_chunk(8 * pp * (pp + 1) + r, cc, 20480)) =
+                    *reinterpret_cast<uint4 *>(sm + SA_KH + sw_chunk(8 * pp * (pp + 1) + r, cc, KH_HALF)) =
                         pack_bf8x2(kh);
                 }
             }
             // the low part of the diagonal block's keys (block u of the stack
-            // holds kg itself): lo(kg) = kg - bf16(kg), rounded to bf16, at row r
-            // of the Klo tile (see the correction MMA after the Gram)
+            // holds kg itself): lo(kg) = kg - bf16(kg), rounded to bf16, at row
+            // 160 + r of the Gram's B operand (the correction columns)
             {
                 float2 kl[4];
 #pragma unroll
@@ -475,7 +501,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     const float2 kh2 = __bfloat1622float2(__floats2bfloat162_rn(kg[m].x, kg[m].y));
                     kl[m] = make_float2(kg[m].x - kh2.x, kg[m].y - kh2.y);
                 }
-                *reinterpret_cast<uint4 *>(sm + SA_KLO + sw_chunk(r, cc, 8192)) = pack_bf8x2(kl);
+                *reinterpret_cast<uint4 *>(sm + SA_KH + sw_chunk(160 + r, cc, KH_HALF)) = pack_bf8x2(kl);
             }
             // Q0 = q e^{b} -> record rows 64..127 of [-W ; Q0];  K0 = k e^{b} -> smem
             {
@@ -509,29 +535,22 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         fence_proxy_async_smem();
         sync_tc();
 
-        // ===== Gram: D_G[128 x 160] = X Khat^T ===============================
+        // ===== Gram: D[128 x 224] = X [Khat ; Klo]^T ========================
+        // Columns 0..159 hold both gated Gram matrices; columns 160..223 the
+        // diagonal q blocks of the Gram in more than bf16 precision, X Klo^T
+        // (every q row against every diagonal key row; row r of sub-block p
+        // uses columns 160 + 16p .. 160 + 16p + 15), added to hi(xq) hi(kg) in
+        // the epilogue.  A' of a short sequence lives in these blocks, where
+        // the bf16 rounding of the keys alone would cost o up to 2^-9 of each
+        // product term.
         if (t == 0) {
-            const uint32_t idg = instr_desc(kFmtBF16, 128, 160, 0, 0);
+            const uint32_t idg = instr_desc(kFmtBF16, 128, 224, 0, 0);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t ko = (uint32_t)(kk >> 2), kb2 = (uint32_t)(kk & 3) * 32u;
                 const uint64_t ax = smem_desc(smem_u32(sm + SA_X + ko * 16384 + kb2), 16, 1024, kSwizzle128B);
-                const uint64_t bk = smem_desc(smem_u32(sm + SA_KH + ko * 20480 + kb2), 16, 1024, kSwizzle128B);
+                const uint64_t bk = smem_desc(smem_u32(sm + SA_KH + ko * KH_HALF + kb2), 16, 1024, kSwizzle128B);
                 mma_bf16_ss(tmem + TMA_G, ax, bk, idg, kk > 0);
-            }
-            // the diagonal q blocks of the Gram in more than bf16 precision:
-            // D_C = X Klo^T (N = 64: every q row against every diagonal key
-            // row; row r of sub-block p uses columns 16p .. 16p + 15), added to
-            // hi(xq) hi(kg) in the epilogue.  A' of a short sequence lives in
-            // these blocks, where the bf16 rounding of the keys alone would
-            // cost o up to 2^-9 of each product term.
-            const uint32_t idc = instr_desc(kFmtBF16, 128, 64, 0, 0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t ko = (uint32_t)(kk >> 2), kb2 = (uint32_t)(kk & 3) * 32u;
-                const uint64_t ax = smem_desc(smem_u32(sm + SA_X + ko * 16384 + kb2), 16, 1024, kSwizzle128B);
-                const uint64_t bl = smem_desc(smem_u32(sm + SA_KLO + ko * 8192 + kb2), 16, 1024, kSwizzle128B);
-                mma_bf16_ss(tmem + TMA_C, ax, bl, idc, kk > 0);
             }
             mma_commit(bar_mma);
         }
@@ -548,7 +567,8 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         }
         // while the Gram runs: decode the next job, load its beta, pull its g into L2
         if (has_next) {
-            Jn = decode(job_next);
+            Jn = decode(job_next, s_tab[(it + 1) & 1]);
+            if (t == 0) prefetch_entry(job_next + (int)gridDim.x, it & 1);
             if (t < C) bnext = load_beta(Jn);
             if (t == 0) {
 #pragma unroll
@@ -811,7 +831,10 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     job = job_next;
     }   // job loop
 
-    if (t == 0) bulk_wait();                 // record copies complete before the CTA exits
+    if (t == 0) {
+        bulk_wait();                         // record copies complete before the CTA exits
+        cp_async_wait_all();
+    }
     if (failed) {
         if (t == 0) atomicOr(&g_kda_device_error, 1u);
         // let copies and MMAs in flight finish (bounded) before freeing TMEM
@@ -1371,10 +1394,16 @@ unsigned long long g_attr_ctx[kMaxDevices] = {};
 
 }  // namespace
 
+// Workspace: chunk_off [N + 1] int32, the chunk table [max_chunks] int2
+// (each padded to 1 KB), then the records.
+static size_t plan_bytes(int N, int64_t max_chunks) {
+    return (((size_t)(N + 1) * sizeof(int32_t) + 1023) & ~(size_t)1023) +
+           (((size_t)max_chunks * sizeof(int2) + 1023) & ~(size_t)1023);
+}
+
 size_t prefill_split_workspace_bytes(int N, int64_t T, int H) {
     const int64_t max_chunks = (T + C - 1) / C + N;
-    const size_t off_bytes = ((size_t)(N + 1) * sizeof(int32_t) + 1023) & ~(size_t)1023;
-    return off_bytes + (size_t)max_chunks * (size_t)H * REC_BYTES;
+    return plan_bytes(N, max_chunks) + (size_t)max_chunks * (size_t)H * REC_BYTES;
 }
 
 namespace {
@@ -1429,13 +1458,14 @@ cudaError_t run_split(const void *q, const void *k, const void *v, const float *
         }
     }
     int32_t *chunk_off = static_cast<int32_t *>(ws);
-    uint8_t *recs = static_cast<uint8_t *>(ws) +
-                    (((size_t)(N + 1) * sizeof(int32_t) + 1023) & ~(size_t)1023);
+    int2 *tab = reinterpret_cast<int2 *>(static_cast<uint8_t *>(ws) +
+                                         (((size_t)(N + 1) * sizeof(int32_t) + 1023) & ~(size_t)1023));
+    uint8_t *recs = static_cast<uint8_t *>(ws) + plan_bytes(N, max_chunks);
     if (ev) cudaEventRecord(ev[0], stream);
-    chunk_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, (int)T, chunk_off);
+    chunk_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, (int)T, chunk_off, tab);
     if (ev) cudaEventRecord(ev[1], stream);
     intra_chunk_kernel<<<intra_grid(max_chunks * H), NTA, SMEM_A_ALLOC, stream>>>(
-        mq, mk, mg, beta, cu_seqlens, chunk_off, N, H, recs, (int)T, (int)max_chunks);
+        mq, mk, mg, beta, tab, chunk_off, N, H, recs, (int)T, (int)max_chunks);
     if (ev) cudaEventRecord(ev[2], stream);
     if (gate)
         state_pass_kernel<true><<<(unsigned)((int64_t)N * H), NTB, SMEM_B_ALLOC, stream>>>(

@@ -263,6 +263,13 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// 8 bytes global -> shared without a register round trip (LDGSTS)
+__device__ __forceinline__ void cp_async8(void *smem_dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(smem_dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // fp32 -> tf32 with round to nearest, ties away from zero, as a 32-bit
 // pattern: add half a unit of the 10-bit mantissa to the magnitude bits and
 // clear the 13 low bits (finite inputs; a carry into the exponent is the
