@@ -37,14 +37,27 @@ __device__ __forceinline__ float sigmoid(float y) { return __fdividef(1.f, 1.f +
 // pairs use packed fp32x2 arithmetic; the SiLU takes one exponential and one
 // hardware reciprocal per element.  The L2 norm of a (token, head) row is a
 // reduction over the half-warp; both half-warps of a warp always take part in
-// it (they may hold different projections, or run past the end).  Runs of
-// 128 tokens with 8 raw rows in flight per lane measured fastest at 4K (32 /
-// 64 / 128 tokens: 173 / 167 / 162 us with 8 in flight; 4 in flight: 175 us
-// at 32; 16 spills).
+// it (they may hold different projections, or run past the end).  The raw
+// rows stream through a ring of kRing rows per lane in shared memory, filled
+// by asynchronous 16-byte copies kRing rows ahead of the walk, so that loads
+// stay in flight while the lane computes.
 // ============================================================================
 constexpr int kRun = 128;
-constexpr int kBatch = 8;
+constexpr int kRing = 8;
 constexpr int kPrologueThreads = 256;
+
+// 16 bytes global -> shared (LDGSTS); with valid = false the destination is
+// zero-filled and nothing is read
+__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(valid ? 16u : 0u)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __device__ __forceinline__ int seq_of(const int32_t *cu, int N, int t) {
     // largest n with cu[n] <= t (t < cu[N]: a non-empty sequence holding t)
@@ -155,18 +168,29 @@ conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *
     const size_t base0 = ((size_t)(t0 < T ? t0 : 0) * H + h) * 128 + c0;   // not dereferenced when t0 = T
     const __nv_bfloat16 *xp = x + base0;
     __nv_bfloat16 *yp = y_out + base0;
+    // the ring: slot r of this lane at s_ring[half-warp][r][lane]
+    __shared__ uint4 s_ring[kPrologueThreads / 16][kRing][16];
+    uint4 *ring = &s_ring[threadIdx.x >> 4][0][lane16];
+#pragma unroll
+    for (int r = 0; r < kRing; ++r) {
+        const bool ok = t0 + r < t_end;
+        cp_async16_zfill(ring + 16 * r, ok ? xp + (size_t)r * rstride : xp, ok);
+        cp_async_commit_group();
+    }
 #pragma unroll 1
-    for (int i = 0; i < kRun; i += kBatch) {
-        uint4 xr[kBatch];
+    for (int i = 0; i < kRun; i += kRing) {
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            xr[u] = make_uint4(0, 0, 0, 0);
-            if (t0 + i + u < t_end) xr[u] = *reinterpret_cast<const uint4 *>(xp + (size_t)(i + u) * rstride);
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
+        for (int u = 0; u < kRing; ++u) {
             const int t = t0 + i + u;
             const bool valid = t < t_end;
+            cp_async_wait_group<kRing - 1>();  // this row has landed (groups complete in order)
+            const uint4 xu = ring[16 * u];
+            const float2 xn[4] = {bf2_to_f2(xu.x), bf2_to_f2(xu.y), bf2_to_f2(xu.z), bf2_to_f2(xu.w)};
+            {   // the slot is read (xn depends on it): the row kRing ahead into it
+                const bool ok = t + kRing < t_end;
+                cp_async16_zfill(ring + 16 * u, ok ? xp + (size_t)(i + u + kRing) * rstride : xp, ok);
+                cp_async_commit_group();
+            }
             if (valid && t >= end && n < N - 1) {   // the run enters the next non-empty sequence
                 do {
                     ++n;
@@ -176,8 +200,6 @@ conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *
                 bad_cu |= start < 0 || end < start || end > T;
                 load_window(t);
             }
-            const float2 xn[4] = {bf2_to_f2(xr[u].x), bf2_to_f2(xr[u].y), bf2_to_f2(xr[u].z),
-                                  bf2_to_f2(xr[u].w)};
             float2 z[4];
             float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -215,6 +237,7 @@ conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *
             }
         }
     }
+    cp_async_wait_group<0>();                  // nothing in flight into the ring at exit
     if (bad_cu) atomicOr(&g_kda_layer_error, kErrWait);
 }
 
