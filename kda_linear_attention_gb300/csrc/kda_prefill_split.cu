@@ -432,10 +432,18 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             const float4 gb = *reinterpret_cast<const float4 *>(rowp + (((c4 + 1) ^ (r & 7)) << 4));
             const float4 ba = *reinterpret_cast<const float4 *>(s_tot + u * 128 + 8 * cc);
             const float4 bb = *reinterpret_cast<const float4 *>(s_tot + u * 128 + 8 * cc + 4);
-            const float gl[8] = {ga.x + ba.x, ga.y + ba.y, ga.z + ba.z, ga.w + ba.w,
-                                 gb.x + bb.x, gb.y + bb.y, gb.z + bb.z, gb.w + bb.w};
+            // e^{b - sigma_u} = 2^{(b - sigma_u) log2 e}: the sums and their
+            // scaling in packed pairs, the powers on the special-function unit
+            const float2 l2e = make_float2(1.4426950408889634f, 1.4426950408889634f);
+            const float2 gl[4] = {__fmul2_rn(__fadd2_rn(make_float2(ga.x, ga.y), make_float2(ba.x, ba.y)), l2e),
+                                  __fmul2_rn(__fadd2_rn(make_float2(ga.z, ga.w), make_float2(ba.z, ba.w)), l2e),
+                                  __fmul2_rn(__fadd2_rn(make_float2(gb.x, gb.y), make_float2(bb.x, bb.y)), l2e),
+                                  __fmul2_rn(__fadd2_rn(make_float2(gb.z, gb.w), make_float2(bb.z, bb.w)), l2e)};
 #pragma unroll
-            for (int c = 0; c < 8; ++c) F[u][c] = valid ? __expf(gl[c]) : 0.f;
+            for (int c = 0; c < 4; ++c) {
+                F[u][2 * c] = valid ? ex2_approx(gl[c].x) : 0.f;
+                F[u][2 * c + 1] = valid ? ex2_approx(gl[c].y) : 0.f;
+            }
         }
         if (t == 0) bulk_wait_read();        // the previous job's -W copy has left the K0 tile
         __syncthreads();                   // the g tile is read: Khat may be written
@@ -907,8 +915,14 @@ __device__ __forceinline__ void ld_vec16(const float *p, float (&x)[16]) {
 // barrier among the 512 epilogue threads only
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
-// 1 / (1 + e^-x) with the fast exponential and division (a few ulp)
-__device__ __forceinline__ float gate_sigmoid(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+// w / (1 + e^-x) for a channel pair: e^-x = 2^(-x log2 e) on the
+// special-function unit (its scaling one packed multiply), the hardware
+// reciprocal (a few ulp; e^-x overflowing to inf gives 0)
+__device__ __forceinline__ float2 gate_sigmoid_w(float2 x, float2 w) {
+    const float2 a = __fmul2_rn(x, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+    const float2 d = __fadd2_rn(make_float2(1.f, 1.f), make_float2(ex2_approx(a.x), ex2_approx(a.y)));
+    return __fmul2_rn(w, make_float2(rcp_fast(d.x), rcp_fast(d.y)));
+}
 
 // GATED: the layer's output epilogue ("Colibri Kimi K3 Metal backend",
 // section 8.4) on every row of o before it is stored: o / sqrt(mean_j o_j^2
@@ -1082,8 +1096,9 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
                 const float2 ga = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.x));
                 const float2 gb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gu.y));
                 const float4 wv = *reinterpret_cast<const float4 *>(s_normw + 32 * m + 4 * p8);
-                gw[m] = make_float4(wv.x * gate_sigmoid(ga.x), wv.y * gate_sigmoid(ga.y),
-                                    wv.z * gate_sigmoid(gb.x), wv.w * gate_sigmoid(gb.y));
+                const float2 sa = gate_sigmoid_w(ga, make_float2(wv.x, wv.y));
+                const float2 sb = gate_sigmoid_w(gb, make_float2(wv.z, wv.w));
+                gw[m] = make_float4(sa.x, sa.y, sb.x, sb.y);
             }
             epi_sync();                          // every row of o is staged
             float4 x[4];
@@ -1097,13 +1112,12 @@ state_pass_kernel(const __grid_constant__ CUtensorMap map_v, const __grid_consta
             ss += __shfl_xor_sync(0xffffffffu, ss, 2);
             ss += __shfl_xor_sync(0xffffffffu, ss, 4);
             const float rs = rsqrtf(ss * (1.f / 128.f) + norm_eps);
+            const float2 rs2 = make_float2(rs, rs);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                float4 y;
-                y.x = x[m].x * rs * gw[m].x;
-                y.y = x[m].y * rs * gw[m].y;
-                y.z = x[m].z * rs * gw[m].z;
-                y.w = x[m].w * rs * gw[m].w;
+                const float2 ya = __fmul2_rn(__fmul2_rn(make_float2(x[m].x, x[m].y), rs2), make_float2(gw[m].x, gw[m].y));
+                const float2 yb = __fmul2_rn(__fmul2_rn(make_float2(x[m].z, x[m].w), rs2), make_float2(gw[m].z, gw[m].w));
+                const float4 y = make_float4(ya.x, ya.y, yb.x, yb.y);
                 if (Lp == C)
                     *reinterpret_cast<float4 *>(sm + sbp + 8192 * m + rr * 128 + 16 * p8) = y;
                 else if (rr < Lp)
