@@ -402,8 +402,9 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             for (int u = 0; u < 4; ++u) sg[u] = (u <= lu) ? base[u] + s_tot[u * 128 + t] : bL;
 #pragma unroll
             for (int u = 0; u < 4; ++u) s_tot[u * 128 + t] = base[u] - sg[u];
-            const float d0 = __expf(sg[0]), d1 = __expf(sg[1] - sg[0]), d2 = __expf(sg[2] - sg[1]),
-                        d3 = __expf(sg[3] - sg[2]);
+            constexpr float kL2e = 1.4426950408889634f;    // e^x = 2^{x log2 e}
+            const float d0 = ex2_approx(sg[0] * kL2e), d1 = ex2_approx((sg[1] - sg[0]) * kL2e),
+                        d2 = ex2_approx((sg[2] - sg[1]) * kL2e), d3 = ex2_approx((sg[3] - sg[2]) * kL2e);
             s_dd[t] = d0;
             s_dd[128 + t] = d1;
             s_dd[256 + t] = d2;
@@ -507,7 +508,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const float2 kh2 = __bfloat1622float2(__floats2bfloat162_rn(kg[m].x, kg[m].y));
-                    kl[m] = make_float2(kg[m].x - kh2.x, kg[m].y - kh2.y);
+                    kl[m] = __ffma2_rn(kh2, make_float2(-1.f, -1.f), kg[m]);   // kg - kh2, exact product
                 }
                 *reinterpret_cast<uint4 *>(sm + SA_KH + sw_chunk(160 + r, cc, KH_HALF)) = pack_bf8x2(kl);
             }
