@@ -307,7 +307,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     int job = blockIdx.x;
     if (job >= total) return;
     Job J = decode(job, tab[KDA_DBG_INDEX(g_kda_device_error, gc_of(job), 0, max_chunks)]);
-    if (t == 0) prefetch_entry(job + (int)gridDim.x, 1);
+    if (t == 32) prefetch_entry(job + (int)gridDim.x, 1);   // thread 32 makes every table copy
     if (warp == 0) tmem_alloc(s_tmem, 256);
     if (t == 0) {
         mbar_init(bar_qk, 1);
@@ -338,7 +338,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     const int job_next = job + gridDim.x;
     const bool has_next = job_next < total;
     Job Jn = J;
-    if (t == 0) cp_async_wait_all();   // the next job's table entry (published by the barrier)
+    if (t == 32) cp_async_wait_all();  // the next job's table entry (published by the barrier)
     if (!wait_all(bar_qk, it & 1) || !wait_all(bar_g, it & 1)) { failed = true; fail_at = 1; fail_it = it; fail_next = has_next; break; }
 
     {
@@ -563,26 +563,29 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             }
             mma_commit(bar_mma);
         }
-        {
+        // while the Gram runs (thread 0 only issues it): the record's vectors
+        // from warps 4..7, the next job's decode, its beta and an L2 pull of
+        // its g from warps 0..3 and 1
+        if (t >= 128) {
+            const int i = t - 128;
             float *rv = reinterpret_cast<float *>(rec + R_VEC);
-            if (t < 64) {
-                float dq = s_tot[t];
+            if (i < 64) {
+                float dq = s_tot[i];
 #pragma unroll
-                for (int w = 1; w < 8; ++w) dq += s_tot[w * 64 + t];
-                rv[t] = s_beta[t];
-                rv[64 + t] = dq;
+                for (int w = 1; w < 8; ++w) dq += s_tot[w * 64 + i];
+                rv[i] = s_beta[i];
+                rv[64 + i] = dq;
             }
-            if (t < 128) rv[128 + t] = s_gam[t];
+            rv[128 + i] = s_gam[i];
         }
-        // while the Gram runs: decode the next job, load its beta, pull its g into L2
         if (has_next) {
             Jn = decode(job_next, s_tab[(it + 1) & 1]);
-            if (t == 0) prefetch_entry(job_next + (int)gridDim.x, it & 1);
-            if (t < C) bnext = load_beta(Jn);
-            if (t == 0) {
+            if (t == 32) {
+                prefetch_entry(job_next + (int)gridDim.x, it & 1);
 #pragma unroll
                 for (int bx = 0; bx < 4; ++bx) tma_prefetch_l2_3d(&map_g, 32 * bx, Jn.h, Jn.tok);
             }
+            if (t < C) bnext = load_beta(Jn);
         }
         if (!wait_all(bar_mma, 0)) { failed = true; fail_at = 2; fail_it = it; fail_next = has_next; break; }
     }
@@ -840,10 +843,8 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     job = job_next;
     }   // job loop
 
-    if (t == 0) {
-        bulk_wait();                         // record copies complete before the CTA exits
-        cp_async_wait_all();
-    }
+    if (t == 0) bulk_wait();                 // record copies complete before the CTA exits
+    if (t == 32) cp_async_wait_all();
     if (failed) {
         if (t == 0) atomicOr(&g_kda_device_error, 1u);
         // let copies and MMAs in flight finish (bounded) before freeing TMEM
