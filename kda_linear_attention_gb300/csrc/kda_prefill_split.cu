@@ -619,22 +619,24 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 const bool have = qt <= p && r < Lc;
                 const bool diag = qside && qt == p;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float x4[4];
+                for (int jp = 0; jp < 2; ++jp) {   // 8 columns: one 16-byte chunk of the packing
+                    float x8[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s = 16 * qt + 4 * j + e;
-                        float val = use_hi ? vb[4 * j + e] : va[4 * j + e];
-                        if (diag) val += use_hi ? cb[4 * j + e] : ca[4 * j + e];
-                        x4[e] = (have && s < r) ? val : 0.f;
+                    for (int e = 0; e < 8; ++e) {
+                        const int s = 16 * qt + 8 * jp + e;
+                        float val = use_hi ? vb[8 * jp + e] : va[8 * jp + e];
+                        if (diag) val += use_hi ? cb[8 * jp + e] : ca[8 * jp + e];
+                        x8[e] = (have && s < r) ? val : 0.f;
                     }
                     if (qside) {
                         if ((r >> 3) >= 2 * qt)      // a row group that block qt of the packing holds
-                            *reinterpret_cast<uint2 *>(rec + R_A + tri_off(r, 16 * qt + 4 * j)) =
-                                make_uint2(pack_h2(x4[0], x4[1]), pack_h2(x4[2], x4[3]));
+                            *reinterpret_cast<uint4 *>(rec + R_A + tri_off(r, 16 * qt + 8 * jp)) =
+                                make_uint4(pack_h2(x8[0], x8[1]), pack_h2(x8[2], x8[3]),
+                                           pack_h2(x8[4], x8[5]), pack_h2(x8[6], x8[7]));
                     } else {
-                        *reinterpret_cast<float4 *>(Mm + r * MLD + 16 * qt + 4 * j) =
-                            make_float4(br * x4[0], br * x4[1], br * x4[2], br * x4[3]);
+                        float *mr = Mm + r * MLD + 16 * qt + 8 * jp;
+                        *reinterpret_cast<float4 *>(mr) = make_float4(br * x8[0], br * x8[1], br * x8[2], br * x8[3]);
+                        *reinterpret_cast<float4 *>(mr + 4) = make_float4(br * x8[4], br * x8[5], br * x8[6], br * x8[7]);
                     }
                 }
             }
@@ -663,8 +665,10 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             for (int s2 = 0; s2 < 15; ++s2) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
+                    // rows r <= s2 have M[r][s2] = 0 (M is strictly lower), so
+                    // every lane applies the update unconditionally
                     const float bv = __shfl_sync(0xffffffffu, x[e], s2, 16);
-                    if (r > s2) x[e] = fmaf(-mr[s2], bv, x[e]);
+                    x[e] = fmaf(-mr[s2], bv, x[e]);
                 }
             }
             __syncthreads();
@@ -769,11 +773,14 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             const float4 a = *reinterpret_cast<const float4 *>(Mm + r * MLD + s0);
             const float4 b4 = *reinterpret_cast<const float4 *>(Mm + r * MLD + s0 + 4);
             const float tv[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
+            const float4 ba = *reinterpret_cast<const float4 *>(s_beta + s0);
+            const float4 bb = *reinterpret_cast<const float4 *>(s_beta + s0 + 4);
+            const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
             float w8[8], d8[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int s3 = s0 + u;
-                const float bs = s_beta[s3];
+                const float bs = bv[u];
                 w8[u] = (s3 < r) ? tv[u] * bs : 0.f;
                 d8[u] = (s3 == r) ? bs : w8[u];
             }
