@@ -379,6 +379,18 @@ int kda_decode_layer_step(const void *xq, const void *xk, const void *xv, const 
                           void *stream);
 
 /*
+ * Gives back the memory that the library's workspace pool on the current
+ * device keeps between kda_prefill_chunked / _events / _gated /
+ * kda_layer_prefill calls (one 60,416-byte record per (chunk, head) of the
+ * largest call so far: about 6 GB after a 66,048-token, 96-head batch).
+ * Memory still held by a call in flight is kept: synchronise the streams
+ * those calls ran on first.  The next call grows the pool again (a driver
+ * allocation).  Host-only bookkeeping plus cudaMemPoolTrimTo; returns KDA_OK
+ * (also when the device has no pool yet) or KDA_ERR_CUDA.
+ */
+int kda_workspace_release(void);
+
+/*
  * Device-side error word of the library.  The outputs of a call that raised
  * a bit are invalid.
  *   Bit 0: the tensor-core prefill kernels never wait without bound: if one

@@ -108,6 +108,8 @@ def lib() -> ctypes.CDLL:
         L.kda_decode_layer_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32,
                                             vp, i32, i32, i32, i32, f32, f32, f32, vp]
         L.kda_decode_layer_step.restype = i32
+        L.kda_workspace_release.argtypes = []
+        L.kda_workspace_release.restype = i32
         L.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         L.kda_device_error.restype = i32
         _lib = L
@@ -489,3 +491,12 @@ def device_error(reset: bool = True) -> int:
     if rc != 0:
         raise KDAError(rc, "kda_device_error")
     return int(code.value)
+
+
+def workspace_release() -> None:
+    """Give the library's workspace pool memory on the current device back to
+    the driver (``kda_workspace_release``); synchronise the streams that ran
+    prefills first."""
+    rc = lib().kda_workspace_release()
+    if rc != 0:
+        raise KDAError(rc, "kda_workspace_release")

@@ -279,6 +279,8 @@ int kda_decode_layer_step(const void *xq, const void *xk, const void *xv, const 
                                                 static_cast<cudaStream_t>(stream)));
 }
 
+int kda_workspace_release(void) { return cuda_status(kda::release_workspace_pool()); }
+
 int kda_device_error(unsigned int *code, int reset) {
     if (!code) return KDA_ERR_NULL;
     unsigned int a = 0, b = 0, c = 0, d = 0;

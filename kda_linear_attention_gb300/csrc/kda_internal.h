@@ -99,6 +99,8 @@ cudaError_t launch_prefill_split_ws(const void *q, const void *k, const void *v,
 // Read (and optionally clear) the device-side error word that the
 // tensor-core kernels set when a bounded wait gives up.
 cudaError_t read_device_error(unsigned int *code, bool reset);
+// Gives the current device's workspace pool memory back to the driver.
+cudaError_t release_workspace_pool();
 
 // The tensor-core prefill with the layer's gated RMSNorm fused into the state
 // pass's output: out = RMSNorm(o) * norm_w * sigmoid(gate) instead of o

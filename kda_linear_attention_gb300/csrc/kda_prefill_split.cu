@@ -1538,6 +1538,18 @@ cudaError_t launch_prefill_split_gated(const void *q, const void *k, const void 
     return e != cudaSuccess ? e : ef;
 }
 
+// Trims the current device's workspace pool to nothing (memory that no
+// allocation still holds goes back to the driver).
+cudaError_t release_workspace_pool() {
+    cudaError_t e;
+    const int dev = current_device_checked(&e);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_pool_mu);
+    const unsigned long long ctx = current_context_id();
+    if (!g_pool[dev].pool || (ctx != 0 && ctx != g_pool[dev].ctx)) return cudaSuccess;   // none in this context
+    return cudaMemPoolTrimTo(g_pool[dev].pool, 0);
+}
+
 // The layer prefill: the conv prologue writes q, k, v (bf16) into the front
 // of one pool allocation, the gated prefill's records follow them.
 cudaError_t launch_prefill_layer(const void *xq, const void *xk, const void *xv, const float *conv_w,

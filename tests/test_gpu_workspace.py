@@ -79,3 +79,25 @@ def test_workspace_too_small_is_refused_before_launch():
     with pytest.raises(kda.KDAError) as e:
         kda.prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, workspace=ws)
     assert e.value.status == 6
+
+
+def test_workspace_release_returns_the_pool_memory():
+    """kda_workspace_release gives the pool's records back to the driver (the
+    device's free memory grows by at least the 4K prefill's workspace), and
+    the next prefill grows the pool again and gives the same bits."""
+    import torch
+    import kda_linear_attention_gb300 as kda
+    inp = ki.workload_prefill("prefill_4k")
+    d = {n: dev_tensor(getattr(inp, n)) for n in ("q", "k", "v", "g", "beta")}
+    cu = dev_tensor(inp.cu_seqlens)
+    o1, S1 = kda.prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], cu)
+    torch.cuda.synchronize()
+    need = kda.prefill_workspace_bytes(inp.N, inp.T, inp.H)
+    free0 = torch.cuda.mem_get_info()[0]
+    kda.workspace_release()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert free1 - free0 >= need - (64 << 20), (free0, free1, need)
+    o2, S2 = kda.prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], cu)
+    torch.cuda.synchronize()
+    assert kda.device_error() == 0
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)
