@@ -99,7 +99,9 @@ __device__ __forceinline__ void ld_f2x4(const float *p, float2 (&x)[4]) {
 
 // ---- the per-(chunk, head) record ------------------------------------------
 // Each piece is stored in the shared-memory operand layout in which the state
-// pass feeds it to the tensor cores, so that one bulk copy places it.
+// pass feeds it to the tensor cores, so that one bulk copy places it.  The
+// intra-chunk kernel writes the pieces it stores from registers with
+// streaming stores (st.global.cs): the state pass reads each record once.
 constexpr uint32_t R_WQ = 0;        // [-W ; Q0] fp16, 128 rows x 128, K-major sw (two 16 KB halves)
 constexpr uint32_t R_T = 32768;     // T' bf16, strictly lower 64 x 64 packed by K-step (tri_off), 5 KB
 constexpr uint32_t R_A = 37888;     // A' fp16, the same packing, 5 KB
@@ -520,7 +522,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     q0[m] = __fmul2_rn(xq[m], ep[m]);
                     k0[m] = __fmul2_rn(xk[m], ep[m]);
                 }
-                *reinterpret_cast<uint4 *>(rec + R_WQ + sw_chunk(64 + r, cc, 16384)) = pack_h8x2(q0);
+                __stcs(reinterpret_cast<uint4 *>(rec + R_WQ + sw_chunk(64 + r, cc, 16384)), pack_h8x2(q0));
                 *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, cc, 8192)) = pack_h8x2(k0);
             }
             // Kbar = e^{b_L - b} k, fp16, row s, in the 128B-swizzled [s][i]
@@ -529,7 +531,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 float2 kb[4];
 #pragma unroll
                 for (int m = 0; m < 4; ++m) kb[m] = __fmul2_rn(kg[m], el[m]);
-                *reinterpret_cast<uint4 *>(rec + R_KB + sw_chunk(r, cc, 8192)) = pack_h8x2(kb);
+                __stcs(reinterpret_cast<uint4 *>(rec + R_KB + sw_chunk(r, cc, 8192)), pack_h8x2(kb));
             }
         }
         // q_r . k_r: each warp's partial over its 16 channels into the
@@ -630,9 +632,9 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     }
                     if (qside) {
                         if ((r >> 3) >= 2 * qt)      // a row group that block qt of the packing holds
-                            *reinterpret_cast<uint4 *>(rec + R_A + tri_off(r, 16 * qt + 8 * jp)) =
-                                make_uint4(pack_h2(x8[0], x8[1]), pack_h2(x8[2], x8[3]),
-                                           pack_h2(x8[4], x8[5]), pack_h2(x8[6], x8[7]));
+                            __stcs(reinterpret_cast<uint4 *>(rec + R_A + tri_off(r, 16 * qt + 8 * jp)),
+                                   make_uint4(pack_h2(x8[0], x8[1]), pack_h2(x8[2], x8[3]),
+                                              pack_h2(x8[4], x8[5]), pack_h2(x8[6], x8[7])));
                     } else {
                         float *mr = Mm + r * MLD + 16 * qt + 8 * jp;
                         *reinterpret_cast<float4 *>(mr) = make_float4(br * x8[0], br * x8[1], br * x8[2], br * x8[3]);
@@ -785,7 +787,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 d8[u] = (s3 == r) ? bs : w8[u];
             }
             if ((r >> 3) >= 2 * (s0 >> 4))     // a row group that the packing holds
-                *reinterpret_cast<uint4 *>(rec + R_T + tri_off(r, s0)) = pack_bf8(w8);
+                __stcs(reinterpret_cast<uint4 *>(rec + R_T + tri_off(r, s0)), pack_bf8(w8));
             // rows 64..127 of the M = 128 operand repeat rows 0..63, so that every
             // TMEM lane quarter of the W accumulator holds real rows
             const uint4 pd = pack_h8(d8);
