@@ -343,6 +343,8 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     if (t == 32) cp_async_wait_all();  // the next job's table entry (published by the barrier)
     if (!wait_all(bar_qk, it & 1) || !wait_all(bar_g, it & 1)) { failed = true; fail_at = 1; fail_it = it; fail_next = has_next; break; }
 
+    // the previous job's -W copy has left the K0 tile (published by the scan's barriers)
+    if (t == 0) bulk_wait_read();
     {
         // ===== decay prefix sums: column scan in place in the g tile =========
         // thread = (channels 4qd..4qd+3, sub-block u); the tile is four 128B-
@@ -447,8 +449,32 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 F[u][2 * c] = valid ? ex2_approx(gl[c].x) : 0.f;
                 F[u][2 * c + 1] = valid ? ex2_approx(gl[c].y) : 0.f;
             }
+            // Q0 = q e^{b} -> record rows 64..127 of [-W ; Q0];  K0 = k e^{b} -> smem,
+            // as (x e^{b - sigma}) e^{sigma}, while X still holds the raw rows
+            // (here rather than in the operand build, whose live ranges are long)
+            {
+                float2 qv[4], kv[4], ep[4], q0[4], k0[4];
+                unpack_bf8x2(*reinterpret_cast<const uint4 *>(sm + SA_X + sw_chunk(r, cc, 16384)), qv);
+                unpack_bf8x2(*reinterpret_cast<const uint4 *>(sm + SA_X + sw_chunk(64 + r, cc, 16384)), kv);
+                // e^{sigma_u} = e^{sigma_0} e^{sigma_1 - sigma_0} ...
+                ld_f2x4(s_dd + 8 * cc, ep);
+#pragma unroll
+                for (int w = 1; w <= u; ++w) {
+                    float2 dw[4];
+                    ld_f2x4(s_dd + w * 128 + 8 * cc, dw);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) ep[m] = __fmul2_rn(ep[m], dw[m]);
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float2 F2 = make_float2(F[u][2 * m], F[u][2 * m + 1]);
+                    q0[m] = __fmul2_rn(__fmul2_rn(qv[m], F2), ep[m]);
+                    k0[m] = __fmul2_rn(__fmul2_rn(kv[m], F2), ep[m]);
+                }
+                __stcs(reinterpret_cast<uint4 *>(rec + R_WQ + sw_chunk(64 + r, cc, 16384)), pack_h8x2(q0));
+                *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, cc, 8192)) = pack_h8x2(k0);
+            }
         }
-        if (t == 0) bulk_wait_read();        // the previous job's -W copy has left the K0 tile
         __syncthreads();                   // the g tile is read: Khat may be written
 
         float dqp[4];
@@ -458,19 +484,9 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             uint8_t *pq = sm + SA_X + sw_chunk(r, cc, 16384);
             uint8_t *pk = sm + SA_X + sw_chunk(64 + r, cc, 16384);
             // channel pairs in packed fp32x2 arithmetic
-            float2 qv[4], kv[4], F2[4], G2[4], xq[4], xk[4], ep[4], el[4], kg[4];
+            float2 qv[4], kv[4], F2[4], G2[4], xq[4], xk[4], el[4], kg[4];
             unpack_bf8x2(*reinterpret_cast<const uint4 *>(pq), qv);
             unpack_bf8x2(*reinterpret_cast<const uint4 *>(pk), kv);
-            // e^{sigma_u} = e^{sigma_0} e^{sigma_1 - sigma_0} ... (the products
-            // that also give e^{b_L})
-            ld_f2x4(s_dd + 8 * cc, ep);
-#pragma unroll
-            for (int w = 1; w <= u; ++w) {
-                float2 dw[4];
-                ld_f2x4(s_dd + w * 128 + 8 * cc, dw);
-#pragma unroll
-                for (int m = 0; m < 4; ++m) ep[m] = __fmul2_rn(ep[m], dw[m]);
-            }
             ld_f2x4(s_el + u * 128 + 8 * cc, el);
             float2 dot2 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -513,17 +529,6 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     kl[m] = __ffma2_rn(kh2, make_float2(-1.f, -1.f), kg[m]);   // kg - kh2, exact product
                 }
                 *reinterpret_cast<uint4 *>(sm + SA_KH + sw_chunk(160 + r, cc, KH_HALF)) = pack_bf8x2(kl);
-            }
-            // Q0 = q e^{b} -> record rows 64..127 of [-W ; Q0];  K0 = k e^{b} -> smem
-            {
-                float2 q0[4], k0[4];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    q0[m] = __fmul2_rn(xq[m], ep[m]);
-                    k0[m] = __fmul2_rn(xk[m], ep[m]);
-                }
-                __stcs(reinterpret_cast<uint4 *>(rec + R_WQ + sw_chunk(64 + r, cc, 16384)), pack_h8x2(q0));
-                *reinterpret_cast<uint4 *>(sm + SA_K0 + sw_chunk(r, cc, 8192)) = pack_h8x2(k0);
             }
             // Kbar = e^{b_L - b} k, fp16, row s, in the 128B-swizzled [s][i]
             // layout of K0: round 2 reads it as an MN-major operand
