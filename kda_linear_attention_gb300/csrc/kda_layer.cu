@@ -95,6 +95,10 @@ conv_prologue_kernel(const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *
     const int lane16 = threadIdx.x & 15;
     const long long hw = (long long)blockIdx.x * (kPrologueThreads / 16) + (threadIdx.x >> 4);
     const bool active = hw < nruns;
+    // a warp whose two half-warps both run past the last run has nothing to
+    // do (with no tokens at all, every warp): it leaves before touching the
+    // inputs, which may then be NULL
+    if ((hw & ~1LL) >= nruns) return;
     const long long hwc = active ? hw : 0;
     const int h = (int)(hwc % H);
     const int p = (int)((hwc / H) % 3);

@@ -392,3 +392,26 @@ def test_conv_prologue_negative_cu_start_is_contained():
     for name, x, r in (("q", q, rq), ("k", k, rk), ("v", v, rv)):
         _assert_bf16_rounding_of(_bf16_np(x), r, "prologue " + name)
     assert np.array_equal(_bf16_np(co), rco)
+
+
+def test_layer_prefill_without_tokens_passes_windows_and_states_through():
+    """kda_layer_prefill on sequences that are all empty: every window and
+    every state comes out as it went in (zeros where none came in)."""
+    import torch
+    kda = _kda()
+    H = 2
+    L = ki.gen_layer(160, [0, 0, 0], H=H, with_s0=True)
+    d = dev_tensor
+    cin = d(L.conv0).view(torch.bfloat16)
+    out, S, co = kda.prefill_layer(d(L.xq), d(L.xk), d(L.xv), d(L.conv_w), d(L.g), d(L.beta),
+                                   d(L.gate), d(L.norm_w), d(L.cu_seqlens), conv_in=cin, S0=d(L.S0))
+    torch.cuda.synchronize()
+    _check_no_device_error()
+    assert out.shape[0] == 0
+    assert torch.equal(co, cin)
+    assert np.array_equal(S.cpu().numpy(), L.S0)
+    _, S2, co2 = kda.prefill_layer(d(L.xq), d(L.xk), d(L.xv), d(L.conv_w), d(L.g), d(L.beta),
+                                   d(L.gate), d(L.norm_w), d(L.cu_seqlens))
+    torch.cuda.synchronize()
+    _check_no_device_error()
+    assert not co2.float().abs().max().item() and not S2.abs().max().item()
