@@ -178,8 +178,9 @@ int kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v,
  * Bytes of caller-owned workspace that kda_prefill_chunked_ws needs for these
  * sizes on the tensor-core path (bf16, chunk 64, T > 0): with
  * C = ceil(T / 64) + N chunks (one spare per sequence for a partial tail),
- * 1024 * ceil(4 (N + 1) / 1024) + 1024 * ceil(8 C / 1024) + C * H * 60416
- * (the chunk offsets, the chunk table, one record per (chunk, head)); 0 for
+ * 1024 * ceil(4 (N + 2) / 1024) + 1024 * ceil(8 C / 1024) + C * H * 60416
+ * (the chunk offsets and a job counter, the chunk table, one record per
+ * (chunk, head)); 0 for
  * every other combination (the CUDA-core kernel needs none) and for invalid sizes.
  * Host-only, no CUDA call.
  */

@@ -129,6 +129,8 @@ __device__ __forceinline__ uint32_t tri_off(int r, int s) {
 
 // ============================================================================
 // chunk plan: chunk_off[n] = sum_{m<n} ceil(len_m / 64), chunk_off[N] = total,
+// chunk_off[N + 1] = 0 (the counter from which the intra-chunk kernel's CTAs
+// take jobs),
 // and per global chunk gc its first token and row count, tab[gc] = (tok, Lc),
 // so that the intra-chunk kernel finds a job's chunk with one 8-byte load.
 // cu_seqlens must start at or above 0, never decrease and end at or below T
@@ -171,7 +173,10 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t *__restr
         if (t == 1023) s_carry = carry + s_scan[1023];
         __syncthreads();
     }
-    if (t == 0) chunk_off[N] = s_bad ? 0 : s_carry;
+    if (t == 0) {
+        chunk_off[N] = s_bad ? 0 : s_carry;
+        chunk_off[N + 1] = 0;              // the intra-chunk kernel's job counter
+    }
     if (s_bad) {
         for (int n = t; n < N; n += 1024) chunk_off[n] = 0;
         if (t == 0) atomicOr(&g_kda_device_error, 1u);
@@ -213,7 +218,8 @@ constexpr uint32_t SA_MISC = 106496;
 constexpr uint32_t MA_BETA = 0;           // float[64]
 constexpr uint32_t MA_GAM = 256;          // float[128]  e^{b_L}
 constexpr uint32_t MA_TAB = 768;          // int2[2]: chunk-table entries of the next two jobs
-                                          // (784..1023 free)
+constexpr uint32_t MA_JOB = 784;          // int[2]: the next two jobs' indices
+                                          // (792..1023 free)
 constexpr uint32_t MA_TOT = 1024;         // float[4][128] sub-block totals, then carry - sigma_u,
                                           //   then the warps' q . k partials [8][64]
 constexpr uint32_t MA_SIG = 3072;         // float[4][128] first-half scan totals, then e^{b_L - sigma_u}
@@ -239,7 +245,7 @@ struct Job {
 __global__ void __launch_bounds__(NTA, 2)
 intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_g, const float *__restrict__ beta,
-                   const int2 *__restrict__ tab, const int32_t *__restrict__ chunk_off, int N,
+                   const int2 *__restrict__ tab, int32_t *__restrict__ chunk_off, int N,
                    int H, uint8_t *__restrict__ recs, int T, int max_chunks) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -268,6 +274,12 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     // k & 1 for the CTA's k-th job) two jobs ahead, so that no decode waits
     // on a global load.
     int2 *s_tab = reinterpret_cast<int2 *>(sm + SA_MISC + MA_TAB);
+    int *s_job = reinterpret_cast<int *>(sm + SA_MISC + MA_JOB);
+    // Jobs: each CTA's first two are static (b and b + G); after that thread
+    // 32 takes the job two ahead from a counter, so that CTAs that finish
+    // early take more jobs and the grid ends together.
+    const int G = (int)gridDim.x;
+    auto take_job = [&]() -> int { return 2 * G + atomicAdd(chunk_off + N + 1, 1); };
     auto gc_of = [&](int job) -> int { return (total - 1 - job) / H; };
     auto prefetch_entry = [&](int job, int slot) {
         if (job < total) {
@@ -309,7 +321,10 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     int job = blockIdx.x;
     if (job >= total) return;
     Job J = decode(job, tab[KDA_DBG_INDEX(g_kda_device_error, gc_of(job), 0, max_chunks)]);
-    if (t == 32) prefetch_entry(job + (int)gridDim.x, 1);   // thread 32 makes every table copy
+    if (t == 32) {                         // thread 32 takes every job and makes every table copy
+        s_job[1] = job + G;
+        prefetch_entry(job + G, 1);
+    }
     if (warp == 0) tmem_alloc(s_tmem, 256);
     if (t == 0) {
         mbar_init(bar_qk, 1);
@@ -337,7 +352,7 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     const int h = J.h, Lc = J.Lc;
     uint8_t *rec = recs + ((size_t)J.gc * H + h) * REC_BYTES;
     if (t < C) s_beta[t] = bnext;
-    const int job_next = job + gridDim.x;
+    const int job_next = s_job[(it + 1) & 1];   // published by the barriers since it was taken
     const bool has_next = job_next < total;
     Job Jn = J;
     if (t == 32) cp_async_wait_all();  // the next job's table entry (published by the barrier)
@@ -588,7 +603,9 @@ intra_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         if (has_next) {
             Jn = decode(job_next, s_tab[(it + 1) & 1]);
             if (t == 32) {
-                prefetch_entry(job_next + (int)gridDim.x, it & 1);
+                const int j2 = take_job();
+                s_job[it & 1] = j2;
+                prefetch_entry(j2, it & 1);
 #pragma unroll
                 for (int bx = 0; bx < 4; ++bx) tma_prefetch_l2_3d(&map_g, 32 * bx, Jn.h, Jn.tok);
             }
@@ -1424,10 +1441,10 @@ unsigned long long g_attr_ctx[kMaxDevices] = {};
 
 }  // namespace
 
-// Workspace: chunk_off [N + 1] int32, the chunk table [max_chunks] int2
-// (each padded to 1 KB), then the records.
+// Workspace: chunk_off [N + 1] int32 and the job counter, the chunk table
+// [max_chunks] int2 (each padded to 1 KB), then the records.
 static size_t plan_bytes(int N, int64_t max_chunks) {
-    return (((size_t)(N + 1) * sizeof(int32_t) + 1023) & ~(size_t)1023) +
+    return (((size_t)(N + 2) * sizeof(int32_t) + 1023) & ~(size_t)1023) +
            (((size_t)max_chunks * sizeof(int2) + 1023) & ~(size_t)1023);
 }
 
@@ -1489,7 +1506,7 @@ cudaError_t run_split(const void *q, const void *k, const void *v, const float *
     }
     int32_t *chunk_off = static_cast<int32_t *>(ws);
     int2 *tab = reinterpret_cast<int2 *>(static_cast<uint8_t *>(ws) +
-                                         (((size_t)(N + 1) * sizeof(int32_t) + 1023) & ~(size_t)1023));
+                                         (((size_t)(N + 2) * sizeof(int32_t) + 1023) & ~(size_t)1023));
     uint8_t *recs = static_cast<uint8_t *>(ws) + plan_bytes(N, max_chunks);
     if (ev) cudaEventRecord(ev[0], stream);
     chunk_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, (int)T, chunk_off, tab);

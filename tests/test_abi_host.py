@@ -126,13 +126,13 @@ def _prefill_ws(L, ws=GOOD, ws_bytes=None, **kw):
 
 def test_prefill_workspace_bytes(L):
     """The caller-owned workspace of the tensor-core path: the chunk offsets
-    (4 (N + 1) bytes) and the chunk table (8 bytes per chunk), each rounded up
-    to 1 KB, then one 60,416-byte record per (chunk, head), with one spare
-    chunk per sequence for a partial tail; no workspace for the CUDA-core path
-    or for invalid sizes."""
-    for N, T, H in [(1, 64, 2), (1, 4096, 96), (3, 130, 5), (300, 4096, 4)]:
+    and a job counter (4 (N + 2) bytes) and the chunk table (8 bytes per
+    chunk), each rounded up to 1 KB, then one 60,416-byte record per (chunk,
+    head), with one spare chunk per sequence for a partial tail; no workspace
+    for the CUDA-core path or for invalid sizes."""
+    for N, T, H in [(1, 64, 2), (1, 4096, 96), (3, 130, 5), (300, 4096, 4), (255, 4096, 2)]:
         chunks = -(-T // 64) + N
-        want = 1024 * (-(-4 * (N + 1) // 1024)) + 1024 * (-(-8 * chunks // 1024)) + chunks * H * 60416
+        want = 1024 * (-(-4 * (N + 2) // 1024)) + 1024 * (-(-8 * chunks // 1024)) + chunks * H * 60416
         assert L.kda_prefill_workspace_bytes(N, T, H, 128, 128, 64, 0) == want
     assert L.kda_prefill_workspace_bytes(1, 64, 2, 128, 128, 64, 1) == 0    # fp32 inputs
     assert L.kda_prefill_workspace_bytes(1, 64, 2, 128, 128, 32, 0) == 0    # chunk 32

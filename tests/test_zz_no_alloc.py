@@ -21,7 +21,7 @@ REC = 60416
 
 def _needed(N, T, H):
     chunks = (T + 63) // 64 + N
-    return ((4 * (N + 1) + 1023) // 1024) * 1024 + ((8 * chunks + 1023) // 1024) * 1024 + chunks * H * REC
+    return ((4 * (N + 2) + 1023) // 1024) * 1024 + ((8 * chunks + 1023) // 1024) * 1024 + chunks * H * REC
 
 
 def test_noalloc_rejects_oversize_before_launch():
