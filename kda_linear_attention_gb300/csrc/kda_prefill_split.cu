@@ -197,12 +197,13 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t *__restr
 }
 
 // ============================================================================
-// intra-chunk kernel: persistent, two CTAs (256 threads each) per SM.  CTA b
-// takes the (chunk, head) jobs b, b + G, b + 2G, ... (G = grid size; job j
-// is (chunk, head) = divmod(total - 1 - j, H): last chunk first) and
-// prefetches the next job's inputs while it finishes the current one: its q
-// and k as soon as the Gram product has consumed X, its g (L2 prefetch early,
-// shared memory once the W product is done).
+// intra-chunk kernel: persistent, two CTAs (256 threads each) per SM.  Job j
+// is (chunk, head) = divmod(total - 1 - j, H) (last chunk first); CTA b
+// takes jobs b and b + G (G = grid size), then further jobs from a counter,
+// each two jobs ahead, and prefetches the next job's inputs while it
+// finishes the current one: its q and k as soon as the Gram product has
+// consumed X, its g (L2 prefetch early, shared memory once the W product is
+// done).
 // ============================================================================
 constexpr int NTA = 256;
 constexpr uint32_t SA_X = 0;              // 32 KB: q|k (TMA) -> X [128][128] sw (A of the Gram)
