@@ -224,3 +224,16 @@ def test_prefill_is_deterministic(dtype, chunk):
     runs = [prefill_on_gpu(inp, chunk=chunk) for _ in range(3)]
     for o, S in runs[1:]:
         assert np.array_equal(o, runs[0][0]) and np.array_equal(S, runs[0][1])
+
+
+def test_prefill_mixed_lengths_many_sequences():
+    """48 sequences of random lengths from 0 to 2,500 tokens (about 60 K
+    tokens, 8 heads, carried states): many more jobs than the intra-chunk
+    kernel's persistent grid holds, of every tail length, so that jobs are
+    handed out from its counter across sequence boundaries.  o and the final
+    state per sequence within the bar."""
+    rng = np.random.Generator(np.random.PCG64(91))
+    lens = [int(x) for x in rng.integers(0, 2500, size=48)]
+    inp = ki.gen_prefill(92, lens, H=8, dtype="bf16", chunk=64, with_s0=True)
+    o, S = prefill_on_gpu(inp)
+    _compare(inp, o, S, TOL_BF16, "48 mixed-length sequences")
